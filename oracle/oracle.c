@@ -1,0 +1,368 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle for paged-KV decode attention and for the
+ * MLA paged causal prefill variant.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg do.  It shares no code, header, table or constant with the CUDA library.
+ *
+ * Every stored value is exact: fp16/bf16 inputs are widened to double bit by
+ * bit (no rounding), all arithmetic is double, and nothing is blocked, fused or
+ * reordered beyond the definitions below, so that a reader can check each
+ * function against the pages it cites.
+ *
+ * Sources (page title, then the function or docstring section):
+ *   [V2]  "paged_attention_v2_triton.py -- CCCL-derived Triton PagedAttention V2":
+ *         _partition_attn_kernel (docstring "Algorithm"), _reduce_partitions_kernel,
+ *         the key/value cache layout comments of its argument list.
+ *   [FD]  "koas-w.github.io flash-decode post": Decode_Paged_GQAAttention_Kernel,
+ *         _flash_decode_partial_kernel, _flash_decode_combine_kernel.
+ *   [MLA] "kernelindex.com flashinfer gemini-2.5-pro triton xvhq2i"
+ *         (mla_paged_prefill_causal_h16_ckv512_kpe64_ps1): sections
+ *         "2. Determine Sequence Boundaries", "3. Pass 1", "4. Pass 2".
+ *
+ * Status codes returned (same numbers as the library's, written out here):
+ *   0 ok, 1 invalid argument, 5 bad block table / bad page index.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+
+enum { OR_OK = 0, OR_INVALID = 1, OR_BAD_TABLE = 5 };
+enum { OR_F16 = 0, OR_BF16 = 1 };
+enum { OR_NHD = 0, OR_VLLM = 1 };
+
+/* ---- exact widening of 16-bit floats ------------------------------------ */
+
+/* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+static double f16_bits_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);                 /* subnormal: f * 2^-24 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f + 1024), e - 25);     /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper half of an IEEE binary32 (8 exponent bits, bias 127). */
+static double bf16_bits_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xff;
+    int f = h & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);                /* subnormal: f * 2^-126 / 2^7 */
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f + 128), e - 134);     /* (1 + f/128) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+static double widen(uint16_t h, int dtype)
+{
+    return dtype == OR_BF16 ? bf16_bits_to_double(h) : f16_bits_to_double(h);
+}
+
+/* Exported so the tests can check the widening against a library routine. */
+double oracle_widen(uint16_t h, int dtype) { return widen(h, dtype); }
+
+/* ---- paged K/V addressing ------------------------------------------------ */
+
+/*
+ * Element d of token slot o in physical page p, KV head g.
+ *   NHD  : k_cache / v_cache [num_blocks][n_kv_heads][block_size][head_dim]
+ *          ([FD] Decode_Paged_GQAAttention_Kernel argument comments).
+ *   VLLM : key_cache   [num_blocks][kv_heads][head_size/x][block_size][x]
+ *          value_cache [num_blocks][kv_heads][head_size][block_size]
+ *          ([V2] _partition_attn_kernel argument comments and its K/V gathers).
+ */
+static size_t k_index(int layout, int Hkv, int BS, int D, int x,
+                      long long p, int g, int o, int d)
+{
+    if (layout == OR_NHD)
+        return (((size_t)p * Hkv + g) * BS + o) * D + d;
+    return ((((size_t)p * Hkv + g) * (D / x) + d / x) * BS + o) * x + d % x;
+}
+
+static size_t v_index(int layout, int Hkv, int BS, int D,
+                      long long p, int g, int o, int d)
+{
+    if (layout == OR_NHD)
+        return (((size_t)p * Hkv + g) * BS + o) * D + d;
+    return (((size_t)p * Hkv + g) * D + d) * BS + o;
+}
+
+typedef struct {
+    int B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x;
+    const uint16_t *q, *k, *v;
+    const int32_t *table, *ctx;
+    double scale;
+} decode_args;
+
+/* Checks the arguments shared by every decode entry point. */
+static int check_decode(const decode_args* a)
+{
+    if (a->B < 0 || a->Hq <= 0 || a->Hkv <= 0 || a->D <= 0 || a->BS <= 0 ||
+        a->MBPS < 0 || a->NB < 0)
+        return OR_INVALID;
+    if (a->Hq % a->Hkv != 0) return OR_INVALID;
+    if (a->dtype != OR_F16 && a->dtype != OR_BF16) return OR_INVALID;
+    if (a->layout == OR_VLLM && (a->x <= 0 || a->D % a->x != 0)) return OR_INVALID;
+    if (a->layout != OR_NHD && a->layout != OR_VLLM) return OR_INVALID;
+    return OR_OK;
+}
+
+/* Context length of sequence b, or -1 if it is out of range. */
+static int seq_len(const decode_args* a, int b)
+{
+    int n = a->ctx[b];
+    if (n < 0 || (long long)n > (long long)a->MBPS * a->BS) return -1;
+    return n;
+}
+
+/* Physical page of token t of sequence b, or -1 if the table entry is bad.
+ * Token t lives in logical block t / block_size at slot t % block_size
+ * ([V2] "Paged K gather"; [FD] block_table comment: -1 = unallocated). */
+static long long page_of(const decode_args* a, int b, int t)
+{
+    long long p = a->table[(size_t)b * a->MBPS + t / a->BS];
+    if (p < 0 || p >= a->NB) return -1;
+    return p;
+}
+
+/* Score of token t for query head h:  scale * sum_d q[b][h][d] * K_t[d]. */
+static double score(const decode_args* a, int b, int h, int g, long long p, int o)
+{
+    double s = 0.0;
+    for (int d = 0; d < a->D; ++d) {
+        double qd = widen(a->q[((size_t)b * a->Hq + h) * a->D + d], a->dtype);
+        double kd = widen(a->k[k_index(a->layout, a->Hkv, a->BS, a->D, a->x, p, g, o, d)], a->dtype);
+        s += qd * kd;
+    }
+    return a->scale * s;
+}
+
+static double value(const decode_args* a, int g, long long p, int o, int d)
+{
+    return widen(a->v[v_index(a->layout, a->Hkv, a->BS, a->D, p, g, o, d)], a->dtype);
+}
+
+/*
+ * Softmax attention of one query head over tokens [t0, t1) of sequence b,
+ * returned unnormalised: m = max_t s_t, l = sum_t exp(s_t - m),
+ * acc[d] = sum_t exp(s_t - m) * V_t[d].  An empty range gives (-inf, 0, 0),
+ * the sentinel of [FD] _flash_decode_partial_kernel ("empty splits").
+ * Returns -1 on a bad table entry.
+ */
+static int attend_range(const decode_args* a, int b, int h, int t0, int t1,
+                        double* m_out, double* l_out, double* acc, double* sbuf)
+{
+    int G = a->Hq / a->Hkv;
+    int g = h / G;           /* consecutive grouping: kv head = q head / group size */
+    for (int d = 0; d < a->D; ++d) acc[d] = 0.0;
+    if (t1 <= t0) {
+        *m_out = -INFINITY;
+        *l_out = 0.0;
+        return 0;
+    }
+    double m = -INFINITY;
+    for (int t = t0; t < t1; ++t) {
+        long long p = page_of(a, b, t);
+        if (p < 0) return -1;
+        sbuf[t - t0] = score(a, b, h, g, p, t % a->BS);
+        if (sbuf[t - t0] > m) m = sbuf[t - t0];
+    }
+    double l = 0.0;
+    for (int t = t0; t < t1; ++t) {
+        long long p = page_of(a, b, t);
+        double w = exp(sbuf[t - t0] - m);
+        l += w;
+        for (int d = 0; d < a->D; ++d) acc[d] += w * value(a, g, p, t % a->BS, d);
+    }
+    *m_out = m;
+    *l_out = l;
+    return 0;
+}
+
+/*
+ * Paged GQA decode attention, the plain definition:
+ *   out[b][h][:] = sum_t softmax_t(scale * q[b][h] . K_t) * V_t,  t in [0, ctx[b]),
+ * K_t, V_t gathered for KV head h / (Hq/Hkv) through block_table.
+ * ctx[b] == 0 gives a zero row (the reading taken for the empty context; [FD]
+ * _flash_decode_combine_kernel writes zeros there).
+ * Only sequences b in [b_lo, b_hi) are computed and written.
+ * sbuf: caller scratch of at least max ctx doubles; acc: D doubles.
+ */
+int oracle_decode(int B, int Hq, int Hkv, int D, int BS, int MBPS, int NB,
+                  int dtype, int layout, int x,
+                  const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                  const int32_t* table, const int32_t* ctx, double scale,
+                  int b_lo, int b_hi, double* out, double* sbuf, double* acc)
+{
+    decode_args a = {B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x, q, k, v, table, ctx, scale};
+    int st = check_decode(&a);
+    if (st) return st;
+    if (b_lo < 0 || b_hi > B || b_lo > b_hi) return OR_INVALID;
+    for (int b = b_lo; b < b_hi; ++b) {
+        int n = seq_len(&a, b);
+        if (n < 0) return OR_INVALID;
+        for (int h = 0; h < Hq; ++h) {
+            double m, l;
+            if (attend_range(&a, b, h, 0, n, &m, &l, acc, sbuf)) return OR_BAD_TABLE;
+            double* o = out + ((size_t)b * Hq + h) * D;
+            for (int d = 0; d < D; ++d) o[d] = (n == 0) ? 0.0 : acc[d] / l;
+        }
+    }
+    return OR_OK;
+}
+
+/*
+ * Split mode ([V2] phase 1 with fixed partitions; [FD] partial kernel):
+ * split s covers tokens [s*P, min((s+1)*P, ctx[b])).  For each (b, h, s) it
+ * stores the unnormalised partial (m, l, acc) of attend_range, with the
+ * (-inf, 0, 0) sentinel for empty splits.  Layouts: m, l [B][Hq][NS],
+ * acc [B][Hq][NS][D].
+ */
+int oracle_decode_partials(int B, int Hq, int Hkv, int D, int BS, int MBPS, int NB,
+                           int dtype, int layout, int x,
+                           const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const int32_t* table, const int32_t* ctx, double scale,
+                           int P, int NS, int b_lo, int b_hi,
+                           double* pm, double* pl, double* pacc, double* sbuf)
+{
+    decode_args a = {B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x, q, k, v, table, ctx, scale};
+    int st = check_decode(&a);
+    if (st) return st;
+    if (P <= 0 || NS <= 0 || b_lo < 0 || b_hi > B || b_lo > b_hi) return OR_INVALID;
+    for (int b = b_lo; b < b_hi; ++b) {
+        int n = seq_len(&a, b);
+        if (n < 0) return OR_INVALID;
+        if ((long long)NS * P < n) return OR_INVALID;   /* splits must cover the context */
+        for (int h = 0; h < Hq; ++h) {
+            for (int s = 0; s < NS; ++s) {
+                long long t0 = (long long)s * P, t1 = t0 + P;
+                if (t1 > n) t1 = n;
+                if (t0 > n) t0 = n;
+                size_t i = ((size_t)b * Hq + h) * NS + s;
+                if (attend_range(&a, b, h, (int)t0, (int)t1, &pm[i], &pl[i], &pacc[i * D], sbuf))
+                    return OR_BAD_TABLE;
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/*
+ * Cross-split combine ([FD] _flash_decode_combine_kernel; [V2]
+ * _reduce_partitions_kernel docstring):  M = max_s m_s, f_s = exp(m_s - M),
+ * out = sum_s f_s acc_s / sum_s f_s l_s.  Sentinel splits (m = -inf) get
+ * f_s = 0.  ctx[b] == 0 gives zeros.
+ */
+int oracle_combine(int B, int Hq, int D, int NS, const int32_t* ctx,
+                   const double* pm, const double* pl, const double* pacc,
+                   int b_lo, int b_hi, double* out)
+{
+    if (B < 0 || Hq <= 0 || D <= 0 || NS <= 0 || b_lo < 0 || b_hi > B || b_lo > b_hi)
+        return OR_INVALID;
+    for (int b = b_lo; b < b_hi; ++b) {
+        for (int h = 0; h < Hq; ++h) {
+            double* o = out + ((size_t)b * Hq + h) * D;
+            const double* m = pm + ((size_t)b * Hq + h) * NS;
+            const double* l = pl + ((size_t)b * Hq + h) * NS;
+            const double* acc = pacc + ((size_t)b * Hq + h) * NS * D;
+            if (ctx[b] == 0) {
+                for (int d = 0; d < D; ++d) o[d] = 0.0;
+                continue;
+            }
+            double M = -INFINITY;
+            for (int s = 0; s < NS; ++s) if (m[s] > M) M = m[s];
+            double L = 0.0;
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            for (int s = 0; s < NS; ++s) {
+                double f = (m[s] == -INFINITY) ? 0.0 : exp(m[s] - M);
+                L += f * l[s];
+                for (int d = 0; d < D; ++d) o[d] += f * acc[(size_t)s * D + d];
+            }
+            for (int d = 0; d < D; ++d) o[d] /= L;
+        }
+    }
+    return OR_OK;
+}
+
+/*
+ * MLA paged causal prefill, page_size 1 ([MLA] sections 2-4):
+ * for query token t of sequence b (qo_indptr[b] <= t < qo_indptr[b+1]) and
+ * head h,
+ *   kv_len = kv_indptr[b+1] - kv_indptr[b],  q_len = qo_indptr[b+1] - qo_indptr[b],
+ *   prefix = kv_len - q_len,  pos = prefix + (t - qo_indptr[b])   (bottom-right causal),
+ *   for j in [0, kv_len) with j <= pos:  page = kv_indices[kv_indptr[b] + j],
+ *     logit_j = sm_scale * (q_nope[t][h] . ckv[page] + q_pe[t][h] . kpe[page]),
+ *   out[t][h] = sum_j softmax(logit)_j * ckv[page_j]       (V is ckv),
+ *   lse[t][h] = log2 sum_j exp(logit_j)                     (base-2 LSE).
+ * kv_len == 0 gives out = 0 and lse = -inf ([MLA] section 2).
+ * Tensors (bf16 bits): q_nope [total_q][H][Dc], q_pe [total_q][H][Dr],
+ * ckv [num_pages][1][Dc], kpe [num_pages][1][Dr].  Only tokens in [t_lo, t_hi)
+ * are computed.  sbuf: at least max kv_len doubles.
+ */
+int oracle_mla(int total_q, int H, int Dc, int Dr, int batch, int num_pages,
+               const uint16_t* q_nope, const uint16_t* q_pe,
+               const uint16_t* ckv, const uint16_t* kpe,
+               const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+               double sm_scale, int t_lo, int t_hi, double* out, double* lse, double* sbuf)
+{
+    if (total_q < 0 || H <= 0 || Dc <= 0 || Dr < 0 || batch < 0 || num_pages < 0)
+        return OR_INVALID;
+    if (t_lo < 0 || t_hi > total_q || t_lo > t_hi) return OR_INVALID;
+    if (qo_indptr[0] != 0 || kv_indptr[0] != 0 || qo_indptr[batch] != total_q) return OR_INVALID;
+    for (int t = t_lo; t < t_hi; ++t) {
+        int b = 0;
+        while (b < batch && !(qo_indptr[b] <= t && t < qo_indptr[b + 1])) ++b;
+        if (b == batch) return OR_INVALID;
+        int q_len = qo_indptr[b + 1] - qo_indptr[b];
+        int kv_len = kv_indptr[b + 1] - kv_indptr[b];
+        if (kv_len < 0) return OR_INVALID;
+        int pos = (kv_len - q_len) + (t - qo_indptr[b]);
+        for (int h = 0; h < H; ++h) {
+            double* o = out + ((size_t)t * H + h) * Dc;
+            for (int d = 0; d < Dc; ++d) o[d] = 0.0;
+            if (kv_len == 0) {
+                lse[(size_t)t * H + h] = -INFINITY;
+                continue;
+            }
+            if (kv_len < q_len) return OR_INVALID;   /* negative prefix */
+            const uint16_t* qn = q_nope + ((size_t)t * H + h) * Dc;
+            const uint16_t* qp = q_pe + ((size_t)t * H + h) * Dr;
+            int nkeys = pos + 1 < kv_len ? pos + 1 : kv_len;
+            double m = -INFINITY;
+            for (int j = 0; j < nkeys; ++j) {
+                long long pg = kv_indices[kv_indptr[b] + j];
+                if (pg < 0 || pg >= num_pages) return OR_BAD_TABLE;
+                double s = 0.0;
+                for (int d = 0; d < Dc; ++d)
+                    s += bf16_bits_to_double(qn[d]) * bf16_bits_to_double(ckv[(size_t)pg * Dc + d]);
+                for (int d = 0; d < Dr; ++d)
+                    s += bf16_bits_to_double(qp[d]) * bf16_bits_to_double(kpe[(size_t)pg * Dr + d]);
+                sbuf[j] = sm_scale * s;
+                if (sbuf[j] > m) m = sbuf[j];
+            }
+            double z = 0.0;
+            for (int j = 0; j < nkeys; ++j) {
+                long long pg = kv_indices[kv_indptr[b] + j];
+                double w = exp(sbuf[j] - m);
+                z += w;
+                for (int d = 0; d < Dc; ++d) o[d] += w * bf16_bits_to_double(ckv[(size_t)pg * Dc + d]);
+            }
+            for (int d = 0; d < Dc; ++d) o[d] /= z;
+            lse[(size_t)t * H + h] = (m + log(z)) / log(2.0);
+        }
+    }
+    return OR_OK;
+}
