@@ -1,0 +1,187 @@
+/*
+ * pkv.h -- C ABI of libpkv: paged-KV-cache attention for LLM decode on GB300
+ * (sm_103a), and its MLA paged causal prefill variant.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers named as tensors are DEVICE pointers owned by the caller; the
+ *    library never allocates, frees, copies to the host or synchronises.
+ *    Shapes are passed explicitly; every tensor is dense and row-major in the
+ *    layout written beside it.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call returns without waiting for it.
+ *  - Every call returns a pkv_status.  Argument errors are found on the host
+ *    before anything is launched; nothing on the device traps or asserts.
+ *  - 16-bit floating-point data is fp16 or bf16 (pkv_dtype); arithmetic is
+ *    fp32 with fp32 softmax statistics.
+ *
+ * Sources, cited by page title and function:
+ *  [V2]  "paged_attention_v2_triton.py -- CCCL-derived Triton PagedAttention V2"
+ *        (paged_attention_v2_triton launcher, _partition_attn_kernel,
+ *        _reduce_partitions_kernel).
+ *  [FD]  koas-w.github.io flash-decode post (paged_decode_attention,
+ *        Decode_Paged_GQAAttention_Kernel, _flash_decode_partial_kernel,
+ *        _flash_decode_combine_kernel).
+ *  [MLA] kernelindex.com "flashinfer gemini-2.5-pro triton xvhq2i"
+ *        (mla_paged_prefill_causal_h16_ckv512_kpe64_ps1: run / _forward and
+ *        the kernel's sections 2-4).
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pkv_stream_t;  /* same type as cudaStream_t */
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_INVALID_ARG = 1,          /* null pointer, bad shape, misaligned pointer, bad enum */
+    PKV_UNSUPPORTED = 2,          /* valid but not compiled: head_dim, group size, block size */
+    PKV_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the size query's answer */
+    PKV_CUDA_ERROR = 4,           /* a CUDA runtime call or a launch failed */
+    PKV_BAD_BLOCK_TABLE = 5       /* reported by pkv_validate_block_table only */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+typedef enum {
+    /* k_cache and v_cache both [num_blocks][Hkv][block_size][D] ([FD]
+     * Decode_Paged_GQAAttention_Kernel argument list). */
+    PKV_LAYOUT_NHD = 0,
+    /* vLLM layout ([V2] _partition_attn_kernel argument list):
+     * key_cache [num_blocks][Hkv][D/x][block_size][x] with x = 16 bytes / element
+     * size (x_pack = 8 for fp16/bf16), value_cache [num_blocks][Hkv][D][block_size]. */
+    PKV_LAYOUT_VLLM = 1
+} pkv_layout;
+
+/* Problem description of one decode step (one query token per sequence). */
+typedef struct {
+    int B;                   /* sequences in the batch */
+    int Hq;                  /* query heads; Hq % Hkv == 0, group G = Hq / Hkv <= 16 */
+    int Hkv;                 /* KV heads; query head h reads KV head h / G */
+    int D;                   /* head dim: 64, 128 or 256 */
+    int block_size;          /* tokens per page: 16 */
+    int max_blocks_per_seq;  /* columns of block_table */
+    int num_blocks;          /* pages in the pool */
+    int max_context_len;     /* host-known upper bound on context_lens[] (plans the grid) */
+    long long sum_context_len; /* host-known sum of context_lens[] (plans the split); may be an estimate */
+    int dtype;               /* pkv_dtype of q, caches and out */
+    int layout;              /* pkv_layout */
+    int x_pack;              /* VLLM layout only: must be 8 */
+} pkv_decode_desc;
+
+/* Optional knobs; pass NULL for the defaults (all zero). */
+typedef struct {
+    int partition_tokens;    /* tokens per split, a multiple of block_size; 0 = planner */
+    int num_splits;          /* used when partition_tokens == 0: split the longest context this many ways */
+    int reserved;            /* must be 0 */
+    /* Optional cudaEvent_t handles recorded on `stream` right before and right
+     * after the phase-1 kernel, so a caller can time that kernel alone inside a
+     * full call.  NULL = not recorded. */
+    void* phase1_event_start;
+    void* phase1_event_stop;
+} pkv_decode_opts;
+
+/* Text of a status code (static storage). */
+const char* pkv_status_string(int status);
+
+/* ABI version of this header: 1. */
+int pkv_version(void);
+
+/*
+ * Split planner (host only, deterministic integer arithmetic).  Splits every
+ * sequence into partitions of *partition_tokens tokens (a multiple of
+ * block_size): split s covers tokens [s*P, min((s+1)*P, n)) ([V2] fixed
+ * 512-token partitions; [FD] page-granular splits).  *num_splits =
+ * ceil(max_context_len / P) (at least 1) is the grid extent along splits.
+ * num_sms <= 0 queries the current device.  The default picks P = 512 tokens
+ * (or the longest context, if shorter), halved while the estimated number of
+ * (sequence, KV head, split) work items stays below 6 * num_sms, down to
+ * 4 * block_size.
+ */
+int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms,
+                    int* num_splits, int* partition_tokens);
+
+/*
+ * Bytes of scratch memory pkv_paged_decode_attention needs for this problem
+ * (256-byte header + fp32 split partials when the plan has more than one
+ * split).  num_sms as for pkv_plan_splits.  The workspace must be 256-byte
+ * aligned.  Word 0 of the header collects device-side error bits (bit 0: a
+ * pipeline wait timed out); zero it once after allocating.
+ */
+int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms,
+                              size_t* bytes);
+
+/*
+ * Paged GQA decode attention ([FD] paged_decode_attention; [V2]
+ * paged_attention_v2_triton):
+ *   out[b][h][:] = sum_t softmax_t(scale * q[b][h] . K_t) V_t,   t < context_lens[b],
+ * with K_t, V_t the slot t % block_size of page block_table[b][t / block_size]
+ * of KV head h / G.  context_lens[b] == 0 gives a zero row.
+ *   q, out        [B][Hq][D] of dtype (4-byte aligned; out 8-byte aligned)
+ *   k/v_cache     per layout (16-byte aligned)
+ *   block_table   int32 [B][max_blocks_per_seq]; entries past a sequence's last
+ *                 page are never read (-1 is the customary filler).  A live entry
+ *                 outside [0, num_blocks) is a caller error: it is clamped to a
+ *                 valid page (no out-of-bounds access, result unspecified);
+ *                 pkv_validate_block_table reports it.
+ *   context_lens  int32 [B]; values are clamped to
+ *                 [0, min(max_context_len, max_blocks_per_seq * block_size)].
+ * Phase 1 runs one CTA per (sequence, KV head, split), loading each page once
+ * for the whole group; sequences with more than one split are merged by a
+ * second, log-sum-exp combine kernel.
+ */
+int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
+                               const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, const int32_t* context_lens,
+                               float scale, void* out,
+                               void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * Phase 1 alone, for layered testing ([FD] _flash_decode_partial_kernel):
+ * writes, for every sequence b, query head h and split s < *num_splits_out,
+ * the unnormalised fp32 partial of split s in natural-log units:
+ *   part_m[b][h][s] = max_t s_t,  part_l[b][h][s] = sum_t exp(s_t - m),
+ *   part_acc[b][h][s][:] = sum_t exp(s_t - m) V_t,
+ * and the sentinel (-inf, 0, 0) for splits past the context.  The arrays
+ * are [B][Hq][num_splits_capacity] (and [...][D]); the call fails with
+ * PKV_WORKSPACE_TOO_SMALL if the plan needs more splits than the capacity.
+ */
+int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
+                        const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_table, const int32_t* context_lens, float scale,
+                        float* part_acc, float* part_m, float* part_l, int num_splits_capacity,
+                        int* partition_tokens_out, int* num_splits_out, pkv_stream_t stream);
+
+/*
+ * Phase 2 alone ([FD] _flash_decode_combine_kernel; [V2]
+ * _reduce_partitions_kernel): for every (b, h) with n = context_lens[b]
+ * (clamped as above), NS_b = ceil(n / partition_tokens) splits are merged:
+ *   M = max_s m_s,  out = sum_s e^{m_s - M} acc_s / sum_s e^{m_s - M} l_s,
+ * and n == 0 gives zeros.  Partials are laid out as pkv_decode_partials
+ * writes them with num_splits columns.
+ */
+int pkv_combine(const pkv_decode_desc* desc, int partition_tokens, int num_splits,
+                const int32_t* context_lens, const float* part_acc, const float* part_m,
+                const float* part_l, void* out, pkv_stream_t stream);
+
+/*
+ * Optional device-side validator of the paged indexing (never traps).  ORs
+ * into *err_word (device, 4 bytes, caller-zeroed):
+ *   bit 0  some context_lens[b] < 0, > max_context_len or > max_blocks_per_seq * block_size
+ *   bit 1  some live block_table entry (block index < ceil(n / block_size)) is
+ *          outside [0, num_blocks)
+ * Entries past a sequence's live range are not inspected.
+ */
+int pkv_validate_block_table(const pkv_decode_desc* desc, const int32_t* block_table,
+                             const int32_t* context_lens, uint32_t* err_word, pkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

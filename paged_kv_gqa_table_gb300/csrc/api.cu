@@ -1,0 +1,360 @@
+// api.cu -- the C ABI of libpkv (declared in include/pkv.h): argument
+// validation, the split planner, TMA descriptor set-up and kernel dispatch.
+// Host code only; nothing here touches device memory directly.
+#include <climits>
+#include <cmath>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "internal.h"
+#include "pkv.h"
+
+using namespace pkv;
+
+namespace {
+
+constexpr int kBS = 16;          // compiled page size
+constexpr int kHeaderBytes = 256;
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+long long round_up(long long a, long long b) { return ceil_div(a, b) * b; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_desc(const pkv_decode_desc* d) {
+    if (!d) return PKV_INVALID_ARG;
+    if (d->B < 0 || d->Hq <= 0 || d->Hkv <= 0 || d->D <= 0 || d->block_size <= 0 || d->max_blocks_per_seq < 0 ||
+        d->num_blocks < 0 || d->max_context_len < 0 || d->sum_context_len < 0)
+        return PKV_INVALID_ARG;
+    if (d->Hq % d->Hkv != 0) return PKV_INVALID_ARG;
+    if (d->dtype != PKV_F16 && d->dtype != PKV_BF16) return PKV_INVALID_ARG;
+    if (d->layout != PKV_LAYOUT_NHD && d->layout != PKV_LAYOUT_VLLM) return PKV_INVALID_ARG;
+    if (d->layout == PKV_LAYOUT_VLLM && d->x_pack != 8) return PKV_INVALID_ARG;
+    if ((long long)d->max_context_len > (long long)d->max_blocks_per_seq * d->block_size) return PKV_INVALID_ARG;
+    if (d->max_context_len > 0 && d->num_blocks == 0) return PKV_INVALID_ARG;
+    if (d->D != 64 && d->D != 128 && d->D != 256) return PKV_UNSUPPORTED;
+    if (d->block_size != kBS) return PKV_UNSUPPORTED;
+    const int G = d->Hq / d->Hkv;
+    if (G > 16 || (G > 8 && d->D > 128)) return PKV_UNSUPPORTED;
+    if ((long long)d->num_blocks * d->Hkv > INT_MAX) return PKV_UNSUPPORTED;
+    if ((long long)d->B * d->Hq > INT_MAX) return PKV_UNSUPPORTED;
+    return PKV_OK;
+}
+
+int current_sm_count(int* out) {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_CUDA_ERROR;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return PKV_CUDA_ERROR;
+        cache[dev] = n;
+    }
+    *out = cache[dev];
+    return PKV_OK;
+}
+
+// Default partition: 512 tokens (or the longest context rounded up to a
+// page, if shorter), halved while the estimated number of non-empty work
+// items Hkv * ceil(sum_n / P) stays below six per SM, down to four pages.
+long long auto_partition(const pkv_decode_desc* d, int num_sms) {
+    const long long BS = d->block_size;
+    const long long maxn = d->max_context_len > 0 ? d->max_context_len : 1;
+    long long P = round_up(maxn < 512 ? maxn : 512, BS);
+    const long long min_p = 4 * BS;
+    const long long target = 6LL * num_sms;
+    const long long sum = d->sum_context_len > 0 ? d->sum_context_len : 1;
+    while (P > min_p) {
+        const long long units = (long long)d->Hkv * ceil_div(sum, P);
+        if (units >= target) break;
+        long long np = round_up(P / 2, BS);
+        if (np < min_p) np = min_p;
+        if (np >= P) break;
+        P = np;
+    }
+    return P;
+}
+
+int plan(const pkv_decode_desc* d, const pkv_decode_opts* o, int num_sms, int* ns, int* P) {
+    int st = check_desc(d);
+    if (st) return st;
+    if (o && o->reserved != 0) return PKV_INVALID_ARG;
+    if (num_sms <= 0) {
+        st = current_sm_count(&num_sms);
+        if (st) return st;
+    }
+    long long p;
+    if (o && o->partition_tokens > 0) {
+        p = o->partition_tokens;
+        if (p % d->block_size != 0) return PKV_INVALID_ARG;
+    } else if (o && o->num_splits > 0) {
+        const long long maxn = d->max_context_len > 0 ? d->max_context_len : 1;
+        p = round_up(ceil_div(maxn, o->num_splits), d->block_size);
+    } else if (o && (o->partition_tokens < 0 || o->num_splits < 0)) {
+        return PKV_INVALID_ARG;
+    } else {
+        p = auto_partition(d, num_sms);
+    }
+    long long n_splits = ceil_div(d->max_context_len, p);
+    if (n_splits < 1) n_splits = 1;
+    if (p > INT_MAX || n_splits > INT_MAX || (long long)d->B * d->Hkv * n_splits > INT_MAX) return PKV_UNSUPPORTED;
+    *P = (int)p;
+    *ns = (int)n_splits;
+    return PKV_OK;
+}
+
+size_t partial_bytes(const pkv_decode_desc* d, int ns) {
+    const size_t rows = (size_t)d->B * d->Hq * ns;
+    return 2 * align256(rows * 4) + align256(rows * d->D * 4);
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Page slice of one KV head as a 3-D tensor {inner, rows, num_blocks * Hkv}.
+//   NHD : {D, BS, NB*Hkv}, box {64, BS, 1}, 128-byte swizzle.
+//   VLLM: the contiguous D*BS-element slice viewed as {256, D*BS/256, NB*Hkv},
+//         box {256, D*BS/256, 1}, no swizzle.
+int encode_cache_map(CUtensorMap* map, const void* base, const pkv_decode_desc* d) {
+    auto fn = encode_fn();
+    if (!fn) return PKV_CUDA_ERROR;
+    const cuuint64_t slices = (cuuint64_t)d->num_blocks * d->Hkv;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3], estr[3] = {1, 1, 1};
+    CUtensorMapSwizzle swz;
+    if (d->layout == PKV_LAYOUT_NHD) {
+        dims[0] = d->D;
+        dims[1] = d->block_size;
+        dims[2] = slices;
+        strides[0] = (cuuint64_t)d->D * 2;
+        strides[1] = (cuuint64_t)d->D * d->block_size * 2;
+        box[0] = 64;
+        box[1] = d->block_size;
+        box[2] = 1;
+        swz = CU_TENSOR_MAP_SWIZZLE_128B;
+    } else {
+        const cuuint64_t e = (cuuint64_t)d->D * d->block_size;
+        dims[0] = 256;
+        dims[1] = e / 256;
+        dims[2] = slices;
+        strides[0] = 512;
+        strides[1] = e * 2;
+        box[0] = 256;
+        box[1] = (cuuint32_t)(e / 256);
+        box[2] = 1;
+        swz = CU_TENSOR_MAP_SWIZZLE_NONE;
+    }
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_INVALID_ARG;
+}
+
+cudaError_t dispatch_phase1(const pkv_decode_desc* d, const DecodeParams& p, const CUtensorMap& k,
+                            const CUtensorMap& v, cudaStream_t s) {
+    const int nt = (d->Hq / d->Hkv) > 8 ? 2 : 1;
+    const bool bf = d->dtype == PKV_BF16;
+    if (d->layout == PKV_LAYOUT_NHD)
+        return bf ? launch_decode_nhd_bf16(d->D, nt, p, k, v, s) : launch_decode_nhd_f16(d->D, nt, p, k, v, s);
+    return bf ? launch_decode_vllm_bf16(d->D, nt, p, k, v, s) : launch_decode_vllm_f16(d->D, nt, p, k, v, s);
+}
+
+int check_tensors(const pkv_decode_desc* d, const void* q, const void* k, const void* v, const int32_t* table,
+                  const int32_t* ctx) {
+    if (!q || !k || !v || !table || !ctx) return PKV_INVALID_ARG;
+    if (!aligned(q, 4) || !aligned(k, 16) || !aligned(v, 16) || !aligned(table, 4) || !aligned(ctx, 4))
+        return PKV_INVALID_ARG;
+    (void)d;
+    return PKV_OK;
+}
+
+// Common set-up of phase 1: parameters and the two tensor maps.
+int prepare_phase1(const pkv_decode_desc* d, int P, int NS, const void* q, const void* k, const void* v,
+                   const int32_t* table, const int32_t* ctx, float scale, DecodeParams* p, CUtensorMap* mk,
+                   CUtensorMap* mv) {
+    *p = DecodeParams{};
+    p->q = q;
+    p->table = table;
+    p->ctx = ctx;
+    p->B = d->B;
+    p->Hq = d->Hq;
+    p->Hkv = d->Hkv;
+    p->G = d->Hq / d->Hkv;
+    p->MBPS = d->max_blocks_per_seq;
+    p->NB = d->num_blocks;
+    p->P = P;
+    p->NS = NS;
+    p->ns_stride = NS;
+    p->n_cap = d->max_context_len;
+    p->scale_log2 = (float)((double)scale * 1.4426950408889634);
+    if (d->max_context_len == 0) return PKV_OK;   // maps unused: every split is empty
+    int st = encode_cache_map(mk, k, d);
+    if (st) return st;
+    return encode_cache_map(mv, v, d);
+}
+
+void record(void* ev, cudaStream_t s) {
+    if (ev) cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev), s);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_INVALID_ARG: return "invalid argument";
+        case PKV_UNSUPPORTED: return "unsupported configuration";
+        case PKV_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case PKV_CUDA_ERROR: return "CUDA error";
+        case PKV_BAD_BLOCK_TABLE: return "bad block table";
+        default: return "unknown status";
+    }
+}
+
+int pkv_version(void) { return 1; }
+
+int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms, int* num_splits,
+                    int* partition_tokens) {
+    if (!num_splits || !partition_tokens) return PKV_INVALID_ARG;
+    return plan(desc, opts, num_sms, num_splits, partition_tokens);
+}
+
+int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms, size_t* bytes) {
+    if (!bytes) return PKV_INVALID_ARG;
+    int ns = 0, P = 0;
+    int st = plan(desc, opts, num_sms, &ns, &P);
+    if (st) return st;
+    *bytes = kHeaderBytes + (ns > 1 ? partial_bytes(desc, ns) : 0);
+    return PKV_OK;
+}
+
+int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opts* opts, const void* q,
+                               const void* k_cache, const void* v_cache, const int32_t* block_table,
+                               const int32_t* context_lens, float scale, void* out, void* workspace,
+                               size_t workspace_bytes, pkv_stream_t stream) {
+    int st = check_desc(desc);
+    if (st) return st;
+    if (desc->B == 0) return PKV_OK;
+    st = check_tensors(desc, q, k_cache, v_cache, block_table, context_lens);
+    if (st) return st;
+    if (!out || !aligned(out, 8) || !workspace || !aligned(workspace, 256) || !std::isfinite(scale))
+        return PKV_INVALID_ARG;
+    int ns = 0, P = 0;
+    st = plan(desc, opts, 0, &ns, &P);
+    if (st) return st;
+    const size_t need = kHeaderBytes + (ns > 1 ? partial_bytes(desc, ns) : 0);
+    if (workspace_bytes < need) return PKV_WORKSPACE_TOO_SMALL;
+
+    DecodeParams p;
+    CUtensorMap mk, mv;
+    st = prepare_phase1(desc, P, ns, q, k_cache, v_cache, block_table, context_lens, scale, &p, &mk, &mv);
+    if (st) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.out = out;
+    p.err = reinterpret_cast<uint32_t*>(ws);
+    const size_t rows = (size_t)desc->B * desc->Hq * ns;
+    p.part_m = reinterpret_cast<float*>(ws + kHeaderBytes);
+    p.part_l = reinterpret_cast<float*>(ws + kHeaderBytes + align256(rows * 4));
+    p.part_acc = reinterpret_cast<float*>(ws + kHeaderBytes + 2 * align256(rows * 4));
+
+    if (desc->max_context_len == 0) {
+        // Every context is empty: the combine kernel writes the zero rows.
+        CombineParams c{context_lens, nullptr, nullptr, nullptr, out, desc->B, desc->Hq, P, ns, 0, 0};
+        return launch_combine(desc->dtype, desc->D, c, s) == cudaSuccess ? PKV_OK : PKV_CUDA_ERROR;
+    }
+    record(opts ? opts->phase1_event_start : nullptr, s);
+    if (dispatch_phase1(desc, p, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
+    record(opts ? opts->phase1_event_stop : nullptr, s);
+    if (ns > 1) {
+        CombineParams c{context_lens, p.part_acc, p.part_m, p.part_l, out, desc->B, desc->Hq, P, ns, p.n_cap, 1};
+        if (launch_combine(desc->dtype, desc->D, c, s) != cudaSuccess) return PKV_CUDA_ERROR;
+    }
+    return PKV_OK;
+}
+
+int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts, const void* q, const void* k_cache,
+                        const void* v_cache, const int32_t* block_table, const int32_t* context_lens, float scale,
+                        float* part_acc, float* part_m, float* part_l, int num_splits_capacity,
+                        int* partition_tokens_out, int* num_splits_out, pkv_stream_t stream) {
+    int st = check_desc(desc);
+    if (st) return st;
+    if (desc->B > 0) {
+        st = check_tensors(desc, q, k_cache, v_cache, block_table, context_lens);
+        if (st) return st;
+        if (!part_acc || !part_m || !part_l || !aligned(part_acc, 16) || !std::isfinite(scale))
+            return PKV_INVALID_ARG;
+    }
+    int ns = 0, P = 0;
+    st = plan(desc, opts, 0, &ns, &P);
+    if (st) return st;
+    if (partition_tokens_out) *partition_tokens_out = P;
+    if (num_splits_out) *num_splits_out = ns;
+    if (ns > num_splits_capacity) return PKV_WORKSPACE_TOO_SMALL;
+    if (desc->B == 0) return PKV_OK;
+    DecodeParams p;
+    CUtensorMap mk, mv;
+    st = prepare_phase1(desc, P, ns, q, k_cache, v_cache, block_table, context_lens, scale, &p, &mk, &mv);
+    if (st) return st;
+    p.partials_only = 1;
+    p.ns_stride = num_splits_capacity;
+    p.part_acc = part_acc;
+    p.part_m = part_m;
+    p.part_l = part_l;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (desc->max_context_len == 0) {
+        // Maps were not encoded; every split is empty, so the kernel only
+        // writes sentinels and never dereferences them.
+        mk = CUtensorMap{};
+        mv = CUtensorMap{};
+    }
+    record(opts ? opts->phase1_event_start : nullptr, s);
+    if (dispatch_phase1(desc, p, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
+    record(opts ? opts->phase1_event_stop : nullptr, s);
+    return PKV_OK;
+}
+
+int pkv_combine(const pkv_decode_desc* desc, int partition_tokens, int num_splits, const int32_t* context_lens,
+                const float* part_acc, const float* part_m, const float* part_l, void* out, pkv_stream_t stream) {
+    int st = check_desc(desc);
+    if (st) return st;
+    if (partition_tokens <= 0 || partition_tokens % desc->block_size != 0 || num_splits <= 0) return PKV_INVALID_ARG;
+    if (ceil_div(desc->max_context_len, partition_tokens) > num_splits) return PKV_INVALID_ARG;
+    if (desc->B == 0) return PKV_OK;
+    if (!context_lens || !part_acc || !part_m || !part_l || !out || !aligned(part_acc, 16)) return PKV_INVALID_ARG;
+    CombineParams c{context_lens, part_acc, part_m, part_l, out, desc->B, desc->Hq, partition_tokens, num_splits,
+                    desc->max_context_len, 0};
+    return launch_combine(desc->dtype, desc->D, c, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_CUDA_ERROR;
+}
+
+int pkv_validate_block_table(const pkv_decode_desc* desc, const int32_t* block_table, const int32_t* context_lens,
+                             uint32_t* err_word, pkv_stream_t stream) {
+    int st = check_desc(desc);
+    if (st) return st;
+    if (desc->B == 0) return PKV_OK;
+    if (!block_table || !context_lens || !err_word) return PKV_INVALID_ARG;
+    return launch_validate(block_table, context_lens, desc->B, desc->max_blocks_per_seq, desc->block_size,
+                           desc->num_blocks, desc->max_context_len, err_word,
+                           reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_CUDA_ERROR;
+}
+
+}  // extern "C"

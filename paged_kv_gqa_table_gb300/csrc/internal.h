@@ -1,0 +1,33 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include "decode.cuh"
+
+namespace pkv {
+
+struct CombineParams {
+    const int32_t* ctx;        // [B]
+    const float* part_acc;     // [B][Hq][ns_stride][D]
+    const float* part_m;       // [B][Hq][ns_stride]
+    const float* part_l;       // [B][Hq][ns_stride]
+    void* out;                 // [B][Hq][D]
+    int B, Hq, P, ns_stride, n_cap;
+    int skip_single;           // 1: rows whose sequence has <= 1 split were written by phase 1
+};
+
+// Phase-1 dispatch, one function per (layout, dtype) translation unit.
+// D in {64, 128, 256}; nt = padded-head tiles of 8 (1, or 2 for D <= 128).
+cudaError_t launch_decode_nhd_f16(int D, int nt, const DecodeParams& p, const CUtensorMap& k, const CUtensorMap& v,
+                                  cudaStream_t s);
+cudaError_t launch_decode_nhd_bf16(int D, int nt, const DecodeParams& p, const CUtensorMap& k, const CUtensorMap& v,
+                                   cudaStream_t s);
+cudaError_t launch_decode_vllm_f16(int D, int nt, const DecodeParams& p, const CUtensorMap& k, const CUtensorMap& v,
+                                   cudaStream_t s);
+cudaError_t launch_decode_vllm_bf16(int D, int nt, const DecodeParams& p, const CUtensorMap& k,
+                                    const CUtensorMap& v, cudaStream_t s);
+
+cudaError_t launch_combine(int dtype, int D, const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_validate(const int32_t* table, const int32_t* ctx, int B, int MBPS, int BS, int NB, int max_ctx,
+                            uint32_t* err, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,81 @@
+"""Device-memory plumbing around the C ABI: uploads synthetic cases into torch
+CUDA tensors, sizes workspaces and wraps the calls with torch-allocated
+outputs.  Nothing here computes attention; every step runs in libpkv."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding as B
+from . import synth
+
+TORCH_DTYPE = {synth.F16: torch.float16, synth.BF16: torch.bfloat16}
+
+
+def bits_to_torch(bits: np.ndarray, dtype: int, device, pin: bool = False) -> torch.Tensor:
+    """uint16 bit patterns -> torch fp16/bf16 tensor (on `device`, or pinned host memory)."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(TORCH_DTYPE[dtype])
+    if device == "cpu":
+        return t.pin_memory() if pin else t
+    return t.to(device)
+
+
+def int_to_torch(a: np.ndarray, device, pin: bool = False) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))
+    if device == "cpu":
+        return t.pin_memory() if pin else t
+    return t.to(device)
+
+
+def decode_desc(case: dict) -> B.pkv_decode_desc:
+    ctx = case["context_lens"]
+    return B.make_desc(case["B"], case["Hq"], case["Hkv"], case["D"], case["block_size"],
+                       case["block_table"].shape[1], case["num_blocks"], int(np.max(ctx, initial=0)),
+                       int(np.sum(ctx, dtype=np.int64)), case["dtype"], case["layout"], case.get("x", 8))
+
+
+def upload_decode_case(case: dict, device="cuda") -> dict:
+    dt = case["dtype"]
+    return dict(q=bits_to_torch(case["q"], dt, device), k_cache=bits_to_torch(case["k_cache"], dt, device),
+                v_cache=bits_to_torch(case["v_cache"], dt, device),
+                block_table=int_to_torch(case["block_table"], device),
+                context_lens=int_to_torch(case["context_lens"], device))
+
+
+def workspace_for(desc, opts=None, device="cuda") -> torch.Tensor:
+    n = B.pkv_decode_workspace_size(desc, opts)
+    ws = torch.zeros((n + 255) // 256 * 256 + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + n]
+
+
+def paged_decode_attention(case: dict, dev: dict | None = None, opts=None, out=None, workspace=None,
+                           stream=None) -> torch.Tensor:
+    """Runs the full decode path on a synthetic case; returns out [B][Hq][D] on the device."""
+    dev = dev if dev is not None else upload_decode_case(case)
+    desc = decode_desc(case)
+    if out is None:
+        out = torch.empty((case["B"], case["Hq"], case["D"]), dtype=TORCH_DTYPE[case["dtype"]],
+                          device=dev["q"].device)
+    if workspace is None:
+        workspace = workspace_for(desc, opts, device=dev["q"].device)
+    B.pkv_paged_decode_attention(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
+                                 dev["context_lens"], case["scale"], out, workspace, opts=opts, stream=stream)
+    return out
+
+
+def decode_partials(case: dict, dev: dict | None = None, opts=None, capacity: int | None = None):
+    """Phase 1 alone; returns (P, NS, m, l, acc) as float64 numpy arrays with NS columns."""
+    dev = dev if dev is not None else upload_decode_case(case)
+    desc = decode_desc(case)
+    ns, P = B.pkv_plan_splits(desc, opts)
+    cap = capacity if capacity is not None else ns
+    d = dev["q"].device
+    Bn, Hq, D = case["B"], case["Hq"], case["D"]
+    acc = torch.full((Bn, Hq, cap, D), float("nan"), dtype=torch.float32, device=d)
+    m = torch.full((Bn, Hq, cap), float("nan"), dtype=torch.float32, device=d)
+    l = torch.full((Bn, Hq, cap), float("nan"), dtype=torch.float32, device=d)
+    P2, ns2 = B.pkv_decode_partials(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
+                                    dev["context_lens"], case["scale"], acc, m, l, cap, opts=opts)
+    torch.cuda.synchronize()
+    return P2, ns2, m.double().cpu().numpy(), l.double().cpu().numpy(), acc.double().cpu().numpy()

@@ -1,0 +1,169 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads, exports
+every function include/pkv.h declares, plans splits by its documented rule
+(checked against an independent restatement), sizes workspaces, and rejects
+bad arguments before launching anything."""
+import ctypes
+import os
+import random
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    from paged_kv_gqa_table_gb300 import binding, build
+    if not os.path.exists(binding.LIB_PATH):
+        build.build()
+    binding.load()
+    return binding
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(pkv_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_function(B):
+    names = declared_functions()
+    assert "pkv_paged_decode_attention" in names and len(names) >= 8
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(B.FUNCTIONS) <= set(names)
+
+
+def test_version_and_status_strings(B):
+    assert B.pkv_version() == 1
+    assert B.status_string(0) == "ok"
+    assert B.status_string(5) == "bad block table"
+    assert B.status_string(99) == "unknown status"
+
+
+def desc(lib, **kw):
+    base = dict(B=64, Hq=32, Hkv=8, D=128, block_size=16, max_blocks_per_seq=256, num_blocks=9000,
+                max_context_len=4096, sum_context_len=131072, dtype=1, layout=0, x_pack=8)
+    base.update(kw)
+    return lib.make_desc(**base)
+
+
+def ref_plan(d, num_sms, P_forced=0, ns_forced=0):
+    """Independent restatement of the planner's documented rule."""
+    bs = d.block_size
+    up = lambda a: -(-a // bs) * bs
+    if P_forced:
+        P = P_forced
+    elif ns_forced:
+        P = up(-(-max(d.max_context_len, 1) // ns_forced))
+    else:
+        P = up(min(max(d.max_context_len, 1), 512))
+        while P > 4 * bs and d.Hkv * -(-max(d.sum_context_len, 1) // P) < 6 * num_sms:
+            P = max(4 * bs, up(P // 2))
+    return max(1, -(-d.max_context_len // P)), P
+
+
+def test_plan_matches_the_documented_rule(B):
+    rng = random.Random(0)
+    for _ in range(2000):
+        Hkv = rng.choice([1, 2, 4, 8])
+        Bn = rng.randint(1, 300)
+        mbps = rng.randint(1, 9000)
+        maxn = rng.randint(0, mbps * 16)
+        s = rng.randint(maxn, max(maxn, maxn * Bn))
+        d = desc(B, B=Bn, Hkv=Hkv, Hq=Hkv * rng.choice([1, 4, 6, 8]), D=rng.choice([64, 128]),
+                 max_blocks_per_seq=mbps, max_context_len=maxn, sum_context_len=s)
+        sms = rng.choice([1, 76, 148, 152])
+        mode = rng.randint(0, 2)
+        if mode == 0:
+            assert B.pkv_plan_splits(d, None, sms) == ref_plan(d, sms)
+        elif mode == 1:
+            P = 16 * rng.randint(1, 300)
+            assert B.pkv_plan_splits(d, B.make_opts(partition_tokens=P), sms) == ref_plan(d, sms, P_forced=P)
+        else:
+            k = rng.randint(1, 400)
+            assert B.pkv_plan_splits(d, B.make_opts(num_splits=k), sms) == ref_plan(d, sms, ns_forced=k)
+
+
+def test_named_workload_plans(B):
+    # 152 SMs: the decode workloads split into 512-token partitions.
+    assert B.pkv_plan_splits(desc(B), None, 152) == (8, 512)
+    long_ctx = desc(B, B=4, max_blocks_per_seq=8192, max_context_len=131072, sum_context_len=4 * 81920)
+    assert B.pkv_plan_splits(long_ctx, None, 152) == (256, 512)
+    tiny = desc(B, B=2, Hq=4, Hkv=2, D=64, max_blocks_per_seq=8, num_blocks=16, max_context_len=100,
+                sum_context_len=137, dtype=0)
+    assert B.pkv_plan_splits(tiny, None, 152) == (2, 64)
+
+
+def test_workspace_size(B):
+    d = desc(B)
+    ns, P = B.pkv_plan_splits(d, None, 152)
+    rows = 64 * 32 * ns
+    al = lambda x: (x + 255) // 256 * 256
+    assert B.pkv_decode_workspace_size(d, None, 152) == 256 + 2 * al(rows * 4) + al(rows * 128 * 4)
+    single = B.make_opts(num_splits=1)
+    assert B.pkv_decode_workspace_size(d, single, 152) == 256
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("Hkv", 3, 1), ("Hq", 0, 1), ("D", 96, 2), ("block_size", 32, 2), ("dtype", 7, 1), ("layout", 2, 1),
+    ("max_context_len", 256 * 16 + 1, 1), ("B", -1, 1), ("num_blocks", 0, 1), ("sum_context_len", -5, 1),
+])
+def test_bad_descriptions_are_rejected(B, field, value, status):
+    d = desc(B, **{field: value})
+    with pytest.raises(B.PkvError) as e:
+        B.pkv_plan_splits(d, None, 152)
+    assert e.value.status == status
+
+
+def test_unsupported_group_sizes(B):
+    with pytest.raises(B.PkvError) as e:
+        B.pkv_plan_splits(desc(B, Hq=8 * 17), None, 152)
+    assert e.value.status == 2
+    with pytest.raises(B.PkvError) as e:
+        B.pkv_plan_splits(desc(B, Hq=8 * 12, D=256), None, 152)
+    assert e.value.status == 2
+    with pytest.raises(B.PkvError) as e:
+        B.pkv_plan_splits(desc(B, layout=1, x_pack=4), None, 152)
+    assert e.value.status == 1
+
+
+def test_pointer_checks_happen_before_any_launch(B):
+    d = desc(B)
+    P = ctypes.c_void_p
+    good = 1 << 20       # aligned fake addresses: the calls must fail before using them
+    args = lambda **kw: [kw.get(k, good) for k in ("q", "k", "v", "t", "c")]
+    for bad in (dict(q=None), dict(k=good + 8), dict(v=None), dict(t=good + 2), dict(c=None)):
+        q, k, v, t, c = args(**bad)
+        st = B.raw_status("pkv_paged_decode_attention", ctypes.byref(d), None, q, k, v, t, c,
+                          ctypes.c_float(0.1), good, good, 1 << 30, None)
+        assert st == B.PKV_INVALID_ARG, bad
+    st = B.raw_status("pkv_paged_decode_attention", ctypes.byref(d), None, good, good, good, good, good,
+                      ctypes.c_float(0.1), good + 4, good, 1 << 30, None)
+    assert st == B.PKV_INVALID_ARG       # misaligned out
+    st = B.raw_status("pkv_paged_decode_attention", ctypes.byref(d), None, good, good, good, good, good,
+                      ctypes.c_float(float("nan")), good, good, 1 << 30, None)
+    assert st == B.PKV_INVALID_ARG       # non-finite scale
+    st = B.raw_status("pkv_paged_decode_attention", None, None, good, good, good, good, good,
+                      ctypes.c_float(0.1), good, good, 1 << 30, None)
+    assert st == B.PKV_INVALID_ARG
+    # partial arrays and combine arguments
+    st = B.raw_status("pkv_combine", ctypes.byref(d), 500, 9, good, good, good, good, good, None)
+    assert st == B.PKV_INVALID_ARG       # 500 is not a multiple of the page size
+    st = B.raw_status("pkv_combine", ctypes.byref(d), 512, 7, good, good, good, good, good, None)
+    assert st == B.PKV_INVALID_ARG       # 7 splits of 512 cannot cover 4096 tokens
+    st = B.raw_status("pkv_validate_block_table", ctypes.byref(d), good, good, None, None)
+    assert st == B.PKV_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(B):
+    d = desc(B, B=0, max_context_len=0, sum_context_len=0)
+    st = B.raw_status("pkv_paged_decode_attention", ctypes.byref(d), None, None, None, None, None, None,
+                      ctypes.c_float(0.1), None, None, 0, None)
+    assert st == B.PKV_OK

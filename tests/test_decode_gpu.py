@@ -1,0 +1,217 @@
+"""GPU parity of paged GQA decode (phase 1 + combine) against the fp64 oracle.
+
+Every call goes through the C ABI (libpkv) via the ctypes binding.  Tolerances
+are the stated bars on outputs: max |diff| <= 4e-3 for fp16 and <= 1.6e-2 for
+bf16, against the unrounded fp64 oracle.  Partials compare lse_s = m_s + ln l_s
+within 1e-3 and acc_s / l_s within the output tolerance.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_gqa_table_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+TOL = {synth.F16: 4e-3, synth.BF16: 1.6e-2}
+
+
+def _tensors():
+    from paged_kv_gqa_table_gb300 import tensors
+    return tensors
+
+
+def _binding():
+    from paged_kv_gqa_table_gb300 import binding
+    return binding
+
+
+def gpu_out(case, opts=None):
+    T = _tensors()
+    out = T.paged_decode_attention(case, opts=opts)
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy()
+
+
+def check_rows(case, got, b_idx, err_out=None):
+    ref = np.full(got.shape, np.nan)
+    for b in b_idx:
+        oracle.decode(case, b, b + 1, out=ref)
+    diff = np.abs(got[b_idx] - ref[b_idx])
+    assert np.all(np.isfinite(got[b_idx])), "non-finite output"
+    worst = float(diff.max(initial=0.0))
+    assert worst <= TOL[case["dtype"]], "max |diff| %.3g over tolerance" % worst
+    return worst
+
+
+def _case(seed, **kw):
+    return synth.decode_case(seed=seed, **kw)
+
+
+# ------------------------------------------------------------------ tiny ----
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3, 4])
+def test_tiny_workload(seed):
+    case = _case(seed, poison=True, **synth.WORKLOADS["tiny"])
+    check_rows(case, gpu_out(case), list(range(case["B"])))
+
+
+# ---------------------------------------------------- shapes and edge cases ----
+
+SHAPES = []
+for layout in (synth.NHD, synth.VLLM):
+    for dtype in (synth.F16, synth.BF16):
+        for D in (64, 128, 256):
+            for G in (1, 2, 4, 6, 8, 16):
+                if G > 8 and D > 128:
+                    continue
+                SHAPES.append((layout, dtype, D, G))
+
+
+@pytest.mark.parametrize("layout,dtype,D,G", SHAPES)
+def test_shapes_and_edge_lengths(layout, dtype, D, G):
+    Hkv = 2
+    lens = [0, 1, 15, 16, 17, 200, 512, 513, 1000]
+    case = _case(7 * D + G, B=len(lens), Hq=G * Hkv, Hkv=Hkv, D=D, block_size=16, dtype=dtype, layout=layout,
+                 context_lens=lens, slack_pages=5, max_blocks_per_seq=70, poison=True)
+    got = gpu_out(case)
+    check_rows(case, got, list(range(case["B"])))
+    assert np.all(got[0] == 0.0)
+
+
+@pytest.mark.parametrize("opts", [dict(partition_tokens=16), dict(partition_tokens=48), dict(partition_tokens=512),
+                                  dict(num_splits=7), dict(num_splits=1), dict(partition_tokens=4096)])
+@pytest.mark.parametrize("layout", [synth.NHD, synth.VLLM])
+def test_forced_splits(opts, layout):
+    B = _binding()
+    case = _case(11, B=5, Hq=8, Hkv=2, D=128, block_size=16, dtype=synth.BF16, layout=layout,
+                 context_lens=[3, 700, 1, 1024, 333], max_blocks_per_seq=64, slack_pages=2, poison=True)
+    got = gpu_out(case, B.make_opts(**opts))
+    check_rows(case, got, list(range(case["B"])))
+
+
+def test_all_contexts_empty():
+    case = _case(5, B=3, Hq=4, Hkv=1, D=64, block_size=16, dtype=synth.F16, layout=synth.NHD,
+                 context_lens=[0, 0, 0], max_blocks_per_seq=2, slack_pages=2)
+    got = gpu_out(case)
+    assert np.all(got == 0.0)
+
+
+# ---------------------------------------------------------- invariants ----
+
+def test_relabelled_pages_are_bit_identical_on_gpu():
+    case = _case(21, B=6, Hq=16, Hkv=4, D=128, block_size=16, dtype=synth.BF16, layout=synth.NHD,
+                 ctx_range=(1, 900), max_blocks_per_seq=64, slack_pages=9)
+    moved = synth.relabel_pages(case, seed=5)
+    a, b = gpu_out(case), gpu_out(moved)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("layout", [synth.NHD, synth.VLLM])
+def test_poisoned_unread_slots_are_bit_identical_on_gpu(layout):
+    kw = dict(B=6, Hq=12, Hkv=2, D=256 if layout == synth.VLLM else 128, block_size=16, dtype=synth.F16,
+              layout=layout, ctx_range=(1, 700), max_blocks_per_seq=64, slack_pages=4)
+    clean = _case(31, **kw)
+    dirty = _case(31, poison=True, **kw)
+    assert np.array_equal(gpu_out(clean), gpu_out(dirty))
+
+
+def test_constant_v_rows_give_the_constant_on_gpu():
+    case = _case(3, B=4, Hq=8, Hkv=2, D=128, block_size=16, dtype=synth.F16, layout=synth.NHD,
+                 context_lens=[1, 17, 600, 1500], max_blocks_per_seq=100)
+    case["v_cache"] = np.full_like(case["v_cache"], 0x4500)   # 5.0
+    got = gpu_out(case)
+    assert np.max(np.abs(got - 5.0)) <= TOL[synth.F16]
+
+
+# ------------------------------------------------------------- layered ----
+
+@pytest.mark.parametrize("layout,dtype,D,G,P", [(synth.NHD, synth.BF16, 128, 4, 64), (synth.NHD, synth.F16, 64, 2, 48),
+                                               (synth.VLLM, synth.F16, 256, 6, 512), (synth.VLLM, synth.BF16, 128, 16, 32)])
+def test_phase1_partials_match_oracle_split_mode(layout, dtype, D, G, P):
+    T, B = _tensors(), _binding()
+    case = _case(41, B=4, Hq=2 * G, Hkv=2, D=D, block_size=16, dtype=dtype, layout=layout,
+                 context_lens=[0, 5, 130, 1100], max_blocks_per_seq=80, slack_pages=3, poison=True)
+    P2, ns, m, l, acc = T.decode_partials(case, opts=B.make_opts(partition_tokens=P), capacity=None)
+    assert P2 == P and ns == -(-1100 // P)
+    rm, rl, racc = oracle.decode_partials(case, P, ns)
+    sentinel = rm == -np.inf
+    assert np.all(m[sentinel] == -np.inf) and np.all(l[sentinel] == 0) and np.all(acc[sentinel] == 0)
+    live = ~sentinel
+    np.testing.assert_allclose(m[live] + np.log(l[live]), rm[live] + np.log(rl[live]), rtol=0, atol=1e-3)
+    np.testing.assert_allclose((acc / l[..., None])[live], (racc / rl[..., None])[live], rtol=0, atol=TOL[dtype])
+
+
+@pytest.mark.parametrize("dtype,D", [(synth.BF16, 128), (synth.F16, 64), (synth.F16, 256)])
+def test_combine_of_oracle_partials(dtype, D):
+    B = _binding()
+    T = _tensors()
+    case = _case(43, B=5, Hq=4, Hkv=2, D=D, block_size=16, dtype=dtype, layout=synth.NHD,
+                 context_lens=[0, 1, 77, 400, 1024], max_blocks_per_seq=64)
+    P = 64
+    ns = 1024 // P + 2
+    rm, rl, racc = oracle.decode_partials(case, P, ns)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+    out = torch.empty((case["B"], case["Hq"], D), dtype=T.TORCH_DTYPE[dtype], device="cuda")
+    ctx = torch.from_numpy(case["context_lens"]).cuda()
+    B.pkv_combine(T.decode_desc(case), P, ns, ctx, dev(racc), dev(rm), dev(rl), out)
+    torch.cuda.synchronize()
+    check_rows(case, out.double().cpu().numpy(), list(range(case["B"])))
+
+
+# ---------------------------------------------------------- validator ----
+
+def test_validator_flags_bad_tables_without_faulting():
+    B, T = _binding(), _tensors()
+    case = _case(51, B=3, Hq=4, Hkv=2, D=64, block_size=16, dtype=synth.F16, layout=synth.NHD,
+                 context_lens=[40, 16, 0], max_blocks_per_seq=4, slack_pages=1)
+    desc = T.decode_desc(case)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev = T.upload_decode_case(case)
+    B.pkv_validate_block_table(desc, dev["block_table"], dev["context_lens"], err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    bad = case["block_table"].copy()
+    bad[0, 1] = -1                     # live entry of sequence 0
+    bad[1, 3] = 10 ** 6                # past sequence 1's live range: not inspected
+    dev_bad = torch.from_numpy(bad).cuda()
+    B.pkv_validate_block_table(desc, dev_bad, dev["context_lens"], err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 2
+    # the decode itself stays in bounds on the same bad table (result unspecified)
+    case_bad = dict(case, block_table=bad)
+    out = gpu_out(case_bad)
+    assert out.shape == (3, 4, 64)
+    err.zero_()
+    ctx_bad = torch.tensor([40, 65, 0], dtype=torch.int32, device="cuda")   # 65 > 4 pages * 16
+    B.pkv_validate_block_table(desc, dev["block_table"], ctx_bad, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 1
+
+
+# ------------------------------------------------- full-size workloads ----
+
+FULL = ["llama3_8b_decode", "long_context_decode", "gqa6_d256_vllm_decode"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workloads_sampled(name):
+    """The benchmark's workloads at full size, in the launch configuration the
+    benchmark times (default plan); sampled sequences checked against the
+    oracle: the shortest, the longest and two in between."""
+    case = synth.decode_case(seed=0, **synth.WORKLOADS[name])
+    got = gpu_out(case)
+    ctx = case["context_lens"]
+    order = np.argsort(ctx, kind="stable")
+    idx = sorted({int(order[0]), int(order[-1]), int(order[len(order) // 3]), int(order[2 * len(order) // 3])})
+    if name == "long_context_decode":
+        idx = [int(order[0]), int(order[-1])]
+    assert np.all(np.isfinite(got))
+    from concurrent.futures import ThreadPoolExecutor
+    ref = np.full(got.shape, np.nan)
+    with ThreadPoolExecutor(len(idx)) as ex:
+        list(ex.map(lambda b: oracle.decode(case, b, b + 1, out=ref), idx))
+    worst = float(np.max(np.abs(got[idx] - ref[idx])))
+    assert worst <= TOL[case["dtype"]], worst
