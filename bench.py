@@ -1,0 +1,386 @@
+"""Benchmark of the paged decode attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one full decode step of the workload (phase 1 + cross-split
+combine) on synthetic inputs already resident in HBM.  Between timed steps a
+256 MiB buffer is written to flush the 129 MB L2; each step is timed with CUDA
+events on the launching stream, the K step times are summed, and the maximum
+over ranks is taken.  The metric is KV-cache bytes per second: live tokens x
+KV heads x head_dim x (K and V) x 2 bytes per step, divided by the step time.
+
+N > 1 runs independent replicas (one process per GPU, launched by torchrun):
+the decode step has no exchange between GPUs, so there is no collective on the
+data path; the only collectives are the timing barrier and the max-over-ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores (bounded samples
+of the same workload) and prints the same JSON line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV-cache GB/s and % of GB300 HBM peak; µs/step"
+FLUSH_BYTES = 256 << 20
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_phase1_llama3_8b_decode.md")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources; a profile's counters are valid only for the sources they were taken on."""
+    csrc = os.path.join(ROOT, "paged_kv_gqa_table_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of phase 1 from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    text = open(PROFILE_SUMMARY).read()
+    m_hash = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+# ----------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the GPU works."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.proc = None
+        self.lines = []
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "50"]
+        if uuid:
+            cmd[1:1] = ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------- distributed ----
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+def oracle_decode_timed(case, seqs, threads):
+    """Runs the fp64 oracle over the given sequences on `threads` host threads; returns seconds."""
+    import oracle
+    out = np.empty((case["B"], case["Hq"], case["D"]))
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda b: oracle.decode(case, b, b + 1, out=out), seqs))
+    return time.perf_counter() - t0
+
+
+def seq_kv_bytes(case, seqs):
+    return int(np.sum(case["context_lens"][list(seqs)], dtype=np.int64)) * case["Hkv"] * case["D"] * 4
+
+
+def cpu_baseline(case, budget_s: float = 15.0):
+    """The oracle as it stands on all host cores over a bounded sample of the workload."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    order = np.random.default_rng(1).permutation(case["B"])
+    # grow the sample until it takes about a second, then extrapolate within the budget
+    n = min(len(order), threads)
+    while True:
+        secs = oracle_decode_timed(case, order[:n], threads)
+        if n == len(order) or secs > 1.0:
+            break
+        n = min(len(order), n * 2)
+    if secs < budget_s / 4 and n < len(order):
+        m = min(len(order), int(n * budget_s / 4 / max(secs, 1e-3)))
+        secs = oracle_decode_timed(case, order[:m], threads)
+        n = m
+    gbs = seq_kv_bytes(case, order[:n]) / secs / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d sequences (all heads), one pass, %.1f s" % (n, case["B"], secs)}
+
+
+# ----------------------------------------------------------------- arms ----
+
+def run_reference(args):
+    """--impl reference: the CPU oracle timed on bounded samples, same metric and workload."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from paged_kv_gqa_table_gb300 import synth
+    import oracle
+    oracle.build()
+    case = synth.decode_case(seed=0, **synth.WORKLOADS[args.workload])
+    threads = os.cpu_count() or 1
+    order = np.random.default_rng(2).permutation(case["B"])
+    # step size: as many sequences as keep K + W steps within ~120 s
+    probe = order[:min(len(order), threads)]
+    t_probe = oracle_decode_timed(case, probe, threads)
+    per_seq = t_probe / len(probe)
+    per_step = max(1, min(len(order), int(120.0 / (args.steps + args.warmup) / max(per_seq, 1e-6))))
+    cursor = 0
+
+    def step():
+        nonlocal cursor
+        seqs = [order[(cursor + i) % len(order)] for i in range(per_step)]
+        cursor += per_step
+        return oracle_decode_timed(case, seqs, threads), seq_kv_bytes(case, seqs)
+
+    for _ in range(args.warmup):
+        step()
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        t, b = step()
+        tot_t += t
+        tot_b += b
+    value = tot_b / tot_t / 1e9
+    sample = "%d of %d sequences (all heads) per step" % (per_step, case["B"])
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(case, args.workload, flushed=False),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(case, name, flushed=True):
+    ctx = case["context_lens"]
+    return {"workload": "%s: B=%d Hq=%d Hkv=%d D=%d block_size=%d %s %s layout, context_lens %d..%d (sum %d)" % (
+        name, case["B"], case["Hq"], case["Hkv"], case["D"], case["block_size"],
+        {0: "fp16", 1: "bf16"}[case["dtype"]], {0: "NHD", 1: "vLLM x-packed"}[case["layout"]],
+        int(ctx.min()), int(ctx.max()), int(ctx.sum())),
+        "seed": 0, "kv_bytes_per_step": int(np.sum(ctx, dtype=np.int64)) * case["Hkv"] * case["D"] * 4,
+        "l2": "flushed between steps (256 MiB write)" if flushed else "n/a (CPU)",
+        "accumulate": "fp32"}
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from paged_kv_gqa_table_gb300 import binding as B
+    from paged_kv_gqa_table_gb300 import synth, tensors
+
+    B.load()
+    case = synth.decode_case(seed=0, **synth.WORKLOADS[args.workload])
+    kvb = synth.kv_bytes(case)
+    dev = tensors.upload_decode_case(case, device)
+    desc = tensors.decode_desc(case)
+    ns, P = B.pkv_plan_splits(desc)
+    out = torch.empty((case["B"], case["Hq"], case["D"]), dtype=tensors.TORCH_DTYPE[case["dtype"]], device=device)
+    ws = tensors.workspace_for(desc, device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    p_start, p_stop = [ev() for _ in range(args.steps)], [ev() for _ in range(args.steps)]
+    s_start, s_stop = [ev() for _ in range(args.steps)], [ev() for _ in range(args.steps)]
+    for e in p_start + p_stop:
+        e.record(stream)       # materialise the CUDA events before the library records them
+    torch.cuda.synchronize(device)
+
+    def step(opts=None):
+        B.pkv_paged_decode_attention(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
+                                     dev["context_lens"], case["scale"], out, ws, opts=opts, stream=stream)
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        s_start[i].record(stream)
+        step(B.make_opts(event_start=p_start[i], event_stop=p_stop[i]))
+        s_stop[i].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+    step_ms = [a.elapsed_time(b) for a, b in zip(s_start, s_stop)]
+    p1_ms = [a.elapsed_time(b) for a, b in zip(p_start, p_stop)]
+    t_total = sum(step_ms) * 1e-3
+    t_max = max_over_ranks(t_total, world, device)
+    value = world * kvb * args.steps / t_max / 1e9
+    launches = args.steps * (1 + (1 if ns > 1 else 0))
+
+    # end to end: pinned host inputs -> device, the C-ABI call, result -> pinned host
+    e2e = None
+    if not args.skip_e2e:
+        host = {k: v.cpu().pin_memory() for k, v in dev.items()}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out.numel() * out.element_size()
+        n_e2e = max(3, min(args.steps, 30))
+        for i in range(n_e2e + 2):
+            if i == 2:
+                torch.cuda.synchronize(device)
+                barrier(world, device)
+                e0 = ev()
+                e0.record(stream)
+            for k in dev:
+                dev[k].copy_(host[k], non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+        e1 = ev()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        t_e2e = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world, device)
+        e2e = {"value": world * kvb * n_e2e / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": n_e2e}
+
+    if rank == 0:
+        peak, peak_kind = measured_peaks()
+        p1_avg = float(np.mean(p1_ms)) * 1e-3
+        achieved = kvb / p1_avg / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": {0: "fp16", 1: "bf16"}[case["dtype"]],
+            "data": "synthetic (seeded N(0,1) K/V/q, uniform context lengths, random page permutation)",
+            "config": dict(workload_config(case, args.workload), parallelism="replicas" if world > 1 else "1 GPU",
+                           partition_tokens=P, num_splits=ns),
+            "us_per_step": t_max / args.steps * 1e6, "hbm_frac_of_measured_peak": value / peak,
+            "clocks": clocks, "e2e": e2e, "gpu_launches": launches,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": profiled_traffic(),
+                         "kernel": "decode_phase1_kernel", "peak_source": peak_kind,
+                         "algorithmic_bytes_per_launch": kvb, "avg_launch_us": p1_avg * 1e6},
+            "wall_s_timed_region": wall,
+        }
+        if world == 1 and not args.skip_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(case)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b_decode",
+                    choices=["llama3_8b_decode", "long_context_decode", "gqa6_d256_vllm_decode", "tiny"])
+    ap.add_argument("--skip-e2e", action="store_true", help="omit the end-to-end leg (profiling runs)")
+    ap.add_argument("--skip-cpu-baseline", action="store_true", help="omit the CPU oracle leg (profiling runs)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
