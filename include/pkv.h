@@ -180,6 +180,39 @@ int pkv_combine(const pkv_decode_desc* desc, int partition_tokens, int num_split
 int pkv_validate_block_table(const pkv_decode_desc* desc, const int32_t* block_table,
                              const int32_t* context_lens, uint32_t* err_word, pkv_stream_t stream);
 
+/*
+ * pkv_paged_decode_attention_static -- the same decode step as
+ * pkv_paged_decode_attention, for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point.
+ *
+ * Who needs it: code that runs where allocating is not allowed or not safe --
+ * a plugin whose enqueue hook is handed a stream but no allocator, an engine
+ * that carves all device memory out of a fixed pool at start-up, or a
+ * latency-critical loop where cudaMalloc could synchronise the device.
+ *
+ * The split partials live in one file-scope device array of
+ * PKV_STATIC_SCRATCH_BYTES (32 MiB), which every GPU that loads libpkv
+ * reserves until the process exits.  This call allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine; it clears the array's
+ * 256-byte error header with cudaMemsetAsync on `stream` and then runs the
+ * regular entry point on the array.
+ *  - A problem whose workspace (pkv_decode_workspace_size) exceeds the array
+ *    is refused with PKV_WORKSPACE_TOO_SMALL before anything is launched.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and it keeps the last call's
+ *    contents: calls whose work overlaps on the GPU (different streams, no
+ *    ordering between them) race on it and produce garbage.  Order them on
+ *    one stream, or use the workspace entry point.
+ * Arguments, layouts and errors are otherwise those of
+ * pkv_paged_decode_attention.
+ */
+#define PKV_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+int pkv_paged_decode_attention_static(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
+                                      const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_table, const int32_t* context_lens,
+                                      float scale, void* out, pkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,7 +20,9 @@ PKV_LAYOUT_NHD, PKV_LAYOUT_VLLM = 0, 1
 FUNCTIONS = [
     "pkv_status_string", "pkv_version", "pkv_plan_splits", "pkv_decode_workspace_size",
     "pkv_paged_decode_attention", "pkv_decode_partials", "pkv_combine", "pkv_validate_block_table",
+    "pkv_paged_decode_attention_static",
 ]
+PKV_STATIC_SCRATCH_BYTES = 32 << 20
 
 
 class pkv_decode_desc(ctypes.Structure):
@@ -62,6 +64,7 @@ def load():
                                         ctypes.POINTER(I), ctypes.POINTER(I), P]
     lib.pkv_combine.argtypes = [D, I, I, P, P, P, P, P, P]
     lib.pkv_validate_block_table.argtypes = [D, P, P, P, P]
+    lib.pkv_paged_decode_attention_static.argtypes = [D, O, P, P, P, P, P, ctypes.c_float, P, P]
     for f in FUNCTIONS[2:]:
         getattr(lib, f).restype = I
     _lib = lib
@@ -154,6 +157,14 @@ def pkv_combine(desc, partition_tokens, num_splits, context_lens, part_acc, part
     _check("pkv_combine", load().pkv_combine(ctypes.byref(desc), int(partition_tokens), int(num_splits),
                                              _ptr(context_lens), _ptr(part_acc), _ptr(part_m), _ptr(part_l),
                                              _ptr(out), _stream(stream)))
+
+
+def pkv_paged_decode_attention_static(desc, q, k_cache, v_cache, block_table, context_lens, scale, out,
+                                      opts=None, stream=None) -> None:
+    """Decode step with the library's static device scratch (allocates nothing)."""
+    _check("pkv_paged_decode_attention_static", load().pkv_paged_decode_attention_static(
+        ctypes.byref(desc), _opt_ref(opts), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        _ptr(context_lens), float(scale), _ptr(out), _stream(stream)))
 
 
 def pkv_validate_block_table(desc, block_table, context_lens, err_word, stream=None) -> None:
