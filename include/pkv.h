@@ -180,6 +180,41 @@ int pkv_combine(const pkv_decode_desc* desc, int partition_tokens, int num_split
 int pkv_validate_block_table(const pkv_decode_desc* desc, const int32_t* block_table,
                              const int32_t* context_lens, uint32_t* err_word, pkv_stream_t stream);
 
+/* Problem description of one MLA paged prefill call (page size 1, bf16). */
+typedef struct {
+    int total_q;    /* query tokens over the batch: rows of q_nope, q_pe, out, lse */
+    int num_heads;  /* query heads: 16 */
+    int d_ckv;      /* latent (ckv) width, also the output width: 512 */
+    int d_kpe;      /* rope (kpe) width: 64 */
+    int batch;      /* sequences; qo_indptr and kv_indptr hold batch + 1 entries */
+    int num_pages;  /* rows of ckv_cache and kpe_cache */
+} pkv_mla_desc;
+
+/*
+ * MLA paged causal prefill ([MLA] run / _forward and the kernel's sections
+ * 2-4).  For sequence b (query tokens qo_indptr[b] .. qo_indptr[b+1]-1, cached
+ * rows kv_indices[kv_indptr[b] .. kv_indptr[b+1]-1], prefix = kv_len - q_len)
+ * and query token i of it, head h:
+ *   logit_j = sm_scale * (q_nope[t][h] . ckv[page_j] + q_pe[t][h] . kpe[page_j])
+ *   for the visible keys j <= prefix + i (bottom-right causal),
+ *   out[t][h][:] = sum_j softmax(logit)_j ckv[page_j][:],
+ *   lse[t][h]    = log2 sum_j exp(logit_j)            (base 2).
+ * A sequence with kv_len == 0 gives out = 0 and lse = -inf.
+ *   q_nope   bf16 [total_q][16][512]     q_pe       bf16 [total_q][16][64]
+ *   ckv_cache bf16 [num_pages][1][512]   kpe_cache  bf16 [num_pages][1][64]
+ *   qo_indptr, kv_indptr int32 [batch+1] (starting at 0), kv_indices int32 [nnz]
+ *   out      bf16 [total_q][16][512]     lse        fp32 [total_q][16]
+ * Tensors 16-byte aligned (lse 4-byte).  kv_len < q_len is a caller error
+ * (rows with no visible key get out = 0, lse = -inf); page ids outside
+ * [0, num_pages) are clamped to page 0 (no out-of-bounds access, result
+ * unspecified).  No workspace: the q -> sequence map of [MLA]'s host loop is
+ * computed on the device from qo_indptr.
+ */
+int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const void* q_pe,
+                          const void* ckv_cache, const void* kpe_cache, const int32_t* qo_indptr,
+                          const int32_t* kv_indptr, const int32_t* kv_indices, float sm_scale,
+                          void* out, float* lse, pkv_stream_t stream);
+
 /*
  * pkv_paged_decode_attention_static -- the same decode step as
  * pkv_paged_decode_attention, for callers that cannot allocate device memory.

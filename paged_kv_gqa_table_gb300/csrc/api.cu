@@ -357,4 +357,39 @@ int pkv_validate_block_table(const pkv_decode_desc* desc, const int32_t* block_t
                : PKV_CUDA_ERROR;
 }
 
+int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                          const void* kpe_cache, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                          const int32_t* kv_indices, float sm_scale, void* out, float* lse, pkv_stream_t stream) {
+    if (!desc) return PKV_INVALID_ARG;
+    const pkv_mla_desc& d = *desc;
+    if (d.total_q < 0 || d.batch < 0 || d.num_pages < 0 || d.num_heads <= 0 || d.d_ckv <= 0 || d.d_kpe <= 0)
+        return PKV_INVALID_ARG;
+    if (d.total_q > 0 && d.batch == 0) return PKV_INVALID_ARG;
+    if (d.num_heads != 16 || d.d_ckv != 512 || d.d_kpe != 64) return PKV_UNSUPPORTED;
+    if ((long long)d.total_q * d.num_heads * d.d_ckv > (long long)1 << 40) return PKV_UNSUPPORTED;
+    if (!std::isfinite(sm_scale)) return PKV_INVALID_ARG;
+    if (d.total_q == 0) return PKV_OK;
+    if (!q_nope || !q_pe || !qo_indptr || !kv_indptr || !out || !lse) return PKV_INVALID_ARG;
+    if (d.num_pages > 0 && (!ckv_cache || !kpe_cache || !kv_indices)) return PKV_INVALID_ARG;
+    if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+        !aligned(qo_indptr, 4) || !aligned(kv_indptr, 4) || (ckv_cache && !aligned(ckv_cache, 16)) ||
+        (kpe_cache && !aligned(kpe_cache, 16)) || (kv_indices && !aligned(kv_indices, 4)))
+        return PKV_INVALID_ARG;
+    MlaParams p{};
+    p.q_nope = static_cast<const __nv_bfloat16*>(q_nope);
+    p.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+    p.ckv = static_cast<const __nv_bfloat16*>(ckv_cache);
+    p.kpe = static_cast<const __nv_bfloat16*>(kpe_cache);
+    p.qo_indptr = qo_indptr;
+    p.kv_indptr = kv_indptr;
+    p.kv_indices = kv_indices;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.lse = lse;
+    p.total_q = d.total_q;
+    p.batch = d.batch;
+    p.num_pages = d.num_pages;
+    p.scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
+    return launch_mla_prefill(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_CUDA_ERROR;
+}
+
 }  // extern "C"

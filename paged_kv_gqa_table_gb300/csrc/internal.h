@@ -26,6 +26,23 @@ cudaError_t launch_decode_vllm_f16(int D, int nt, const DecodeParams& p, const C
 cudaError_t launch_decode_vllm_bf16(int D, int nt, const DecodeParams& p, const CUtensorMap& k,
                                     const CUtensorMap& v, cudaStream_t s);
 
+// MLA paged causal prefill (mla.cu); bf16 tensors, page size 1.
+struct MlaParams {
+    const __nv_bfloat16* q_nope;   // [total_q][16][512]
+    const __nv_bfloat16* q_pe;     // [total_q][16][64]
+    const __nv_bfloat16* ckv;      // [num_pages][512]
+    const __nv_bfloat16* kpe;      // [num_pages][64]
+    const int32_t* qo_indptr;      // [batch + 1]
+    const int32_t* kv_indptr;      // [batch + 1]
+    const int32_t* kv_indices;     // [nnz]
+    __nv_bfloat16* out;            // [total_q][16][512]
+    float* lse;                    // [total_q][16]
+    int total_q, batch, num_pages;
+    float scale_log2;              // sm_scale * log2(e)
+};
+
+cudaError_t launch_mla_prefill(const MlaParams& p, cudaStream_t stream);
+
 cudaError_t launch_combine(int dtype, int D, const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_validate(const int32_t* table, const int32_t* ctx, int B, int MBPS, int BS, int NB, int max_ctx,
                             uint32_t* err, cudaStream_t stream);

@@ -79,3 +79,31 @@ def decode_partials(case: dict, dev: dict | None = None, opts=None, capacity: in
                                     dev["context_lens"], case["scale"], acc, m, l, cap, opts=opts)
     torch.cuda.synchronize()
     return P2, ns2, m.double().cpu().numpy(), l.double().cpu().numpy(), acc.double().cpu().numpy()
+
+
+def mla_desc(case: dict) -> B.pkv_mla_desc:
+    return B.make_mla_desc(case["total_q"], case["batch"], case["num_pages"], case["H"], case["Dc"], case["Dr"])
+
+
+def upload_mla_case(case: dict, device="cuda") -> dict:
+    bf = synth.BF16
+    return dict(q_nope=bits_to_torch(case["q_nope"], bf, device), q_pe=bits_to_torch(case["q_pe"], bf, device),
+                ckv_cache=bits_to_torch(case["ckv_cache"], bf, device),
+                kpe_cache=bits_to_torch(case["kpe_cache"], bf, device),
+                qo_indptr=int_to_torch(case["qo_indptr"], device), kv_indptr=int_to_torch(case["kv_indptr"], device),
+                kv_indices=int_to_torch(case["kv_indices"], device))
+
+
+def mla_paged_prefill(case: dict, dev: dict | None = None, out=None, lse=None, stream=None):
+    """Runs the MLA prefill on a synthetic case; returns (out [T][H][Dc] bf16, lse [T][H] fp32) on the device."""
+    dev = dev if dev is not None else upload_mla_case(case)
+    d = dev["q_nope"].device
+    T, H, Dc = case["total_q"], case["H"], case["Dc"]
+    if out is None:
+        out = torch.empty((T, H, Dc), dtype=torch.bfloat16, device=d)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=d)
+    B.pkv_mla_paged_prefill(mla_desc(case), dev["q_nope"], dev["q_pe"], dev["ckv_cache"], dev["kpe_cache"],
+                            dev["qo_indptr"], dev["kv_indptr"], dev["kv_indices"], case["sm_scale"], out, lse,
+                            stream=stream)
+    return out, lse

@@ -1,0 +1,112 @@
+"""GPU parity of the MLA paged causal prefill (tcgen05 path) against the fp64 oracle.
+
+Calls go through the C ABI.  Bars: bf16 output max |diff| <= 1.6e-2, base-2
+LSE max |diff| <= 1e-3 (absolute), both against the unrounded fp64 oracle.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_gqa_table_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+TOL_OUT, TOL_LSE = 1.6e-2, 1e-3
+
+
+def gpu_mla(case):
+    from paged_kv_gqa_table_gb300 import tensors
+    out, lse = tensors.mla_paged_prefill(case)
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+def check(case, got_out, got_lse, tokens=None):
+    T = case["total_q"]
+    tokens = list(range(T)) if tokens is None else tokens
+    ref_out = np.full(got_out.shape, np.nan)
+    ref_lse = np.full(got_lse.shape, np.nan)
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(8) as ex:
+        list(ex.map(lambda t: oracle.mla(case, t, t + 1, out=ref_out, lse=ref_lse), tokens))
+    o, l = got_out[tokens], got_lse[tokens]
+    ro, rl = ref_out[tokens], ref_lse[tokens]
+    assert np.all(np.isfinite(o)), "non-finite output"
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isfinite(l), fin)
+    assert np.all(l[~fin] == rl[~fin])
+    err_o = float(np.max(np.abs(o - ro), initial=0.0))
+    err_l = float(np.max(np.abs(l[fin] - rl[fin]), initial=0.0))
+    assert err_o <= TOL_OUT, "out max |diff| %.3g" % err_o
+    assert err_l <= TOL_LSE, "lse max |diff| %.3g" % err_l
+    return err_o, err_l
+
+
+SMALL = [
+    dict(batch=3, q_len_range=(1, 20), prefix_range=(0, 300), slack_pages=7),
+    dict(batch=2, q_len_range=(8, 8), prefix_range=(120, 136), slack_pages=3),
+    dict(batch=4, q_len_range=(1, 1), prefix_range=(0, 700)),
+    dict(batch=2, q_len_range=(33, 70), prefix_range=(0, 0), sm_scale=1.0),
+    dict(batch=2, q_len_range=(100, 140), prefix_range=(250, 270), sm_scale=1.0 / 24.0),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL)))
+def test_mla_small_cases(idx):
+    case = synth.mla_case(seed=idx, poison=True, **SMALL[idx])
+    check(case, *gpu_mla(case))
+
+
+def test_mla_empty_sequences():
+    # q_len = 0 in the middle, and a sequence whose KV is empty (out 0, lse -inf)
+    case = synth.mla_case(seed=3, batch=3, q_len_range=(1, 1), prefix_range=(0, 0), q_lens=[5, 0, 9],
+                          prefixes=[30, 0, 200])
+    check(case, *gpu_mla(case))
+    empty = synth.mla_case(seed=4, batch=2, q_len_range=(1, 1), prefix_range=(0, 0), q_lens=[3, 4],
+                           prefixes=[10, 0])
+    empty["kv_indptr"] = np.array([0, 13, 13], np.int32)          # second sequence: 4 queries, no KV
+    empty["kv_indices"] = empty["kv_indices"][:13].copy()
+    out, lse = gpu_mla(empty)
+    assert np.all(out[3:] == 0) and np.all(lse[3:] == -np.inf)
+    check(empty, out, lse)
+
+
+def test_mla_zero_query_closed_form():
+    case = synth.mla_case(seed=9, batch=2, q_len_range=(20, 40), prefix_range=(100, 300))
+    case["q_nope"] = np.zeros_like(case["q_nope"])
+    case["q_pe"] = np.zeros_like(case["q_pe"])
+    out, lse = gpu_mla(case)
+    qo, kvp = case["qo_indptr"], case["kv_indptr"]
+    for b in range(2):
+        q_len, kv_len = qo[b + 1] - qo[b], kvp[b + 1] - kvp[b]
+        for i in range(q_len):
+            assert np.max(np.abs(lse[qo[b] + i] - np.log2(kv_len - q_len + i + 1))) <= TOL_LSE
+    check(case, out, lse)
+
+
+def test_mla_relabelled_pages_are_bit_identical():
+    case = synth.mla_case(seed=12, batch=3, q_len_range=(10, 30), prefix_range=(50, 400), slack_pages=11)
+    a = gpu_mla(case)
+    perm = np.random.default_rng(5).permutation(case["num_pages"])   # page p moves to perm[p]
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(len(perm))
+    moved = dict(case, ckv_cache=case["ckv_cache"][inv].copy(), kpe_cache=case["kpe_cache"][inv].copy(),
+                 kv_indices=perm[case["kv_indices"]].astype(np.int32))
+    b = gpu_mla(moved)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_mla_full_size_workload_sampled():
+    """The benchmark's MLA workload at full size, sampled tokens checked against the oracle:
+    the first and last token of every sequence and 4 more per sequence."""
+    case = synth.mla_case(seed=0, **synth.MLA_WORKLOADS["mla_prefill_h16"])
+    out, lse = gpu_mla(case)
+    qo = case["qo_indptr"]
+    rng = np.random.default_rng(0)
+    tokens = set()
+    for b in range(case["batch"]):
+        tokens |= {int(qo[b]), int(qo[b + 1] - 1)} | set(rng.integers(qo[b], qo[b + 1], size=4).tolist())
+    check(case, out, lse, sorted(tokens))
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
