@@ -68,7 +68,7 @@ typedef struct {
     int max_blocks_per_seq;  /* columns of block_table */
     int num_blocks;          /* pages in the pool */
     int max_context_len;     /* host-known upper bound on context_lens[] (plans the grid) */
-    long long sum_context_len; /* host-known sum of context_lens[] (plans the split); may be an estimate */
+    long long sum_context_len; /* host-known sum of context_lens[], or an upper bound on it (sizes the grid) */
     int dtype;               /* pkv_dtype of q, caches and out */
     int layout;              /* pkv_layout */
     int x_pack;              /* VLLM layout only: must be 8 */
@@ -108,10 +108,13 @@ int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, in
 
 /*
  * Bytes of scratch memory pkv_paged_decode_attention needs for this problem
- * (256-byte header + fp32 split partials when the plan has more than one
- * split).  num_sms as for pkv_plan_splits.  The workspace must be 256-byte
- * aligned.  Word 0 of the header collects device-side error bits (bit 0: a
- * pipeline wait timed out); zero it once after allocating.
+ * and these options (256-byte header, one int32 arrival counter per
+ * (sequence, KV head), and fp32 split partials m, l [B][Hq][NS] and
+ * acc [B][Hq][NS][D] when the plan has more than one split).  num_sms as for
+ * pkv_plan_splits.  The workspace must be 256-byte aligned and ZEROED ONCE
+ * after allocation: word 0 of the header collects device-side error bits
+ * (bit 0: a pipeline wait timed out) and the counters must start at zero;
+ * every call leaves them at zero again.
  */
 int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms,
                               size_t* bytes);
@@ -131,9 +134,12 @@ int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts
  *                 pkv_validate_block_table reports it.
  *   context_lens  int32 [B]; values are clamped to
  *                 [0, min(max_context_len, max_blocks_per_seq * block_size)].
- * Phase 1 runs one CTA per (sequence, KV head, split), loading each page once
- * for the whole group; sequences with more than one split are merged by a
- * second, log-sum-exp combine kernel.
+ * Phase 1 runs one CTA per non-empty (sequence, KV head, split) of the
+ * pkv_plan_splits plan, loading each page once for the whole group.  A
+ * sequence with several splits is merged by log-sum-exp by the last of its
+ * splits to finish (plans of at most 32 splits) or by a second combine kernel
+ * (longer plans).  Calls sharing one workspace must be ordered on the GPU
+ * (one stream).
  */
 int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
                                const void* q, const void* k_cache, const void* v_cache,
@@ -225,12 +231,12 @@ int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const vo
  * that carves all device memory out of a fixed pool at start-up, or a
  * latency-critical loop where cudaMalloc could synchronise the device.
  *
- * The split partials live in one file-scope device array of
- * PKV_STATIC_SCRATCH_BYTES (32 MiB), which every GPU that loads libpkv
- * reserves until the process exits.  This call allocates nothing: no
- * cudaMalloc, cudaFree or allocating library routine; it clears the array's
- * 256-byte error header with cudaMemsetAsync on `stream` and then runs the
- * regular entry point on the array.
+ * The step's scratch (error word, merge counters, partial results) lives in
+ * one file-scope device array of PKV_STATIC_SCRATCH_BYTES (32 MiB), which
+ * every GPU that loads libpkv reserves until the process exits.  This call
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library routine;
+ * it clears the array's header and merge counters with cudaMemsetAsync on
+ * `stream` and then runs the regular entry point on the array.
  *  - A problem whose workspace (pkv_decode_workspace_size) exceeds the array
  *    is refused with PKV_WORKSPACE_TOO_SMALL before anything is launched.
  *  - The first call on a device looks up the array's device address (with

@@ -109,6 +109,26 @@ size_t partial_bytes(const pkv_decode_desc* d, int ns) {
     return 2 * align256(rows * 4) + align256(rows * d->D * 4);
 }
 
+// Workspace: 256-byte header | arrival counters [B * Hkv] | m, l [B][Hq][NS],
+// acc [B][Hq][NS][D] (the partials only when some sequence has two splits).
+size_t counter_bytes(const pkv_decode_desc* d) { return align256((size_t)d->B * d->Hkv * 4); }
+size_t workspace_bytes_for(const pkv_decode_desc* d, int ns) {
+    return kHeaderBytes + counter_bytes(d) + (ns > 1 ? partial_bytes(d, ns) : 0);
+}
+
+// Sequences with at most this many splits are merged inside phase 1 by the
+// last split to finish; longer plans keep the separate combine kernel, whose
+// merge work is spread over many CTAs.
+constexpr int kFuseMaxSplits = 32;
+
+// Compact grid: Hkv x (an upper bound on the number of non-empty (sequence,
+// split) pairs, from the host-known maximum and sum of the context lengths).
+long long compact_grid(const pkv_decode_desc* d, int P, int ns) {
+    const long long by_max = (long long)d->B * ns;
+    const long long by_sum = ceil_div(d->sum_context_len, P) + d->B;
+    return (long long)d->Hkv * (by_max < by_sum ? by_max : by_sum);
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -163,13 +183,15 @@ int encode_cache_map(CUtensorMap* map, const void* base, const pkv_decode_desc* 
     return r == CUDA_SUCCESS ? PKV_OK : PKV_INVALID_ARG;
 }
 
-cudaError_t dispatch_phase1(const pkv_decode_desc* d, const DecodeParams& p, const CUtensorMap& k,
+cudaError_t dispatch_phase1(const pkv_decode_desc* d, const DecodeParams& p, long long grid, const CUtensorMap& k,
                             const CUtensorMap& v, cudaStream_t s) {
     const int nt = (d->Hq / d->Hkv) > 8 ? 2 : 1;
     const bool bf = d->dtype == PKV_BF16;
     if (d->layout == PKV_LAYOUT_NHD)
-        return bf ? launch_decode_nhd_bf16(d->D, nt, p, k, v, s) : launch_decode_nhd_f16(d->D, nt, p, k, v, s);
-    return bf ? launch_decode_vllm_bf16(d->D, nt, p, k, v, s) : launch_decode_vllm_f16(d->D, nt, p, k, v, s);
+        return bf ? launch_decode_nhd_bf16(d->D, nt, p, grid, k, v, s)
+                  : launch_decode_nhd_f16(d->D, nt, p, grid, k, v, s);
+    return bf ? launch_decode_vllm_bf16(d->D, nt, p, grid, k, v, s)
+              : launch_decode_vllm_f16(d->D, nt, p, grid, k, v, s);
 }
 
 int check_tensors(const pkv_decode_desc* d, const void* q, const void* k, const void* v, const int32_t* table,
@@ -239,7 +261,7 @@ int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts
     int ns = 0, P = 0;
     int st = plan(desc, opts, num_sms, &ns, &P);
     if (st) return st;
-    *bytes = kHeaderBytes + (ns > 1 ? partial_bytes(desc, ns) : 0);
+    *bytes = workspace_bytes_for(desc, ns);
     return PKV_OK;
 }
 
@@ -257,21 +279,24 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
     int ns = 0, P = 0;
     st = plan(desc, opts, 0, &ns, &P);
     if (st) return st;
-    const size_t need = kHeaderBytes + (ns > 1 ? partial_bytes(desc, ns) : 0);
-    if (workspace_bytes < need) return PKV_WORKSPACE_TOO_SMALL;
+    if (workspace_bytes < workspace_bytes_for(desc, ns)) return PKV_WORKSPACE_TOO_SMALL;
 
     DecodeParams p;
-    CUtensorMap mk, mv;
+    CUtensorMap mk{}, mv{};
     st = prepare_phase1(desc, P, ns, q, k_cache, v_cache, block_table, context_lens, scale, &p, &mk, &mv);
     if (st) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.out = out;
     p.err = reinterpret_cast<uint32_t*>(ws);
+    p.seg_count = reinterpret_cast<int*>(ws + kHeaderBytes);
+    uint8_t* parts = ws + kHeaderBytes + counter_bytes(desc);
     const size_t rows = (size_t)desc->B * desc->Hq * ns;
-    p.part_m = reinterpret_cast<float*>(ws + kHeaderBytes);
-    p.part_l = reinterpret_cast<float*>(ws + kHeaderBytes + align256(rows * 4));
-    p.part_acc = reinterpret_cast<float*>(ws + kHeaderBytes + 2 * align256(rows * 4));
+    p.part_m = reinterpret_cast<float*>(parts);
+    p.part_l = reinterpret_cast<float*>(parts + align256(rows * 4));
+    p.part_acc = reinterpret_cast<float*>(parts + 2 * align256(rows * 4));
+    p.compact = 1;
+    p.fuse = ns <= kFuseMaxSplits ? 1 : 0;
 
     if (desc->max_context_len == 0) {
         // Every context is empty: the combine kernel writes the zero rows.
@@ -279,9 +304,9 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
         return launch_combine(desc->dtype, desc->D, c, s) == cudaSuccess ? PKV_OK : PKV_CUDA_ERROR;
     }
     record(opts ? opts->phase1_event_start : nullptr, s);
-    if (dispatch_phase1(desc, p, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
+    if (dispatch_phase1(desc, p, compact_grid(desc, P, ns), mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
     record(opts ? opts->phase1_event_stop : nullptr, s);
-    if (ns > 1) {
+    if (ns > 1 && !p.fuse) {
         CombineParams c{context_lens, p.part_acc, p.part_m, p.part_l, out, desc->B, desc->Hq, P, ns, p.n_cap, 1};
         if (launch_combine(desc->dtype, desc->D, c, s) != cudaSuccess) return PKV_CUDA_ERROR;
     }
@@ -324,7 +349,7 @@ int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts
         mv = CUtensorMap{};
     }
     record(opts ? opts->phase1_event_start : nullptr, s);
-    if (dispatch_phase1(desc, p, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
+    if (dispatch_phase1(desc, p, (long long)desc->B * desc->Hkv * ns, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
     record(opts ? opts->phase1_event_stop : nullptr, s);
     return PKV_OK;
 }

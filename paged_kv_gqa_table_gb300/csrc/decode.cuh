@@ -4,6 +4,9 @@
 // [s*P, min((s+1)*P, n)) of the sequence (fixed partitions as in
 // "paged_attention_v2_triton.py", _partition_attn_kernel; page-granular
 // splits as in the flash-decode post's _flash_decode_partial_kernel).
+// In the compact grid only the non-empty splits are launched: CTA i handles
+// KV head i % Hkv of the (i / Hkv)-th non-empty (sequence, split) pair,
+// found by a warp scan over the per-sequence split counts.
 //
 // Roles: warp NWC is the producer: it reads the split's block-table entries
 // (32 per coalesced load, one chunk ahead) and, per page, issues TMA tensor
@@ -21,7 +24,11 @@
 // warps' states are merged through shared memory at the end; the CTA writes
 // either the final normalised row (the sequence has a single split) or the
 // unnormalised fp32 partial (acc, m, l) of its split, m in natural-log units
-// (the partial-buffer convention of the flash-decode post).
+// (the partial-buffer convention of the flash-decode post).  With `fuse`, the
+// last split of a (sequence, KV head) to finish -- an arrival counter per
+// pair, reset by that CTA -- merges all the pair's partials by log-sum-exp
+// (the flash-decode post's _flash_decode_combine_kernel) and writes the
+// output, so no second kernel runs.
 //
 // Shared-memory layouts of one page slice (BS = 16 tokens):
 //   NHD : TMA boxes of 64 elements x BS rows, 128-byte swizzle, so that the
@@ -30,11 +37,9 @@
 //         for ldmatrix), V [D][BS] (two-way conflicts at most).
 #pragma once
 
-#include "ptx.cuh"
+#include "decode_common.cuh"
 
 namespace pkv {
-
-enum { kLayoutNHD = 0, kLayoutVLLM = 1 };
 
 struct DecodeParams {
     const void* q;           // [B][Hq][D]
@@ -52,28 +57,22 @@ struct DecodeParams {
     int n_cap;               // context lengths are clamped to [0, n_cap]
     float scale_log2;        // scale * log2(e)
     int partials_only;       // 1: always write partials (+ sentinels), never out
+    int compact;             // 1: grid over non-empty (sequence, split) pairs x Hkv; 0: dense B x Hkv x NS
+    int fuse;                // 1: the last split of a (sequence, KV head) merges the partials
+    int* seg_count;          // [B * Hkv] arrival counters (fuse), zero between calls
 };
 
 template <int D>
 struct DecodeTile {
-    static constexpr int BS = 16;
+    static constexpr int BS = kPageTokens;
     static constexpr int NWC = 4;                                   // consumer warps
     static constexpr int SLICE = BS * D * 2;                        // bytes of one page slice
     static constexpr int STAGES = D == 64 ? 12 : (D == 128 ? 8 : 4);
     static constexpr int RED_STRIDE = D + 4;                        // floats per reduction row
     static constexpr int smem_bytes(int nt) {
-        return 1024 + STAGES * 2 * SLICE + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 16;
+        return 1024 + STAGES * 2 * SLICE + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 32;
     }
 };
-
-__device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
-
-// Byte offset of 16-byte chunk c (c < D/8) of token row t in an NHD slice
-// written by 64-element TMA boxes with 128-byte swizzle.
-template <int BS>
-__device__ __forceinline__ uint32_t nhd_off(int t, int c) {
-    return (uint32_t)((c >> 3) * (BS * 128) + t * 128 + (((c & 7) ^ (t & 7)) << 4));
-}
 
 template <typename T, int LAYOUT, int D, int NT>
 __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
@@ -85,6 +84,10 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
     constexpr int HP = NT * 8;   // padded heads
     constexpr int RS = Tile::RED_STRIDE;
     static_assert(NWC * HP * RS * 4 <= STAGES * 2 * SLICE, "reduction buffer must fit in the ring");
+    // Pages go to consumer warps round-robin: with STAGES a multiple of NWC a
+    // warp only re-waits on stages it consumed itself, so a parity wait can
+    // never be satisfied by the previous lap's phase.
+    static_assert(STAGES % NWC == 0, "ring depth must be a multiple of the consumer warps");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -94,13 +97,62 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
     float* st_m = reinterpret_cast<float*>(empty + STAGES);
     float* st_l = st_m + NWC * HP;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(st_l + NWC * HP);   // set on a wait timeout
+    volatile int* bcast = abort_flag + 1;                                           // [3]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int item = blockIdx.x;
-    const int s = item % p.NS;
-    item /= p.NS;
-    const int kvh = item % p.Hkv;
-    const int b = item / p.Hkv;
+    int b, s, kvh;
+    if (p.compact) {
+        kvh = blockIdx.x % p.Hkv;
+        const int t = blockIdx.x / p.Hkv;
+        if (warp == 0) {
+            // Zero rows of empty contexts: CTA i looks after sequences [32 i, 32 i + 32).
+            if ((int)blockIdx.x * 32 < p.B) {
+                const int bz = blockIdx.x * 32 + lane;
+                const bool empty_ctx = bz < p.B && clampi(p.ctx[bz], 0, p.n_cap) == 0;
+                unsigned m = __ballot_sync(0xffffffffu, empty_ctx);
+                while (m) {
+                    const int j = __ffs(m) - 1;
+                    m &= m - 1;
+                    T* o = reinterpret_cast<T*>(p.out) + (size_t)(blockIdx.x * 32 + j) * p.Hq * D;
+                    for (int i = lane; i < p.Hq * D; i += 32) o[i] = from_float<T>(0.f);
+                }
+            }
+            // (sequence, split) of non-empty pair t
+            int base = 0, fb = -1, fs = 0;
+            for (int chunk = 0; chunk < p.B; chunk += 32) {
+                const int bb = chunk + lane;
+                const int nsb = bb < p.B ? (clampi(p.ctx[bb], 0, p.n_cap) + p.P - 1) / p.P : 0;
+                int incl = nsb;
+#pragma unroll
+                for (int k = 1; k < 32; k <<= 1) {
+                    const int u = __shfl_up_sync(0xffffffffu, incl, k);
+                    if (lane >= k) incl += u;
+                }
+                const unsigned hit = __ballot_sync(0xffffffffu, base + incl > t);
+                if (hit) {
+                    const int first = __ffs(hit) - 1;
+                    fb = chunk + first;
+                    fs = t - (base + __shfl_sync(0xffffffffu, incl - nsb, first));
+                    break;
+                }
+                base += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) {
+                bcast[1] = fb;
+                bcast[2] = fs;
+            }
+        }
+        __syncthreads();
+        b = bcast[1];
+        s = bcast[2];
+        if (b < 0) return;   // past the last non-empty split (uniform)
+    } else {
+        int item = blockIdx.x;
+        s = item % p.NS;
+        item /= p.NS;
+        kvh = item % p.Hkv;
+        b = item / p.Hkv;
+    }
     const int h0 = kvh * p.G;
 
     const int n = clampi(p.ctx[b], 0, p.n_cap);
@@ -166,19 +218,7 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
             phys = (phys < 0 || phys >= p.NB) ? 0 : phys;   // bad entries never leave the pool
             if (lane == 0) {
                 uint8_t* kd = ring + stg * 2 * SLICE;
-                uint8_t* vd = kd + SLICE;
-                const int z = phys * p.Hkv + kvh;
-                mbar_arrive_expect_tx(&full[stg], 2 * SLICE);
-                if (LAYOUT == kLayoutNHD) {
-#pragma unroll
-                    for (int j = 0; j < D / 64; ++j) {
-                        tma_load_3d(kd + j * BS * 128, &tmk, &full[stg], j * 64, 0, z, pol);
-                        tma_load_3d(vd + j * BS * 128, &tmv, &full[stg], j * 64, 0, z, pol);
-                    }
-                } else {
-                    tma_load_3d(kd, &tmk, &full[stg], 0, 0, z, pol);
-                    tma_load_3d(vd, &tmv, &full[stg], 0, 0, z, pol);
-                }
+                issue_page_loads<LAYOUT, D>(kd, kd + SLICE, &tmk, &tmv, &full[stg], phys * p.Hkv + kvh, pol);
             }
             issued = i + 1;
             if ((i & 31) == 31) {
@@ -196,41 +236,11 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
 
     // ---------------------------------------------------------------- consumers
     uint32_t qf[NT][KT][2];
-    {
-        const T* qb = reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + h0) * D;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int hh = nt * 8 + (lane >> 2);
-#pragma unroll
-            for (int kk = 0; kk < KT; ++kk) {
-                if (hh < p.G) {
-                    const uint32_t* qr = reinterpret_cast<const uint32_t*>(qb + hh * D + kk * 16 + 2 * (lane & 3));
-                    qf[nt][kk][0] = qr[0];
-                    qf[nt][kk][1] = qr[4];
-                } else {
-                    qf[nt][kk][0] = 0u;
-                    qf[nt][kk][1] = 0u;
-                }
-            }
-        }
-    }
-
-    float acc[KT][NT][4];
-    float mrun[NT][2], lrun[NT][2];
-#pragma unroll
-    for (int dt = 0; dt < KT; ++dt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[dt][nt][e] = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        mrun[nt][0] = mrun[nt][1] = -INFINITY;
-        lrun[nt][0] = lrun[nt][1] = 0.f;
-    }
+    load_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + h0) * D, p.G, lane);
+    WarpState<D, NT> ws;
+    ws.reset();
 
     const int last_pg = (n - 1) / BS;
-    const int mi = lane >> 3, r8 = lane & 7;   // ldmatrix: matrix index and row within it
     bool ok = true;
 
     for (int i = warp; i < npg; i += NWC) {
@@ -242,123 +252,22 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
             break;
         }
         uint8_t* ks = ring + stg * 2 * SLICE;
-        uint8_t* vs = ks + SLICE;
-        const uint32_t ks_a = smem_u32(ks), vs_a = smem_u32(vs);
         const int valid = (pg0 + i == last_pg) ? n - last_pg * BS : BS;
-
-        // S^T = K . Q^T  (16 tokens x 8 heads per n-tile)
-        float sc[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < KT; ++kk) {
-            uint32_t a[4];
-            const int t = r8 + ((mi & 1) << 3);
-            const int c = kk * 2 + (mi >> 1);
-            if (LAYOUT == kLayoutNHD)
-                ldsm_x4(ks_a + nhd_off<BS>(t, c), a);
-            else
-                ldsm_x4(ks_a + (uint32_t)(c * BS * 16 + t * 16), a);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) Mma<T>::run(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
-        }
-
-        // scale to log2 units, mask tokens past the context (select, so a NaN
-        // in an unread slot cannot leak), online-softmax update
-        const int tr = lane >> 2;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int t = tr + ((e >> 1) << 3);
-                sc[nt][e] = t < valid ? sc[nt][e] * p.scale_log2 : -INFINITY;
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float mx = fmaxf(sc[nt][j], sc[nt][j + 2]);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float mnew = fmaxf(mrun[nt][j], mx);
-                const float alpha = ex2(mrun[nt][j] - mnew);
-                mrun[nt][j] = mnew;
-                sc[nt][j] = ex2(sc[nt][j] - mnew);
-                sc[nt][j + 2] = ex2(sc[nt][j + 2] - mnew);
-                lrun[nt][j] = lrun[nt][j] * alpha + (sc[nt][j] + sc[nt][j + 2]);
-#pragma unroll
-                for (int dt = 0; dt < KT; ++dt) {
-                    acc[dt][nt][j] *= alpha;
-                    acc[dt][nt][j + 2] *= alpha;
-                }
-            }
-        }
-
-        // P^T as the B operand: transpose the two 8x8 (token x head) halves.
-        uint32_t pb[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            pb[nt][0] = movmatrix_trans(Mma<T>::pack(sc[nt][0], sc[nt][1]));
-            pb[nt][1] = movmatrix_trans(Mma<T>::pack(sc[nt][2], sc[nt][3]));
-        }
-
-        // Zero the V rows past the context on the sequence's last page so
-        // that P = 0 times whatever they hold stays 0.
-        if (valid < BS) {
-            if (LAYOUT == kLayoutNHD) {
-                const int chunks = (BS - valid) * (D / 8);
-                for (int c = lane; c < chunks; c += 32) {
-                    const int t = valid + c / (D / 8);
-                    const int rem = c % (D / 8);
-                    *reinterpret_cast<uint4*>(vs + (rem >> 3) * (BS * 128) + t * 128 + ((rem & 7) << 4)) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-            } else {
-                for (int d = lane; d < D; d += 32)
-                    for (int t = valid; t < BS; ++t) reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
-
-        // O^T += V^T . P^T
-#pragma unroll
-        for (int dt = 0; dt < KT; ++dt) {
-            uint32_t a[4];
-            if (LAYOUT == kLayoutNHD) {
-                const int t = r8 + ((mi >> 1) << 3);
-                const int c = dt * 2 + (mi & 1);
-                ldsm_x4_trans(vs_a + nhd_off<BS>(t, c), a);
-            } else {
-                const int d = dt * 16 + r8 + ((mi & 1) << 3);
-                const int jc = mi >> 1;
-                ldsm_x4(vs_a + (uint32_t)(d * BS * 2 + jc * 16), a);
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) Mma<T>::run(acc[dt][nt], a, pb[nt][0], pb[nt][1]);
-        }
+        page_step<T, LAYOUT, D, NT>(ks, ks + SLICE, valid, p.scale_log2, qf, ws, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stg]);
     }
     if (!ok && lane == 0 && p.err) atomicOr(p.err, kErrTimeout);
 
     // ------------------------------------------------- merge the warps' states
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            float l = lrun[nt][j];
-            l += __shfl_xor_sync(0xffffffffu, l, 4);
-            l += __shfl_xor_sync(0xffffffffu, l, 8);
-            l += __shfl_xor_sync(0xffffffffu, l, 16);
-            lrun[nt][j] = l;
-        }
+    ws.finish_l();
     if (lane < 4) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                st_m[warp * HP + nt * 8 + 2 * lane + j] = mrun[nt][j];
-                st_l[warp * HP + nt * 8 + 2 * lane + j] = lrun[nt][j];
+                st_m[warp * HP + nt * 8 + 2 * lane + j] = ws.m[nt][j];
+                st_l[warp * HP + nt * 8 + 2 * lane + j] = ws.l[nt][j];
             }
     }
     named_bar_sync(1, NWC * 32);   // every consumer is past its last page
@@ -372,12 +281,12 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < NWC; ++w) M = fmaxf(M, st_m[w * HP + h]);
-            const float f = ex2(mrun[nt][j] - M);   // 0 for a warp that saw no page
+            const float f = ex2(ws.m[nt][j] - M);   // 0 for a warp that saw no page
             float* row = red + (warp * HP + h) * RS + (lane >> 2);
 #pragma unroll
             for (int dt = 0; dt < KT; ++dt) {
-                row[dt * 16] = acc[dt][nt][j] * f;
-                row[dt * 16 + 8] = acc[dt][nt][j + 2] * f;
+                row[dt * 16] = ws.acc[dt][nt][j] * f;
+                row[dt * 16 + 8] = ws.acc[dt][nt][j + 2] * f;
             }
         }
     named_bar_sync(1, NWC * 32);
@@ -415,12 +324,55 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
             }
         }
     }
+    if (direct || !p.fuse) return;
+
+    // ---- fused combine: the last split of this (sequence, KV head) merges all
+    // of them.  Writers' stores reach the CTA barrier, one thread makes them
+    // visible device-wide and counts the arrival.
+    __threadfence();
+    named_bar_sync(1, NWC * 32);
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        __threadfence();
+        bcast[0] = atomicAdd(&p.seg_count[b * p.Hkv + kvh], 1);
+        __threadfence();
+    }
+    named_bar_sync(1, NWC * 32);
+    if (bcast[0] != ns_b - 1) return;
+    constexpr float kLog2e = 1.4426950408889634f;
+    for (int idx = tid; idx < p.G * (D / 4); idx += NWC * 32) {
+        const int h = idx / (D / 4);
+        const int d = (idx % (D / 4)) * 4;
+        const size_t bh = (size_t)b * p.Hq + h0 + h;
+        const float* pm = p.part_m + bh * p.ns_stride;
+        const float* pl = p.part_l + bh * p.ns_stride;
+        const float* pa = p.part_acc + bh * p.ns_stride * D + d;
+        float M = -INFINITY;
+        for (int k = 0; k < ns_b; ++k) M = fmaxf(M, __ldcg(pm + k));
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int k = 0; k < ns_b; ++k) {
+            const float f = ex2((__ldcg(pm + k) - M) * kLog2e);
+            L += f * __ldcg(pl + k);
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(pa + (size_t)k * D));
+            acc.x += f * v.x;
+            acc.y += f * v.y;
+            acc.z += f * v.z;
+            acc.w += f * v.w;
+        }
+        const float inv = 1.f / L;
+        T o4[4] = {from_float<T>(acc.x * inv), from_float<T>(acc.y * inv), from_float<T>(acc.z * inv),
+                   from_float<T>(acc.w * inv)};
+        *reinterpret_cast<uint2*>(reinterpret_cast<T*>(p.out) + bh * D + d) = *reinterpret_cast<uint2*>(o4);
+    }
+    if (tid == 0) p.seg_count[b * p.Hkv + kvh] = 0;   // ready for the next call
 }
 
 // Host-side launcher for one instantiation.
 template <typename T, int LAYOUT, int D, int NT>
-cudaError_t launch_decode_phase1(const DecodeParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                                 cudaStream_t stream) {
+cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
+                                 const CUtensorMap& tmv, cudaStream_t stream) {
     using Tile = DecodeTile<D>;
     auto kern = decode_phase1_kernel<T, LAYOUT, D, NT>;
     const int smem = Tile::smem_bytes(NT);
@@ -434,7 +386,6 @@ cudaError_t launch_decode_phase1(const DecodeParams& p, const CUtensorMap& tmk, 
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    const long long grid = (long long)p.B * p.Hkv * p.NS;
     kern<<<(unsigned)grid, (Tile::NWC + 1) * 32, smem, stream>>>(p, tmk, tmv);
     return cudaGetLastError();
 }

@@ -1,0 +1,207 @@
+// decode_common.cuh -- the per-page arithmetic of paged GQA decode, shared by
+// the fixed-partition kernel (decode.cuh) and the balanced persistent kernel
+// (decode_streamk.cuh).
+//
+// One consumer warp handles one 16-token page of one KV head for all G query
+// heads of its group (padded to NT tiles of 8):
+//   S^T[t][h] = K[t][:] . Q[h][:]           mma.sync m16n8k16, tokens = M, heads = N
+//   m' = max(m, max_t S), alpha = 2^(m - m'), P = 2^(S - m'), l' = alpha l + sum_t P
+//   O^T[d][h] = alpha O^T[d][h] + V^T[d][t] P^T[t][h]   (P^T via movmatrix)
+// ("paged_attention_v2_triton.py", _partition_attn_kernel docstring steps 1-4;
+// flash-decode post, _flash_decode_partial_kernel loop body.)  Scores are in
+// log2 units: scale_log2 = scale * log2(e).
+#pragma once
+
+#include "ptx.cuh"
+
+namespace pkv {
+
+enum { kLayoutNHD = 0, kLayoutVLLM = 1 };
+constexpr int kPageTokens = 16;
+
+__device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+// Byte offset of 16-byte chunk c (c < D/8) of token row t in an NHD slice
+// written by 64-element TMA boxes with 128-byte swizzle.
+template <int BS>
+__device__ __forceinline__ uint32_t nhd_off(int t, int c) {
+    return (uint32_t)((c >> 3) * (BS * 128) + t * 128 + (((c & 7) ^ (t & 7)) << 4));
+}
+
+// Q^T fragments (mma B operand) of heads [nt*8, nt*8+8) of the group; heads
+// at or past G are zero.  qb points at head 0 of the group.
+template <typename T, int D, int NT>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[NT][D / 16][2], const T* qb, int G, int lane) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hh = nt * 8 + (lane >> 2);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            if (hh < G) {
+                const uint32_t* qr = reinterpret_cast<const uint32_t*>(qb + hh * D + kk * 16 + 2 * (lane & 3));
+                qf[nt][kk][0] = qr[0];
+                qf[nt][kk][1] = qr[4];
+            } else {
+                qf[nt][kk][0] = 0u;
+                qf[nt][kk][1] = 0u;
+            }
+        }
+    }
+}
+
+template <int D, int NT>
+struct WarpState {
+    float acc[D / 16][NT][4];   // O^T fragments: (d = dt*16 + lane/4 (+8), h = nt*8 + 2*(lane&3) + j)
+    float m[NT][2];             // running max per head column (log2 units), uniform across lane/4
+    float l[NT][2];             // running sum, per lane (reduced across lane/4 at the end)
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[dt][nt][e] = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            m[nt][0] = m[nt][1] = -INFINITY;
+            l[nt][0] = l[nt][1] = 0.f;
+        }
+    }
+
+    // Completes l: sums the per-lane partial sums over the 8 token rows.
+    __device__ __forceinline__ void finish_l() {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float v = l[nt][j];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                l[nt][j] = v;
+            }
+    }
+};
+
+// Folds one page (K slice ks, V slice vs in shared memory) into the warp's
+// state; `valid` = tokens of the page inside the context (1..16).  Tokens past
+// it are masked by select, and their V rows are zeroed first, so whatever the
+// unread slots hold (NaN included) cannot reach the result.
+template <typename T, int LAYOUT, int D, int NT>
+__device__ __forceinline__ void page_step(uint8_t* ks, uint8_t* vs, int valid, float scale_log2,
+                                          const uint32_t (&qf)[NT][D / 16][2], WarpState<D, NT>& st, int lane) {
+    constexpr int BS = kPageTokens, KT = D / 16;
+    const int mi = lane >> 3, r8 = lane & 7;   // ldmatrix: matrix index and row within it
+    const uint32_t ks_a = smem_u32(ks), vs_a = smem_u32(vs);
+
+    // S^T = K . Q^T  (16 tokens x 8 heads per n-tile)
+    float sc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+        uint32_t a[4];
+        const int t = r8 + ((mi & 1) << 3);
+        const int c = kk * 2 + (mi >> 1);
+        if (LAYOUT == kLayoutNHD)
+            ldsm_x4(ks_a + nhd_off<BS>(t, c), a);
+        else
+            ldsm_x4(ks_a + (uint32_t)(c * BS * 16 + t * 16), a);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) Mma<T>::run(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+    }
+
+    // scale to log2 units, mask, online-softmax update
+    const int tr = lane >> 2;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int t = tr + ((e >> 1) << 3);
+            sc[nt][e] = t < valid ? sc[nt][e] * scale_log2 : -INFINITY;
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float mx = fmaxf(sc[nt][j], sc[nt][j + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mnew = fmaxf(st.m[nt][j], mx);
+            const float alpha = ex2(st.m[nt][j] - mnew);
+            st.m[nt][j] = mnew;
+            sc[nt][j] = ex2(sc[nt][j] - mnew);
+            sc[nt][j + 2] = ex2(sc[nt][j + 2] - mnew);
+            st.l[nt][j] = st.l[nt][j] * alpha + (sc[nt][j] + sc[nt][j + 2]);
+#pragma unroll
+            for (int dt = 0; dt < KT; ++dt) {
+                st.acc[dt][nt][j] *= alpha;
+                st.acc[dt][nt][j + 2] *= alpha;
+            }
+        }
+    }
+
+    // P^T as the B operand: transpose the two 8x8 (token x head) halves.
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        pb[nt][0] = movmatrix_trans(Mma<T>::pack(sc[nt][0], sc[nt][1]));
+        pb[nt][1] = movmatrix_trans(Mma<T>::pack(sc[nt][2], sc[nt][3]));
+    }
+
+    // Zero the V rows past the context so that P = 0 times whatever they hold stays 0.
+    if (valid < BS) {
+        if (LAYOUT == kLayoutNHD) {
+            const int chunks = (BS - valid) * (D / 8);
+            for (int c = lane; c < chunks; c += 32) {
+                const int t = valid + c / (D / 8);
+                const int rem = c % (D / 8);
+                *reinterpret_cast<uint4*>(vs + (rem >> 3) * (BS * 128) + t * 128 + ((rem & 7) << 4)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+        } else {
+            for (int d = lane; d < D; d += 32)
+                for (int t = valid; t < BS; ++t) reinterpret_cast<uint16_t*>(vs)[d * BS + t] = 0;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+    }
+
+    // O^T += V^T . P^T
+#pragma unroll
+    for (int dt = 0; dt < KT; ++dt) {
+        uint32_t a[4];
+        if (LAYOUT == kLayoutNHD) {
+            const int t = r8 + ((mi >> 1) << 3);
+            const int c = dt * 2 + (mi & 1);
+            ldsm_x4_trans(vs_a + nhd_off<BS>(t, c), a);
+        } else {
+            const int d = dt * 16 + r8 + ((mi & 1) << 3);
+            const int jc = mi >> 1;
+            ldsm_x4(vs_a + (uint32_t)(d * BS * 2 + jc * 16), a);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) Mma<T>::run(st.acc[dt][nt], a, pb[nt][0], pb[nt][1]);
+    }
+}
+
+// Issues the TMA loads of one page slice pair (K and V of one KV head) into a
+// ring stage, completing on `bar` (2 * BS * D * 2 bytes).
+template <int LAYOUT, int D>
+__device__ __forceinline__ void issue_page_loads(uint8_t* kd, uint8_t* vd, const CUtensorMap* tmk,
+                                                 const CUtensorMap* tmv, uint64_t* bar, int slice, uint64_t pol) {
+    constexpr int BS = kPageTokens;
+    mbar_arrive_expect_tx(bar, 2 * BS * D * 2);
+    if (LAYOUT == kLayoutNHD) {
+#pragma unroll
+        for (int j = 0; j < D / 64; ++j) {
+            tma_load_3d(kd + j * BS * 128, tmk, bar, j * 64, 0, slice, pol);
+            tma_load_3d(vd + j * BS * 128, tmv, bar, j * 64, 0, slice, pol);
+        }
+    } else {
+        tma_load_3d(kd, tmk, bar, 0, 0, slice, pol);
+        tma_load_3d(vd, tmv, bar, 0, 0, slice, pol);
+    }
+}
+
+}  // namespace pkv

@@ -5,13 +5,14 @@
 
 namespace pkv {
 
-cudaError_t launch_decode_vllm_bf16(int D, int nt, const DecodeParams& p, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_decode_vllm_bf16(int D, int nt, const DecodeParams& p, long long grid, const CUtensorMap& k,
+                                  const CUtensorMap& v,
                                    cudaStream_t s) {
-    if (D == 64 && nt == 1) return launch_decode_phase1<__nv_bfloat16, kLayoutVLLM, 64, 1>(p, k, v, s);
-    if (D == 64 && nt == 2) return launch_decode_phase1<__nv_bfloat16, kLayoutVLLM, 64, 2>(p, k, v, s);
-    if (D == 128 && nt == 1) return launch_decode_phase1<__nv_bfloat16, kLayoutVLLM, 128, 1>(p, k, v, s);
-    if (D == 128 && nt == 2) return launch_decode_phase1<__nv_bfloat16, kLayoutVLLM, 128, 2>(p, k, v, s);
-    if (D == 256 && nt == 1) return launch_decode_phase1<__nv_bfloat16, kLayoutVLLM, 256, 1>(p, k, v, s);
+    if (D == 64 && nt == 1) return launch_decode_phase1<__nv_bfloat16, kLayoutVLLM, 64, 1>(p, grid, k, v, s);
+    if (D == 64 && nt == 2) return launch_decode_phase1<__nv_bfloat16, kLayoutVLLM, 64, 2>(p, grid, k, v, s);
+    if (D == 128 && nt == 1) return launch_decode_phase1<__nv_bfloat16, kLayoutVLLM, 128, 1>(p, grid, k, v, s);
+    if (D == 128 && nt == 2) return launch_decode_phase1<__nv_bfloat16, kLayoutVLLM, 128, 2>(p, grid, k, v, s);
+    if (D == 256 && nt == 1) return launch_decode_phase1<__nv_bfloat16, kLayoutVLLM, 256, 1>(p, grid, k, v, s);
     return cudaErrorInvalidValue;
 }
 

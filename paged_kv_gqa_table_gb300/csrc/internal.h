@@ -17,13 +17,13 @@ struct CombineParams {
 
 // Phase-1 dispatch, one function per (layout, dtype) translation unit.
 // D in {64, 128, 256}; nt = padded-head tiles of 8 (1, or 2 for D <= 128).
-cudaError_t launch_decode_nhd_f16(int D, int nt, const DecodeParams& p, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_decode_nhd_f16(int D, int nt, const DecodeParams& p, long long grid, const CUtensorMap& k, const CUtensorMap& v,
                                   cudaStream_t s);
-cudaError_t launch_decode_nhd_bf16(int D, int nt, const DecodeParams& p, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_decode_nhd_bf16(int D, int nt, const DecodeParams& p, long long grid, const CUtensorMap& k, const CUtensorMap& v,
                                    cudaStream_t s);
-cudaError_t launch_decode_vllm_f16(int D, int nt, const DecodeParams& p, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_decode_vllm_f16(int D, int nt, const DecodeParams& p, long long grid, const CUtensorMap& k, const CUtensorMap& v,
                                    cudaStream_t s);
-cudaError_t launch_decode_vllm_bf16(int D, int nt, const DecodeParams& p, const CUtensorMap& k,
+cudaError_t launch_decode_vllm_bf16(int D, int nt, const DecodeParams& p, long long grid, const CUtensorMap& k,
                                     const CUtensorMap& v, cudaStream_t s);
 
 // MLA paged causal prefill (mla.cu); bf16 tensors, page size 1.

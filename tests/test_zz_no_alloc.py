@@ -2,8 +2,9 @@
 
 It exists for callers that may not allocate device memory when they run a
 decode step (a plugin's enqueue hook, an engine with a fixed memory pool, a
-latency-critical loop).  It keeps the split partials in the library's own
-static device array instead of a caller workspace.  These tests call it
+latency-critical loop).  It keeps the decode step's scratch (merge counters
+and partial results) in the library's own static device array instead of a
+caller workspace.  These tests call it
 through the C ABI and compare it with the workspace entry point on the same
 inputs, twice in a row with different problems (the array keeps the previous
 call's contents, which must not matter), within the tolerance the parity
@@ -21,38 +22,41 @@ pytestmark = [pytest.mark.gpu,
 TOL = {synth.F16: 4e-3, synth.BF16: 1.6e-2}
 
 
-def _run_both(case):
+def _run_both(case, opts=None):
     from paged_kv_gqa_table_gb300 import binding as B
     from paged_kv_gqa_table_gb300 import tensors as T
     dev = T.upload_decode_case(case)
     desc = T.decode_desc(case)
-    ns, _ = B.pkv_plan_splits(desc)
-    assert ns > 1, "the case must use split partials (scratch memory)"
-    ref = T.paged_decode_attention(case, dev=dev)
+    ref = T.paged_decode_attention(case, dev=dev, opts=opts)
     out = torch.full_like(ref, float("nan"))
     B.pkv_paged_decode_attention_static(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
-                                        dev["context_lens"], case["scale"], out)
+                                        dev["context_lens"], case["scale"], out, opts=opts)
     torch.cuda.synchronize()
     return out.double().cpu().numpy(), ref.double().cpu().numpy()
 
 
 def test_static_scratch_matches_workspace_entry_point_twice():
+    from paged_kv_gqa_table_gb300 import binding as B
+    # Both calls need scratch: their sequences are split, so the split
+    # partials and the merge counters live in the static array (default plan
+    # first, then fixed 512-token partitions).
     first = synth.decode_case(seed=0, B=16, Hq=32, Hkv=8, D=128, block_size=16, dtype=synth.BF16,
                               layout=synth.NHD, ctx_range=(1, 4096), max_blocks_per_seq=256)
     second = synth.decode_case(seed=1, B=24, Hq=24, Hkv=4, D=256, block_size=16, dtype=synth.F16,
                                layout=synth.VLLM, ctx_range=(600, 3000), max_blocks_per_seq=200)
-    for case in (first, second):
-        got, ref = _run_both(case)
+    for case, opts in ((first, None), (second, B.make_opts(partition_tokens=512))):
+        got, ref = _run_both(case, opts)
         assert np.all(np.isfinite(got))
         assert float(np.max(np.abs(got - ref))) <= TOL[case["dtype"]]
 
 
 def test_static_scratch_refuses_problems_that_do_not_fit():
     from paged_kv_gqa_table_gb300 import binding as B
-    # 256 sequences x 64 heads x 256 splits of fp32 partials is far beyond 32 MiB
+    # 256 sequences x 64 heads x 256 fixed partitions of fp32 partials is far beyond 32 MiB
     desc = B.make_desc(256, 64, 8, 128, 16, 8192, 300000, 131072, 256 * 131072, synth.BF16)
-    assert B.pkv_decode_workspace_size(desc) > B.PKV_STATIC_SCRATCH_BYTES
+    opts = B.make_opts(partition_tokens=512)
+    assert B.pkv_decode_workspace_size(desc, opts) > B.PKV_STATIC_SCRATCH_BYTES
     dummy = torch.zeros(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(B.PkvError) as e:
-        B.pkv_paged_decode_attention_static(desc, dummy, dummy, dummy, dummy, dummy, 0.1, dummy)
+        B.pkv_paged_decode_attention_static(desc, dummy, dummy, dummy, dummy, dummy, 0.1, dummy, opts=opts)
     assert e.value.status == B.PKV_WORKSPACE_TOO_SMALL
