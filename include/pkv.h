@@ -108,13 +108,11 @@ int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, in
 
 /*
  * Bytes of scratch memory pkv_paged_decode_attention needs for this problem
- * and these options (256-byte header, one int32 arrival counter per
- * (sequence, KV head), and fp32 split partials m, l [B][Hq][NS] and
- * acc [B][Hq][NS][D] when the plan has more than one split).  num_sms as for
- * pkv_plan_splits.  The workspace must be 256-byte aligned and ZEROED ONCE
- * after allocation: word 0 of the header collects device-side error bits
- * (bit 0: a pipeline wait timed out) and the counters must start at zero;
- * every call leaves them at zero again.
+ * and these options (256-byte header, then fp32 split partials m, l
+ * [B][Hq][NS] and acc [B][Hq][NS][D] when the plan has more than one split).
+ * num_sms as for pkv_plan_splits.  The workspace must be 256-byte aligned.
+ * Word 0 of the header collects device-side error bits (bit 0: a pipeline
+ * wait timed out); zero it once after allocating.
  */
 int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms,
                               size_t* bytes);
@@ -134,12 +132,11 @@ int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts
  *                 pkv_validate_block_table reports it.
  *   context_lens  int32 [B]; values are clamped to
  *                 [0, min(max_context_len, max_blocks_per_seq * block_size)].
- * Phase 1 runs one CTA per non-empty (sequence, KV head, split) of the
- * pkv_plan_splits plan, loading each page once for the whole group.  A
- * sequence with several splits is merged by log-sum-exp by the last of its
- * splits to finish (plans of at most 32 splits) or by a second combine kernel
- * (longer plans).  Calls sharing one workspace must be ordered on the GPU
- * (one stream).
+ * Phase 1 runs one CTA per (sequence, KV head, split) of the pkv_plan_splits
+ * plan, loading each page once for the whole group; sequences with more than
+ * one split are merged by a log-sum-exp combine kernel launched as a
+ * programmatic dependent of phase 1.  Calls sharing one workspace must be
+ * ordered on the GPU (one stream).
  */
 int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
                                const void* q, const void* k_cache, const void* v_cache,
@@ -231,11 +228,11 @@ int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const vo
  * that carves all device memory out of a fixed pool at start-up, or a
  * latency-critical loop where cudaMalloc could synchronise the device.
  *
- * The step's scratch (error word, merge counters, partial results) lives in
- * one file-scope device array of PKV_STATIC_SCRATCH_BYTES (32 MiB), which
+ * The step's scratch (error word and split partials) lives in one
+ * file-scope device array of PKV_STATIC_SCRATCH_BYTES (32 MiB), which
  * every GPU that loads libpkv reserves until the process exits.  This call
  * allocates nothing: no cudaMalloc, cudaFree or allocating library routine;
- * it clears the array's header and merge counters with cudaMemsetAsync on
+ * it clears the array's 256-byte error header with cudaMemsetAsync on
  * `stream` and then runs the regular entry point on the array.
  *  - A problem whose workspace (pkv_decode_workspace_size) exceeds the array
  *    is refused with PKV_WORKSPACE_TOO_SMALL before anything is launched.

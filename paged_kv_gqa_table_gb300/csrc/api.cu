@@ -109,26 +109,6 @@ size_t partial_bytes(const pkv_decode_desc* d, int ns) {
     return 2 * align256(rows * 4) + align256(rows * d->D * 4);
 }
 
-// Workspace: 256-byte header | arrival counters [B * Hkv] | m, l [B][Hq][NS],
-// acc [B][Hq][NS][D] (the partials only when some sequence has two splits).
-size_t counter_bytes(const pkv_decode_desc* d) { return align256((size_t)d->B * d->Hkv * 4); }
-size_t workspace_bytes_for(const pkv_decode_desc* d, int ns) {
-    return kHeaderBytes + counter_bytes(d) + (ns > 1 ? partial_bytes(d, ns) : 0);
-}
-
-// Sequences with at most this many splits are merged inside phase 1 by the
-// last split to finish; longer plans keep the separate combine kernel, whose
-// merge work is spread over many CTAs.
-constexpr int kFuseMaxSplits = 32;
-
-// Compact grid: Hkv x (an upper bound on the number of non-empty (sequence,
-// split) pairs, from the host-known maximum and sum of the context lengths).
-long long compact_grid(const pkv_decode_desc* d, int P, int ns) {
-    const long long by_max = (long long)d->B * ns;
-    const long long by_sum = ceil_div(d->sum_context_len, P) + d->B;
-    return (long long)d->Hkv * (by_max < by_sum ? by_max : by_sum);
-}
-
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -261,7 +241,7 @@ int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts
     int ns = 0, P = 0;
     int st = plan(desc, opts, num_sms, &ns, &P);
     if (st) return st;
-    *bytes = workspace_bytes_for(desc, ns);
+    *bytes = kHeaderBytes + (ns > 1 ? partial_bytes(desc, ns) : 0);
     return PKV_OK;
 }
 
@@ -279,7 +259,7 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
     int ns = 0, P = 0;
     st = plan(desc, opts, 0, &ns, &P);
     if (st) return st;
-    if (workspace_bytes < workspace_bytes_for(desc, ns)) return PKV_WORKSPACE_TOO_SMALL;
+    if (workspace_bytes < kHeaderBytes + (ns > 1 ? partial_bytes(desc, ns) : 0)) return PKV_WORKSPACE_TOO_SMALL;
 
     DecodeParams p;
     CUtensorMap mk{}, mv{};
@@ -289,26 +269,25 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.out = out;
     p.err = reinterpret_cast<uint32_t*>(ws);
-    p.seg_count = reinterpret_cast<int*>(ws + kHeaderBytes);
-    uint8_t* parts = ws + kHeaderBytes + counter_bytes(desc);
+    uint8_t* parts = ws + kHeaderBytes;
     const size_t rows = (size_t)desc->B * desc->Hq * ns;
     p.part_m = reinterpret_cast<float*>(parts);
     p.part_l = reinterpret_cast<float*>(parts + align256(rows * 4));
     p.part_acc = reinterpret_cast<float*>(parts + 2 * align256(rows * 4));
-    p.compact = 1;
-    p.fuse = ns <= kFuseMaxSplits ? 1 : 0;
 
     if (desc->max_context_len == 0) {
         // Every context is empty: the combine kernel writes the zero rows.
         CombineParams c{context_lens, nullptr, nullptr, nullptr, out, desc->B, desc->Hq, P, ns, 0, 0};
-        return launch_combine(desc->dtype, desc->D, c, s) == cudaSuccess ? PKV_OK : PKV_CUDA_ERROR;
+        return launch_combine(desc->dtype, desc->D, c, s, false) == cudaSuccess ? PKV_OK : PKV_CUDA_ERROR;
     }
     record(opts ? opts->phase1_event_start : nullptr, s);
-    if (dispatch_phase1(desc, p, compact_grid(desc, P, ns), mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
+    if (dispatch_phase1(desc, p, (long long)desc->B * desc->Hkv * ns, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
     record(opts ? opts->phase1_event_stop : nullptr, s);
-    if (ns > 1 && !p.fuse) {
+    if (ns > 1) {
+        // Programmatic dependent of phase 1 (unless an event sits between them).
         CombineParams c{context_lens, p.part_acc, p.part_m, p.part_l, out, desc->B, desc->Hq, P, ns, p.n_cap, 1};
-        if (launch_combine(desc->dtype, desc->D, c, s) != cudaSuccess) return PKV_CUDA_ERROR;
+        if (launch_combine(desc->dtype, desc->D, c, s, !(opts && opts->phase1_event_stop)) != cudaSuccess)
+            return PKV_CUDA_ERROR;
     }
     return PKV_OK;
 }
@@ -364,7 +343,7 @@ int pkv_combine(const pkv_decode_desc* desc, int partition_tokens, int num_split
     if (!context_lens || !part_acc || !part_m || !part_l || !out || !aligned(part_acc, 16)) return PKV_INVALID_ARG;
     CombineParams c{context_lens, part_acc, part_m, part_l, out, desc->B, desc->Hq, partition_tokens, num_splits,
                     desc->max_context_len, 0};
-    return launch_combine(desc->dtype, desc->D, c, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+    return launch_combine(desc->dtype, desc->D, c, reinterpret_cast<cudaStream_t>(stream), false) == cudaSuccess
                ? PKV_OK
                : PKV_CUDA_ERROR;
 }

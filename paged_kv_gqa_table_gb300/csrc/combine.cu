@@ -4,166 +4,209 @@
 // Combine ("koas-w.github.io flash-decode post", _flash_decode_combine_kernel;
 // "paged_attention_v2_triton.py", _reduce_partitions_kernel):
 //   M = max_s m_s,  f_s = e^{m_s - M},  out = sum_s f_s acc_s / sum_s f_s l_s.
-// One CTA of 8 warps per (sequence, query head): warp w takes splits
-// s = w, w+8, ...; each lane owns D/32 consecutive elements of acc (vector
-// loads), so a warp reads one split's row as one coalesced request.
 #include "internal.h"
 
 namespace pkv {
 
+// One warp per (sequence, query head); lane l owns elements [l*D/32, (l+1)*D/32).
+// Splits are merged a chunk at a time (32 / (D/32) splits): the chunk's m, l
+// and acc rows are all loaded before any is used, so a chunk costs one memory
+// round trip,
+// and the chunks fold into a running (M, L, acc) by log-sum-exp rescaling.
+// Launched as a programmatic dependent of phase 1: the prologue (context
+// length) runs while phase 1 finishes; griddepcontrol.wait precedes every
+// read of the partials.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
-    constexpr int NW = 8;
     constexpr int EPL = D / 32;   // elements per lane
-    __shared__ float s_red[NW][D];
-    __shared__ float s_l[NW];
-    __shared__ float s_m[NW];
-
-    const int bh = blockIdx.x;
-    const int b = bh / p.Hq;
+    constexpr int CH = 32 / EPL;  // splits per chunk: 32 floats of acc in flight per lane
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int n = p.ctx[b];
-    n = n < 0 ? 0 : (n > p.n_cap ? p.n_cap : n);
+    const long long bh = (long long)blockIdx.x * 8 + warp;
+    const bool live = bh < (long long)p.B * p.Hq;
+    int n = 0;
+    if (live) {
+        n = p.ctx[bh / p.Hq];
+        n = n < 0 ? 0 : (n > p.n_cap ? p.n_cap : n);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!live) return;
     const int ns = (n + p.P - 1) / p.P;
     if (p.skip_single && ns <= 1) return;   // phase 1 wrote this row directly
-    T* o = reinterpret_cast<T*>(p.out) + (size_t)bh * D;
+    T* o = reinterpret_cast<T*>(p.out) + bh * D + lane * EPL;
     if (n == 0) {
-        for (int d = threadIdx.x; d < D; d += blockDim.x) o[d] = from_float<T>(0.f);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = from_float<T>(0.f);
         return;
     }
-    const float* pm = p.part_m + (size_t)bh * p.ns_stride;
-    const float* pl = p.part_l + (size_t)bh * p.ns_stride;
-    const float* pa = p.part_acc + (size_t)bh * p.ns_stride * D;
-
-    float mx = -INFINITY;
-    for (int s = threadIdx.x; s < ns; s += blockDim.x) mx = fmaxf(mx, pm[s]);
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
-    if (lane == 0) s_m[warp] = mx;
-    __syncthreads();
-    float M = s_m[0];
-#pragma unroll
-    for (int w = 1; w < NW; ++w) M = fmaxf(M, s_m[w]);
-
+    const float* pm = p.part_m + bh * p.ns_stride;
+    const float* pl = p.part_l + bh * p.ns_stride;
+    const float* pa = p.part_acc + bh * p.ns_stride * D + lane * EPL;
     constexpr float kLog2e = 1.4426950408889634f;
-    float a[EPL];
+    float M = -INFINITY, L = 0.f, acc[EPL];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) a[e] = 0.f;
-    float L = 0.f;
-#pragma unroll 4
-    for (int s = warp; s < ns; s += NW) {
-        const float f = ex2((pm[s] - M) * kLog2e);   // a sentinel (-inf) gives 0
-        L += f * pl[s];
-        const float* row = pa + (size_t)s * D + lane * EPL;
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    for (int c0 = 0; c0 < ns; c0 += CH) {
+        // Unconditional loads (index clamped to the last split) so that all
+        // of the chunk's loads are in flight together; padding gets m = -inf.
+        float m[CH], l[CH], a[CH][EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; e += 4) {
-            const float4 v = *reinterpret_cast<const float4*>(row + e);
-            a[e] += f * v.x;
-            a[e + 1] += f * v.y;
-            a[e + 2] += f * v.z;
-            a[e + 3] += f * v.w;
+        for (int j = 0; j < CH; ++j) {
+            const int sj = min(c0 + j, ns - 1);
+            m[j] = __ldg(pm + sj);
+            l[j] = __ldg(pl + sj);
+#pragma unroll
+            for (int e = 0; e < EPL; e += 2) {
+                const float2 v = __ldg(reinterpret_cast<const float2*>(pa + (size_t)sj * D + e));
+                a[j][e] = v.x;
+                a[j][e + 1] = v.y;
+            }
         }
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+            if (c0 + j >= ns) m[j] = -INFINITY;
+        float Mc = M;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) Mc = fmaxf(Mc, m[j]);
+        const float r = ex2((M - Mc) * kLog2e);   // rescale of the running sums (0 at the start)
+        L *= r;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] *= r;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const float f = ex2((m[j] - Mc) * kLog2e);   // a sentinel or padding (-inf) gives 0
+            L += f * l[j];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] += f * a[j][e];
+        }
+        M = Mc;
     }
+    const float inv = 1.f / L;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) s_red[warp][lane * EPL + e] = a[e];
-    if (lane == 0) s_l[warp] = L;
-    __syncthreads();
-    float Lt = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) Lt += s_l[w];
-    const float inv = 1.f / Lt;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) v += s_red[w][d];
-        o[d] = from_float<T>(v * inv);
+    for (int e = 0; e < EPL; e += 2) {
+        const uint32_t packed = Mma<T>::pack(acc[e] * inv, acc[e + 1] * inv);
+        *reinterpret_cast<uint32_t*>(o + e) = packed;
     }
 }
 
-// D = 64 leaves two elements per lane; the float4 loop above needs four.
-template <typename T>
-__global__ void __launch_bounds__(256) combine_kernel_d64(const CombineParams p) {
-    constexpr int D = 64, NW = 8;
-    __shared__ float s_red[NW][D];
-    __shared__ float s_l[NW];
-    __shared__ float s_m[NW];
-    const int bh = blockIdx.x;
-    const int b = bh / p.Hq;
+// Rows with many splits (long contexts): one CTA of 8 warps per row; warp w
+// folds chunks w, w+8, ... of splits, so the chunks' memory round
+// trips overlap across warps; the warps' running (M, L, acc) are then merged
+// through shared memory.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) combine_wide_kernel(const CombineParams p) {
+    constexpr int EPL = D / 32, CH = 32 / EPL, NW = 8;
+    __shared__ float s_acc[NW][D];
+    __shared__ float s_m[NW], s_l[NW];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int n = p.ctx[b];
+    const long long bh = blockIdx.x;
+    int n = p.ctx[bh / p.Hq];
     n = n < 0 ? 0 : (n > p.n_cap ? p.n_cap : n);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int ns = (n + p.P - 1) / p.P;
     if (p.skip_single && ns <= 1) return;
-    T* o = reinterpret_cast<T*>(p.out) + (size_t)bh * D;
+    T* o = reinterpret_cast<T*>(p.out) + bh * D;
     if (n == 0) {
         for (int d = threadIdx.x; d < D; d += blockDim.x) o[d] = from_float<T>(0.f);
         return;
     }
-    const float* pm = p.part_m + (size_t)bh * p.ns_stride;
-    const float* pl = p.part_l + (size_t)bh * p.ns_stride;
-    const float* pa = p.part_acc + (size_t)bh * p.ns_stride * D;
-    float mx = -INFINITY;
-    for (int s = threadIdx.x; s < ns; s += blockDim.x) mx = fmaxf(mx, pm[s]);
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
-    if (lane == 0) s_m[warp] = mx;
-    __syncthreads();
-    float M = s_m[0];
-#pragma unroll
-    for (int w = 1; w < NW; ++w) M = fmaxf(M, s_m[w]);
+    const float* pm = p.part_m + bh * p.ns_stride;
+    const float* pl = p.part_l + bh * p.ns_stride;
+    const float* pa = p.part_acc + bh * p.ns_stride * D + lane * EPL;
     constexpr float kLog2e = 1.4426950408889634f;
-    float a0 = 0.f, a1 = 0.f, L = 0.f;
-#pragma unroll 4
-    for (int s = warp; s < ns; s += NW) {
-        const float f = ex2((pm[s] - M) * kLog2e);
-        L += f * pl[s];
-        const float2 v = *reinterpret_cast<const float2*>(pa + (size_t)s * D + lane * 2);
-        a0 += f * v.x;
-        a1 += f * v.y;
-    }
-    s_red[warp][lane * 2] = a0;
-    s_red[warp][lane * 2 + 1] = a1;
-    if (lane == 0) s_l[warp] = L;
-    __syncthreads();
-    float Lt = 0.f;
+    float M = -INFINITY, L = 0.f, acc[EPL];
 #pragma unroll
-    for (int w = 0; w < NW; ++w) Lt += s_l[w];
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    for (int c0 = warp * CH; c0 < ns; c0 += NW * CH) {
+        // Unconditional loads (index clamped to the last split) so that all
+        // of the chunk's loads are in flight together; padding gets m = -inf.
+        float m[CH], l[CH], a[CH][EPL];
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const int sj = min(c0 + j, ns - 1);
+            m[j] = __ldg(pm + sj);
+            l[j] = __ldg(pl + sj);
+#pragma unroll
+            for (int e = 0; e < EPL; e += 2) {
+                const float2 v = __ldg(reinterpret_cast<const float2*>(pa + (size_t)sj * D + e));
+                a[j][e] = v.x;
+                a[j][e + 1] = v.y;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+            if (c0 + j >= ns) m[j] = -INFINITY;
+        float Mc = M;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) Mc = fmaxf(Mc, m[j]);
+        const float r = ex2((M - Mc) * kLog2e);
+        L *= r;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] *= r;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const float f = ex2((m[j] - Mc) * kLog2e);
+            L += f * l[j];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] += f * a[j][e];
+        }
+        M = Mc;
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) s_acc[warp][lane * EPL + e] = acc[e];
+    if (lane == 0) {
+        s_m[warp] = M;
+        s_l[warp] = L;
+    }
+    __syncthreads();
+    float Mt = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) Mt = fmaxf(Mt, s_m[w]);
+    float f[NW], Lt = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        f[w] = ex2((s_m[w] - Mt) * kLog2e);   // 0 for a warp that had no chunk
+        Lt += f[w] * s_l[w];
+    }
     const float inv = 1.f / Lt;
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) v += s_red[w][d];
+        for (int w = 0; w < NW; ++w) v += f[w] * s_acc[w][d];
         o[d] = from_float<T>(v * inv);
     }
 }
 
-cudaError_t launch_combine(int dtype, int D, const CombineParams& p, cudaStream_t stream) {
-    const unsigned grid = (unsigned)((long long)p.B * p.Hq);
-    if (grid == 0) return cudaSuccess;
+// Plans with more splits than this use one CTA per row instead of one warp.
+constexpr int kWideCombineSplits = 32;
+
+template <typename T, int D>
+cudaError_t launch_combine_t(const CombineParams& p, cudaLaunchConfig_t& cfg) {
+    const long long rows = (long long)p.B * p.Hq;
+    if (p.ns_stride > kWideCombineSplits) {
+        cfg.gridDim = dim3((unsigned)rows);
+        return cudaLaunchKernelEx(&cfg, combine_wide_kernel<T, D>, p);
+    }
+    cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
+    return cudaLaunchKernelEx(&cfg, combine_kernel<T, D>, p);
+}
+
+cudaError_t launch_combine(int dtype, int D, const CombineParams& p, cudaStream_t stream, bool after_phase1) {
+    if ((long long)p.B * p.Hq == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_phase1 ? 1 : 0;
     const bool bf = dtype == 1;
     switch (D) {
-        case 64:
-            if (bf)
-                combine_kernel_d64<__nv_bfloat16><<<grid, 256, 0, stream>>>(p);
-            else
-                combine_kernel_d64<__half><<<grid, 256, 0, stream>>>(p);
-            break;
-        case 128:
-            if (bf)
-                combine_kernel<__nv_bfloat16, 128><<<grid, 256, 0, stream>>>(p);
-            else
-                combine_kernel<__half, 128><<<grid, 256, 0, stream>>>(p);
-            break;
-        case 256:
-            if (bf)
-                combine_kernel<__nv_bfloat16, 256><<<grid, 256, 0, stream>>>(p);
-            else
-                combine_kernel<__half, 256><<<grid, 256, 0, stream>>>(p);
-            break;
-        default:
-            return cudaErrorInvalidValue;
+        case 64: return bf ? launch_combine_t<__nv_bfloat16, 64>(p, cfg) : launch_combine_t<__half, 64>(p, cfg);
+        case 128: return bf ? launch_combine_t<__nv_bfloat16, 128>(p, cfg) : launch_combine_t<__half, 128>(p, cfg);
+        case 256: return bf ? launch_combine_t<__nv_bfloat16, 256>(p, cfg) : launch_combine_t<__half, 256>(p, cfg);
+        default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- validator

@@ -4,9 +4,6 @@
 // [s*P, min((s+1)*P, n)) of the sequence (fixed partitions as in
 // "paged_attention_v2_triton.py", _partition_attn_kernel; page-granular
 // splits as in the flash-decode post's _flash_decode_partial_kernel).
-// In the compact grid only the non-empty splits are launched: CTA i handles
-// KV head i % Hkv of the (i / Hkv)-th non-empty (sequence, split) pair,
-// found by a warp scan over the per-sequence split counts.
 //
 // Roles: warp NWC is the producer: it reads the split's block-table entries
 // (32 per coalesced load, one chunk ahead) and, per page, issues TMA tensor
@@ -24,11 +21,7 @@
 // warps' states are merged through shared memory at the end; the CTA writes
 // either the final normalised row (the sequence has a single split) or the
 // unnormalised fp32 partial (acc, m, l) of its split, m in natural-log units
-// (the partial-buffer convention of the flash-decode post).  With `fuse`, the
-// last split of a (sequence, KV head) to finish -- an arrival counter per
-// pair, reset by that CTA -- merges all the pair's partials by log-sum-exp
-// (the flash-decode post's _flash_decode_combine_kernel) and writes the
-// output, so no second kernel runs.
+// (the partial-buffer convention of the flash-decode post).
 //
 // Shared-memory layouts of one page slice (BS = 16 tokens):
 //   NHD : TMA boxes of 64 elements x BS rows, 128-byte swizzle, so that the
@@ -57,9 +50,6 @@ struct DecodeParams {
     int n_cap;               // context lengths are clamped to [0, n_cap]
     float scale_log2;        // scale * log2(e)
     int partials_only;       // 1: always write partials (+ sentinels), never out
-    int compact;             // 1: grid over non-empty (sequence, split) pairs x Hkv; 0: dense B x Hkv x NS
-    int fuse;                // 1: the last split of a (sequence, KV head) merges the partials
-    int* seg_count;          // [B * Hkv] arrival counters (fuse), zero between calls
 };
 
 template <int D>
@@ -70,7 +60,7 @@ struct DecodeTile {
     static constexpr int STAGES = D == 64 ? 12 : (D == 128 ? 8 : 4);
     static constexpr int RED_STRIDE = D + 4;                        // floats per reduction row
     static constexpr int smem_bytes(int nt) {
-        return 1024 + STAGES * 2 * SLICE + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 32;
+        return 1024 + STAGES * 2 * SLICE + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 16;
     }
 };
 
@@ -97,62 +87,16 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
     float* st_m = reinterpret_cast<float*>(empty + STAGES);
     float* st_l = st_m + NWC * HP;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(st_l + NWC * HP);   // set on a wait timeout
-    volatile int* bcast = abort_flag + 1;                                           // [3]
 
+    // Lets the combine kernel queued behind this one start its prologue as
+    // soon as every CTA of this grid is running (it waits for our results).
+    asm volatile("griddepcontrol.launch_dependents;");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int b, s, kvh;
-    if (p.compact) {
-        kvh = blockIdx.x % p.Hkv;
-        const int t = blockIdx.x / p.Hkv;
-        if (warp == 0) {
-            // Zero rows of empty contexts: CTA i looks after sequences [32 i, 32 i + 32).
-            if ((int)blockIdx.x * 32 < p.B) {
-                const int bz = blockIdx.x * 32 + lane;
-                const bool empty_ctx = bz < p.B && clampi(p.ctx[bz], 0, p.n_cap) == 0;
-                unsigned m = __ballot_sync(0xffffffffu, empty_ctx);
-                while (m) {
-                    const int j = __ffs(m) - 1;
-                    m &= m - 1;
-                    T* o = reinterpret_cast<T*>(p.out) + (size_t)(blockIdx.x * 32 + j) * p.Hq * D;
-                    for (int i = lane; i < p.Hq * D; i += 32) o[i] = from_float<T>(0.f);
-                }
-            }
-            // (sequence, split) of non-empty pair t
-            int base = 0, fb = -1, fs = 0;
-            for (int chunk = 0; chunk < p.B; chunk += 32) {
-                const int bb = chunk + lane;
-                const int nsb = bb < p.B ? (clampi(p.ctx[bb], 0, p.n_cap) + p.P - 1) / p.P : 0;
-                int incl = nsb;
-#pragma unroll
-                for (int k = 1; k < 32; k <<= 1) {
-                    const int u = __shfl_up_sync(0xffffffffu, incl, k);
-                    if (lane >= k) incl += u;
-                }
-                const unsigned hit = __ballot_sync(0xffffffffu, base + incl > t);
-                if (hit) {
-                    const int first = __ffs(hit) - 1;
-                    fb = chunk + first;
-                    fs = t - (base + __shfl_sync(0xffffffffu, incl - nsb, first));
-                    break;
-                }
-                base += __shfl_sync(0xffffffffu, incl, 31);
-            }
-            if (lane == 0) {
-                bcast[1] = fb;
-                bcast[2] = fs;
-            }
-        }
-        __syncthreads();
-        b = bcast[1];
-        s = bcast[2];
-        if (b < 0) return;   // past the last non-empty split (uniform)
-    } else {
-        int item = blockIdx.x;
-        s = item % p.NS;
-        item /= p.NS;
-        kvh = item % p.Hkv;
-        b = item / p.Hkv;
-    }
+    int item = blockIdx.x;
+    const int s = item % p.NS;
+    item /= p.NS;
+    const int kvh = item % p.Hkv;
+    const int b = item / p.Hkv;
     const int h0 = kvh * p.G;
 
     const int n = clampi(p.ctx[b], 0, p.n_cap);
@@ -324,49 +268,6 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
             }
         }
     }
-    if (direct || !p.fuse) return;
-
-    // ---- fused combine: the last split of this (sequence, KV head) merges all
-    // of them.  Writers' stores reach the CTA barrier, one thread makes them
-    // visible device-wide and counts the arrival.
-    __threadfence();
-    named_bar_sync(1, NWC * 32);
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        __threadfence();
-        bcast[0] = atomicAdd(&p.seg_count[b * p.Hkv + kvh], 1);
-        __threadfence();
-    }
-    named_bar_sync(1, NWC * 32);
-    if (bcast[0] != ns_b - 1) return;
-    constexpr float kLog2e = 1.4426950408889634f;
-    for (int idx = tid; idx < p.G * (D / 4); idx += NWC * 32) {
-        const int h = idx / (D / 4);
-        const int d = (idx % (D / 4)) * 4;
-        const size_t bh = (size_t)b * p.Hq + h0 + h;
-        const float* pm = p.part_m + bh * p.ns_stride;
-        const float* pl = p.part_l + bh * p.ns_stride;
-        const float* pa = p.part_acc + bh * p.ns_stride * D + d;
-        float M = -INFINITY;
-        for (int k = 0; k < ns_b; ++k) M = fmaxf(M, __ldcg(pm + k));
-        float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int k = 0; k < ns_b; ++k) {
-            const float f = ex2((__ldcg(pm + k) - M) * kLog2e);
-            L += f * __ldcg(pl + k);
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(pa + (size_t)k * D));
-            acc.x += f * v.x;
-            acc.y += f * v.y;
-            acc.z += f * v.z;
-            acc.w += f * v.w;
-        }
-        const float inv = 1.f / L;
-        T o4[4] = {from_float<T>(acc.x * inv), from_float<T>(acc.y * inv), from_float<T>(acc.z * inv),
-                   from_float<T>(acc.w * inv)};
-        *reinterpret_cast<uint2*>(reinterpret_cast<T*>(p.out) + bh * D + d) = *reinterpret_cast<uint2*>(o4);
-    }
-    if (tid == 0) p.seg_count[b * p.Hkv + kvh] = 0;   // ready for the next call
 }
 
 // Host-side launcher for one instantiation.

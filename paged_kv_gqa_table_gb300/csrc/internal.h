@@ -43,7 +43,9 @@ struct MlaParams {
 
 cudaError_t launch_mla_prefill(const MlaParams& p, cudaStream_t stream);
 
-cudaError_t launch_combine(int dtype, int D, const CombineParams& p, cudaStream_t stream);
+// after_phase1: launched as a programmatic dependent of the phase-1 kernel just
+// enqueued on the same stream (its prologue overlaps phase 1's tail).
+cudaError_t launch_combine(int dtype, int D, const CombineParams& p, cudaStream_t stream, bool after_phase1);
 cudaError_t launch_validate(const int32_t* table, const int32_t* ctx, int B, int MBPS, int BS, int NB, int max_ctx,
                             uint32_t* err, cudaStream_t stream);
 

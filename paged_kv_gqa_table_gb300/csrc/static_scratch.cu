@@ -55,11 +55,9 @@ int pkv_paged_decode_attention_static(const pkv_decode_desc* desc, const pkv_dec
     void* scratch = nullptr;
     st = scratch_address(&scratch);
     if (st) return st;
-    // What must start at zero: the header's error word and the per-segment
-    // arrival counters that follow it.  The partials are always written
-    // before they are read, so they need no clearing.
-    const size_t counters = ((size_t)desc->B * desc->Hkv * 4 + 255) & ~size_t(255);
-    if (cudaMemsetAsync(scratch, 0, kHeaderBytes + counters, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // The header's error word must start at zero; the partials are fully
+    // written by phase 1 before phase 2 reads them, so they need no clearing.
+    if (cudaMemsetAsync(scratch, 0, kHeaderBytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PKV_CUDA_ERROR;
     return pkv_paged_decode_attention(desc, opts, q, k_cache, v_cache, block_table, context_lens, scale, out,
                                       scratch, kStaticScratchBytes, stream);

@@ -104,12 +104,12 @@ def test_named_workload_plans(B):
 def test_workspace_size(B):
     al = lambda x: (x + 255) // 256 * 256
     d = desc(B)
-    # header | counters [B*Hkv] | m, l [B][Hq][NS] | acc [B][Hq][NS][D]
+    # header | m, l [B][Hq][NS] | acc [B][Hq][NS][D]
     ns, P = B.pkv_plan_splits(d, None, 152)
     rows = 64 * 32 * ns
-    assert B.pkv_decode_workspace_size(d, None, 152) == 256 + al(64 * 8 * 4) + 2 * al(rows * 4) + al(rows * 128 * 4)
+    assert B.pkv_decode_workspace_size(d, None, 152) == 256 + 2 * al(rows * 4) + al(rows * 128 * 4)
     single = B.make_opts(num_splits=1)
-    assert B.pkv_decode_workspace_size(d, single, 152) == 256 + al(64 * 8 * 4)
+    assert B.pkv_decode_workspace_size(d, single, 152) == 256
 
 
 @pytest.mark.parametrize("field,value,status", [

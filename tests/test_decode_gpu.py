@@ -144,13 +144,14 @@ def test_phase1_partials_match_oracle_split_mode(layout, dtype, D, G, P):
     np.testing.assert_allclose((acc / l[..., None])[live], (racc / rl[..., None])[live], rtol=0, atol=TOL[dtype])
 
 
-@pytest.mark.parametrize("dtype,D", [(synth.BF16, 128), (synth.F16, 64), (synth.F16, 256)])
-def test_combine_of_oracle_partials(dtype, D):
+@pytest.mark.parametrize("dtype,D,P", [(synth.BF16, 128, 64), (synth.F16, 64, 64), (synth.F16, 256, 64),
+                                       (synth.BF16, 128, 16), (synth.F16, 64, 16)])
+def test_combine_of_oracle_partials(dtype, D, P):
+    """Phase 2 fed the oracle's partials; P = 16 gives 66 splits (the many-split variant)."""
     B = _binding()
     T = _tensors()
     case = _case(43, B=5, Hq=4, Hkv=2, D=D, block_size=16, dtype=dtype, layout=synth.NHD,
                  context_lens=[0, 1, 77, 400, 1024], max_blocks_per_seq=64)
-    P = 64
     ns = 1024 // P + 2
     rm, rl, racc = oracle.decode_partials(case, P, ns)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()

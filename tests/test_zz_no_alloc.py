@@ -2,8 +2,8 @@
 
 It exists for callers that may not allocate device memory when they run a
 decode step (a plugin's enqueue hook, an engine with a fixed memory pool, a
-latency-critical loop).  It keeps the decode step's scratch (merge counters
-and partial results) in the library's own static device array instead of a
+latency-critical loop).  It keeps the decode step's scratch (error word and
+split partials) in the library's own static device array instead of a
 caller workspace.  These tests call it
 through the C ABI and compare it with the workspace entry point on the same
 inputs, twice in a row with different problems (the array keeps the previous
@@ -38,8 +38,8 @@ def _run_both(case, opts=None):
 def test_static_scratch_matches_workspace_entry_point_twice():
     from paged_kv_gqa_table_gb300 import binding as B
     # Both calls need scratch: their sequences are split, so the split
-    # partials and the merge counters live in the static array (default plan
-    # first, then fixed 512-token partitions).
+    # partials live in the static array (default plan first, then fixed
+    # 512-token partitions).
     first = synth.decode_case(seed=0, B=16, Hq=32, Hkv=8, D=128, block_size=16, dtype=synth.BF16,
                               layout=synth.NHD, ctx_range=(1, 4096), max_blocks_per_seq=256)
     second = synth.decode_case(seed=1, B=24, Hq=24, Hkv=4, D=256, block_size=16, dtype=synth.F16,
