@@ -372,6 +372,154 @@ def run_gpu(args):
     return 0
 
 
+MLA_METRIC = "MLA paged causal prefill: TFLOP/s (algorithmic) and µs/step"
+
+
+def mla_pairs(case):
+    """(query token, visible key) pairs of an MLA prefill batch (bottom-right causal)."""
+    qo, kvp = case["qo_indptr"].astype(np.int64), case["kv_indptr"].astype(np.int64)
+    total = 0
+    for b in range(case["batch"]):
+        q_len, kv_len = int(qo[b + 1] - qo[b]), int(kvp[b + 1] - kvp[b])
+        if kv_len == 0:
+            continue
+        prefix = kv_len - q_len
+        total += q_len * (prefix + 1) + q_len * (q_len - 1) // 2
+    return total
+
+
+def mla_flops(case):
+    """Algorithmic flops: per pair and head, 2 x (576 + 512) for Q.K^T and P.V."""
+    return mla_pairs(case) * case["H"] * 2 * (case["Dc"] + case["Dr"] + case["Dc"])
+
+
+def mla_workload_config(case, name):
+    qo, kvp = case["qo_indptr"], case["kv_indptr"]
+    return {"workload": "%s: %d sequences, q_len %d..%d, kv_len %d..%d (total_q %d, %d cached rows), "
+                        "16 heads, ckv 512 + kpe 64, bf16, page size 1" % (
+                            name, case["batch"], int(np.diff(qo).min()), int(np.diff(qo).max()),
+                            int(np.diff(kvp).min()), int(np.diff(kvp).max()), case["total_q"], int(kvp[-1])),
+            "seed": 0, "flops_per_step": int(mla_flops(case)), "pairs": int(mla_pairs(case)),
+            "sm_scale": case["sm_scale"], "l2": "flushed between steps (256 MiB write)", "accumulate": "fp32"}
+
+
+def mla_cpu_baseline(case, budget_s: float = 15.0):
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    T = case["total_q"]
+    order = np.random.default_rng(3).permutation(T)
+    out = np.empty((T, case["H"], case["Dc"]))
+    lse = np.empty((T, case["H"]))
+
+    def run(tokens):
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda t: oracle.mla(case, int(t), int(t) + 1, out=out, lse=lse), tokens))
+        return time.perf_counter() - t0
+
+    n = min(T, threads * 2)
+    secs = run(order[:n])
+    m = min(T, max(n, int(n * budget_s / 4 / max(secs, 1e-3))))
+    if m > n:
+        secs = run(order[:m])
+        n = m
+    sub = dict(case)
+    qo, kvp = case["qo_indptr"], case["kv_indptr"]
+    # flops of the sampled tokens
+    b_of = np.searchsorted(qo, order[:n], side="right") - 1
+    pairs = 0
+    for t, b in zip(order[:n], b_of):
+        q_len, kv_len = qo[b + 1] - qo[b], kvp[b + 1] - kvp[b]
+        pairs += (kv_len - q_len) + (t - qo[b]) + 1
+    flops = pairs * case["H"] * 2 * (2 * case["Dc"] + case["Dr"])
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d query tokens (all heads), %.1f s" % (n, T, secs)}
+
+
+def run_mla(args):
+    """The MLA prefill workload (one call per step), same timing rules as the decode arm."""
+    import torch
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    from paged_kv_gqa_table_gb300 import binding as B
+    from paged_kv_gqa_table_gb300 import synth, tensors
+    B.load()
+    case = synth.mla_case(seed=0, **synth.MLA_WORKLOADS[args.workload])
+    flops = mla_flops(case)
+    dev = tensors.upload_mla_case(case, device)
+    T, H, Dc = case["total_q"], case["H"], case["Dc"]
+    out = torch.empty((T, H, Dc), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((T, H), dtype=torch.float32, device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    starts, stops = [ev() for _ in range(args.steps)], [ev() for _ in range(args.steps)]
+    step = lambda: tensors.mla_paged_prefill(case, dev, out, lse, stream=stream)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        stops[i].record(stream)
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    t = sum(a.elapsed_time(b) for a, b in zip(starts, stops)) * 1e-3
+    e2e = None
+    if not args.skip_e2e:
+        host = {k: v.cpu().pin_memory() for k, v in dev.items()}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in host.values())
+        d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+        n_e2e = max(3, min(args.steps, 30))
+        for i in range(n_e2e + 2):
+            if i == 2:
+                torch.cuda.synchronize(device)
+                e0 = ev()
+                e0.record(stream)
+            for k in dev:
+                dev[k].copy_(host[k], non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+        e1 = ev()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        t_e2e = e0.elapsed_time(e1) * 1e-3
+        e2e = {"value": flops * n_e2e / t_e2e / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": n_e2e}
+    pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(pk.get("bf16_tflops", 1900.0))
+    achieved = flops / (t / args.steps) / 1e12
+    line = {"metric": MLA_METRIC, "value": achieved, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
+            "config": mla_workload_config(case, args.workload), "us_per_step": t / args.steps * 1e6,
+            "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None, "kernel": "mla_prefill_kernel",
+                         "peak_source": "measured" if pk else "fallback",
+                         "algorithmic_flops_per_launch": int(flops), "avg_launch_us": t / args.steps * 1e6},
+            "wall_s_timed_region": wall}
+    if not args.skip_cpu_baseline:
+        line["cpu_baseline"] = mla_cpu_baseline(case)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -379,12 +527,17 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b_decode",
-                    choices=["llama3_8b_decode", "long_context_decode", "gqa6_d256_vllm_decode", "tiny"])
+                    choices=["llama3_8b_decode", "long_context_decode", "gqa6_d256_vllm_decode", "tiny",
+                             "mla_prefill_h16"])
     ap.add_argument("--skip-e2e", action="store_true", help="omit the end-to-end leg (profiling runs)")
     ap.add_argument("--skip-cpu-baseline", action="store_true", help="omit the CPU oracle leg (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.workload == "mla_prefill_h16":
+        if args.impl == "reference":
+            ap.error("the reference arm covers the decode workloads")
+        return run_mla(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
