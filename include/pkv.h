@@ -191,7 +191,18 @@ typedef struct {
     int d_kpe;      /* rope (kpe) width: 64 */
     int batch;      /* sequences; qo_indptr and kv_indptr hold batch + 1 entries */
     int num_pages;  /* rows of ckv_cache and kpe_cache */
+    int nnz;        /* kv_indptr[batch] (entries of kv_indices), or an upper bound of it */
 } pkv_mla_desc;
+
+/*
+ * Bytes of scratch memory pkv_mla_paged_prefill needs: a 256-byte header,
+ * then nnz staged key rows of 1152 bytes (ckv 512 + kpe 64 bf16), rounded
+ * up to 256 bytes.  The workspace must be 256-byte aligned.  Word 0 of the
+ * header collects device-side error bits (bit 0: a pipeline wait timed out;
+ * bit 1: kv_indptr[batch] > nnz, so keys past nnz were not staged and the
+ * result is unspecified); zero it once after allocating.
+ */
+int pkv_mla_workspace_size(const pkv_mla_desc* desc, size_t* bytes);
 
 /*
  * MLA paged causal prefill ([MLA] run / _forward and the kernel's sections
@@ -210,13 +221,22 @@ typedef struct {
  * Tensors 16-byte aligned (lse 4-byte).  kv_len < q_len is a caller error
  * (rows with no visible key get out = 0, lse = -inf); page ids outside
  * [0, num_pages) are clamped to page 0 (no out-of-bounds access, result
- * unspecified).  No workspace: the q -> sequence map of [MLA]'s host loop is
- * computed on the device from qo_indptr.
+ * unspecified).  Rows that kv_indices references must be finite: a row a
+ * query does not see still enters the tensor-core products with weight 0.
+ * The q -> sequence map of [MLA]'s host loop is computed on the device from
+ * qo_indptr.
+ * Two kernels run: the first copies every referenced key row, in kv_indptr
+ * order, into the workspace (one gather per call instead of one per query
+ * tile); the second, launched as its programmatic dependent, streams those
+ * rows with 16 KB tensor-memory-access boxes.  workspace / workspace_bytes as
+ * pkv_mla_workspace_size describes; calls sharing one workspace must be
+ * ordered on the GPU (one stream).
  */
 int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const void* q_pe,
                           const void* ckv_cache, const void* kpe_cache, const int32_t* qo_indptr,
                           const int32_t* kv_indptr, const int32_t* kv_indices, float sm_scale,
-                          void* out, float* lse, pkv_stream_t stream);
+                          void* out, float* lse, void* workspace, size_t workspace_bytes,
+                          pkv_stream_t stream);
 
 /*
  * pkv_paged_decode_attention_static -- the same decode step as

@@ -20,7 +20,7 @@ PKV_LAYOUT_NHD, PKV_LAYOUT_VLLM = 0, 1
 FUNCTIONS = [
     "pkv_status_string", "pkv_version", "pkv_plan_splits", "pkv_decode_workspace_size",
     "pkv_paged_decode_attention", "pkv_decode_partials", "pkv_combine", "pkv_validate_block_table",
-    "pkv_paged_decode_attention_static", "pkv_mla_paged_prefill",
+    "pkv_paged_decode_attention_static", "pkv_mla_workspace_size", "pkv_mla_paged_prefill",
 ]
 PKV_STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -39,7 +39,8 @@ class pkv_decode_opts(ctypes.Structure):
 
 class pkv_mla_desc(ctypes.Structure):
     _fields_ = [("total_q", ctypes.c_int), ("num_heads", ctypes.c_int), ("d_ckv", ctypes.c_int),
-                ("d_kpe", ctypes.c_int), ("batch", ctypes.c_int), ("num_pages", ctypes.c_int)]
+                ("d_kpe", ctypes.c_int), ("batch", ctypes.c_int), ("num_pages", ctypes.c_int),
+                ("nnz", ctypes.c_int)]
 
 
 class PkvError(RuntimeError):
@@ -70,8 +71,9 @@ def load():
     lib.pkv_combine.argtypes = [D, I, I, P, P, P, P, P, P]
     lib.pkv_validate_block_table.argtypes = [D, P, P, P, P]
     lib.pkv_paged_decode_attention_static.argtypes = [D, O, P, P, P, P, P, ctypes.c_float, P, P]
+    lib.pkv_mla_workspace_size.argtypes = [ctypes.POINTER(pkv_mla_desc), ctypes.POINTER(SZ)]
     lib.pkv_mla_paged_prefill.argtypes = [ctypes.POINTER(pkv_mla_desc), P, P, P, P, P, P, P, ctypes.c_float,
-                                          P, P, P]
+                                          P, P, P, SZ, P]
     for f in FUNCTIONS[2:]:
         getattr(lib, f).restype = I
     _lib = lib
@@ -174,15 +176,25 @@ def pkv_paged_decode_attention_static(desc, q, k_cache, v_cache, block_table, co
         _ptr(context_lens), float(scale), _ptr(out), _stream(stream)))
 
 
-def make_mla_desc(total_q, batch, num_pages, num_heads=16, d_ckv=512, d_kpe=64) -> pkv_mla_desc:
-    return pkv_mla_desc(int(total_q), int(num_heads), int(d_ckv), int(d_kpe), int(batch), int(num_pages))
+def make_mla_desc(total_q, batch, num_pages, nnz, num_heads=16, d_ckv=512, d_kpe=64) -> pkv_mla_desc:
+    return pkv_mla_desc(int(total_q), int(num_heads), int(d_ckv), int(d_kpe), int(batch), int(num_pages),
+                        int(nnz))
+
+
+def pkv_mla_workspace_size(desc) -> int:
+    n = ctypes.c_size_t(0)
+    _check("pkv_mla_workspace_size", load().pkv_mla_workspace_size(ctypes.byref(desc), ctypes.byref(n)))
+    return n.value
 
 
 def pkv_mla_paged_prefill(desc, q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr, kv_indices, sm_scale,
-                          out, lse, stream=None) -> None:
+                          out, lse, workspace, workspace_bytes=None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
     _check("pkv_mla_paged_prefill", load().pkv_mla_paged_prefill(
         ctypes.byref(desc), _ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache), _ptr(qo_indptr),
-        _ptr(kv_indptr), _ptr(kv_indices), float(sm_scale), _ptr(out), _ptr(lse), _stream(stream)))
+        _ptr(kv_indptr), _ptr(kv_indices), float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        int(workspace_bytes), _stream(stream)))
 
 
 def pkv_validate_block_table(desc, block_table, context_lens, err_word, stream=None) -> None:

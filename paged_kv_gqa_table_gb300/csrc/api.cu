@@ -4,6 +4,7 @@
 #include <climits>
 #include <cmath>
 #include <cudaTypedefs.h>
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -159,6 +160,20 @@ int encode_cache_map(CUtensorMap* map, const void* base, const pkv_decode_desc* 
     }
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_INVALID_ARG;
+}
+
+// Row-major 2-D bf16 tensor {cols, rows} with a {box_cols, box_rows} box and
+// 128-byte swizzle (box_cols * 2 <= 128).
+int encode_rows_map(CUtensorMap* map, const void* base, cuuint64_t cols, cuuint64_t rows, cuuint32_t box_cols,
+                    cuuint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return PKV_CUDA_ERROR;
+    cuuint64_t dims[2] = {cols, rows}, strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows}, estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PKV_OK : PKV_INVALID_ARG;
 }
@@ -361,24 +376,47 @@ int pkv_validate_block_table(const pkv_decode_desc* desc, const int32_t* block_t
                : PKV_CUDA_ERROR;
 }
 
-int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const void* q_pe, const void* ckv_cache,
-                          const void* kpe_cache, const int32_t* qo_indptr, const int32_t* kv_indptr,
-                          const int32_t* kv_indices, float sm_scale, void* out, float* lse, pkv_stream_t stream) {
+static int check_mla_desc(const pkv_mla_desc* desc) {
     if (!desc) return PKV_INVALID_ARG;
     const pkv_mla_desc& d = *desc;
-    if (d.total_q < 0 || d.batch < 0 || d.num_pages < 0 || d.num_heads <= 0 || d.d_ckv <= 0 || d.d_kpe <= 0)
+    if (d.total_q < 0 || d.batch < 0 || d.num_pages < 0 || d.nnz < 0 || d.num_heads <= 0 || d.d_ckv <= 0 ||
+        d.d_kpe <= 0)
         return PKV_INVALID_ARG;
     if (d.total_q > 0 && d.batch == 0) return PKV_INVALID_ARG;
     if (d.num_heads != 16 || d.d_ckv != 512 || d.d_kpe != 64) return PKV_UNSUPPORTED;
     if ((long long)d.total_q * d.num_heads * d.d_ckv > (long long)1 << 40) return PKV_UNSUPPORTED;
+    return PKV_OK;
+}
+
+static size_t mla_workspace_bytes(const pkv_mla_desc& d) {
+    return kHeaderBytes + align256((size_t)d.nnz * kMlaStageRowBytes);
+}
+
+int pkv_mla_workspace_size(const pkv_mla_desc* desc, size_t* bytes) {
+    const int st = check_mla_desc(desc);
+    if (st != PKV_OK) return st;
+    if (!bytes) return PKV_INVALID_ARG;
+    *bytes = mla_workspace_bytes(*desc);
+    return PKV_OK;
+}
+
+int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                          const void* kpe_cache, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                          const int32_t* kv_indices, float sm_scale, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, pkv_stream_t stream) {
+    int st = check_mla_desc(desc);
+    if (st != PKV_OK) return st;
+    const pkv_mla_desc& d = *desc;
     if (!std::isfinite(sm_scale)) return PKV_INVALID_ARG;
     if (d.total_q == 0) return PKV_OK;
-    if (!q_nope || !q_pe || !qo_indptr || !kv_indptr || !out || !lse) return PKV_INVALID_ARG;
-    if (d.num_pages > 0 && (!ckv_cache || !kpe_cache || !kv_indices)) return PKV_INVALID_ARG;
+    if (!q_nope || !q_pe || !qo_indptr || !kv_indptr || !out || !lse || !workspace) return PKV_INVALID_ARG;
+    if (d.num_pages > 0 && d.nnz > 0 && (!ckv_cache || !kpe_cache || !kv_indices)) return PKV_INVALID_ARG;
     if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
         !aligned(qo_indptr, 4) || !aligned(kv_indptr, 4) || (ckv_cache && !aligned(ckv_cache, 16)) ||
-        (kpe_cache && !aligned(kpe_cache, 16)) || (kv_indices && !aligned(kv_indices, 4)))
+        (kpe_cache && !aligned(kpe_cache, 16)) || (kv_indices && !aligned(kv_indices, 4)) ||
+        !aligned(workspace, 256))
         return PKV_INVALID_ARG;
+    if (workspace_bytes < mla_workspace_bytes(d)) return PKV_WORKSPACE_TOO_SMALL;
     MlaParams p{};
     p.q_nope = static_cast<const __nv_bfloat16*>(q_nope);
     p.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
@@ -389,11 +427,22 @@ int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const vo
     p.kv_indices = kv_indices;
     p.out = static_cast<__nv_bfloat16*>(out);
     p.lse = lse;
+    p.err = static_cast<uint32_t*>(workspace);
+    p.stage = static_cast<uint8_t*>(workspace) + kHeaderBytes;
     p.total_q = d.total_q;
     p.batch = d.batch;
     p.num_pages = d.num_pages;
+    p.nnz = d.nnz;
     p.scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
-    return launch_mla_prefill(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_CUDA_ERROR;
+    MlaMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    const cuuint64_t q_rows = (cuuint64_t)d.total_q * 16;
+    st = encode_rows_map(&maps.q_nope, q_nope, 512, q_rows, 64, 128);
+    if (st == PKV_OK) st = encode_rows_map(&maps.q_pe, q_pe, 64, q_rows, 64, 128);
+    if (st == PKV_OK && d.num_pages > 0 && d.nnz > 0) st = encode_rows_map(&maps.kv, p.stage, 576, (cuuint64_t)d.nnz, 64, 128);
+    if (st != PKV_OK) return st;
+    return launch_mla_prefill(p, maps, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK
+                                                                                              : PKV_CUDA_ERROR;
 }
 
 }  // extern "C"

@@ -34,14 +34,25 @@ struct MlaParams {
     const __nv_bfloat16* kpe;      // [num_pages][64]
     const int32_t* qo_indptr;      // [batch + 1]
     const int32_t* kv_indptr;      // [batch + 1]
-    const int32_t* kv_indices;     // [nnz]
+    const int32_t* kv_indices;     // [kv_indptr[batch]]
     __nv_bfloat16* out;            // [total_q][16][512]
     float* lse;                    // [total_q][16]
-    int total_q, batch, num_pages;
+    uint8_t* stage;                // [nnz][1152]: ckv row | kpe row of key r in kv_indptr order
+    uint32_t* err;                 // header word 0
+    int total_q, batch, num_pages, nnz;
     float scale_log2;              // sm_scale * log2(e)
 };
 
-cudaError_t launch_mla_prefill(const MlaParams& p, cudaStream_t stream);
+constexpr int kMlaStageRowBytes = (512 + 64) * 2;
+
+// TMA descriptors of the MLA operands: q_nope / q_pe as 2-D {512 | 64,
+// total_q * 16} tensors and the staged keys as {576, nnz}, all with {64, 128}
+// boxes and 128-byte swizzle.  kv is unused (zero) when the pool is empty.
+struct MlaMaps {
+    CUtensorMap q_nope, q_pe, kv;
+};
+
+cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStream_t stream);
 
 // after_phase1: launched as a programmatic dependent of the phase-1 kernel just
 // enqueued on the same stream (its prologue overlaps phase 1's tail).

@@ -13,20 +13,33 @@
 // that shares each gathered key row.
 //
 // CTA = (sequence, 8-token row tile, half of the 512 output columns).  TMEM
-// (512 columns x 128 lanes, fp32) holds two S tiles of 128 keys (double
-// buffer) and the CTA's 256 output columns, which is why the output is split
-// across two CTAs that each recompute S.  Shared memory holds the whole Q
-// tile (9 chunks of 128 rows x 64 bf16 = 144 KB), a 3-stage ring of 16 KB
-// key chunks (128 gathered rows x 64 bf16) and the bf16 P tile (32 KB), all
-// in the 128-byte-swizzled layout the UMMA descriptors describe.  A ckv chunk
-// serves as the K-major B operand of S = Q.K^T and, re-described MN-major,
-// as the B operand V of O = P.V.
+// (512 columns x 128 lanes, fp32) holds the CTA's 256 output columns O, one
+// S tile of 128 keys and two bf16 P tiles (the A operand of O += P.V, read
+// from TMEM), which is why the output is split across two CTAs that each
+// recompute S.  Shared memory holds the whole Q tile (9 chunks of 128 rows x
+// 64 bf16 = 144 KB, one 2-D TMA box each) and a 5-stage ring of 16 KB key
+// chunks (128 key rows x 64 bf16), all in the 128-byte-swizzled layout the
+// UMMA descriptors describe.  A ckv chunk serves as the K-major B operand of
+// S = Q.K^T and, re-described MN-major, as the B operand V of O = P.V.
 //
-// Warps: 0 = producer (cp.async gathers rows through kv_indices, zero-filling
-// rows past the visible range); 1 = TMEM allocator and single-thread MMA
-// issuer; 2..5 = softmax (one thread per row / TMEM lane): online max/sum in
-// log2 units, lazy O rescaling (only when the running max grows by more than
-// 8, i.e. a factor 256), P written as bf16, final O / l and the base-2 LSE.
+// Page size 1 makes every key its own page.  Gathering 128-byte row pieces
+// per tile (up to ~100 tiles read each key) keeps too few bytes in flight
+// per TMA operation, so mla_stage_kernel first copies each referenced row
+// (ckv | kpe, 1152 bytes) once into a workspace in kv_indptr order; the
+// attention kernel then loads 128 consecutive staged rows per 16 KB box.
+// Rows of a box past the tile's keys are the next sequence's keys (finite
+// by contract), zero rows the stage kernel wrote past the last key, or
+// out-of-range rows TMA fills with zeros; they are masked in the softmax.
+//
+// Warps: 0 = producer (one thread issues the Q boxes and then, after the
+// staging grid has completed, the key boxes); 1 = TMEM allocator and
+// single-thread MMA issuer;
+// 2..5 = softmax (one thread per row / TMEM lane): online max/sum in log2
+// units, lazy O rescaling (only when the running max grows by more than 8,
+// i.e. a factor 256), P stored to TMEM as bf16, final O / l and the base-2
+// LSE.
+#include <algorithm>
+
 #include "internal.h"
 #include "tcgen05.cuh"
 
@@ -40,32 +53,63 @@ constexpr int kKeys = 128;              // keys per block
 constexpr int kChunk = kRows * 64 * 2;  // 16 KB: 128 rows x 64 bf16
 constexpr int kQChunks = 9;             // 8 x ckv + 1 x kpe
 constexpr int kVChunks = 4;             // 256 output columns / 64
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kThreads = 192;
 constexpr int kBars = 2 * kStages + 8;
-constexpr int kSmemBytes = 1024 + (kQChunks + kStages + 2) * kChunk + kBars * 8 + 2 * kKeys * 4 + 16;
+constexpr int kSmemBytes = 1024 + (kQChunks + kStages) * kChunk + kBars * 8 + 16;
+constexpr uint32_t kColS = 256, kColP = 384;   // TMEM columns: O [0,256), S [256,384), P x2 [384,512)
 constexpr float kLazyRescale = 8.f;     // log2 units
 }  // namespace mla
 
 
-__global__ void __launch_bounds__(mla::kThreads, 1) mla_prefill_kernel(const MlaParams p) {
+// staged[r] = ckv[kv_indices[r]] | kpe[kv_indices[r]] for r < min(kv_indptr[batch], nnz),
+// then zeros for the next 128 rows (within nnz), which a box that starts at a
+// sequence's last keys can reach.  One warp per row.
+__global__ void __launch_bounds__(256) mla_stage_kernel(const MlaParams p) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int total = p.kv_indptr[p.batch];
+    const int rows = min(total, p.nnz);
+    const int zero_end = total > p.nnz ? rows : (rows > p.nnz - 128 ? p.nnz : max(rows, 0) + 128);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && total > p.nnz) atomicOr(p.err, 2u);
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < zero_end; r += warps) {
+        uint4* dst = reinterpret_cast<uint4*>(p.stage + (size_t)r * kMlaStageRowBytes);
+        uint4 a = zero, b = zero, c = zero;
+        if (r < rows) {
+            int pg = p.kv_indices[r];
+            pg = (pg < 0 || pg >= p.num_pages) ? 0 : pg;
+            const uint4* ck = reinterpret_cast<const uint4*>(p.ckv + (size_t)pg * mla::kDc);
+            const uint4* kp = reinterpret_cast<const uint4*>(p.kpe + (size_t)pg * mla::kDr);
+            a = __ldg(ck + lane);
+            b = __ldg(ck + 32 + lane);
+            if (lane < 8) c = __ldg(kp + lane);
+        }
+        dst[lane] = a;
+        dst[32 + lane] = b;
+        if (lane < 8) dst[64 + lane] = c;
+    }
+}
+
+__global__ void __launch_bounds__(mla::kThreads, 1)
+    mla_prefill_kernel(const MlaParams p, const __grid_constant__ CUtensorMap tm_qn,
+                       const __grid_constant__ CUtensorMap tm_qp, const __grid_constant__ CUtensorMap tm_kv) {
     using namespace mla;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;
     uint8_t* sRing = sQ + kQChunks * kChunk;
-    uint8_t* sP = sRing + kStages * kChunk;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kChunk);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + kStages * kChunk);
     uint64_t* ring_full = bars;
     uint64_t* ring_empty = bars + kStages;
     uint64_t* q_full = bars + 2 * kStages;
-    uint64_t* s_full = q_full + 1;     // [2]
-    uint64_t* s_free = s_full + 2;     // [2]
-    uint64_t* p_full = s_free + 2;
-    uint64_t* p_free = p_full + 1;
-    uint64_t* mma_done = p_free + 1;
-    int32_t* s_pages = reinterpret_cast<int32_t*>(bars + kBars);   // [2][kKeys]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_pages + 2 * kKeys);
+    uint64_t* s_full = q_full + 1;
+    uint64_t* s_free = s_full + 1;
+    uint64_t* p_full = s_free + 1;     // [2]
+    uint64_t* p_free = p_full + 2;     // [2]
+    uint64_t* mma_done = p_free + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -89,8 +133,8 @@ __global__ void __launch_bounds__(mla::kThreads, 1) mla_prefill_kernel(const Mla
     const int kv0 = p.kv_indptr[b], kv_len = p.kv_indptr[b + 1] - kv0;
     const int prefix = kv_len - q_len;
     const int ntok = min(kTok, q_len - i0);
-    // keys any row of the tile may see (none when the pool is empty)
-    const int n_keys = p.num_pages > 0 ? max(0, min(kv_len, prefix + i0 + ntok)) : 0;
+    // keys any row of the tile may see (none when the pool or the staging area is empty)
+    const int n_keys = (p.num_pages > 0 && p.nnz > 0) ? max(0, min(kv_len, prefix + i0 + ntok)) : 0;
     const int J = (n_keys + kKeys - 1) / kKeys;
 
     if (J == 0) {   // no visible key (empty KV): out = 0, lse = -inf
@@ -106,16 +150,16 @@ __global__ void __launch_bounds__(mla::kThreads, 1) mla_prefill_kernel(const Mla
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&ring_full[i], 32);
+            mbar_init(&ring_full[i], 1);
             mbar_init(&ring_empty[i], 1);
         }
-        mbar_init(q_full, 32);
+        mbar_init(q_full, 1);
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 128);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 128);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&p_free[i], 1);
         }
-        mbar_init(p_full, 128);
-        mbar_init(p_free, 1);
         mbar_init(mma_done, 1);
         fence_barrier_init();
         *abort_flag = 0;
@@ -131,88 +175,54 @@ __global__ void __launch_bounds__(mla::kThreads, 1) mla_prefill_kernel(const Mla
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        const __nv_bfloat16* qn_base = p.q_nope + (size_t)(q0 + i0) * kHeads * kDc;
-        const __nv_bfloat16* qp_base = p.q_pe + (size_t)(q0 + i0) * kHeads * kDr;
-        for (int idx = lane; idx < kRows * kQChunks * 8; idx += 32) {
-            const int r = idx / (kQChunks * 8), rem = idx % (kQChunks * 8);
-            const int c = rem >> 3, piece = rem & 7;
-            const bool ok = r / kHeads < ntok;
-            const __nv_bfloat16* src = c < 8 ? qn_base + (size_t)r * kDc + c * 64 + piece * 8
-                                             : qp_base + (size_t)r * kDr + piece * 8;
-            cp_async16(smem_u32(sQ + c * kChunk + r * 128 + ((piece ^ (r & 7)) << 4)), ok ? src : p.q_nope,
-                       ok ? 16u : 0u);
+        if (lane == 0) {
+            prefetch_tensormap(&tm_kv);
+            const int y = (q0 + i0) * kHeads;   // rows past the tensor are zero-filled
+            mbar_arrive_expect_tx(q_full, kQChunks * kChunk);
+            for (int c = 0; c < kQChunks - 1; ++c) tma_load_2d(sQ + c * kChunk, &tm_qn, q_full, c * 64, y);
+            tma_load_2d(sQ + (kQChunks - 1) * kChunk, &tm_qp, q_full, 0, y);
+            // the staged keys are written by the preceding grid
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            bool ok = true;
+            int k = 0;   // running chunk index (same order as the MMA issuer consumes them)
+            auto load_chunk = [&](int jb, int x) -> bool {
+                const int stage = k % kStages;
+                if (k >= kStages && !(mbar_wait(&ring_empty[stage], ((k / kStages) - 1) & 1) && *abort_flag == 0))
+                    return false;
+                mbar_arrive_expect_tx(&ring_full[stage], kChunk);
+                tma_load_2d(sRing + stage * kChunk, &tm_kv, &ring_full[stage], x, kv0 + jb * kKeys);
+                ++k;
+                return true;
+            };
+            for (int step = 0; step <= J && ok; ++step) {
+                if (step < J)
+                    for (int c = 0; c < kQChunks && ok; ++c) ok = load_chunk(step, c * 64);
+                if (step >= 1)
+                    for (int v = 0; v < kVChunks && ok; ++v) ok = load_chunk(step - 1, (half * kVChunks + v) * 64);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(p.err, kErrTimeout);
+            }
+            // Never leave with copies in flight: wait for the last fill of
+            // every stage and for Q (immediate unless the pipeline aborted).
+            for (int kk = max(0, k - kStages); kk < k; ++kk) mbar_wait(&ring_full[kk % kStages], (kk / kStages) & 1);
+            mbar_wait(q_full, 0);
         }
-        cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(q_full);
-
-        bool ok = true;
-        int k = 0;   // running chunk index (same order as the MMA issuer consumes them)
-        auto retire = [&](int kk) {
-            fence_proxy_async_smem();
-            mbar_arrive(&ring_full[kk % kStages]);
-        };
-        auto load_chunk = [&](int jb, int c) -> bool {
-            const int stage = k % kStages;
-            if (k >= kStages) {
-                const bool got = mbar_wait(&ring_empty[stage], ((k / kStages) - 1) & 1);
-                if (!__all_sync(0xffffffffu, got && *abort_flag == 0)) return false;
-            }
-            const int32_t* pages = s_pages + (jb & 1) * kKeys;
-            uint8_t* dst = sRing + stage * kChunk;
-            for (int idx = lane; idx < kKeys * 8; idx += 32) {
-                const int row = idx >> 3, piece = idx & 7;
-                const bool live = jb * kKeys + row < n_keys;
-                const int page = pages[row];
-                const __nv_bfloat16* src = c < 8 ? p.ckv + (size_t)page * kDc + c * 64 + piece * 8
-                                                 : p.kpe + (size_t)page * kDr + piece * 8;
-                cp_async16(smem_u32(dst + row * 128 + ((piece ^ (row & 7)) << 4)), live ? src : p.ckv,
-                           live ? 16u : 0u);
-            }
-            cp_async_commit();
-            if (k >= kStages - 1) {
-                cp_async_wait<kStages - 1>();
-                retire(k - (kStages - 1));
-            }
-            ++k;
-            return true;
-        };
-        for (int step = 0; step <= J && ok; ++step) {
-            if (step < J) {
-                // page ids of key block `step` (clamped into the pool)
-                __syncwarp();
-                for (int row = lane; row < kKeys; row += 32) {
-                    const int key = step * kKeys + row;
-                    int pg = key < n_keys ? p.kv_indices[kv0 + key] : 0;
-                    pg = (pg < 0 || pg >= p.num_pages) ? 0 : pg;
-                    s_pages[(step & 1) * kKeys + row] = pg;
-                }
-                __syncwarp();
-                for (int c = 0; c < kQChunks && ok; ++c) ok = load_chunk(step, c);
-            }
-            if (step >= 1)
-                for (int v = 0; v < kVChunks && ok; ++v) ok = load_chunk(step - 1, half * kVChunks + v);
-        }
-        cp_async_wait<0>();
-        if (ok)
-            for (int kk = max(0, k - (kStages - 1)); kk < k; ++kk) retire(kk);
-        else
-            *abort_flag = 1;
+        __syncwarp();
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc_qk = umma_idesc_bf16_f32(kRows, kKeys, false);
             const uint32_t idesc_pv = umma_idesc_bf16_f32(kRows, 64, true);
-            const uint32_t q_addr = smem_u32(sQ), ring_addr = smem_u32(sRing), p_addr = smem_u32(sP);
+            const uint32_t q_addr = smem_u32(sQ), ring_addr = smem_u32(sRing);
             bool ok = mbar_wait(q_full, 0);
             tc_fence_after();
             int k = 0;
             for (int step = 0; step <= J && ok; ++step) {
                 if (step < J) {
-                    const int sb = step & 1;
-                    if (step >= 2) {
-                        ok = mbar_wait(&s_free[sb], ((step >> 1) - 1) & 1) && *abort_flag == 0;
+                    if (step >= 1) {   // softmax has read S(step - 1)
+                        ok = mbar_wait(s_free, (step - 1) & 1) && *abort_flag == 0;
                         tc_fence_after();
                     }
                     for (int c = 0; c < kQChunks && ok; ++c, ++k) {
@@ -222,17 +232,16 @@ __global__ void __launch_bounds__(mla::kThreads, 1) mla_prefill_kernel(const Mla
                         if (!ok) break;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            umma_bf16(tmem + sb * kKeys,
-                                      umma_desc_sw128(q_addr + c * kChunk + kk * 32, 16, 1024),
+                            umma_bf16(tmem + kColS, umma_desc_sw128(q_addr + c * kChunk + kk * 32, 16, 1024),
                                       umma_desc_sw128(ring_addr + stage * kChunk + kk * 32, 16, 1024), idesc_qk,
                                       (c | kk) != 0);
                         umma_commit(&ring_empty[stage]);
                     }
-                    if (ok) umma_commit(&s_full[sb]);
+                    if (ok) umma_commit(s_full);
                 }
                 if (step >= 1 && ok) {
-                    const int jb = step - 1;
-                    ok = mbar_wait(p_full, jb & 1) && *abort_flag == 0;
+                    const int jb = step - 1, pb = jb & 1;
+                    ok = mbar_wait(&p_full[pb], (jb >> 1) & 1) && *abort_flag == 0;
                     tc_fence_after();
                     for (int v = 0; v < kVChunks && ok; ++v, ++k) {
                         const int stage = k % kStages;
@@ -241,16 +250,18 @@ __global__ void __launch_bounds__(mla::kThreads, 1) mla_prefill_kernel(const Mla
                         if (!ok) break;
 #pragma unroll
                         for (int kk = 0; kk < kKeys / 16; ++kk)
-                            umma_bf16(tmem + 2 * kKeys + v * 64,
-                                      umma_desc_sw128(p_addr + (kk >> 2) * kChunk + (kk & 3) * 32, 16, 1024),
-                                      umma_desc_sw128(ring_addr + stage * kChunk + kk * 2048, kChunk, 1024),
-                                      idesc_pv, jb > 0 || kk > 0);
+                            umma_bf16_tmem_a(tmem + v * 64, tmem + kColP + pb * 64 + kk * 8,
+                                             umma_desc_sw128(ring_addr + stage * kChunk + kk * 2048, kChunk, 1024),
+                                             idesc_pv, jb > 0 || kk > 0);
                         umma_commit(&ring_empty[stage]);
                     }
-                    if (ok) umma_commit(p_free);
+                    if (ok) umma_commit(&p_free[pb]);
                 }
             }
-            if (!ok) *abort_flag = 1;
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(p.err, kErrTimeout);
+            }
             // never release TMEM with MMAs in flight
             umma_commit(mma_done);
             mbar_wait(mma_done, 0);
@@ -266,8 +277,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1) mla_prefill_kernel(const Mla
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < J; ++j) {
-            const int sb = j & 1;
-            const bool got = mbar_wait(&s_full[sb], (j >> 1) & 1);
+            const bool got = mbar_wait(s_full, j & 1);
             if (!__all_sync(0xffffffffu, got && *abort_flag == 0)) {
                 ok = false;
                 break;
@@ -277,13 +287,13 @@ __global__ void __launch_bounds__(mla::kThreads, 1) mla_prefill_kernel(const Mla
 #pragma unroll
             for (int c = 0; c < kKeys / 32; ++c) {
                 float v[32];
-                tmem_ld32(t_row + sb * kKeys + c * 32, v);
+                tmem_ld32(t_row + kColS + c * 32, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
             }
             tc_fence_before();
-            mbar_arrive(&s_free[sb]);
+            mbar_arrive(s_free);
 
             float mx = -INFINITY;
 #pragma unroll
@@ -307,43 +317,47 @@ __global__ void __launch_bounds__(mla::kThreads, 1) mla_prefill_kernel(const Mla
             l = l * alpha + ls;
             m = m_use;
 
-            if (j >= 1) {
-                // P(j-1) has been consumed and O holds it: rescale O, reuse P.
-                const bool got2 = mbar_wait(p_free, (j - 1) & 1);
-                if (!__all_sync(0xffffffffu, got2 && *abort_flag == 0)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            const int pb = j & 1;
+            bool got2 = true;
+            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                // O holds P(j-1).V: wait for it, then rescale this warp's rows.
+                got2 = mbar_wait(&p_free[pb ^ 1], ((j - 1) >> 1) & 1);
+                if (__all_sync(0xffffffffu, got2 && *abort_flag == 0)) {
+                    tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 256 / 32; ++c) {
                         float o[32];
-                        tmem_ld32(t_row + 2 * kKeys + c * 32, o);
+                        tmem_ld32(t_row + c * 32, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(t_row + 2 * kKeys + c * 32, o);
+                        tmem_st32(t_row + c * 32, o);
                     }
                     tmem_wait_st();
                 }
+            } else if (j >= 2) {
+                // P buffer pb was last read by P(j-2).V
+                got2 = mbar_wait(&p_free[pb], ((j - 2) >> 1) & 1);
+                tc_fence_after();
+            }
+            if (!__all_sync(0xffffffffu, got2 && *abort_flag == 0)) {
+                ok = false;
+                break;
             }
 #pragma unroll
-            for (int pc = 0; pc < kKeys / 8; ++pc) {
-                uint4 v;
-                v.x = Mma<__nv_bfloat16>::pack(s[pc * 8 + 0], s[pc * 8 + 1]);
-                v.y = Mma<__nv_bfloat16>::pack(s[pc * 8 + 2], s[pc * 8 + 3]);
-                v.z = Mma<__nv_bfloat16>::pack(s[pc * 8 + 4], s[pc * 8 + 5]);
-                v.w = Mma<__nv_bfloat16>::pack(s[pc * 8 + 6], s[pc * 8 + 7]);
-                const int khalf = pc >> 3, piece = pc & 7;
-                *reinterpret_cast<uint4*>(sP + khalf * kChunk + row * 128 + ((piece ^ (row & 7)) << 4)) = v;
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    pk[i] = Mma<__nv_bfloat16>::pack(s[h2 * 64 + 2 * i], s[h2 * 64 + 2 * i + 1]);
+                tmem_st32(t_row + kColP + pb * 64 + h2 * 32, pk);
             }
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(&p_full[pb]);
         }
         if (ok) {
-            const bool got = mbar_wait(p_free, (J - 1) & 1);
+            const bool got = mbar_wait(&p_free[(J - 1) & 1], ((J - 1) >> 1) & 1);
             ok = __all_sync(0xffffffffu, got && *abort_flag == 0);
             tc_fence_after();
         }
@@ -356,7 +370,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1) mla_prefill_kernel(const Mla
 #pragma unroll 1
             for (int c = 0; c < 256 / 32; ++c) {
                 float o[32];
-                tmem_ld32(t_row + 2 * kKeys + c * 32, o);
+                tmem_ld32(t_row + c * 32, o);
                 tmem_wait_ld();
                 if (live) {
 #pragma unroll
@@ -373,6 +387,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1) mla_prefill_kernel(const Mla
             if (live && half == 0) p.lse[t * kHeads + h] = l > 0.f ? m + log2f(l) : -INFINITY;
         } else {
             *abort_flag = 1;
+            if (lane == 0) atomicOr(p.err, kErrTimeout);
         }
     }
 
@@ -384,7 +399,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1) mla_prefill_kernel(const Mla
     }
 }
 
-cudaError_t launch_mla_prefill(const MlaParams& p, cudaStream_t stream) {
+cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStream_t stream) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -397,8 +412,25 @@ cudaError_t launch_mla_prefill(const MlaParams& p, cudaStream_t stream) {
     }
     const long long tiles = (long long)(p.total_q + mla::kTok - 1) / mla::kTok + p.batch;
     if (tiles <= 0) return cudaSuccess;
-    mla_prefill_kernel<<<(unsigned)(2 * tiles), mla::kThreads, mla::kSmemBytes, stream>>>(p);
-    return cudaGetLastError();
+    const bool staged = p.num_pages > 0;
+    if (staged) {
+        // one warp per row of the nnz (+128 zero) rows, capped at 16 waves of 8-warp CTAs
+        const long long want = ((long long)p.nnz + 128 + 7) / 8;
+        mla_stage_kernel<<<(unsigned)std::min<long long>(want, 152LL * 8 * 16), 256, 0, stream>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * tiles));
+    cfg.blockDim = dim3(mla::kThreads);
+    cfg.dynamicSmemBytes = mla::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = staged ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, mla_prefill_kernel, p, maps.q_nope, maps.q_pe, maps.kv);
 }
 
 }  // namespace pkv

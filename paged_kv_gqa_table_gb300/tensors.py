@@ -42,11 +42,20 @@ def upload_decode_case(case: dict, device="cuda") -> dict:
                 context_lens=int_to_torch(case["context_lens"], device))
 
 
-def workspace_for(desc, opts=None, device="cuda") -> torch.Tensor:
-    n = B.pkv_decode_workspace_size(desc, opts)
+def _aligned_zeros(n: int, device) -> torch.Tensor:
     ws = torch.zeros((n + 255) // 256 * 256 + 256, dtype=torch.uint8, device=device)
     off = (-ws.data_ptr()) % 256
     return ws[off:off + n]
+
+
+def workspace_for(desc, opts=None, device="cuda") -> torch.Tensor:
+    """Zeroed, 256-byte-aligned decode workspace of pkv_decode_workspace_size bytes."""
+    return _aligned_zeros(B.pkv_decode_workspace_size(desc, opts), device)
+
+
+def mla_workspace_for(desc, device="cuda") -> torch.Tensor:
+    """Zeroed, 256-byte-aligned MLA workspace of pkv_mla_workspace_size bytes."""
+    return _aligned_zeros(B.pkv_mla_workspace_size(desc), device)
 
 
 def paged_decode_attention(case: dict, dev: dict | None = None, opts=None, out=None, workspace=None,
@@ -82,7 +91,8 @@ def decode_partials(case: dict, dev: dict | None = None, opts=None, capacity: in
 
 
 def mla_desc(case: dict) -> B.pkv_mla_desc:
-    return B.make_mla_desc(case["total_q"], case["batch"], case["num_pages"], case["H"], case["Dc"], case["Dr"])
+    return B.make_mla_desc(case["total_q"], case["batch"], case["num_pages"], int(case["kv_indptr"][-1]),
+                           case["H"], case["Dc"], case["Dr"])
 
 
 def upload_mla_case(case: dict, device="cuda") -> dict:
@@ -94,16 +104,20 @@ def upload_mla_case(case: dict, device="cuda") -> dict:
                 kv_indices=int_to_torch(case["kv_indices"], device))
 
 
-def mla_paged_prefill(case: dict, dev: dict | None = None, out=None, lse=None, stream=None):
+def mla_paged_prefill(case: dict, dev: dict | None = None, out=None, lse=None, workspace=None, stream=None,
+                      desc=None):
     """Runs the MLA prefill on a synthetic case; returns (out [T][H][Dc] bf16, lse [T][H] fp32) on the device."""
     dev = dev if dev is not None else upload_mla_case(case)
     d = dev["q_nope"].device
     T, H, Dc = case["total_q"], case["H"], case["Dc"]
+    desc = desc if desc is not None else mla_desc(case)
     if out is None:
         out = torch.empty((T, H, Dc), dtype=torch.bfloat16, device=d)
     if lse is None:
         lse = torch.empty((T, H), dtype=torch.float32, device=d)
-    B.pkv_mla_paged_prefill(mla_desc(case), dev["q_nope"], dev["q_pe"], dev["ckv_cache"], dev["kpe_cache"],
+    if workspace is None:
+        workspace = mla_workspace_for(desc, device=d)
+    B.pkv_mla_paged_prefill(desc, dev["q_nope"], dev["q_pe"], dev["ckv_cache"], dev["kpe_cache"],
                             dev["qo_indptr"], dev["kv_indptr"], dev["kv_indices"], case["sm_scale"], out, lse,
-                            stream=stream)
+                            workspace, stream=stream)
     return out, lse

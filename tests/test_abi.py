@@ -168,3 +168,27 @@ def test_empty_batch_is_a_no_op(B):
     st = B.raw_status("pkv_paged_decode_attention", ctypes.byref(d), None, None, None, None, None, None,
                       ctypes.c_float(0.1), None, None, 0, None)
     assert st == B.PKV_OK
+
+
+def test_mla_workspace_size_and_argument_checks(B):
+    al = lambda x: (x + 255) // 256 * 256
+    for nnz in (0, 1, 8070, 123457):
+        d = B.make_mla_desc(2866, 8, 9000, nnz)
+        assert B.pkv_mla_workspace_size(d) == 256 + al(nnz * 1152)
+    for bad in (dict(nnz=-1), dict(total_q=-1), dict(num_pages=-3)):
+        kw = dict(total_q=100, batch=2, num_pages=50, nnz=40)
+        kw.update(bad)
+        with pytest.raises(B.PkvError) as e:
+            B.pkv_mla_workspace_size(B.make_mla_desc(**kw))
+        assert e.value.status == B.PKV_INVALID_ARG
+    with pytest.raises(B.PkvError) as e:
+        B.pkv_mla_workspace_size(B.make_mla_desc(100, 2, 50, 40, num_heads=8))
+    assert e.value.status == B.PKV_UNSUPPORTED
+    d = B.make_mla_desc(100, 2, 50, 40)
+    need = B.pkv_mla_workspace_size(d)
+    good = 1 << 20
+    args = lambda ws, n: [ctypes.byref(d), good, good, good, good, good, good, good, ctypes.c_float(0.1), good, good,
+                          ws, n, None]
+    assert B.raw_status("pkv_mla_paged_prefill", *args(good, need - 1)) == B.PKV_WORKSPACE_TOO_SMALL
+    assert B.raw_status("pkv_mla_paged_prefill", *args(good + 128, need)) == B.PKV_INVALID_ARG   # misaligned
+    assert B.raw_status("pkv_mla_paged_prefill", *args(None, need)) == B.PKV_INVALID_ARG

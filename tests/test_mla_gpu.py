@@ -110,3 +110,40 @@ def test_mla_full_size_workload_sampled():
         tokens |= {int(qo[b]), int(qo[b + 1] - 1)} | set(rng.integers(qo[b], qo[b + 1], size=4).tolist())
     check(case, out, lse, sorted(tokens))
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+
+
+def _run_with(case, nnz=None, fill=None):
+    from paged_kv_gqa_table_gb300 import binding as B
+    from paged_kv_gqa_table_gb300 import tensors
+    desc = tensors.mla_desc(case)
+    if nnz is not None:
+        desc.nnz = int(nnz)
+    ws = tensors.mla_workspace_for(desc)
+    if fill is not None:
+        ws[256:].fill_(fill)           # leave the error header zeroed
+    out, lse = tensors.mla_paged_prefill(case, workspace=ws, desc=desc)
+    torch.cuda.synchronize()
+    err = int(ws[:4].view(torch.int32).item())
+    return out.double().cpu().numpy(), lse.double().cpu().numpy(), err
+
+
+def test_mla_workspace_contents_do_not_matter():
+    # 0xFF bytes are NaN in bf16: every staged row the kernel reads must have
+    # been written by this call, including the zero rows past the last key.
+    case = synth.mla_case(seed=21, batch=3, q_len_range=(5, 140), prefix_range=(0, 260), slack_pages=5)
+    out, lse, err = _run_with(case, fill=0xFF)
+    assert err == 0
+    check(case, out, lse)
+    # an upper bound for nnz (more rows than kv_indptr[batch]) gives the same bits
+    out2, lse2, err2 = _run_with(case, nnz=int(case["kv_indptr"][-1]) + 1000, fill=0xFF)
+    assert err2 == 0
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def test_mla_short_nnz_is_reported():
+    # nnz below kv_indptr[batch]: keys past it are not staged (their boxes read
+    # TMA zero fill), the call completes and error bit 1 is set.
+    case = synth.mla_case(seed=22, batch=2, q_len_range=(20, 40), prefix_range=(100, 200))
+    out, lse, err = _run_with(case, nnz=int(case["kv_indptr"][-1]) // 2)
+    assert err == 2
+    assert out.shape == (case["total_q"], 16, 512)
