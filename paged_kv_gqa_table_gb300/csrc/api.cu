@@ -440,6 +440,7 @@ int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const vo
     st = encode_rows_map(&maps.q_nope, q_nope, 512, q_rows, 64, 128);
     if (st == PKV_OK) st = encode_rows_map(&maps.q_pe, q_pe, 64, q_rows, 64, 128);
     if (st == PKV_OK && d.num_pages > 0 && d.nnz > 0) st = encode_rows_map(&maps.kv, p.stage, 576, (cuuint64_t)d.nnz, 64, 128);
+    if (st == PKV_OK && d.num_pages > 0 && d.nnz > 0) st = encode_rows_map(&maps.v, p.stage, 576, (cuuint64_t)d.nnz, 64, 32);
     if (st != PKV_OK) return st;
     return launch_mla_prefill(p, maps, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK
                                                                                               : PKV_CUDA_ERROR;

@@ -46,10 +46,11 @@ struct MlaParams {
 constexpr int kMlaStageRowBytes = (512 + 64) * 2;
 
 // TMA descriptors of the MLA operands: q_nope / q_pe as 2-D {512 | 64,
-// total_q * 16} tensors and the staged keys as {576, nnz}, all with {64, 128}
-// boxes and 128-byte swizzle.  kv is unused (zero) when the pool is empty.
+// total_q * 16} tensors and the staged keys as {576, nnz}, with {64, 128}
+// boxes (kv: K chunks) or {64, 32} boxes (v: V chunk blocks), all with
+// 128-byte swizzle.  kv and v are unused (zero) when the pool is empty.
 struct MlaMaps {
-    CUtensorMap q_nope, q_pe, kv;
+    CUtensorMap q_nope, q_pe, kv, v;
 };
 
 cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStream_t stream);

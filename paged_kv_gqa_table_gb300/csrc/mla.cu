@@ -17,10 +17,13 @@
 // S tile of 128 keys and two bf16 P tiles (the A operand of O += P.V, read
 // from TMEM), which is why the output is split across two CTAs that each
 // recompute S.  Shared memory holds the whole Q tile (9 chunks of 128 rows x
-// 64 bf16 = 144 KB, one 2-D TMA box each) and a 5-stage ring of 16 KB key
-// chunks (128 key rows x 64 bf16), all in the 128-byte-swizzled layout the
-// UMMA descriptors describe.  A ckv chunk serves as the K-major B operand of
-// S = Q.K^T and, re-described MN-major, as the B operand V of O = P.V.
+// 64 bf16 = 144 KB, one 2-D TMA box each) and a 5-stage ring of 16 KB
+// chunks, all in the 128-byte-swizzled layout the UMMA descriptors describe.
+// Per block of 128 keys the ring carries 9 K chunks (128 keys x 64 columns,
+// the K-major B operand of S = Q.K^T, N = 128) and 4 V chunks (32 keys x the
+// CTA's 256 output columns as four 64-column blocks 4 KB apart, the MN-major
+// B operand of O += P.V, N = 256).  Both are cut from the same staged ckv
+// rows.
 //
 // Page size 1 makes every key its own page.  Gathering 128-byte row pieces
 // per tile (up to ~100 tiles read each key) keeps too few bytes in flight
@@ -52,7 +55,7 @@ constexpr int kRows = kTok * kHeads;    // 128 TMEM lanes
 constexpr int kKeys = 128;              // keys per block
 constexpr int kChunk = kRows * 64 * 2;  // 16 KB: 128 rows x 64 bf16
 constexpr int kQChunks = 9;             // 8 x ckv + 1 x kpe
-constexpr int kVChunks = 4;             // 256 output columns / 64
+constexpr int kVChunks = 4;             // 128 keys / 32 keys per V chunk
 constexpr int kStages = 5;
 constexpr int kThreads = 192;
 constexpr int kBars = 2 * kStages + 8;
@@ -94,7 +97,8 @@ __global__ void __launch_bounds__(256) mla_stage_kernel(const MlaParams p) {
 
 __global__ void __launch_bounds__(mla::kThreads, 1)
     mla_prefill_kernel(const MlaParams p, const __grid_constant__ CUtensorMap tm_qn,
-                       const __grid_constant__ CUtensorMap tm_qp, const __grid_constant__ CUtensorMap tm_kv) {
+                       const __grid_constant__ CUtensorMap tm_qp, const __grid_constant__ CUtensorMap tm_kv,
+                       const __grid_constant__ CUtensorMap tm_v) {
     using namespace mla;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -185,20 +189,30 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
             asm volatile("griddepcontrol.wait;" ::: "memory");
             bool ok = true;
             int k = 0;   // running chunk index (same order as the MMA issuer consumes them)
-            auto load_chunk = [&](int jb, int x) -> bool {
+            // v < 0: K chunk (128 keys of block jb, columns [x, x + 64));
+            // v >= 0: V chunk v (keys 32v .. 32v + 31 of block jb, the CTA's 256 columns)
+            auto load_chunk = [&](int jb, int x, int v) -> bool {
                 const int stage = k % kStages;
                 if (k >= kStages && !(mbar_wait(&ring_empty[stage], ((k / kStages) - 1) & 1) && *abort_flag == 0))
                     return false;
+                uint8_t* dst = sRing + stage * kChunk;
                 mbar_arrive_expect_tx(&ring_full[stage], kChunk);
-                tma_load_2d(sRing + stage * kChunk, &tm_kv, &ring_full[stage], x, kv0 + jb * kKeys);
+                if (v < 0) {
+                    tma_load_2d(dst, &tm_kv, &ring_full[stage], x, kv0 + jb * kKeys);
+                } else {
+#pragma unroll
+                    for (int n = 0; n < 4; ++n)
+                        tma_load_2d(dst + n * 4096, &tm_v, &ring_full[stage], (half * 4 + n) * 64,
+                                    kv0 + jb * kKeys + v * 32);
+                }
                 ++k;
                 return true;
             };
             for (int step = 0; step <= J && ok; ++step) {
                 if (step < J)
-                    for (int c = 0; c < kQChunks && ok; ++c) ok = load_chunk(step, c * 64);
+                    for (int c = 0; c < kQChunks && ok; ++c) ok = load_chunk(step, c * 64, -1);
                 if (step >= 1)
-                    for (int v = 0; v < kVChunks && ok; ++v) ok = load_chunk(step - 1, (half * kVChunks + v) * 64);
+                    for (int v = 0; v < kVChunks && ok; ++v) ok = load_chunk(step - 1, 0, v);
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -214,7 +228,7 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
         // ----------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc_qk = umma_idesc_bf16_f32(kRows, kKeys, false);
-            const uint32_t idesc_pv = umma_idesc_bf16_f32(kRows, 64, true);
+            const uint32_t idesc_pv = umma_idesc_bf16_f32(kRows, 256, true);
             const uint32_t q_addr = smem_u32(sQ), ring_addr = smem_u32(sRing);
             bool ok = mbar_wait(q_full, 0);
             tc_fence_after();
@@ -226,9 +240,11 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
                         tc_fence_after();
                     }
                     for (int c = 0; c < kQChunks && ok; ++c, ++k) {
+                        // TMA data only: no tcgen05 fence, and no abort-flag load on this
+                        // path (the issue thread's extra latency stalls the tensor pipe; a
+                        // stalled pipeline ends in a timed-out wait anyway)
                         const int stage = k % kStages;
-                        ok = mbar_wait(&ring_full[stage], (k / kStages) & 1) && *abort_flag == 0;
-                        tc_fence_after();
+                        ok = mbar_wait(&ring_full[stage], (k / kStages) & 1);
                         if (!ok) break;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
@@ -245,14 +261,16 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
                     tc_fence_after();
                     for (int v = 0; v < kVChunks && ok; ++v, ++k) {
                         const int stage = k % kStages;
-                        ok = mbar_wait(&ring_full[stage], (k / kStages) & 1) && *abort_flag == 0;
-                        tc_fence_after();
+                        ok = mbar_wait(&ring_full[stage], (k / kStages) & 1);
                         if (!ok) break;
+                        // keys 32v + 16kk .. +15: P columns (32v + 16kk) / 2; B = 16 key rows
+                        // of the four 64-column blocks (MN-major: blocks 4 KB apart, 8-row
+                        // groups 1 KB apart)
 #pragma unroll
-                        for (int kk = 0; kk < kKeys / 16; ++kk)
-                            umma_bf16_tmem_a(tmem + v * 64, tmem + kColP + pb * 64 + kk * 8,
-                                             umma_desc_sw128(ring_addr + stage * kChunk + kk * 2048, kChunk, 1024),
-                                             idesc_pv, jb > 0 || kk > 0);
+                        for (int kk = 0; kk < 2; ++kk)
+                            umma_bf16_tmem_a(tmem, tmem + kColP + pb * 64 + v * 16 + kk * 8,
+                                             umma_desc_sw128(ring_addr + stage * kChunk + kk * 2048, 4096, 1024),
+                                             idesc_pv, (jb | v | kk) != 0);
                         umma_commit(&ring_empty[stage]);
                     }
                     if (ok) umma_commit(&p_free[pb]);
@@ -430,7 +448,7 @@ cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = staged ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, mla_prefill_kernel, p, maps.q_nope, maps.q_pe, maps.kv);
+    return cudaLaunchKernelEx(&cfg, mla_prefill_kernel, p, maps.q_nope, maps.q_pe, maps.kv, maps.v);
 }
 
 }  // namespace pkv
