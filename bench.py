@@ -37,6 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attention: KV-cache GB/s and % of GB300 HBM peak; µs/step"
 FLUSH_BYTES = 256 << 20
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_phase1_llama3_8b_decode.md")
+MLA_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "mla_prefill_kernel_mla_prefill_h16.md")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -59,12 +60,12 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic():
-    """Per-launch DRAM bytes of phase 1 from the committed ncu summary, if it
-    was taken on the current kernel sources; else None."""
-    if not os.path.exists(PROFILE_SUMMARY):
+def profiled_traffic(summary=PROFILE_SUMMARY):
+    """Per-launch DRAM bytes of the profiled kernel from a committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    if not os.path.exists(summary):
         return None
-    text = open(PROFILE_SUMMARY).read()
+    text = open(summary).read()
     m_hash = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
     if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
@@ -512,7 +513,8 @@ def run_mla(args):
             "config": mla_workload_config(case, args.workload), "us_per_step": t / args.steps * 1e6,
             "clocks": clocks, "e2e": e2e, "gpu_launches": 2 * args.steps,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None, "kernel": "mla_prefill_kernel",
+                         "frac": achieved / peak, "traffic": profiled_traffic(MLA_PROFILE_SUMMARY),
+                         "kernel": "mla_prefill_kernel",
                          "timed": "whole step: mla_stage_kernel + mla_prefill_kernel (its programmatic dependent)",
                          "peak_source": "measured" if pk else "fallback",
                          "algorithmic_flops_per_launch": int(flops), "avg_launch_us": t / args.steps * 1e6},
