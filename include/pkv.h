@@ -37,6 +37,14 @@ extern "C" {
 
 typedef struct CUstream_st* pkv_stream_t;  /* same type as cudaStream_t */
 
+/* The library is built with hidden symbol visibility and exports only the
+ * functions below (so two copies of it in one process share no state). */
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
 typedef enum {
     PKV_OK = 0,
     PKV_INVALID_ARG = 1,          /* null pointer, bad shape, misaligned pointer, bad enum */
@@ -87,10 +95,10 @@ typedef struct {
 } pkv_decode_opts;
 
 /* Text of a status code (static storage). */
-const char* pkv_status_string(int status);
+PKV_API const char* pkv_status_string(int status);
 
 /* ABI version of this header: 1. */
-int pkv_version(void);
+PKV_API int pkv_version(void);
 
 /*
  * Split planner (host only, deterministic integer arithmetic).  Splits every
@@ -103,7 +111,7 @@ int pkv_version(void);
  * (sequence, KV head, split) work items stays below 6 * num_sms, down to
  * 4 * block_size.
  */
-int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms,
+PKV_API int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms,
                     int* num_splits, int* partition_tokens);
 
 /*
@@ -114,7 +122,7 @@ int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, in
  * Word 0 of the header collects device-side error bits (bit 0: a pipeline
  * wait timed out); zero it once after allocating.
  */
-int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms,
+PKV_API int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms,
                               size_t* bytes);
 
 /*
@@ -138,7 +146,7 @@ int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts
  * programmatic dependent of phase 1.  Calls sharing one workspace must be
  * ordered on the GPU (one stream).
  */
-int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
+PKV_API int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
                                const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* block_table, const int32_t* context_lens,
                                float scale, void* out,
@@ -154,7 +162,7 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
  * are [B][Hq][num_splits_capacity] (and [...][D]); the call fails with
  * PKV_WORKSPACE_TOO_SMALL if the plan needs more splits than the capacity.
  */
-int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
+PKV_API int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
                         const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* block_table, const int32_t* context_lens, float scale,
                         float* part_acc, float* part_m, float* part_l, int num_splits_capacity,
@@ -168,7 +176,7 @@ int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts
  * and n == 0 gives zeros.  Partials are laid out as pkv_decode_partials
  * writes them with num_splits columns.
  */
-int pkv_combine(const pkv_decode_desc* desc, int partition_tokens, int num_splits,
+PKV_API int pkv_combine(const pkv_decode_desc* desc, int partition_tokens, int num_splits,
                 const int32_t* context_lens, const float* part_acc, const float* part_m,
                 const float* part_l, void* out, pkv_stream_t stream);
 
@@ -180,7 +188,7 @@ int pkv_combine(const pkv_decode_desc* desc, int partition_tokens, int num_split
  *          outside [0, num_blocks)
  * Entries past a sequence's live range are not inspected.
  */
-int pkv_validate_block_table(const pkv_decode_desc* desc, const int32_t* block_table,
+PKV_API int pkv_validate_block_table(const pkv_decode_desc* desc, const int32_t* block_table,
                              const int32_t* context_lens, uint32_t* err_word, pkv_stream_t stream);
 
 /* Problem description of one MLA paged prefill call (page size 1, bf16). */
@@ -202,7 +210,7 @@ typedef struct {
  * bit 1: kv_indptr[batch] > nnz, so keys past nnz were not staged and the
  * result is unspecified); zero it once after allocating.
  */
-int pkv_mla_workspace_size(const pkv_mla_desc* desc, size_t* bytes);
+PKV_API int pkv_mla_workspace_size(const pkv_mla_desc* desc, size_t* bytes);
 
 /*
  * MLA paged causal prefill ([MLA] run / _forward and the kernel's sections
@@ -232,7 +240,7 @@ int pkv_mla_workspace_size(const pkv_mla_desc* desc, size_t* bytes);
  * pkv_mla_workspace_size describes; calls sharing one workspace must be
  * ordered on the GPU (one stream).
  */
-int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const void* q_pe,
+PKV_API int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const void* q_pe,
                           const void* ckv_cache, const void* kpe_cache, const int32_t* qo_indptr,
                           const int32_t* kv_indptr, const int32_t* kv_indices, float sm_scale,
                           void* out, float* lse, void* workspace, size_t workspace_bytes,
@@ -266,7 +274,7 @@ int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const vo
  * pkv_paged_decode_attention.
  */
 #define PKV_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
-int pkv_paged_decode_attention_static(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
+PKV_API int pkv_paged_decode_attention_static(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
                                       const void* q, const void* k_cache, const void* v_cache,
                                       const int32_t* block_table, const int32_t* context_lens,
                                       float scale, void* out, pkv_stream_t stream);

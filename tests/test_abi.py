@@ -6,6 +6,8 @@ import ctypes
 import os
 import random
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -192,3 +194,21 @@ def test_mla_workspace_size_and_argument_checks(B):
     assert B.raw_status("pkv_mla_paged_prefill", *args(good, need - 1)) == B.PKV_WORKSPACE_TOO_SMALL
     assert B.raw_status("pkv_mla_paged_prefill", *args(good + 128, need)) == B.PKV_INVALID_ARG   # misaligned
     assert B.raw_status("pkv_mla_paged_prefill", *args(None, need)) == B.PKV_INVALID_ARG
+
+
+def test_library_exports_only_the_declared_functions(B):
+    # Built with hidden visibility: any other exported symbol (a template's
+    # static "attribute already set" flag, say) would be shared with a second
+    # copy of the library loaded in the same process.
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = set()
+    for line in out.splitlines():
+        parts = line.split()
+        if len(parts) == 3 and parts[1] in "TtDdBbRrVvWwu":
+            exported.add(parts[2])
+    ours = {n for n in exported if not n.startswith("_")}
+    assert ours == set(declared_functions()), sorted(ours ^ set(declared_functions()))
+    assert not any(parts.split()[1] == "u" for parts in out.splitlines() if len(parts.split()) == 3)
