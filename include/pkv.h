@@ -134,7 +134,7 @@ PKV_API int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_dec
  *   q, out        [B][Hq][D] of dtype (4-byte aligned; out 8-byte aligned)
  *   k/v_cache     per layout (16-byte aligned)
  *   block_table   int32 [B][max_blocks_per_seq]; entries past a sequence's last
- *                 page are never read (-1 is the customary filler).  A live entry
+ *                 page are never used (-1 is the customary filler).  A live entry
  *                 outside [0, num_blocks) is a caller error: it is clamped to a
  *                 valid page (no out-of-bounds access, result unspecified);
  *                 pkv_validate_block_table reports it.
