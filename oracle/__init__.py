@@ -26,7 +26,7 @@ _lock = threading.Lock()
 _lib = None
 
 STATUS_OK, STATUS_INVALID, STATUS_BAD_TABLE = 0, 1, 5
-F16, BF16 = 0, 1
+F16, BF16, FP8_E4M3 = 0, 1, 2
 NHD, VLLM = 0, 1
 
 
@@ -47,9 +47,11 @@ def _load():
             i, d, p = ctypes.c_int, ctypes.c_double, ctypes.c_void_p
             lib.oracle_widen.argtypes = [ctypes.c_uint16, i]
             lib.oracle_widen.restype = d
-            lib.oracle_decode.argtypes = [i] * 10 + [p] * 5 + [d, i, i, p, p, p]
+            lib.oracle_widen8.argtypes = [ctypes.c_uint8]
+            lib.oracle_widen8.restype = d
+            lib.oracle_decode.argtypes = [i] * 11 + [p] * 5 + [d, d, d, i, i, p, p, p]
             lib.oracle_decode.restype = i
-            lib.oracle_decode_partials.argtypes = [i] * 10 + [p] * 5 + [d, i, i, i, i, p, p, p, p]
+            lib.oracle_decode_partials.argtypes = [i] * 11 + [p] * 5 + [d, d, d, i, i, i, i, p, p, p, p]
             lib.oracle_decode_partials.restype = i
             lib.oracle_combine.argtypes = [i, i, i, i, p, p, p, p, i, i, p]
             lib.oracle_combine.restype = i
@@ -78,21 +80,29 @@ def widen(bits: int, dtype: int) -> float:
     return _load().oracle_widen(int(bits) & 0xFFFF, int(dtype))
 
 
+def widen8(bits: int) -> float:
+    """Exact value of one FP8 E4M3 bit pattern."""
+    return _load().oracle_widen8(int(bits) & 0xFF)
+
+
 def _decode_common(case):
+    kv_dtype = case.get("kv_dtype", case["dtype"])
+    kv_np = np.uint8 if kv_dtype == FP8_E4M3 else np.uint16
     q = _c(case["q"], np.uint16)
-    k = _c(case["k_cache"], np.uint16)
-    v = _c(case["v_cache"], np.uint16)
+    k = _c(case["k_cache"], kv_np)
+    v = _c(case["v_cache"], kv_np)
     table = _c(case["block_table"], np.int32)
     ctx = _c(case["context_lens"], np.int32)
     dims = [case["B"], case["Hq"], case["Hkv"], case["D"], case["block_size"],
             table.shape[1] if table.ndim == 2 else 0, case["num_blocks"],
-            case["dtype"], case["layout"], case.get("x", 8)]
-    return dims, (q, k, v, table, ctx)
+            case["dtype"], case["layout"], case.get("x", 8), kv_dtype]
+    scales = [float(case["scale"]), float(case.get("k_scale", 1.0)), float(case.get("v_scale", 1.0))]
+    return dims, (q, k, v, table, ctx), scales
 
 
 def decode(case, b_lo: int = 0, b_hi: int | None = None, out: np.ndarray | None = None) -> np.ndarray:
     """fp64 attention output [B][Hq][D] (only rows b in [b_lo, b_hi) are filled)."""
-    dims, arrs = _decode_common(case)
+    dims, arrs, scales = _decode_common(case)
     B, Hq, D = case["B"], case["Hq"], case["D"]
     b_hi = B if b_hi is None else b_hi
     if out is None:
@@ -100,7 +110,7 @@ def decode(case, b_lo: int = 0, b_hi: int | None = None, out: np.ndarray | None 
     maxn = int(max(1, int(np.max(arrs[4][b_lo:b_hi], initial=1))))
     sbuf = np.zeros(maxn)
     acc = np.zeros(D)
-    st = _load().oracle_decode(*dims, *[_ptr(a) for a in arrs], float(case["scale"]),
+    st = _load().oracle_decode(*dims, *[_ptr(a) for a in arrs], *scales,
                                b_lo, b_hi, _ptr(out), _ptr(sbuf), _ptr(acc))
     if st:
         raise OracleError(st)
@@ -109,14 +119,14 @@ def decode(case, b_lo: int = 0, b_hi: int | None = None, out: np.ndarray | None 
 
 def decode_partials(case, P: int, NS: int, b_lo: int = 0, b_hi: int | None = None):
     """Split-mode partials (m, l, acc) with split s = tokens [s*P, min((s+1)*P, n))."""
-    dims, arrs = _decode_common(case)
+    dims, arrs, scales = _decode_common(case)
     B, Hq, D = case["B"], case["Hq"], case["D"]
     b_hi = B if b_hi is None else b_hi
     pm = np.full((B, Hq, NS), np.nan)
     pl = np.full((B, Hq, NS), np.nan)
     pacc = np.full((B, Hq, NS, D), np.nan)
     sbuf = np.zeros(max(1, P))
-    st = _load().oracle_decode_partials(*dims, *[_ptr(a) for a in arrs], float(case["scale"]),
+    st = _load().oracle_decode_partials(*dims, *[_ptr(a) for a in arrs], *scales,
                                         int(P), int(NS), b_lo, b_hi,
                                         _ptr(pm), _ptr(pl), _ptr(pacc), _ptr(sbuf))
     if st:

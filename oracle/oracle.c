@@ -17,6 +17,9 @@
  *         the key/value cache layout comments of its argument list.
  *   [FD]  "koas-w.github.io flash-decode post": Decode_Paged_GQAAttention_Kernel,
  *         _flash_decode_partial_kernel, _flash_decode_combine_kernel.
+ *         Its launcher also takes kv_cache_dtype, k_scale and v_scale (and ignores
+ *         them); the fp8 KV cache here reads them the plainest way: cache bytes
+ *         are OCP FP8 E4M3 values and K = k_scale * fp8, V = v_scale * fp8.
  *   [MLA] "kernelindex.com flashinfer gemini-2.5-pro triton xvhq2i"
  *         (mla_paged_prefill_causal_h16_ckv512_kpe64_ps1): sections
  *         "2. Determine Sequence Boundaries", "3. Pass 1", "4. Pass 2".
@@ -29,7 +32,7 @@
 #include <stddef.h>
 
 enum { OR_OK = 0, OR_INVALID = 1, OR_BAD_TABLE = 5 };
-enum { OR_F16 = 0, OR_BF16 = 1 };
+enum { OR_F16 = 0, OR_BF16 = 1, OR_FP8 = 2 };
 enum { OR_NHD = 0, OR_VLLM = 1 };
 
 /* ---- exact widening of 16-bit floats ------------------------------------ */
@@ -74,6 +77,26 @@ static double widen(uint16_t h, int dtype)
 /* Exported so the tests can check the widening against a library routine. */
 double oracle_widen(uint16_t h, int dtype) { return widen(h, dtype); }
 
+/* OCP FP8 E4M3 (the "e4m3fn" encoding): 1 sign, 4 exponent (bias 7) and 3
+ * fraction bits; exponent 0 is subnormal, S.1111.111 is NaN, there is no
+ * infinity (largest finite 1.75 * 2^8 = 448). */
+static double e4m3_bits_to_double(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xf;
+    int f = b & 0x7;
+    double v;
+    if (e == 0xf && f == 0x7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);                  /* subnormal: f/8 * 2^-6 */
+    else
+        v = ldexp((double)(f + 8), e - 10);        /* (1 + f/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+double oracle_widen8(uint8_t b) { return e4m3_bits_to_double(b); }
+
 /* ---- paged K/V addressing ------------------------------------------------ */
 
 /*
@@ -102,10 +125,19 @@ static size_t v_index(int layout, int Hkv, int BS, int D,
 
 typedef struct {
     int B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x;
-    const uint16_t *q, *k, *v;
+    int kv_dtype;              /* dtype of the caches: OR_F16, OR_BF16 or OR_FP8 */
+    const uint16_t* q;
+    const void *k, *v;         /* 16-bit or 8-bit elements per kv_dtype */
     const int32_t *table, *ctx;
-    double scale;
+    double scale, k_scale, v_scale;   /* k_scale, v_scale multiply fp8 cache values (1 otherwise) */
 } decode_args;
+
+/* Value of cache element i: exact widening, times the fp8 scale. */
+static double cache_value(const decode_args* a, const void* base, size_t i, double fp8_scale)
+{
+    if (a->kv_dtype == OR_FP8) return fp8_scale * e4m3_bits_to_double(((const uint8_t*)base)[i]);
+    return widen(((const uint16_t*)base)[i], a->kv_dtype);
+}
 
 /* Checks the arguments shared by every decode entry point. */
 static int check_decode(const decode_args* a)
@@ -115,6 +147,7 @@ static int check_decode(const decode_args* a)
         return OR_INVALID;
     if (a->Hq % a->Hkv != 0) return OR_INVALID;
     if (a->dtype != OR_F16 && a->dtype != OR_BF16) return OR_INVALID;
+    if (a->kv_dtype != a->dtype && !(a->kv_dtype == OR_FP8 && a->layout == OR_NHD)) return OR_INVALID;
     if (a->layout == OR_VLLM && (a->x <= 0 || a->D % a->x != 0)) return OR_INVALID;
     if (a->layout != OR_NHD && a->layout != OR_VLLM) return OR_INVALID;
     return OR_OK;
@@ -144,7 +177,7 @@ static double score(const decode_args* a, int b, int h, int g, long long p, int 
     double s = 0.0;
     for (int d = 0; d < a->D; ++d) {
         double qd = widen(a->q[((size_t)b * a->Hq + h) * a->D + d], a->dtype);
-        double kd = widen(a->k[k_index(a->layout, a->Hkv, a->BS, a->D, a->x, p, g, o, d)], a->dtype);
+        double kd = cache_value(a, a->k, k_index(a->layout, a->Hkv, a->BS, a->D, a->x, p, g, o, d), a->k_scale);
         s += qd * kd;
     }
     return a->scale * s;
@@ -152,7 +185,7 @@ static double score(const decode_args* a, int b, int h, int g, long long p, int 
 
 static double value(const decode_args* a, int g, long long p, int o, int d)
 {
-    return widen(a->v[v_index(a->layout, a->Hkv, a->BS, a->D, p, g, o, d)], a->dtype);
+    return cache_value(a, a->v, v_index(a->layout, a->Hkv, a->BS, a->D, p, g, o, d), a->v_scale);
 }
 
 /*
@@ -202,12 +235,13 @@ static int attend_range(const decode_args* a, int b, int h, int t0, int t1,
  * sbuf: caller scratch of at least max ctx doubles; acc: D doubles.
  */
 int oracle_decode(int B, int Hq, int Hkv, int D, int BS, int MBPS, int NB,
-                  int dtype, int layout, int x,
-                  const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                  const int32_t* table, const int32_t* ctx, double scale,
+                  int dtype, int layout, int x, int kv_dtype,
+                  const uint16_t* q, const void* k, const void* v,
+                  const int32_t* table, const int32_t* ctx, double scale, double k_scale, double v_scale,
                   int b_lo, int b_hi, double* out, double* sbuf, double* acc)
 {
-    decode_args a = {B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x, q, k, v, table, ctx, scale};
+    decode_args a = {B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x, kv_dtype, q, k, v, table, ctx,
+                     scale, k_scale, v_scale};
     int st = check_decode(&a);
     if (st) return st;
     if (b_lo < 0 || b_hi > B || b_lo > b_hi) return OR_INVALID;
@@ -232,13 +266,14 @@ int oracle_decode(int B, int Hq, int Hkv, int D, int BS, int MBPS, int NB,
  * acc [B][Hq][NS][D].
  */
 int oracle_decode_partials(int B, int Hq, int Hkv, int D, int BS, int MBPS, int NB,
-                           int dtype, int layout, int x,
-                           const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                           const int32_t* table, const int32_t* ctx, double scale,
-                           int P, int NS, int b_lo, int b_hi,
+                           int dtype, int layout, int x, int kv_dtype,
+                           const uint16_t* q, const void* k, const void* v,
+                           const int32_t* table, const int32_t* ctx, double scale, double k_scale,
+                           double v_scale, int P, int NS, int b_lo, int b_hi,
                            double* pm, double* pl, double* pacc, double* sbuf)
 {
-    decode_args a = {B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x, q, k, v, table, ctx, scale};
+    decode_args a = {B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x, kv_dtype, q, k, v, table, ctx,
+                     scale, k_scale, v_scale};
     int st = check_decode(&a);
     if (st) return st;
     if (P <= 0 || NS <= 0 || b_lo < 0 || b_hi > B || b_lo > b_hi) return OR_INVALID;

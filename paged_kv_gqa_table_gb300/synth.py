@@ -16,9 +16,9 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-F16, BF16 = 0, 1
+F16, BF16, FP8_E4M3 = 0, 1, 2
 NHD, VLLM = 0, 1
-NAN_BITS = {F16: 0x7E00, BF16: 0x7FC0}
+NAN_BITS = {F16: 0x7E00, BF16: 0x7FC0, FP8_E4M3: 0x7F}
 _CHUNK = 1 << 24
 _STREAM_LENS, _STREAM_PAGES, _STREAM_Q, _STREAM_K, _STREAM_V = 1, 2, 3, 4, 5
 _STREAM_QPE, _STREAM_KPE = 6, 7
@@ -38,6 +38,24 @@ def f32_to_bits(x: np.ndarray, dtype: int) -> np.ndarray:
     return u.astype(np.uint16)
 
 
+# The 127 non-negative finite FP8 E4M3 values in bit order (0x00 .. 0x7E), as
+# float64: exponent field e (bias 7) and 3 fraction bits f, e = 0 subnormal.
+_E4M3_POS = np.array([(f / 8.0) * 2.0 ** -6 if (b >> 3) == 0 else (1 + f / 8.0) * 2.0 ** ((b >> 3) - 7)
+                      for b in range(0x7F) for f in [b & 7]], dtype=np.float64)
+
+
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round values to nearest-even FP8 E4M3 (saturating at +-448), as uint8 bits."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), _E4M3_POS[-1])
+    hi = np.clip(np.searchsorted(_E4M3_POS, a), 0, len(_E4M3_POS) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return code | (np.signbit(x).astype(np.uint8) << 7)
+
+
 def bits_to_f32(bits: np.ndarray, dtype: int) -> np.ndarray:
     """Widen fp16 / bf16 bit patterns to float32 (exact)."""
     bits = np.ascontiguousarray(bits, dtype=np.uint16)
@@ -46,15 +64,19 @@ def bits_to_f32(bits: np.ndarray, dtype: int) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32)
 
 
-def normal_bits(seed: int, stream: int, n: int, dtype: int, threads: int = 8) -> np.ndarray:
-    """n N(0,1) samples as fp16/bf16 bits, drawn chunk by chunk from independent streams."""
-    out = np.empty(n, dtype=np.uint16)
+def normal_bits(seed: int, stream: int, n: int, dtype: int, threads: int = 8, fp8_scale: float = 1.0) -> np.ndarray:
+    """n N(0,1) samples as fp16/bf16 bits (uint16), or as FP8 E4M3 bits (uint8) of
+    sample / fp8_scale, drawn chunk by chunk from independent streams."""
+    out = np.empty(n, dtype=np.uint8 if dtype == FP8_E4M3 else np.uint16)
     nchunks = (n + _CHUNK - 1) // _CHUNK
 
     def fill(c: int) -> None:
         lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
         x = _rng(seed, stream, c).standard_normal(hi - lo, dtype=np.float32)
-        out[lo:hi] = f32_to_bits(x, dtype)
+        if dtype == FP8_E4M3:
+            out[lo:hi] = f32_to_e4m3_bits(x / np.float32(fp8_scale))
+        else:
+            out[lo:hi] = f32_to_bits(x, dtype)
 
     if nchunks <= 1:
         for c in range(nchunks):
@@ -86,14 +108,18 @@ def assign_pages(seed: int, pages_per_seq: np.ndarray, max_blocks_per_seq: int, 
 def decode_case(seed: int, B: int, Hq: int, Hkv: int, D: int, block_size: int, dtype: int,
                 layout: int = NHD, context_lens=None, ctx_range=None, max_blocks_per_seq=None,
                 slack_pages: int = 0, poison: bool = False, scale: float | None = None,
-                x: int = 8) -> dict:
+                x: int = 8, kv_dtype: int | None = None, k_scale: float = 1.0 / 16,
+                v_scale: float = 1.0 / 16) -> dict:
     """One paged GQA decode problem (a query token per sequence).
 
     Layouts: NHD k/v_cache [num_blocks][Hkv][block_size][D]; VLLM key_cache
     [num_blocks][Hkv][D/x][block_size][x], value_cache [num_blocks][Hkv][D][block_size].
+    kv_dtype=FP8_E4M3 (NHD only) stores the caches as FP8 E4M3 bits of
+    N(0,1) / k_scale and N(0,1) / v_scale (uint8); q stays fp16/bf16.
     poison=True writes NaN into every slot no query may read: the tail slots of
     each sequence's last page and all slack pages.
     """
+    kv_dtype = dtype if kv_dtype is None else kv_dtype
     if context_lens is None:
         lo, hi = ctx_range
         context_lens = _rng(seed, _STREAM_LENS).integers(lo, hi + 1, size=B)
@@ -103,8 +129,8 @@ def decode_case(seed: int, B: int, Hq: int, Hkv: int, D: int, block_size: int, d
     table, nb, unused = assign_pages(seed, pages, mbps, slack_pages)
     q = normal_bits(seed, _STREAM_Q, B * Hq * D, dtype).reshape(B, Hq, D)
     n_kv = nb * Hkv * block_size * D
-    k = normal_bits(seed, _STREAM_K, n_kv, dtype)
-    v = normal_bits(seed, _STREAM_V, n_kv, dtype)
+    k = normal_bits(seed, _STREAM_K, n_kv, kv_dtype, fp8_scale=k_scale)
+    v = normal_bits(seed, _STREAM_V, n_kv, kv_dtype, fp8_scale=v_scale)
     if layout == NHD:
         k = k.reshape(nb, Hkv, block_size, D)
         v = v.reshape(nb, Hkv, block_size, D)
@@ -114,6 +140,8 @@ def decode_case(seed: int, B: int, Hq: int, Hkv: int, D: int, block_size: int, d
     case = dict(B=B, Hq=Hq, Hkv=Hkv, D=D, block_size=block_size, dtype=dtype, layout=layout, x=x,
                 num_blocks=nb, q=q, k_cache=k, v_cache=v, block_table=table, context_lens=ctx,
                 scale=float(scale if scale is not None else 1.0 / math.sqrt(D)), unused_pages=unused)
+    if kv_dtype != dtype:
+        case.update(kv_dtype=kv_dtype, k_scale=float(k_scale), v_scale=float(v_scale))
     if poison:
         poison_decode_case(case)
     return case
@@ -121,7 +149,7 @@ def decode_case(seed: int, B: int, Hq: int, Hkv: int, D: int, block_size: int, d
 
 def poison_decode_case(case: dict) -> None:
     """Fill unread KV slots (last-page tails, unused pages) with NaN, in place."""
-    nan = NAN_BITS[case["dtype"]]
+    nan = NAN_BITS[case.get("kv_dtype", case["dtype"])]
     BS, k, v = case["block_size"], case["k_cache"], case["v_cache"]
     vllm = case["layout"] == VLLM
     for p in case["unused_pages"]:

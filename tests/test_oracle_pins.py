@@ -93,6 +93,60 @@ def test_widen_bf16_all_patterns():
     assert np.array_equal(got[~nan], ref[~nan])
 
 
+def test_widen_e4m3_all_patterns():
+    # FP8 E4M3 ("e4m3fn"): against torch's float8_e4m3fn conversion.
+    torch = pytest.importorskip("torch")
+    bits = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(bits).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.widen8(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert nan.sum() == 2 and np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def _fp8_case(seed, **kw):
+    base = dict(B=4, Hq=8, Hkv=2, D=32, block_size=16, dtype=synth.BF16, ctx_range=(1, 70),
+                kv_dtype=synth.FP8_E4M3, k_scale=1.0 / 16, v_scale=1.0 / 16, slack_pages=3)
+    base.update(kw)
+    return synth.decode_case(seed=seed, **base)
+
+
+def _fp8_as_bf16(case):
+    """The same problem with the caches rewritten as bf16 bits of scale * fp8 value
+    (exact: E4M3 values times a power of two fit bf16), via torch's conversions."""
+    torch = pytest.importorskip("torch")
+    def conv(bits, sc):
+        v = torch.from_numpy(np.ascontiguousarray(bits)).view(torch.float8_e4m3fn).to(torch.float32) * sc
+        return v.to(torch.bfloat16).view(torch.uint16).numpy().astype(np.uint16)
+    new = {k: v for k, v in case.items() if k not in ("kv_dtype", "k_scale", "v_scale")}
+    new["k_cache"] = conv(case["k_cache"], case["k_scale"])
+    new["v_cache"] = conv(case["v_cache"], case["v_scale"])
+    return new
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_fp8_cache_decode_equals_bf16_decode_of_the_same_values(seed):
+    case = _fp8_case(seed)
+    got = oracle.decode(case)
+    ref = oracle.decode(_fp8_as_bf16(case))
+    assert np.array_equal(got, ref)
+    P = 32
+    NS = -(-int(case["context_lens"].max()) // P)
+    for a, b in zip(oracle.decode_partials(case, P, NS), oracle.decode_partials(_fp8_as_bf16(case), P, NS)):
+        assert np.array_equal(a, b)
+
+
+def test_fp8_scales_act_as_stated():
+    # k_scale multiplies every score, v_scale the output (closed forms).
+    a = _fp8_case(5)
+    b = dict(a, k_scale=a["k_scale"] * 2.0)
+    c = dict(a, scale=a["scale"] * 2.0)
+    assert np.allclose(oracle.decode(b), oracle.decode(c), rtol=1e-12, atol=1e-14)
+    d = dict(a, v_scale=a["v_scale"] * 3.0)
+    assert np.allclose(oracle.decode(d), 3.0 * oracle.decode(a), rtol=1e-12, atol=1e-14)
+
+
 def _golden_scale(s):
     return {"ln3": math.log(3.0), "ln2/2": math.log(2.0) / 2, "ln2": math.log(2.0)}[s] if isinstance(s, str) else s
 
@@ -401,6 +455,11 @@ MUTANTS = [
     ("lse natural log", "lse[(size_t)t * H + h] = (m + log(z)) / log(2.0);", "lse[(size_t)t * H + h] = (m + log(z));"),
     ("kpe term dropped", "s += bf16_bits_to_double(qp[d])", "s += 0 * bf16_bits_to_double(qp[d])"),
     ("bf16 exponent bias", "v = ldexp((double)(f + 128), e - 134);", "v = ldexp((double)(f + 128), e - 133);"),
+    ("e4m3 exponent bias", "v = ldexp((double)(f + 8), e - 10);", "v = ldexp((double)(f + 8), e - 9);"),
+    ("e4m3 subnormal scale", "v = ldexp((double)f, -9);", "v = ldexp((double)f, -10);"),
+    ("fp8 k_scale dropped", "cache_value(a, a->k, k_index(a->layout, a->Hkv, a->BS, a->D, a->x, p, g, o, d), a->k_scale)",
+     "cache_value(a, a->k, k_index(a->layout, a->Hkv, a->BS, a->D, a->x, p, g, o, d), 1.0)"),
+    ("fp8 v_scale dropped", "a->v_scale);\n}", "1.0);\n}"),
 ]
 
 
@@ -423,7 +482,8 @@ def test_planted_mistakes_are_caught(tmp_path, monkeypatch, name, old, new):
     failures = 0
     for fn in (lambda: test_decode_vs_numpy_brute_force(2), lambda: test_decode_vs_numpy_brute_force(0),
                lambda: test_split_then_combine_equals_unsplit(8), lambda: test_mla_vs_numpy_brute_force(0),
-               test_widen_bf16_all_patterns):
+               test_widen_bf16_all_patterns, test_widen_e4m3_all_patterns,
+               lambda: test_fp8_cache_decode_equals_bf16_decode_of_the_same_values(0)):
         try:
             fn()
         except (AssertionError, oracle.OracleError):
