@@ -169,7 +169,9 @@ def oracle_decode_timed(case, seqs, threads):
 
 
 def seq_kv_bytes(case, seqs):
-    return int(np.sum(case["context_lens"][list(seqs)], dtype=np.int64)) * case["Hkv"] * case["D"] * 4
+    """KV bytes of the given sequences (K and V, the cache's element size)."""
+    e = 1 if tensors_fp8(case) else 2
+    return int(np.sum(case["context_lens"][list(seqs)], dtype=np.int64)) * case["Hkv"] * case["D"] * 2 * e
 
 
 def cpu_baseline(case, budget_s: float = 15.0):
@@ -239,13 +241,26 @@ def run_reference(args):
     return 0
 
 
+def dtype_label(case):
+    q = {0: "fp16", 1: "bf16"}[case["dtype"]]
+    if tensors_fp8(case):
+        return "%s q/out, fp8-e4m3 KV (k_scale %g, v_scale %g)" % (q, case["k_scale"], case["v_scale"])
+    return q
+
+
+def tensors_fp8(case):
+    from paged_kv_gqa_table_gb300 import synth
+    return case.get("kv_dtype", case["dtype"]) == synth.FP8_E4M3
+
+
 def workload_config(case, name, flushed=True):
+    from paged_kv_gqa_table_gb300 import synth
     ctx = case["context_lens"]
     return {"workload": "%s: B=%d Hq=%d Hkv=%d D=%d block_size=%d %s %s layout, context_lens %d..%d (sum %d)" % (
         name, case["B"], case["Hq"], case["Hkv"], case["D"], case["block_size"],
-        {0: "fp16", 1: "bf16"}[case["dtype"]], {0: "NHD", 1: "vLLM x-packed"}[case["layout"]],
+        dtype_label(case), {0: "NHD", 1: "vLLM x-packed"}[case["layout"]],
         int(ctx.min()), int(ctx.max()), int(ctx.sum())),
-        "seed": 0, "kv_bytes_per_step": int(np.sum(ctx, dtype=np.int64)) * case["Hkv"] * case["D"] * 4,
+        "seed": 0, "kv_bytes_per_step": synth.kv_bytes(case),
         "l2": "flushed between steps (256 MiB write)" if flushed else "n/a (CPU)",
         "accumulate": "fp32"}
 
@@ -352,14 +367,15 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": {0: "fp16", 1: "bf16"}[case["dtype"]],
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(case),
             "data": "synthetic (seeded N(0,1) K/V/q, uniform context lengths, random page permutation)",
             "config": dict(workload_config(case, args.workload), parallelism="replicas" if world > 1 else "1 GPU",
                            partition_tokens=P, num_splits=ns),
             "us_per_step": t_max / args.steps * 1e6, "hbm_frac_of_measured_peak": value / peak,
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": profiled_traffic(),
+                         "frac": achieved / peak,
+                         "traffic": profiled_traffic() if args.workload == "llama3_8b_decode" else None,
                          "kernel": "decode_phase1_kernel", "peak_source": peak_kind,
                          "algorithmic_bytes_per_launch": kvb, "avg_launch_us": p1_avg * 1e6},
             "wall_s_timed_region": wall,
@@ -533,7 +549,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b_decode",
                     choices=["llama3_8b_decode", "long_context_decode", "gqa6_d256_vllm_decode", "tiny",
-                             "mla_prefill_h16"])
+                             "llama3_8b_decode_fp8", "mla_prefill_h16"])
     ap.add_argument("--skip-e2e", action="store_true", help="omit the end-to-end leg (profiling runs)")
     ap.add_argument("--skip-cpu-baseline", action="store_true", help="omit the CPU oracle leg (profiling runs)")
     args = ap.parse_args(argv)

@@ -54,7 +54,18 @@ typedef enum {
     PKV_BAD_BLOCK_TABLE = 5       /* reported by pkv_validate_block_table only */
 } pkv_status;
 
-typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+typedef enum {
+    PKV_F16 = 0,
+    PKV_BF16 = 1,
+    /* OCP FP8 E4M3 ("e4m3fn"), for KV caches only (pkv_decode_desc.kv_dtype):
+     * cached value = scale * fp8, with the per-tensor k_scale / v_scale.  [V2]'s
+     * launcher carries kv_cache_dtype, k_scale and v_scale but ignores them;
+     * this is the plain reading of those arguments. */
+    PKV_FP8_E4M3 = 2
+} pkv_dtype;
+
+/* pkv_decode_desc.kv_dtype: the caches hold elements of `dtype` (fp16 / bf16). */
+#define PKV_KV_AS_Q 0
 
 typedef enum {
     /* k_cache and v_cache both [num_blocks][Hkv][block_size][D] ([FD]
@@ -80,6 +91,9 @@ typedef struct {
     int dtype;               /* pkv_dtype of q, caches and out */
     int layout;              /* pkv_layout */
     int x_pack;              /* VLLM layout only: must be 8 */
+    int kv_dtype;            /* PKV_KV_AS_Q, or PKV_FP8_E4M3 (NHD layout; q and out stay `dtype`) */
+    float k_scale;           /* FP8 caches: K = k_scale * fp8 (finite, > 0); ignored otherwise */
+    float v_scale;           /* FP8 caches: V = v_scale * fp8 (finite, > 0); ignored otherwise */
 } pkv_decode_desc;
 
 /* Optional knobs; pass NULL for the defaults (all zero). */
@@ -97,7 +111,7 @@ typedef struct {
 /* Text of a status code (static storage). */
 PKV_API const char* pkv_status_string(int status);
 
-/* ABI version of this header: 1. */
+/* ABI version of this header: 2 (1 had no kv_dtype / k_scale / v_scale). */
 PKV_API int pkv_version(void);
 
 /*

@@ -14,7 +14,8 @@ LIB_PATH = os.path.join(_HERE, "libpkv.so")
 _lib = None
 
 PKV_OK, PKV_INVALID_ARG, PKV_UNSUPPORTED, PKV_WORKSPACE_TOO_SMALL, PKV_CUDA_ERROR, PKV_BAD_BLOCK_TABLE = range(6)
-PKV_F16, PKV_BF16 = 0, 1
+PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
+PKV_KV_AS_Q = 0
 PKV_LAYOUT_NHD, PKV_LAYOUT_VLLM = 0, 1
 
 FUNCTIONS = [
@@ -29,7 +30,8 @@ class pkv_decode_desc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
                 ("block_size", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int), ("num_blocks", ctypes.c_int),
                 ("max_context_len", ctypes.c_int), ("sum_context_len", ctypes.c_longlong),
-                ("dtype", ctypes.c_int), ("layout", ctypes.c_int), ("x_pack", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("layout", ctypes.c_int), ("x_pack", ctypes.c_int),
+                ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class pkv_decode_opts(ctypes.Structure):
@@ -107,10 +109,11 @@ def _stream(stream) -> int | None:
 
 
 def make_desc(B, Hq, Hkv, D, block_size, max_blocks_per_seq, num_blocks, max_context_len, sum_context_len,
-              dtype, layout=PKV_LAYOUT_NHD, x_pack=8) -> pkv_decode_desc:
+              dtype, layout=PKV_LAYOUT_NHD, x_pack=8, kv_dtype=PKV_KV_AS_Q, k_scale=1.0,
+              v_scale=1.0) -> pkv_decode_desc:
     return pkv_decode_desc(int(B), int(Hq), int(Hkv), int(D), int(block_size), int(max_blocks_per_seq),
                            int(num_blocks), int(max_context_len), int(sum_context_len), int(dtype), int(layout),
-                           int(x_pack))
+                           int(x_pack), int(kv_dtype), float(k_scale), float(v_scale))
 
 
 def make_opts(partition_tokens=0, num_splits=0, event_start=None, event_stop=None) -> pkv_decode_opts:

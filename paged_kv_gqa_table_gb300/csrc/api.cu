@@ -31,6 +31,12 @@ int check_desc(const pkv_decode_desc* d) {
     if (d->dtype != PKV_F16 && d->dtype != PKV_BF16) return PKV_INVALID_ARG;
     if (d->layout != PKV_LAYOUT_NHD && d->layout != PKV_LAYOUT_VLLM) return PKV_INVALID_ARG;
     if (d->layout == PKV_LAYOUT_VLLM && d->x_pack != 8) return PKV_INVALID_ARG;
+    if (d->kv_dtype != PKV_KV_AS_Q && d->kv_dtype != PKV_FP8_E4M3) return PKV_INVALID_ARG;
+    if (d->kv_dtype == PKV_FP8_E4M3) {
+        if (!(std::isfinite(d->k_scale) && d->k_scale > 0.f && std::isfinite(d->v_scale) && d->v_scale > 0.f))
+            return PKV_INVALID_ARG;
+        if (d->layout != PKV_LAYOUT_NHD) return PKV_UNSUPPORTED;
+    }
     if ((long long)d->max_context_len > (long long)d->max_blocks_per_seq * d->block_size) return PKV_INVALID_ARG;
     if (d->max_context_len > 0 && d->num_blocks == 0) return PKV_INVALID_ARG;
     if (d->D != 64 && d->D != 128 && d->D != 256) return PKV_UNSUPPORTED;
@@ -136,7 +142,20 @@ int encode_cache_map(CUtensorMap* map, const void* base, const pkv_decode_desc* 
     cuuint64_t dims[3], strides[2];
     cuuint32_t box[3], estr[3] = {1, 1, 1};
     CUtensorMapSwizzle swz;
-    if (d->layout == PKV_LAYOUT_NHD) {
+    CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    if (d->kv_dtype == PKV_FP8_E4M3) {
+        // {D, BS, NB*Hkv} bytes, one unswizzled {D, BS} box per page slice
+        type = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        dims[0] = d->D;
+        dims[1] = d->block_size;
+        dims[2] = slices;
+        strides[0] = (cuuint64_t)d->D;
+        strides[1] = (cuuint64_t)d->D * d->block_size;
+        box[0] = d->D;
+        box[1] = d->block_size;
+        box[2] = 1;
+        swz = CU_TENSOR_MAP_SWIZZLE_NONE;
+    } else if (d->layout == PKV_LAYOUT_NHD) {
         dims[0] = d->D;
         dims[1] = d->block_size;
         dims[2] = slices;
@@ -158,7 +177,7 @@ int encode_cache_map(CUtensorMap* map, const void* base, const pkv_decode_desc* 
         box[2] = 1;
         swz = CU_TENSOR_MAP_SWIZZLE_NONE;
     }
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = fn(map, type, 3, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PKV_OK : PKV_INVALID_ARG;
@@ -182,6 +201,9 @@ cudaError_t dispatch_phase1(const pkv_decode_desc* d, const DecodeParams& p, lon
                             const CUtensorMap& v, cudaStream_t s) {
     const int nt = (d->Hq / d->Hkv) > 8 ? 2 : 1;
     const bool bf = d->dtype == PKV_BF16;
+    if (d->kv_dtype == PKV_FP8_E4M3)
+        return bf ? launch_decode_nhd8_bf16(d->D, nt, p, grid, k, v, s)
+                  : launch_decode_nhd8_f16(d->D, nt, p, grid, k, v, s);
     if (d->layout == PKV_LAYOUT_NHD)
         return bf ? launch_decode_nhd_bf16(d->D, nt, p, grid, k, v, s)
                   : launch_decode_nhd_f16(d->D, nt, p, grid, k, v, s);
@@ -216,7 +238,9 @@ int prepare_phase1(const pkv_decode_desc* d, int P, int NS, const void* q, const
     p->NS = NS;
     p->ns_stride = NS;
     p->n_cap = d->max_context_len;
-    p->scale_log2 = (float)((double)scale * 1.4426950408889634);
+    const bool fp8 = d->kv_dtype == PKV_FP8_E4M3;
+    p->scale_log2 = (float)((double)scale * (fp8 ? (double)d->k_scale : 1.0) * 1.4426950408889634);
+    p->v_scale = fp8 ? d->v_scale : 1.f;
     if (d->max_context_len == 0) return PKV_OK;   // maps unused: every split is empty
     int st = encode_cache_map(mk, k, d);
     if (st) return st;
@@ -243,7 +267,7 @@ const char* pkv_status_string(int status) {
     }
 }
 
-int pkv_version(void) { return 1; }
+int pkv_version(void) { return 2; }
 
 int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms, int* num_splits,
                     int* partition_tokens) {

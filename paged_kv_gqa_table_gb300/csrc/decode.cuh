@@ -30,6 +30,8 @@
 //         for ldmatrix), V [D][BS] (two-way conflicts at most).
 #pragma once
 
+#include <type_traits>
+
 #include "decode_common.cuh"
 
 namespace pkv {
@@ -48,32 +50,39 @@ struct DecodeParams {
     int NS;                  // splits in the grid
     int ns_stride;           // split extent of the partial arrays
     int n_cap;               // context lengths are clamped to [0, n_cap]
-    float scale_log2;        // scale * log2(e)
+    float scale_log2;        // scale * log2(e) (times k_scale for FP8 caches)
+    float v_scale;           // multiplies the output / partial acc (FP8 caches; 1 otherwise)
     int partials_only;       // 1: always write partials (+ sentinels), never out
 };
 
-template <int D>
+template <int D, int LAYOUT>
 struct DecodeTile {
     static constexpr int BS = kPageTokens;
     static constexpr int NWC = 4;                                   // consumer warps
-    static constexpr int SLICE = BS * D * 2;                        // bytes of one page slice
+    static constexpr int KVB = LAYOUT == kLayoutNHD8 ? 1 : 2;       // bytes per cache element
+    static constexpr int SLICE = BS * D * KVB;                      // bytes of one page slice
     static constexpr int STAGES = D == 64 ? 12 : (D == 128 ? 8 : 4);
+    // FP8 pages are expanded to fp16 in a per-consumer-warp K/V slice pair
+    static constexpr int STAGING = KVB == 1 ? NWC * 2 * BS * D * 2 : 0;
     static constexpr int RED_STRIDE = D + 4;                        // floats per reduction row
     static constexpr int smem_bytes(int nt) {
-        return 1024 + STAGES * 2 * SLICE + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 16;
+        return 1024 + STAGES * 2 * SLICE + STAGING + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 16;
     }
 };
 
 template <typename T, int LAYOUT, int D, int NT>
-__global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
+__global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     decode_phase1_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv) {
-    using Tile = DecodeTile<D>;
+    using Tile = DecodeTile<D, LAYOUT>;
+    constexpr bool KV8 = LAYOUT == kLayoutNHD8;
+    using MT = typename std::conditional<KV8, __half, T>::type;   // tensor-core operand type
     constexpr int BS = Tile::BS, NWC = Tile::NWC, SLICE = Tile::SLICE, STAGES = Tile::STAGES;
     constexpr int KT = D / 16;   // k-steps of Q.K^T and d-tiles of P.V
     constexpr int HP = NT * 8;   // padded heads
     constexpr int RS = Tile::RED_STRIDE;
-    static_assert(NWC * HP * RS * 4 <= STAGES * 2 * SLICE, "reduction buffer must fit in the ring");
+    static_assert(NWC * HP * RS * 4 <= STAGES * 2 * SLICE + Tile::STAGING,
+                  "reduction buffer must fit in the ring (and staging)");
     // Pages go to consumer warps round-robin: with STAGES a multiple of NWC a
     // warp only re-waits on stages it consumed itself, so a parity wait can
     // never be satisfied by the previous lap's phase.
@@ -82,7 +91,8 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * 2 * SLICE);
+    uint8_t* staging = smem + STAGES * 2 * SLICE;   // FP8 only: [NWC][K, V][BS][D] fp16
+    uint64_t* full = reinterpret_cast<uint64_t*>(staging + Tile::STAGING);
     uint64_t* empty = full + STAGES;
     float* st_m = reinterpret_cast<float*>(empty + STAGES);
     float* st_l = st_m + NWC * HP;
@@ -181,6 +191,37 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
     // ---------------------------------------------------------------- consumers
     uint32_t qf[NT][KT][2];
     load_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + h0) * D, p.G, lane);
+    float scale_log2 = p.scale_log2;
+    if constexpr (KV8 && std::is_same<T, __nv_bfloat16>::value) {
+        // bf16 queries meet fp16 keys: convert them, scaled by 2^-e when
+        // |q| > 2^15 so that they stay inside the fp16 range (e is the same
+        // in every warp: each holds the whole group's Q); 2^e goes into the
+        // score scale.
+        uint32_t mx = 0;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    mx = max(mx, max((qf[nt][kk][j] << 16) & 0x7FFFFFFFu, qf[nt][kk][j] & 0x7FFF0000u));
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        const int ex = (int)((mx >> 23) & 0xFF) - 127;   // floor(log2 max|q|) for normal values
+        const int e = min(max(ex - 14, 0), 120);
+        const float down = exp2f((float)-e);
+        scale_log2 *= exp2f((float)e);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t w = qf[nt][kk][j];
+                    const __half2 h = __floats2half2_rn(__uint_as_float(w << 16) * down,
+                                                        __uint_as_float(w & 0xFFFF0000u) * down);
+                    qf[nt][kk][j] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+    }
     WarpState<D, NT> ws;
     ws.reset();
 
@@ -197,9 +238,20 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
         }
         uint8_t* ks = ring + stg * 2 * SLICE;
         const int valid = (pg0 + i == last_pg) ? n - last_pg * BS : BS;
-        page_step<T, LAYOUT, D, NT>(ks, ks + SLICE, valid, p.scale_log2, qf, ws, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stg]);
+        if constexpr (KV8) {
+            // expand into this warp's fp16 slices; the ring stage is free again at once
+            uint8_t* sk = staging + warp * 2 * (BS * D * 2);
+            expand_fp8_slice<D>(ks, sk, lane);
+            expand_fp8_slice<D>(ks + SLICE, sk + BS * D * 2, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stg]);
+            page_step<MT, kLayoutNHD, D, NT>(sk, sk + BS * D * 2, valid, scale_log2, qf, ws, lane);
+            __syncwarp();
+        } else {
+            page_step<T, LAYOUT, D, NT>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stg]);
+        }
     }
     if (!ok && lane == 0 && p.err) atomicOr(p.err, kErrTimeout);
 
@@ -253,6 +305,10 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
             sum.z += v.z;
             sum.w += v.w;
         }
+        sum.x *= p.v_scale;
+        sum.y *= p.v_scale;
+        sum.z *= p.v_scale;
+        sum.w *= p.v_scale;
         const size_t bh = (size_t)b * p.Hq + h0 + h;
         if (direct) {
             const float inv = 1.f / L;
@@ -274,7 +330,7 @@ __global__ void __launch_bounds__((DecodeTile<D>::NWC + 1) * 32)
 template <typename T, int LAYOUT, int D, int NT>
 cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                  const CUtensorMap& tmv, cudaStream_t stream) {
-    using Tile = DecodeTile<D>;
+    using Tile = DecodeTile<D, LAYOUT>;
     auto kern = decode_phase1_kernel<T, LAYOUT, D, NT>;
     const int smem = Tile::smem_bytes(NT);
     static bool attr_set[64] = {};

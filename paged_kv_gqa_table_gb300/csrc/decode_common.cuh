@@ -16,7 +16,10 @@
 
 namespace pkv {
 
-enum { kLayoutNHD = 0, kLayoutVLLM = 1 };
+// kLayoutNHD8: the NHD layout with FP8 E4M3 elements (K = k_scale * fp8,
+// V = v_scale * fp8).  Its pages are expanded to fp16 in shared memory and
+// then take the kLayoutNHD path with fp16 tensor-core arithmetic.
+enum { kLayoutNHD = 0, kLayoutVLLM = 1, kLayoutNHD8 = 2 };
 constexpr int kPageTokens = 16;
 
 __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
@@ -185,12 +188,45 @@ __device__ __forceinline__ void page_step(uint8_t* ks, uint8_t* vs, int valid, f
     }
 }
 
+// Two FP8 E4M3 values (low byte first) to two fp16 values, exactly (every
+// E4M3 value is an fp16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+// Expands one FP8 page slice ([BS][D] bytes, row-major, as TMA copied it)
+// into the fp16 NHD slice layout page_step reads (nhd_off: 64-element blocks,
+// 128-byte swizzle).  One warp; each lane converts 8 bytes at a time.
+template <int D>
+__device__ __forceinline__ void expand_fp8_slice(const uint8_t* src, uint8_t* dst, int lane) {
+    constexpr int BS = kPageTokens, CH = D / 8;   // 16-byte fp16 chunks per row
+#pragma unroll
+    for (int idx = lane; idx < BS * CH; idx += 32) {
+        const int t = idx / CH, c = idx % CH;
+        const uint2 w = *reinterpret_cast<const uint2*>(src + t * D + c * 8);
+        uint4 o;
+        o.x = e4m3x2_to_f16x2((uint16_t)(w.x & 0xFFFFu));
+        o.y = e4m3x2_to_f16x2((uint16_t)(w.x >> 16));
+        o.z = e4m3x2_to_f16x2((uint16_t)(w.y & 0xFFFFu));
+        o.w = e4m3x2_to_f16x2((uint16_t)(w.y >> 16));
+        *reinterpret_cast<uint4*>(dst + nhd_off<BS>(t, c)) = o;
+    }
+}
+
 // Issues the TMA loads of one page slice pair (K and V of one KV head) into a
-// ring stage, completing on `bar` (2 * BS * D * 2 bytes).
+// ring stage, completing on `bar` (2 * BS * D * element-size bytes).
 template <int LAYOUT, int D>
 __device__ __forceinline__ void issue_page_loads(uint8_t* kd, uint8_t* vd, const CUtensorMap* tmk,
                                                  const CUtensorMap* tmv, uint64_t* bar, int slice, uint64_t pol) {
     constexpr int BS = kPageTokens;
+    if (LAYOUT == kLayoutNHD8) {   // one unswizzled {D, BS} byte box per slice
+        mbar_arrive_expect_tx(bar, 2 * BS * D);
+        tma_load_3d(kd, tmk, bar, 0, 0, slice, pol);
+        tma_load_3d(vd, tmv, bar, 0, 0, slice, pol);
+        return;
+    }
     mbar_arrive_expect_tx(bar, 2 * BS * D * 2);
     if (LAYOUT == kLayoutNHD) {
 #pragma unroll

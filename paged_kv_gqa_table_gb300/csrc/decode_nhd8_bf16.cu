@@ -1,0 +1,17 @@
+// decode_nhd8_bf16.cu -- phase-1 instantiations for FP8 E4M3 caches in the NHD
+// layout ([num_blocks][Hkv][block_size][D] bytes) with bf16 queries and output.
+#include "internal.h"
+
+namespace pkv {
+
+cudaError_t launch_decode_nhd8_bf16(int D, int nt, const DecodeParams& p, long long grid, const CUtensorMap& k,
+                                 const CUtensorMap& v, cudaStream_t s) {
+    if (D == 64 && nt == 1) return launch_decode_phase1<__nv_bfloat16, kLayoutNHD8, 64, 1>(p, grid, k, v, s);
+    if (D == 64 && nt == 2) return launch_decode_phase1<__nv_bfloat16, kLayoutNHD8, 64, 2>(p, grid, k, v, s);
+    if (D == 128 && nt == 1) return launch_decode_phase1<__nv_bfloat16, kLayoutNHD8, 128, 1>(p, grid, k, v, s);
+    if (D == 128 && nt == 2) return launch_decode_phase1<__nv_bfloat16, kLayoutNHD8, 128, 2>(p, grid, k, v, s);
+    if (D == 256 && nt == 1) return launch_decode_phase1<__nv_bfloat16, kLayoutNHD8, 256, 1>(p, grid, k, v, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

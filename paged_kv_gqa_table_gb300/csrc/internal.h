@@ -25,6 +25,11 @@ cudaError_t launch_decode_vllm_f16(int D, int nt, const DecodeParams& p, long lo
                                    cudaStream_t s);
 cudaError_t launch_decode_vllm_bf16(int D, int nt, const DecodeParams& p, long long grid, const CUtensorMap& k,
                                     const CUtensorMap& v, cudaStream_t s);
+// FP8 E4M3 caches (NHD layout), fp16 / bf16 queries and output.
+cudaError_t launch_decode_nhd8_f16(int D, int nt, const DecodeParams& p, long long grid, const CUtensorMap& k,
+                                   const CUtensorMap& v, cudaStream_t s);
+cudaError_t launch_decode_nhd8_bf16(int D, int nt, const DecodeParams& p, long long grid, const CUtensorMap& k,
+                                    const CUtensorMap& v, cudaStream_t s);
 
 // MLA paged causal prefill (mla.cu); bf16 tensors, page size 1.
 struct MlaParams {

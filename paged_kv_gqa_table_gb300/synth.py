@@ -236,6 +236,9 @@ WORKLOADS = {
                                 ctx_range=(32768, 131072), max_blocks_per_seq=8192),
     "gqa6_d256_vllm_decode": dict(B=128, Hq=24, Hkv=4, D=256, block_size=16, dtype=F16, layout=VLLM,
                                   ctx_range=(512, 8192), max_blocks_per_seq=512),
+    # the Llama-3-8B-shaped step with an FP8 E4M3 KV cache (K, V = N(0,1) / 16 stored, scales 1/16)
+    "llama3_8b_decode_fp8": dict(B=64, Hq=32, Hkv=8, D=128, block_size=16, dtype=BF16, layout=NHD,
+                                 ctx_range=(1, 4096), max_blocks_per_seq=256, kv_dtype=FP8_E4M3),
 }
 MLA_WORKLOADS = {
     "mla_prefill_h16": dict(batch=8, q_len_range=(64, 512), prefix_range=(0, 2048)),
@@ -243,5 +246,7 @@ MLA_WORKLOADS = {
 
 
 def kv_bytes(case: dict) -> int:
-    """Algorithmic KV bytes of one decode step: live tokens x Hkv x D x (K and V) x 2 bytes."""
-    return int(np.sum(case["context_lens"], dtype=np.int64)) * case["Hkv"] * case["D"] * 2 * 2
+    """Algorithmic KV bytes of one decode step: live tokens x Hkv x D x (K and V) x element bytes
+    (2 for fp16/bf16 caches, 1 for FP8 E4M3)."""
+    e = 1 if case.get("kv_dtype", case["dtype"]) == FP8_E4M3 else 2
+    return int(np.sum(case["context_lens"], dtype=np.int64)) * case["Hkv"] * case["D"] * 2 * e

@@ -27,17 +27,29 @@ def int_to_torch(a: np.ndarray, device, pin: bool = False) -> torch.Tensor:
     return t.to(device)
 
 
+def fp8_kv(case: dict) -> bool:
+    return case.get("kv_dtype", case["dtype"]) == synth.FP8_E4M3
+
+
 def decode_desc(case: dict) -> B.pkv_decode_desc:
     ctx = case["context_lens"]
+    kv = dict(kv_dtype=B.PKV_FP8_E4M3, k_scale=case["k_scale"], v_scale=case["v_scale"]) if fp8_kv(case) else {}
     return B.make_desc(case["B"], case["Hq"], case["Hkv"], case["D"], case["block_size"],
                        case["block_table"].shape[1], case["num_blocks"], int(np.max(ctx, initial=0)),
-                       int(np.sum(ctx, dtype=np.int64)), case["dtype"], case["layout"], case.get("x", 8))
+                       int(np.sum(ctx, dtype=np.int64)), case["dtype"], case["layout"], case.get("x", 8), **kv)
+
+
+def cache_to_torch(bits: np.ndarray, case: dict, device) -> torch.Tensor:
+    """A KV cache array: fp16/bf16 bits as that dtype, FP8 E4M3 bits as uint8."""
+    if fp8_kv(case):
+        return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).to(device)
+    return bits_to_torch(bits, case["dtype"], device)
 
 
 def upload_decode_case(case: dict, device="cuda") -> dict:
     dt = case["dtype"]
-    return dict(q=bits_to_torch(case["q"], dt, device), k_cache=bits_to_torch(case["k_cache"], dt, device),
-                v_cache=bits_to_torch(case["v_cache"], dt, device),
+    return dict(q=bits_to_torch(case["q"], dt, device), k_cache=cache_to_torch(case["k_cache"], case, device),
+                v_cache=cache_to_torch(case["v_cache"], case, device),
                 block_table=int_to_torch(case["block_table"], device),
                 context_lens=int_to_torch(case["context_lens"], device))
 

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_function(B):
 
 
 def test_version_and_status_strings(B):
-    assert B.pkv_version() == 1
+    assert B.pkv_version() == 2
     assert B.status_string(0) == "ok"
     assert B.status_string(5) == "bad block table"
     assert B.status_string(99) == "unknown status"
@@ -212,3 +212,18 @@ def test_library_exports_only_the_declared_functions(B):
     ours = {n for n in exported if not n.startswith("_")}
     assert ours == set(declared_functions()), sorted(ours ^ set(declared_functions()))
     assert not any(parts.split()[1] == "u" for parts in out.splitlines() if len(parts.split()) == 3)
+
+
+def test_fp8_descriptions(B):
+    base = dict(B=8, Hq=32, Hkv=8, D=128, block_size=16, max_blocks_per_seq=64, num_blocks=500,
+                max_context_len=1000, sum_context_len=8000, dtype=1)
+    ok = B.make_desc(**base, kv_dtype=B.PKV_FP8_E4M3, k_scale=0.1, v_scale=0.2)
+    assert B.pkv_plan_splits(ok, None, 152) == B.pkv_plan_splits(B.make_desc(**base), None, 152)
+    assert B.pkv_decode_workspace_size(ok, None, 152) == B.pkv_decode_workspace_size(B.make_desc(**base), None, 152)
+    for kw, status in ((dict(kv_dtype=3), B.PKV_INVALID_ARG), (dict(kv_dtype=1), B.PKV_INVALID_ARG),
+                       (dict(kv_dtype=2, k_scale=0.0, v_scale=1.0), B.PKV_INVALID_ARG),
+                       (dict(kv_dtype=2, k_scale=1.0, v_scale=float("nan")), B.PKV_INVALID_ARG),
+                       (dict(kv_dtype=2, k_scale=1.0, v_scale=1.0, layout=1), B.PKV_UNSUPPORTED)):
+        with pytest.raises(B.PkvError) as e:
+            B.pkv_plan_splits(B.make_desc(**{**base, **kw}), None, 152)
+        assert e.value.status == status, kw

@@ -216,3 +216,70 @@ def test_full_size_workloads_sampled(name):
         list(ex.map(lambda b: oracle.decode(case, b, b + 1, out=ref), idx))
     worst = float(np.max(np.abs(got[idx] - ref[idx])))
     assert worst <= TOL[case["dtype"]], worst
+
+
+# ------------------------------------------------------------ FP8 caches ----
+
+FP8_CASES = [
+    (synth.BF16, 128, 4, (1, 3000), 0),      # Llama-3-8B-shaped heads, planner
+    (synth.F16, 128, 4, (0, 700), 64),       # fp16 queries, empty contexts, small splits
+    (synth.BF16, 64, 8, (1, 500), 0),
+    (synth.F16, 256, 6, (17, 1200), 256),    # D = 256
+    (synth.BF16, 128, 16, (1, 900), 128),    # two head tiles
+]
+
+
+@pytest.mark.parametrize("dtype,D,G,ctx,P", FP8_CASES)
+def test_fp8_kv_cache_matches_oracle(dtype, D, G, ctx, P):
+    B = _binding()
+    case = _case(21, B=19, Hq=2 * G, Hkv=2, D=D, block_size=16, dtype=dtype, layout=synth.NHD, ctx_range=ctx,
+                 max_blocks_per_seq=200, kv_dtype=synth.FP8_E4M3, k_scale=0.05, v_scale=0.07, slack_pages=5,
+                 poison=True)
+    got = gpu_out(case, B.make_opts(partition_tokens=P) if P else None)
+    check_rows(case, got, list(range(case["B"])))
+
+
+def test_fp8_poisoned_unread_slots_are_bit_identical():
+    kw = dict(B=11, Hq=16, Hkv=4, D=128, block_size=16, dtype=synth.BF16, layout=synth.NHD, ctx_range=(1, 600),
+              kv_dtype=synth.FP8_E4M3, slack_pages=9)
+    clean = gpu_out(_case(22, **kw))
+    dirty = gpu_out(_case(22, poison=True, **kw))
+    assert np.array_equal(clean, dirty)
+
+
+def test_fp8_partials_match_oracle():
+    B = _binding()
+    T = _tensors()
+    case = _case(23, B=9, Hq=8, Hkv=2, D=128, block_size=16, dtype=synth.F16, layout=synth.NHD,
+                 ctx_range=(0, 900), kv_dtype=synth.FP8_E4M3, k_scale=0.03, v_scale=0.1)
+    dev = T.upload_decode_case(case)
+    NS_cap = 8
+    acc = torch.empty((9, 8, NS_cap, 128), device="cuda")
+    m = torch.empty((9, 8, NS_cap), device="cuda")
+    l = torch.empty((9, 8, NS_cap), device="cuda")
+    P, ns = B.pkv_decode_partials(T.decode_desc(case), dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
+                                  dev["context_lens"], case["scale"], acc, m, l, NS_cap,
+                                  opts=B.make_opts(partition_tokens=128))
+    torch.cuda.synchronize()
+    pm, pl, pacc = oracle.decode_partials(case, P, ns)
+    gm, gl, gacc = m.cpu().numpy()[:, :, :ns], l.cpu().numpy()[:, :, :ns], acc.cpu().numpy()[:, :, :ns]
+    live = pl > 0
+    assert np.array_equal(live, gl > 0)
+    assert np.all(np.isneginf(gm[~live]))
+    lse_g, lse_r = gm[live] + np.log(gl[live]), pm[live] + np.log(pl[live])
+    assert np.max(np.abs(lse_g - lse_r)) <= 1e-3
+    assert np.max(np.abs(gacc[live] / gl[live][:, None] - pacc[live] / pl[live][:, None])) <= TOL[synth.F16]
+
+
+def test_fp8_with_bf16_queries_beyond_the_fp16_range():
+    # bf16 queries up to ~2^22 (scaled by 2^20) with the score scale reduced by
+    # the same factor: same attention, but the queries only fit fp16 after the
+    # kernel's power-of-two down-scaling.
+    case = _case(24, B=6, Hq=8, Hkv=2, D=128, block_size=16, dtype=synth.BF16, layout=synth.NHD,
+                 ctx_range=(20, 400), kv_dtype=synth.FP8_E4M3)
+    qf = synth.bits_to_f32(case["q"], synth.BF16) * np.float32(2.0 ** 20)
+    case["q"] = synth.f32_to_bits(qf, synth.BF16).reshape(case["q"].shape)
+    case["scale"] = case["scale"] * 2.0 ** -20
+    got = gpu_out(case)
+    assert np.all(np.isfinite(got))
+    check_rows(case, got, list(range(case["B"])))
