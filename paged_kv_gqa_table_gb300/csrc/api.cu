@@ -151,10 +151,12 @@ int encode_cache_map(CUtensorMap* map, const void* base, const pkv_decode_desc* 
         dims[2] = slices;
         strides[0] = (cuuint64_t)d->D;
         strides[1] = (cuuint64_t)d->D * d->block_size;
-        box[0] = d->D;
+        // D >= 128: 128-byte-wide boxes with 128-byte swizzle (read straight into mma
+        // fragments); D = 64: one unswizzled {64, BS} box (expanded in shared memory)
+        box[0] = d->D >= 128 ? 128 : d->D;
         box[1] = d->block_size;
         box[2] = 1;
-        swz = CU_TENSOR_MAP_SWIZZLE_NONE;
+        swz = d->D >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
     } else if (d->layout == PKV_LAYOUT_NHD) {
         dims[0] = d->D;
         dims[1] = d->block_size;

@@ -61,9 +61,11 @@ struct DecodeTile {
     static constexpr int NWC = 4;                                   // consumer warps
     static constexpr int KVB = LAYOUT == kLayoutNHD8 ? 1 : 2;       // bytes per cache element
     static constexpr int SLICE = BS * D * KVB;                      // bytes of one page slice
-    static constexpr int STAGES = D == 64 ? 12 : (D == 128 ? 8 : 4);
-    // FP8 pages are expanded to fp16 in a per-consumer-warp K/V slice pair
-    static constexpr int STAGING = KVB == 1 ? NWC * 2 * BS * D * 2 : 0;
+    // FP8 pages with D >= 128 keep twice the stages: the same bytes in flight as 16-bit pages
+    static constexpr int STAGES = (D == 64 ? 12 : (D == 128 ? 8 : 4)) * ((KVB == 1 && D >= 128) ? 2 : 1);
+    // FP8 pages with D = 64 are expanded to fp16 in a per-consumer-warp K/V
+    // slice pair; D >= 128 goes straight from the ring into mma fragments.
+    static constexpr int STAGING = (KVB == 1 && D < 128) ? NWC * 2 * BS * D * 2 : 0;
     static constexpr int RED_STRIDE = D + 4;                        // floats per reduction row
     static constexpr int smem_bytes(int nt) {
         return 1024 + STAGES * 2 * SLICE + STAGING + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 16;
@@ -76,6 +78,7 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
                          const __grid_constant__ CUtensorMap tmv) {
     using Tile = DecodeTile<D, LAYOUT>;
     constexpr bool KV8 = LAYOUT == kLayoutNHD8;
+    constexpr bool DIRECT8 = KV8 && D >= 128;   // page_step_fp8, no staging
     using MT = typename std::conditional<KV8, __half, T>::type;   // tensor-core operand type
     constexpr int BS = Tile::BS, NWC = Tile::NWC, SLICE = Tile::SLICE, STAGES = Tile::STAGES;
     constexpr int KT = D / 16;   // k-steps of Q.K^T and d-tiles of P.V
@@ -190,9 +193,15 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
 
     // ---------------------------------------------------------------- consumers
     uint32_t qf[NT][KT][2];
-    load_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + h0) * D, p.G, lane);
     float scale_log2 = p.scale_log2;
-    if constexpr (KV8 && std::is_same<T, __nv_bfloat16>::value) {
+    if constexpr (DIRECT8) {
+        const int qe = fp8_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + h0) * D,
+                                             p.G, lane);
+        scale_log2 *= exp2f((float)qe);
+    } else {
+        load_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + h0) * D, p.G, lane);
+    }
+    if constexpr (KV8 && !DIRECT8 && std::is_same<T, __nv_bfloat16>::value) {
         // bf16 queries meet fp16 keys: convert them, scaled by 2^-e when
         // |q| > 2^15 so that they stay inside the fp16 range (e is the same
         // in every warp: each holds the whole group's Q); 2^e goes into the
@@ -238,7 +247,11 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
         }
         uint8_t* ks = ring + stg * 2 * SLICE;
         const int valid = (pg0 + i == last_pg) ? n - last_pg * BS : BS;
-        if constexpr (KV8) {
+        if constexpr (DIRECT8) {
+            page_step_fp8<D, NT>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stg]);
+        } else if constexpr (KV8) {
             // expand into this warp's fp16 slices; the ring stage is free again at once
             uint8_t* sk = staging + warp * 2 * (BS * D * 2);
             expand_fp8_slice<D>(ks, sk, lane);
@@ -278,11 +291,20 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
 #pragma unroll
             for (int w = 0; w < NWC; ++w) M = fmaxf(M, st_m[w * HP + h]);
             const float f = ex2(ws.m[nt][j] - M);   // 0 for a warp that saw no page
-            float* row = red + (warp * HP + h) * RS + (lane >> 2);
+            if constexpr (DIRECT8) {   // mma rows g, g+8 of d-tile dt hold d = 16dt + 2g, 16dt + 2g + 1
+                float* row = red + (warp * HP + h) * RS + 2 * (lane >> 2);
 #pragma unroll
-            for (int dt = 0; dt < KT; ++dt) {
-                row[dt * 16] = ws.acc[dt][nt][j] * f;
-                row[dt * 16 + 8] = ws.acc[dt][nt][j + 2] * f;
+                for (int dt = 0; dt < KT; ++dt) {
+                    row[dt * 16] = ws.acc[dt][nt][j] * f;
+                    row[dt * 16 + 1] = ws.acc[dt][nt][j + 2] * f;
+                }
+            } else {
+                float* row = red + (warp * HP + h) * RS + (lane >> 2);
+#pragma unroll
+                for (int dt = 0; dt < KT; ++dt) {
+                    row[dt * 16] = ws.acc[dt][nt][j] * f;
+                    row[dt * 16 + 8] = ws.acc[dt][nt][j + 2] * f;
+                }
             }
         }
     named_bar_sync(1, NWC * 32);

@@ -12,6 +12,8 @@
 // log2 units: scale_log2 = scale * log2(e).
 #pragma once
 
+#include <type_traits>
+
 #include "ptx.cuh"
 
 namespace pkv {
@@ -215,16 +217,188 @@ __device__ __forceinline__ void expand_fp8_slice(const uint8_t* src, uint8_t* ds
     }
 }
 
+// ---- FP8 pages straight into fp16 mma fragments (D >= 128) ------------------
+//
+// The slices arrive as 128-byte-wide TMA boxes with 128-byte swizzle: token row
+// t of 128-column block j, 16-byte chunk c (16 elements) at
+// j*BS*128 + t*128 + ((c ^ (t & 7)) << 4).  An ldmatrix.x4 (b16 view) of
+// chunks (c, c+1), rows 0-7 and 8-15 gives lane (g = lane/4, q = lane%4) the
+// bytes 4q..4q+3 of its row in each chunk.
+//
+// S^T = K.Q^T: the four bytes of one chunk feed one m16n8k16 with the
+// k-index permuted -- mma k = 2q+j <-> d = 16c+4q+j and k = 2q+8+j <->
+// d = 16c+4q+2+j -- so the Q (B) fragments are loaded with the same
+// permutation (fp8_q_frags) and the dot products are unchanged.
+// O^T += V^T.P^T: ldmatrix.x4.trans gives lane (g, q) the bytes
+// V[2q][2g], V[2q][2g+1], V[2q+1][2g], V[2q+1][2g+1] of a chunk; one byte
+// permute splits them into rows d = 2g and 2g+1 for tokens (2q, 2q+1), i.e.
+// mma rows g and g+8 hold d = 16c+2g and 16c+2g+1: the output rows are
+// permuted, and the merge writes them back in order.
+
+__device__ __forceinline__ uint32_t fp8_off(int t, int c) {   // chunk c (16 B) of row t
+    return (uint32_t)((c >> 3) * (kPageTokens * 128) + t * 128 + (((c & 7) ^ (t & 7)) << 4));
+}
+
+// Q fragments in the permuted k order above: qf[nt][kk][0] = (q[16kk+4q], q[16kk+4q+1]),
+// qf[nt][kk][1] = (q[16kk+4q+2], q[16kk+4q+3]) of head nt*8 + g, as fp16 pairs.
+// bf16 queries are scaled by 2^-e (returned) when |q| > 2^15 to fit fp16; e is
+// a warp-wide maximum, the same in every warp of the CTA.
+template <typename T, int D, int NT>
+__device__ __forceinline__ int fp8_q_frags(uint32_t (&qf)[NT][D / 16][2], const T* qb, int G, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+    uint2 raw[NT][D / 16];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hh = nt * 8 + g;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+            raw[nt][kk] = hh < G ? *reinterpret_cast<const uint2*>(qb + hh * D + kk * 16 + 4 * q) : make_uint2(0u, 0u);
+    }
+    if constexpr (std::is_same<T, __half>::value) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                qf[nt][kk][0] = raw[nt][kk].x;
+                qf[nt][kk][1] = raw[nt][kk].y;
+            }
+        return 0;
+    } else {
+        uint32_t mx = 0;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t w0 = raw[nt][kk].x, w1 = raw[nt][kk].y;
+                mx = max(mx, max((w0 << 16) & 0x7FFFFFFFu, w0 & 0x7FFF0000u));
+                mx = max(mx, max((w1 << 16) & 0x7FFFFFFFu, w1 & 0x7FFF0000u));
+            }
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        const int e = min(max((int)((mx >> 23) & 0xFF) - 127 - 14, 0), 120);
+        const float down = exp2f((float)-e);
+        auto cv = [&](uint32_t w) {
+            const __half2 h = __floats2half2_rn(__uint_as_float(w << 16) * down, __uint_as_float(w & 0xFFFF0000u) * down);
+            return *reinterpret_cast<const uint32_t*>(&h);
+        };
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                qf[nt][kk][0] = cv(raw[nt][kk].x);
+                qf[nt][kk][1] = cv(raw[nt][kk].y);
+            }
+        return e;
+    }
+}
+
+// One FP8 page (swizzled K and V slices in the ring) into the warp's state, as
+// page_step; fp16 tensor-core arithmetic.  V rows past `valid` are zeroed in
+// the ring stage first (the caller fences before the stage is refilled).
+template <int D, int NT>
+__device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int valid, float scale_log2,
+                                              const uint32_t (&qf)[NT][D / 16][2], WarpState<D, NT>& st, int lane) {
+    constexpr int BS = kPageTokens, KT = D / 16;
+    const int mi = lane >> 3, r8 = lane & 7;
+    const int t_l = r8 + ((mi & 1) << 3), c_l = mi >> 1;   // this lane's ldmatrix row and chunk offset
+    const uint32_t ks_a = smem_u32(ks), vs_a = smem_u32(vs);
+
+    float sc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int c2 = 0; c2 < KT / 2; ++c2) {
+        uint32_t r[4];
+        ldsm_x4(ks_a + fp8_off(t_l, 2 * c2 + c_l), r);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {   // chunk 2*c2 + h: k-step kk
+            const uint32_t* rr = r + 2 * h;
+            const uint32_t a[4] = {e4m3x2_to_f16x2((uint16_t)(rr[0] & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(rr[1] & 0xFFFFu)),
+                                   e4m3x2_to_f16x2((uint16_t)(rr[0] >> 16)), e4m3x2_to_f16x2((uint16_t)(rr[1] >> 16))};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) Mma<__half>::run(sc[nt], a, qf[nt][2 * c2 + h][0], qf[nt][2 * c2 + h][1]);
+        }
+    }
+
+    // scale to log2 units, mask, online-softmax update (as page_step)
+    const int tr = lane >> 2;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int t = tr + ((e >> 1) << 3);
+            sc[nt][e] = t < valid ? sc[nt][e] * scale_log2 : -INFINITY;
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float mx = fmaxf(sc[nt][j], sc[nt][j + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mnew = fmaxf(st.m[nt][j], mx);
+            const float alpha = ex2(st.m[nt][j] - mnew);
+            st.m[nt][j] = mnew;
+            sc[nt][j] = ex2(sc[nt][j] - mnew);
+            sc[nt][j + 2] = ex2(sc[nt][j + 2] - mnew);
+            st.l[nt][j] = st.l[nt][j] * alpha + (sc[nt][j] + sc[nt][j + 2]);
+#pragma unroll
+            for (int dt = 0; dt < KT; ++dt) {
+                st.acc[dt][nt][j] *= alpha;
+                st.acc[dt][nt][j + 2] *= alpha;
+            }
+        }
+    }
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        pb[nt][0] = movmatrix_trans(Mma<__half>::pack(sc[nt][0], sc[nt][1]));
+        pb[nt][1] = movmatrix_trans(Mma<__half>::pack(sc[nt][2], sc[nt][3]));
+    }
+
+    if (valid < BS) {   // zero whole V rows past the context (layout-agnostic within a row)
+        constexpr int ROWB = 128 / 16;   // 16-byte pieces per 128-byte row
+        const int pieces = (BS - valid) * ROWB * (D / 128);
+        for (int i = lane; i < pieces; i += 32) {
+            const int blk = i / ((BS - valid) * ROWB), rem = i % ((BS - valid) * ROWB);
+            *reinterpret_cast<uint4*>(vs + blk * (BS * 128) + (valid + rem / ROWB) * 128 + (rem % ROWB) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+    }
+
+#pragma unroll
+    for (int c2 = 0; c2 < KT / 2; ++c2) {
+        uint32_t r[4];
+        ldsm_x4_trans(vs_a + fp8_off(t_l, 2 * c2 + c_l), r);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {   // chunk 2*c2 + h: output rows dt = 2*c2 + h
+            const uint32_t lo = __byte_perm(r[2 * h], 0u, 0x3120), hi = __byte_perm(r[2 * h + 1], 0u, 0x3120);
+            const uint32_t a[4] = {e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(lo >> 16)),
+                                   e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(hi >> 16))};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) Mma<__half>::run(st.acc[2 * c2 + h][nt], a, pb[nt][0], pb[nt][1]);
+        }
+    }
+}
+
 // Issues the TMA loads of one page slice pair (K and V of one KV head) into a
 // ring stage, completing on `bar` (2 * BS * D * element-size bytes).
 template <int LAYOUT, int D>
 __device__ __forceinline__ void issue_page_loads(uint8_t* kd, uint8_t* vd, const CUtensorMap* tmk,
                                                  const CUtensorMap* tmv, uint64_t* bar, int slice, uint64_t pol) {
     constexpr int BS = kPageTokens;
-    if (LAYOUT == kLayoutNHD8) {   // one unswizzled {D, BS} byte box per slice
+    if (LAYOUT == kLayoutNHD8) {
         mbar_arrive_expect_tx(bar, 2 * BS * D);
-        tma_load_3d(kd, tmk, bar, 0, 0, slice, pol);
-        tma_load_3d(vd, tmv, bar, 0, 0, slice, pol);
+        if (D >= 128) {   // 128-byte-wide swizzled boxes (page_step_fp8)
+#pragma unroll
+            for (int j = 0; j < D / 128; ++j) {
+                tma_load_3d(kd + j * BS * 128, tmk, bar, j * 128, 0, slice, pol);
+                tma_load_3d(vd + j * BS * 128, tmv, bar, j * 128, 0, slice, pol);
+            }
+        } else {          // one unswizzled {D, BS} byte box (expanded by expand_fp8_slice)
+            tma_load_3d(kd, tmk, bar, 0, 0, slice, pol);
+            tma_load_3d(vd, tmv, bar, 0, 0, slice, pol);
+        }
         return;
     }
     mbar_arrive_expect_tx(bar, 2 * BS * D * 2);
