@@ -49,9 +49,9 @@ def _load():
             lib.oracle_widen.restype = d
             lib.oracle_widen8.argtypes = [ctypes.c_uint8]
             lib.oracle_widen8.restype = d
-            lib.oracle_decode.argtypes = [i] * 11 + [p] * 5 + [d, d, d, i, i, p, p, p]
+            lib.oracle_decode.argtypes = [i] * 11 + [p] * 5 + [d, d, d, p, i, i, p, p, p]
             lib.oracle_decode.restype = i
-            lib.oracle_decode_partials.argtypes = [i] * 11 + [p] * 5 + [d, d, d, i, i, i, i, p, p, p, p]
+            lib.oracle_decode_partials.argtypes = [i] * 11 + [p] * 5 + [d, d, d, p, i, i, i, i, p, p, p, p]
             lib.oracle_decode_partials.restype = i
             lib.oracle_combine.argtypes = [i, i, i, i, p, p, p, p, i, i, p]
             lib.oracle_combine.restype = i
@@ -97,12 +97,16 @@ def _decode_common(case):
             table.shape[1] if table.ndim == 2 else 0, case["num_blocks"],
             case["dtype"], case["layout"], case.get("x", 8), kv_dtype]
     scales = [float(case["scale"]), float(case.get("k_scale", 1.0)), float(case.get("v_scale", 1.0))]
-    return dims, (q, k, v, table, ctx), scales
+    alibi = case.get("alibi_slopes")
+    if alibi is not None:
+        alibi = _c(alibi, np.float64)
+        assert alibi.shape == (case["Hq"],)
+    return dims, (q, k, v, table, ctx), scales, alibi
 
 
 def decode(case, b_lo: int = 0, b_hi: int | None = None, out: np.ndarray | None = None) -> np.ndarray:
     """fp64 attention output [B][Hq][D] (only rows b in [b_lo, b_hi) are filled)."""
-    dims, arrs, scales = _decode_common(case)
+    dims, arrs, scales, alibi = _decode_common(case)
     B, Hq, D = case["B"], case["Hq"], case["D"]
     b_hi = B if b_hi is None else b_hi
     if out is None:
@@ -110,7 +114,7 @@ def decode(case, b_lo: int = 0, b_hi: int | None = None, out: np.ndarray | None 
     maxn = int(max(1, int(np.max(arrs[4][b_lo:b_hi], initial=1))))
     sbuf = np.zeros(maxn)
     acc = np.zeros(D)
-    st = _load().oracle_decode(*dims, *[_ptr(a) for a in arrs], *scales,
+    st = _load().oracle_decode(*dims, *[_ptr(a) for a in arrs], *scales, None if alibi is None else _ptr(alibi),
                                b_lo, b_hi, _ptr(out), _ptr(sbuf), _ptr(acc))
     if st:
         raise OracleError(st)
@@ -119,7 +123,7 @@ def decode(case, b_lo: int = 0, b_hi: int | None = None, out: np.ndarray | None 
 
 def decode_partials(case, P: int, NS: int, b_lo: int = 0, b_hi: int | None = None):
     """Split-mode partials (m, l, acc) with split s = tokens [s*P, min((s+1)*P, n))."""
-    dims, arrs, scales = _decode_common(case)
+    dims, arrs, scales, alibi = _decode_common(case)
     B, Hq, D = case["B"], case["Hq"], case["D"]
     b_hi = B if b_hi is None else b_hi
     pm = np.full((B, Hq, NS), np.nan)
@@ -127,7 +131,7 @@ def decode_partials(case, P: int, NS: int, b_lo: int = 0, b_hi: int | None = Non
     pacc = np.full((B, Hq, NS, D), np.nan)
     sbuf = np.zeros(max(1, P))
     st = _load().oracle_decode_partials(*dims, *[_ptr(a) for a in arrs], *scales,
-                                        int(P), int(NS), b_lo, b_hi,
+                                        None if alibi is None else _ptr(alibi), int(P), int(NS), b_lo, b_hi,
                                         _ptr(pm), _ptr(pl), _ptr(pacc), _ptr(sbuf))
     if st:
         raise OracleError(st)

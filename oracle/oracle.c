@@ -20,6 +20,10 @@
  *         Its launcher also takes kv_cache_dtype, k_scale and v_scale (and ignores
  *         them); the fp8 KV cache here reads them the plainest way: cache bytes
  *         are OCP FP8 E4M3 values and K = k_scale * fp8, V = v_scale * fp8.
+ *         It also takes alibi_slopes (ignored too); read as ALiBi's additive
+ *         bias: the score of key position t for query head h of a sequence of
+ *         length n gains slopes[h] * (t - (n - 1)) -- zero at the query's own
+ *         position, decreasing linearly with distance.
  *   [MLA] "kernelindex.com flashinfer gemini-2.5-pro triton xvhq2i"
  *         (mla_paged_prefill_causal_h16_ckv512_kpe64_ps1): sections
  *         "2. Determine Sequence Boundaries", "3. Pass 1", "4. Pass 2".
@@ -130,6 +134,7 @@ typedef struct {
     const void *k, *v;         /* 16-bit or 8-bit elements per kv_dtype */
     const int32_t *table, *ctx;
     double scale, k_scale, v_scale;   /* k_scale, v_scale multiply fp8 cache values (1 otherwise) */
+    const double* alibi;       /* per query head ALiBi slope, or NULL */
 } decode_args;
 
 /* Value of cache element i: exact widening, times the fp8 scale. */
@@ -207,10 +212,12 @@ static int attend_range(const decode_args* a, int b, int h, int t0, int t1,
         return 0;
     }
     double m = -INFINITY;
+    int n = seq_len(a, b);
     for (int t = t0; t < t1; ++t) {
         long long p = page_of(a, b, t);
         if (p < 0) return -1;
         sbuf[t - t0] = score(a, b, h, g, p, t % a->BS);
+        if (a->alibi) sbuf[t - t0] += a->alibi[h] * (double)(t - (n - 1));
         if (sbuf[t - t0] > m) m = sbuf[t - t0];
     }
     double l = 0.0;
@@ -238,10 +245,10 @@ int oracle_decode(int B, int Hq, int Hkv, int D, int BS, int MBPS, int NB,
                   int dtype, int layout, int x, int kv_dtype,
                   const uint16_t* q, const void* k, const void* v,
                   const int32_t* table, const int32_t* ctx, double scale, double k_scale, double v_scale,
-                  int b_lo, int b_hi, double* out, double* sbuf, double* acc)
+                  const double* alibi, int b_lo, int b_hi, double* out, double* sbuf, double* acc)
 {
     decode_args a = {B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x, kv_dtype, q, k, v, table, ctx,
-                     scale, k_scale, v_scale};
+                     scale, k_scale, v_scale, alibi};
     int st = check_decode(&a);
     if (st) return st;
     if (b_lo < 0 || b_hi > B || b_lo > b_hi) return OR_INVALID;
@@ -269,11 +276,11 @@ int oracle_decode_partials(int B, int Hq, int Hkv, int D, int BS, int MBPS, int 
                            int dtype, int layout, int x, int kv_dtype,
                            const uint16_t* q, const void* k, const void* v,
                            const int32_t* table, const int32_t* ctx, double scale, double k_scale,
-                           double v_scale, int P, int NS, int b_lo, int b_hi,
+                           double v_scale, const double* alibi, int P, int NS, int b_lo, int b_hi,
                            double* pm, double* pl, double* pacc, double* sbuf)
 {
     decode_args a = {B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x, kv_dtype, q, k, v, table, ctx,
-                     scale, k_scale, v_scale};
+                     scale, k_scale, v_scale, alibi};
     int st = check_decode(&a);
     if (st) return st;
     if (P <= 0 || NS <= 0 || b_lo < 0 || b_hi > B || b_lo > b_hi) return OR_INVALID;

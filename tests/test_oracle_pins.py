@@ -223,6 +223,53 @@ def test_decode_vs_torch_sdpa(idx):
     np.testing.assert_allclose(oracle.decode(case), ref, rtol=1e-10, atol=1e-12)
 
 
+@pytest.mark.parametrize("idx", [0, 1, 2])
+def test_alibi_decode_vs_torch_sdpa_with_additive_mask(idx):
+    # ALiBi as the additive float mask slope_h * (t - (n - 1)) of torch's SDPA.
+    torch = pytest.importorskip("torch")
+    case = synth.decode_case(seed=200 + idx, **SMALL_CASES[idx])
+    slopes = np.float32(2.0) ** -np.arange(1, case["Hq"] + 1, dtype=np.float32) * np.float32(3.0)
+    case["alibi_slopes"] = slopes
+    G = case["Hq"] // case["Hkv"]
+    q = widen_np(case["q"], case["dtype"])
+    ref = np.zeros((case["B"], case["Hq"], case["D"]))
+    for b in range(case["B"]):
+        n = int(case["context_lens"][b])
+        if n == 0:
+            continue
+        k, v = depage_dense(case, b)
+        kt = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        vt = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        qt = torch.from_numpy(q[b]).unsqueeze(1)
+        bias = torch.from_numpy(slopes.astype(np.float64))[:, None, None] * (torch.arange(n, dtype=torch.float64) - (n - 1))
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=bias, scale=case["scale"])
+        ref[b] = o[:, 0, :].numpy()
+    np.testing.assert_allclose(oracle.decode(case), ref, rtol=1e-10, atol=1e-12)
+
+
+def test_alibi_geometric_closed_form():
+    # q = 0 leaves only the bias: weights rho^j over distances j = n-1-t with
+    # rho = e^-s.  With V_t = t (every element), out = (n-1) - E[j], and
+    # E[j] = rho (1 - n rho^(n-1) + (n-1) rho^n) / ((1 - rho)(1 - rho^n)).
+    n_list = [1, 2, 5, 37, 100]
+    case = synth.decode_case(seed=3, B=len(n_list), Hq=2, Hkv=1, D=16, block_size=16, dtype=synth.BF16,
+                             context_lens=n_list)
+    case["q"] = np.zeros_like(case["q"])
+    v = np.zeros(case["v_cache"].shape, np.float32)
+    for b, n in enumerate(n_list):
+        for t in range(n):
+            v[case["block_table"][b, t // 16], 0, t % 16, :] = t
+    case["v_cache"] = synth.f32_to_bits(v, synth.BF16).reshape(case["v_cache"].shape)
+    s_h = [0.25, 1.5]
+    case["alibi_slopes"] = np.array(s_h, np.float32)
+    out = oracle.decode(case)
+    for b, n in enumerate(n_list):
+        for h, sl in enumerate(s_h):
+            rho = math.exp(-sl)
+            ej = 0.0 if n == 1 else rho * (1 - n * rho ** (n - 1) + (n - 1) * rho ** n) / ((1 - rho) * (1 - rho ** n))
+            np.testing.assert_allclose(out[b, h], (n - 1) - ej, rtol=1e-12, atol=1e-12)
+
+
 def test_relabel_pages_is_bit_identical():
     case = synth.decode_case(seed=7, **SMALL_CASES[2])
     moved = synth.relabel_pages(case, seed=3)
@@ -460,6 +507,8 @@ MUTANTS = [
     ("fp8 k_scale dropped", "cache_value(a, a->k, k_index(a->layout, a->Hkv, a->BS, a->D, a->x, p, g, o, d), a->k_scale)",
      "cache_value(a, a->k, k_index(a->layout, a->Hkv, a->BS, a->D, a->x, p, g, o, d), 1.0)"),
     ("fp8 v_scale dropped", "a->v_scale);\n}", "1.0);\n}"),
+    ("alibi sign flipped", "a->alibi[h] * (double)(t - (n - 1));", "a->alibi[h] * (double)((n - 1) - t);"),
+    ("alibi dropped", "if (a->alibi) sbuf[t - t0] += a->alibi[h] * (double)(t - (n - 1));", "(void)n;"),
 ]
 
 
@@ -483,7 +532,8 @@ def test_planted_mistakes_are_caught(tmp_path, monkeypatch, name, old, new):
     for fn in (lambda: test_decode_vs_numpy_brute_force(2), lambda: test_decode_vs_numpy_brute_force(0),
                lambda: test_split_then_combine_equals_unsplit(8), lambda: test_mla_vs_numpy_brute_force(0),
                test_widen_bf16_all_patterns, test_widen_e4m3_all_patterns,
-               lambda: test_fp8_cache_decode_equals_bf16_decode_of_the_same_values(0)):
+               lambda: test_fp8_cache_decode_equals_bf16_decode_of_the_same_values(0),
+               test_alibi_geometric_closed_form):
         try:
             fn()
         except (AssertionError, oracle.OracleError):
