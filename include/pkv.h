@@ -106,6 +106,11 @@ typedef struct {
      * full call.  NULL = not recorded. */
     void* phase1_event_start;
     void* phase1_event_stop;
+    /* Optional ALiBi slopes, device fp32 [Hq] (4-byte aligned): the score of
+     * key position t of a sequence of length n gains alibi_slopes[h] * (t - (n - 1))
+     * before the softmax (ALiBi's linear bias, zero at the query's own position;
+     * [V2]'s launcher takes alibi_slopes and ignores them).  NULL = no bias. */
+    const float* alibi_slopes;
 } pkv_decode_opts;
 
 /* Text of a status code (static storage). */

@@ -36,7 +36,8 @@ class pkv_decode_desc(ctypes.Structure):
 
 class pkv_decode_opts(ctypes.Structure):
     _fields_ = [("partition_tokens", ctypes.c_int), ("num_splits", ctypes.c_int), ("reserved", ctypes.c_int),
-                ("phase1_event_start", ctypes.c_void_p), ("phase1_event_stop", ctypes.c_void_p)]
+                ("phase1_event_start", ctypes.c_void_p), ("phase1_event_stop", ctypes.c_void_p),
+                ("alibi_slopes", ctypes.c_void_p)]
 
 
 class pkv_mla_desc(ctypes.Structure):
@@ -116,9 +117,12 @@ def make_desc(B, Hq, Hkv, D, block_size, max_blocks_per_seq, num_blocks, max_con
                            int(x_pack), int(kv_dtype), float(k_scale), float(v_scale))
 
 
-def make_opts(partition_tokens=0, num_splits=0, event_start=None, event_stop=None) -> pkv_decode_opts:
+def make_opts(partition_tokens=0, num_splits=0, event_start=None, event_stop=None,
+              alibi_slopes=None) -> pkv_decode_opts:
+    """alibi_slopes: a device fp32 tensor [Hq] (kept alive by the caller) or None."""
     ev = lambda e: None if e is None else (e if isinstance(e, int) else e.cuda_event)
-    return pkv_decode_opts(int(partition_tokens), int(num_splits), 0, ev(event_start), ev(event_stop))
+    return pkv_decode_opts(int(partition_tokens), int(num_splits), 0, ev(event_start), ev(event_stop),
+                           _ptr(alibi_slopes))
 
 
 def _opt_ref(opts):

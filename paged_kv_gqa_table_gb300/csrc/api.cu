@@ -297,6 +297,7 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
     if (st) return st;
     if (!out || !aligned(out, 8) || !workspace || !aligned(workspace, 256) || !std::isfinite(scale))
         return PKV_INVALID_ARG;
+    if (opts && opts->alibi_slopes && !aligned(opts->alibi_slopes, 4)) return PKV_INVALID_ARG;
     int ns = 0, P = 0;
     st = plan(desc, opts, 0, &ns, &P);
     if (st) return st;
@@ -306,6 +307,7 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
     CUtensorMap mk{}, mv{};
     st = prepare_phase1(desc, P, ns, q, k_cache, v_cache, block_table, context_lens, scale, &p, &mk, &mv);
     if (st) return st;
+    if (opts) p.alibi = opts->alibi_slopes;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.out = out;
@@ -344,6 +346,7 @@ int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts
         if (st) return st;
         if (!part_acc || !part_m || !part_l || !aligned(part_acc, 16) || !std::isfinite(scale))
             return PKV_INVALID_ARG;
+        if (opts && opts->alibi_slopes && !aligned(opts->alibi_slopes, 4)) return PKV_INVALID_ARG;
     }
     int ns = 0, P = 0;
     st = plan(desc, opts, 0, &ns, &P);
@@ -356,6 +359,7 @@ int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts
     CUtensorMap mk, mv;
     st = prepare_phase1(desc, P, ns, q, k_cache, v_cache, block_table, context_lens, scale, &p, &mk, &mv);
     if (st) return st;
+    if (opts) p.alibi = opts->alibi_slopes;
     p.partials_only = 1;
     p.ns_stride = num_splits_capacity;
     p.part_acc = part_acc;

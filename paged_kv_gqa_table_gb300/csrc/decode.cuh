@@ -52,6 +52,7 @@ struct DecodeParams {
     int n_cap;               // context lengths are clamped to [0, n_cap]
     float scale_log2;        // scale * log2(e) (times k_scale for FP8 caches)
     float v_scale;           // multiplies the output / partial acc (FP8 caches; 1 otherwise)
+    const float* alibi;      // [Hq] ALiBi slopes (natural-log units) or nullptr
     int partials_only;       // 1: always write partials (+ sentinels), never out
 };
 
@@ -68,11 +69,13 @@ struct DecodeTile {
     static constexpr int STAGING = (KVB == 1 && D < 128) ? NWC * 2 * BS * D * 2 : 0;
     static constexpr int RED_STRIDE = D + 4;                        // floats per reduction row
     static constexpr int smem_bytes(int nt) {
-        return 1024 + STAGES * 2 * SLICE + STAGING + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 16;
+        return 1024 + STAGES * 2 * SLICE + STAGING + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + nt * 8 * 4 + 16;
     }
 };
 
-template <typename T, int LAYOUT, int D, int NT>
+// ALIBI: compiled separately so that kernels without the bias keep their
+// register allocation.
+template <typename T, int LAYOUT, int D, int NT, bool ALIBI>
 __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     decode_phase1_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv) {
@@ -99,7 +102,8 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     uint64_t* empty = full + STAGES;
     float* st_m = reinterpret_cast<float*>(empty + STAGES);
     float* st_l = st_m + NWC * HP;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(st_l + NWC * HP);   // set on a wait timeout
+    float* slopes = st_l + NWC * HP;   // [HP] ALiBi slopes of the group's heads, log2 units (0 without ALiBi)
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(slopes + HP);   // set on a wait timeout
 
     // Lets the combine kernel queued behind this one start its prologue as
     // soon as every CTA of this grid is running (it waits for our results).
@@ -144,6 +148,8 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
         fence_barrier_init();
         *abort_flag = 0;
     }
+    for (int hh = threadIdx.x; hh < HP; hh += blockDim.x)
+        slopes[hh] = (p.alibi && hh < p.G) ? __ldg(p.alibi + h0 + hh) * 1.4426950408889634f : 0.f;
     __syncthreads();
 
     const int pg0 = t0 / BS;                        // first page of the split (sequence-relative)
@@ -233,6 +239,8 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     }
     WarpState<D, NT> ws;
     ws.reset();
+    PageBias<NT> bias;
+    bias.slopes = slopes;
 
     const int last_pg = (n - 1) / BS;
     bool ok = true;
@@ -247,8 +255,9 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
         }
         uint8_t* ks = ring + stg * 2 * SLICE;
         const int valid = (pg0 + i == last_pg) ? n - last_pg * BS : BS;
+        bias.pos0 = (pg0 + i) * BS - (n - 1);
         if constexpr (DIRECT8) {
-            page_step_fp8<D, NT>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane);
+            page_step_fp8<D, NT, ALIBI>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, bias);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stg]);
         } else if constexpr (KV8) {
@@ -258,10 +267,10 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
             expand_fp8_slice<D>(ks + SLICE, sk + BS * D * 2, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stg]);
-            page_step<MT, kLayoutNHD, D, NT>(sk, sk + BS * D * 2, valid, scale_log2, qf, ws, lane);
+            page_step<MT, kLayoutNHD, D, NT, ALIBI>(sk, sk + BS * D * 2, valid, scale_log2, qf, ws, lane, bias);
             __syncwarp();
         } else {
-            page_step<T, LAYOUT, D, NT>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane);
+            page_step<T, LAYOUT, D, NT, ALIBI>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, bias);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stg]);
         }
@@ -348,12 +357,12 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     }
 }
 
-// Host-side launcher for one instantiation.
-template <typename T, int LAYOUT, int D, int NT>
-cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
-                                 const CUtensorMap& tmv, cudaStream_t stream) {
+// Host-side launcher for one instantiation (with or without ALiBi).
+template <typename T, int LAYOUT, int D, int NT, bool ALIBI>
+cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
+                                         const CUtensorMap& tmv, cudaStream_t stream) {
     using Tile = DecodeTile<D, LAYOUT>;
-    auto kern = decode_phase1_kernel<T, LAYOUT, D, NT>;
+    auto kern = decode_phase1_kernel<T, LAYOUT, D, NT, ALIBI>;
     const int smem = Tile::smem_bytes(NT);
     static bool attr_set[64] = {};
     int dev = 0;
@@ -367,6 +376,13 @@ cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CU
     }
     kern<<<(unsigned)grid, (Tile::NWC + 1) * 32, smem, stream>>>(p, tmk, tmv);
     return cudaGetLastError();
+}
+
+template <typename T, int LAYOUT, int D, int NT>
+cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
+                                 const CUtensorMap& tmv, cudaStream_t stream) {
+    return p.alibi ? launch_decode_phase1_variant<T, LAYOUT, D, NT, true>(p, grid, tmk, tmv, stream)
+                   : launch_decode_phase1_variant<T, LAYOUT, D, NT, false>(p, grid, tmk, tmv, stream);
 }
 
 }  // namespace pkv

@@ -93,9 +93,20 @@ struct WarpState {
 // state; `valid` = tokens of the page inside the context (1..16).  Tokens past
 // it are masked by select, and their V rows are zeroed first, so whatever the
 // unread slots hold (NaN included) cannot reach the result.
-template <typename T, int LAYOUT, int D, int NT>
+// ALiBi bias of a page, in log2 units: score(t, h) += slopes[h] * (pos0 + t) for
+// page-relative token t and head h of the group; pos0 is the page's first
+// position minus (n - 1).  slopes (shared memory, padded heads included) are 0
+// without ALiBi.
+template <int NT>
+struct PageBias {
+    const float* slopes;
+    int pos0;
+};
+
+template <typename T, int LAYOUT, int D, int NT, bool ALIBI>
 __device__ __forceinline__ void page_step(uint8_t* ks, uint8_t* vs, int valid, float scale_log2,
-                                          const uint32_t (&qf)[NT][D / 16][2], WarpState<D, NT>& st, int lane) {
+                                          const uint32_t (&qf)[NT][D / 16][2], WarpState<D, NT>& st, int lane,
+                                          const PageBias<NT>& bias) {
     constexpr int BS = kPageTokens, KT = D / 16;
     const int mi = lane >> 3, r8 = lane & 7;   // ldmatrix: matrix index and row within it
     const uint32_t ks_a = smem_u32(ks), vs_a = smem_u32(vs);
@@ -124,7 +135,9 @@ __device__ __forceinline__ void page_step(uint8_t* ks, uint8_t* vs, int valid, f
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int t = tr + ((e >> 1) << 3);
-            sc[nt][e] = t < valid ? sc[nt][e] * scale_log2 : -INFINITY;
+            float v = sc[nt][e] * scale_log2;
+            if constexpr (ALIBI) v = fmaf(bias.slopes[nt * 8 + 2 * (lane & 3) + (e & 1)], (float)(bias.pos0 + t), v);
+            sc[nt][e] = t < valid ? v : -INFINITY;
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -294,9 +307,10 @@ __device__ __forceinline__ int fp8_q_frags(uint32_t (&qf)[NT][D / 16][2], const 
 // One FP8 page (swizzled K and V slices in the ring) into the warp's state, as
 // page_step; fp16 tensor-core arithmetic.  V rows past `valid` are zeroed in
 // the ring stage first (the caller fences before the stage is refilled).
-template <int D, int NT>
+template <int D, int NT, bool ALIBI>
 __device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int valid, float scale_log2,
-                                              const uint32_t (&qf)[NT][D / 16][2], WarpState<D, NT>& st, int lane) {
+                                              const uint32_t (&qf)[NT][D / 16][2], WarpState<D, NT>& st, int lane,
+                                              const PageBias<NT>& bias) {
     constexpr int BS = kPageTokens, KT = D / 16;
     const int mi = lane >> 3, r8 = lane & 7;
     const int t_l = r8 + ((mi & 1) << 3), c_l = mi >> 1;   // this lane's ldmatrix row and chunk offset
@@ -326,7 +340,9 @@ __device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int vali
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int t = tr + ((e >> 1) << 3);
-            sc[nt][e] = t < valid ? sc[nt][e] * scale_log2 : -INFINITY;
+            float v = sc[nt][e] * scale_log2;
+            if constexpr (ALIBI) v = fmaf(bias.slopes[nt * 8 + 2 * (lane & 3) + (e & 1)], (float)(bias.pos0 + t), v);
+            sc[nt][e] = t < valid ? v : -INFINITY;
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {

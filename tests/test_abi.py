@@ -227,3 +227,12 @@ def test_fp8_descriptions(B):
         with pytest.raises(B.PkvError) as e:
             B.pkv_plan_splits(B.make_desc(**{**base, **kw}), None, 152)
         assert e.value.status == status, kw
+
+
+def test_misaligned_alibi_slopes_are_rejected(B):
+    d = desc(B)
+    good = 1 << 20
+    opts = B.pkv_decode_opts(0, 0, 0, None, None, good + 2)
+    st = B.raw_status("pkv_paged_decode_attention", ctypes.byref(d), ctypes.byref(opts), good, good, good, good, good,
+                      ctypes.c_float(0.1), good, good, 1 << 30, None)
+    assert st == B.PKV_INVALID_ARG

@@ -283,3 +283,55 @@ def test_fp8_with_bf16_queries_beyond_the_fp16_range():
     got = gpu_out(case)
     assert np.all(np.isfinite(got))
     check_rows(case, got, list(range(case["B"])))
+
+
+# ------------------------------------------------------------------ ALiBi ----
+
+def _slopes(Hq):
+    # the usual geometric ALiBi slopes 2^(-8 i / Hq), i = 1..Hq
+    return (2.0 ** (-8.0 * np.arange(1, Hq + 1) / Hq)).astype(np.float32)
+
+
+@pytest.mark.parametrize("layout,dtype,D,G,kv8,P", [
+    (synth.NHD, synth.BF16, 128, 4, False, 0),
+    (synth.VLLM, synth.F16, 256, 6, False, 256),
+    (synth.NHD, synth.F16, 64, 8, False, 64),
+    (synth.NHD, synth.BF16, 128, 16, False, 128),
+    (synth.NHD, synth.BF16, 128, 4, True, 0),
+    (synth.NHD, synth.F16, 256, 2, True, 256),
+])
+def test_alibi_matches_oracle(layout, dtype, D, G, kv8, P):
+    B = _binding()
+    extra = dict(kv_dtype=synth.FP8_E4M3) if kv8 else {}
+    case = _case(31, B=13, Hq=2 * G, Hkv=2, D=D, block_size=16, dtype=dtype, layout=layout, ctx_range=(0, 1800),
+                 max_blocks_per_seq=128, poison=True, **extra)
+    case["alibi_slopes"] = _slopes(case["Hq"])
+    slopes = torch.from_numpy(case["alibi_slopes"]).cuda()
+    got = gpu_out(case, B.make_opts(partition_tokens=P, alibi_slopes=slopes))
+    check_rows(case, got, list(range(case["B"])))
+    # and it is a different problem: without the slopes the output changes
+    plain = gpu_out(case, B.make_opts(partition_tokens=P))
+    assert not np.allclose(plain, got)
+
+
+def test_alibi_partials_match_oracle():
+    B = _binding()
+    T = _tensors()
+    case = _case(32, B=7, Hq=8, Hkv=2, D=128, block_size=16, dtype=synth.BF16, layout=synth.NHD,
+                 ctx_range=(1, 700))
+    case["alibi_slopes"] = _slopes(8)
+    dev = T.upload_decode_case(case)
+    slopes = torch.from_numpy(case["alibi_slopes"]).cuda()
+    acc = torch.empty((7, 8, 8, 128), device="cuda")
+    m = torch.empty((7, 8, 8), device="cuda")
+    l = torch.empty((7, 8, 8), device="cuda")
+    P, ns = B.pkv_decode_partials(T.decode_desc(case), dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
+                                  dev["context_lens"], case["scale"], acc, m, l, 8,
+                                  opts=B.make_opts(partition_tokens=96, alibi_slopes=slopes))
+    torch.cuda.synchronize()
+    pm, pl, pacc = oracle.decode_partials(case, P, ns)
+    gm, gl, gacc = m.cpu().numpy()[:, :, :ns], l.cpu().numpy()[:, :, :ns], acc.cpu().numpy()[:, :, :ns]
+    live = pl > 0
+    assert np.array_equal(live, gl > 0)
+    assert np.max(np.abs((gm[live] + np.log(gl[live])) - (pm[live] + np.log(pl[live])))) <= 1e-3
+    assert np.max(np.abs(gacc[live] / gl[live][:, None] - pacc[live] / pl[live][:, None])) <= TOL[synth.BF16]
