@@ -335,3 +335,42 @@ def test_alibi_partials_match_oracle():
     assert np.array_equal(live, gl > 0)
     assert np.max(np.abs((gm[live] + np.log(gl[live])) - (pm[live] + np.log(pl[live])))) <= 1e-3
     assert np.max(np.abs(gacc[live] / gl[live][:, None] - pacc[live] / pl[live][:, None])) <= TOL[synth.BF16]
+
+
+# ---------------------------------------------------------- CUDA graphs ----
+
+@pytest.mark.parametrize("kv8", [False, True])
+def test_decode_step_replays_in_a_cuda_graph(kv8):
+    """One call captured into a CUDA graph (phase 1, and the combine as its
+    programmatic dependent) replays correctly after context_lens change on the
+    device: the plan only needs host-known upper bounds (here the block-table
+    capacity), so the captured grid covers every replay."""
+    B = _binding()
+    T = _tensors()
+    cap = 80 * 16
+    extra = dict(kv_dtype=synth.FP8_E4M3) if kv8 else {}
+    case = _case(41, B=12, Hq=16, Hkv=4, D=128, block_size=16, dtype=synth.BF16, layout=synth.NHD,
+                 context_lens=[cap] * 12, max_blocks_per_seq=80, **extra)
+    dev = T.upload_decode_case(case)
+    desc = T.decode_desc(case)            # max_context_len = cap, sum = 12 * cap: bounds for any replay
+    out = torch.empty((12, 16, 128), dtype=torch.bfloat16, device="cuda")
+    ws = T.workspace_for(desc)
+    run = lambda: B.pkv_paged_decode_attention(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
+                                               dev["context_lens"], case["scale"], out, ws)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        run()                             # first call on the device: kernel attributes, outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run()
+    rng = np.random.default_rng(7)
+    for trial in range(3):
+        lens = rng.integers(0, cap + 1, size=12).astype(np.int32)
+        lens[trial] = 0
+        dev["context_lens"].copy_(torch.from_numpy(lens))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        sub = dict(case, context_lens=lens)
+        check_rows(sub, out.double().cpu().numpy(), list(range(12)))
