@@ -49,11 +49,11 @@ def _load():
             lib.oracle_widen.restype = d
             lib.oracle_widen8.argtypes = [ctypes.c_uint8]
             lib.oracle_widen8.restype = d
-            lib.oracle_decode.argtypes = [i] * 11 + [p] * 5 + [d, d, d, p, i, i, p, p, p]
+            lib.oracle_decode.argtypes = [i] * 12 + [p] * 5 + [d, d, d, p, i, i, p, p, p]
             lib.oracle_decode.restype = i
-            lib.oracle_decode_partials.argtypes = [i] * 11 + [p] * 5 + [d, d, d, p, i, i, i, i, p, p, p, p]
+            lib.oracle_decode_partials.argtypes = [i] * 12 + [p] * 5 + [d, d, d, p, i, i, i, i, p, p, p, p]
             lib.oracle_decode_partials.restype = i
-            lib.oracle_combine.argtypes = [i, i, i, i, p, p, p, p, i, i, p]
+            lib.oracle_combine.argtypes = [i, i, i, i, i, p, p, p, p, i, i, p]
             lib.oracle_combine.restype = i
             lib.oracle_mla.argtypes = [i] * 6 + [p] * 7 + [d, i, i, p, p, p]
             lib.oracle_mla.restype = i
@@ -85,8 +85,15 @@ def widen8(bits: int) -> float:
     return _load().oracle_widen8(int(bits) & 0xFF)
 
 
+def q_len_of(case) -> int:
+    """Query tokens per sequence: q is [B][Hq][D] (one) or [B][q_len][Hq][D]."""
+    return int(case.get("q_len", 1))
+
+
 def _decode_common(case):
     kv_dtype = case.get("kv_dtype", case["dtype"])
+    q_len = q_len_of(case)
+    assert case["q"].size == case["B"] * q_len * case["Hq"] * case["D"]
     kv_np = np.uint8 if kv_dtype == FP8_E4M3 else np.uint16
     q = _c(case["q"], np.uint16)
     k = _c(case["k_cache"], kv_np)
@@ -95,7 +102,7 @@ def _decode_common(case):
     ctx = _c(case["context_lens"], np.int32)
     dims = [case["B"], case["Hq"], case["Hkv"], case["D"], case["block_size"],
             table.shape[1] if table.ndim == 2 else 0, case["num_blocks"],
-            case["dtype"], case["layout"], case.get("x", 8), kv_dtype]
+            case["dtype"], case["layout"], case.get("x", 8), kv_dtype, q_len]
     scales = [float(case["scale"]), float(case.get("k_scale", 1.0)), float(case.get("v_scale", 1.0))]
     alibi = case.get("alibi_slopes")
     if alibi is not None:
@@ -105,12 +112,13 @@ def _decode_common(case):
 
 
 def decode(case, b_lo: int = 0, b_hi: int | None = None, out: np.ndarray | None = None) -> np.ndarray:
-    """fp64 attention output [B][Hq][D] (only rows b in [b_lo, b_hi) are filled)."""
+    """fp64 attention output shaped like q: [B][Hq][D], or [B][q_len][Hq][D] with
+    several query tokens (only sequences b in [b_lo, b_hi) are filled)."""
     dims, arrs, scales, alibi = _decode_common(case)
-    B, Hq, D = case["B"], case["Hq"], case["D"]
+    B, D = case["B"], case["D"]
     b_hi = B if b_hi is None else b_hi
     if out is None:
-        out = np.full((B, Hq, D), np.nan)
+        out = np.full(case["q"].shape, np.nan)
     maxn = int(max(1, int(np.max(arrs[4][b_lo:b_hi], initial=1))))
     sbuf = np.zeros(maxn)
     acc = np.zeros(D)
@@ -122,13 +130,15 @@ def decode(case, b_lo: int = 0, b_hi: int | None = None, out: np.ndarray | None 
 
 
 def decode_partials(case, P: int, NS: int, b_lo: int = 0, b_hi: int | None = None):
-    """Split-mode partials (m, l, acc) with split s = tokens [s*P, min((s+1)*P, n))."""
+    """Split-mode partials (m, l, acc) with split s = tokens [s*P, min((s+1)*P, n)),
+    cut at each query's causal window; leading dimensions those of q without D."""
     dims, arrs, scales, alibi = _decode_common(case)
-    B, Hq, D = case["B"], case["Hq"], case["D"]
+    B, D = case["B"], case["D"]
     b_hi = B if b_hi is None else b_hi
-    pm = np.full((B, Hq, NS), np.nan)
-    pl = np.full((B, Hq, NS), np.nan)
-    pacc = np.full((B, Hq, NS, D), np.nan)
+    lead = case["q"].shape[:-1]
+    pm = np.full(lead + (NS,), np.nan)
+    pl = np.full(lead + (NS,), np.nan)
+    pacc = np.full(lead + (NS, D), np.nan)
     sbuf = np.zeros(max(1, P))
     st = _load().oracle_decode_partials(*dims, *[_ptr(a) for a in arrs], *scales,
                                         None if alibi is None else _ptr(alibi), int(P), int(NS), b_lo, b_hi,
@@ -139,12 +149,17 @@ def decode_partials(case, P: int, NS: int, b_lo: int = 0, b_hi: int | None = Non
 
 
 def combine(context_lens, pm, pl, pacc) -> np.ndarray:
-    """Log-sum-exp combine of split partials into the output [B][Hq][D]."""
+    """Log-sum-exp combine of split partials ([B][Hq][NS][D] or [B][q_len][Hq][NS][D])
+    into the output ([B][Hq][D] or [B][q_len][Hq][D])."""
     ctx = _c(context_lens, np.int32)
     pm, pl, pacc = _c(pm, np.float64), _c(pl, np.float64), _c(pacc, np.float64)
-    B, Hq, NS, D = pacc.shape
-    out = np.full((B, Hq, D), np.nan)
-    st = _load().oracle_combine(B, Hq, D, NS, _ptr(ctx), _ptr(pm), _ptr(pl), _ptr(pacc), 0, B, _ptr(out))
+    if pacc.ndim == 4:
+        B, Hq, NS, D = pacc.shape
+        q_len = 1
+    else:
+        B, q_len, Hq, NS, D = pacc.shape
+    out = np.full(pacc.shape[:-2] + (D,), np.nan)
+    st = _load().oracle_combine(B, q_len, Hq, D, NS, _ptr(ctx), _ptr(pm), _ptr(pl), _ptr(pacc), 0, B, _ptr(out))
     if st:
         raise OracleError(st)
     return out

@@ -21,9 +21,16 @@
  *         them); the fp8 KV cache here reads them the plainest way: cache bytes
  *         are OCP FP8 E4M3 values and K = k_scale * fp8, V = v_scale * fp8.
  *         It also takes alibi_slopes (ignored too); read as ALiBi's additive
- *         bias: the score of key position t for query head h of a sequence of
- *         length n gains slopes[h] * (t - (n - 1)) -- zero at the query's own
- *         position, decreasing linearly with distance.
+ *         bias: the score of key position t for query head h gains
+ *         slopes[h] * (t - pos), pos the query's own position -- zero there,
+ *         decreasing linearly with distance.
+ *   [MTD] Several query tokens per sequence (speculative / multi-token decode):
+ *         the bottom-right causal rule of [MLA] section "3. Pass 1" applied to
+ *         the [FD] cache layouts.  A sequence of context length n carries q_len
+ *         query tokens, the last q_len of its n positions: query i (0-based)
+ *         sits at pos = n - q_len + i and attends keys t <= pos.  Where
+ *         n - q_len + i < 0 the window is empty and the row is zero (the [FD]
+ *         empty-context reading, extended per query).  q_len = 1 is plain decode.
  *   [MLA] "kernelindex.com flashinfer gemini-2.5-pro triton xvhq2i"
  *         (mla_paged_prefill_causal_h16_ckv512_kpe64_ps1): sections
  *         "2. Determine Sequence Boundaries", "3. Pass 1", "4. Pass 2".
@@ -130,7 +137,8 @@ static size_t v_index(int layout, int Hkv, int BS, int D,
 typedef struct {
     int B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x;
     int kv_dtype;              /* dtype of the caches: OR_F16, OR_BF16 or OR_FP8 */
-    const uint16_t* q;
+    int q_len;                 /* query tokens per sequence ([MTD]); 1 = plain decode */
+    const uint16_t* q;         /* [B][q_len][Hq][D] */
     const void *k, *v;         /* 16-bit or 8-bit elements per kv_dtype */
     const int32_t *table, *ctx;
     double scale, k_scale, v_scale;   /* k_scale, v_scale multiply fp8 cache values (1 otherwise) */
@@ -148,7 +156,7 @@ static double cache_value(const decode_args* a, const void* base, size_t i, doub
 static int check_decode(const decode_args* a)
 {
     if (a->B < 0 || a->Hq <= 0 || a->Hkv <= 0 || a->D <= 0 || a->BS <= 0 ||
-        a->MBPS < 0 || a->NB < 0)
+        a->MBPS < 0 || a->NB < 0 || a->q_len <= 0)
         return OR_INVALID;
     if (a->Hq % a->Hkv != 0) return OR_INVALID;
     if (a->dtype != OR_F16 && a->dtype != OR_BF16) return OR_INVALID;
@@ -176,12 +184,12 @@ static long long page_of(const decode_args* a, int b, int t)
     return p;
 }
 
-/* Score of token t for query head h:  scale * sum_d q[b][h][d] * K_t[d]. */
-static double score(const decode_args* a, int b, int h, int g, long long p, int o)
+/* Score of token t for query token i, head h:  scale * sum_d q[b][i][h][d] * K_t[d]. */
+static double score(const decode_args* a, int b, int i, int h, int g, long long p, int o)
 {
     double s = 0.0;
     for (int d = 0; d < a->D; ++d) {
-        double qd = widen(a->q[((size_t)b * a->Hq + h) * a->D + d], a->dtype);
+        double qd = widen(a->q[(((size_t)b * a->q_len + i) * a->Hq + h) * a->D + d], a->dtype);
         double kd = cache_value(a, a->k, k_index(a->layout, a->Hkv, a->BS, a->D, a->x, p, g, o, d), a->k_scale);
         s += qd * kd;
     }
@@ -194,13 +202,13 @@ static double value(const decode_args* a, int g, long long p, int o, int d)
 }
 
 /*
- * Softmax attention of one query head over tokens [t0, t1) of sequence b,
- * returned unnormalised: m = max_t s_t, l = sum_t exp(s_t - m),
+ * Softmax attention of query token i, head h over tokens [t0, t1) of sequence b
+ * (the caller keeps t1 inside the query's causal window), returned unnormalised: m = max_t s_t, l = sum_t exp(s_t - m),
  * acc[d] = sum_t exp(s_t - m) * V_t[d].  An empty range gives (-inf, 0, 0),
  * the sentinel of [FD] _flash_decode_partial_kernel ("empty splits").
  * Returns -1 on a bad table entry.
  */
-static int attend_range(const decode_args* a, int b, int h, int t0, int t1,
+static int attend_range(const decode_args* a, int b, int i, int h, int t0, int t1,
                         double* m_out, double* l_out, double* acc, double* sbuf)
 {
     int G = a->Hq / a->Hkv;
@@ -212,12 +220,12 @@ static int attend_range(const decode_args* a, int b, int h, int t0, int t1,
         return 0;
     }
     double m = -INFINITY;
-    int n = seq_len(a, b);
+    int pos = seq_len(a, b) - a->q_len + i;   /* the query's own position */
     for (int t = t0; t < t1; ++t) {
         long long p = page_of(a, b, t);
         if (p < 0) return -1;
-        sbuf[t - t0] = score(a, b, h, g, p, t % a->BS);
-        if (a->alibi) sbuf[t - t0] += a->alibi[h] * (double)(t - (n - 1));
+        sbuf[t - t0] = score(a, b, i, h, g, p, t % a->BS);
+        if (a->alibi) sbuf[t - t0] += a->alibi[h] * (double)(t - pos);
         if (sbuf[t - t0] > m) m = sbuf[t - t0];
     }
     double l = 0.0;
@@ -232,22 +240,27 @@ static int attend_range(const decode_args* a, int b, int h, int t0, int t1,
     return 0;
 }
 
+/* End of query token i's causal window in a sequence of n tokens ([MTD]):
+ * it attends keys t < n - q_len + i + 1 (t <= its position); <= 0 is empty. */
+static int window_end(int n, int q_len, int i) { return n - q_len + i + 1; }
+
 /*
  * Paged GQA decode attention, the plain definition:
- *   out[b][h][:] = sum_t softmax_t(scale * q[b][h] . K_t) * V_t,  t in [0, ctx[b]),
+ *   out[b][i][h][:] = sum_t softmax_t(scale * q[b][i][h] . K_t) * V_t,
+ *   t in [0, window_end(ctx[b], q_len, i)),
  * K_t, V_t gathered for KV head h / (Hq/Hkv) through block_table.
- * ctx[b] == 0 gives a zero row (the reading taken for the empty context; [FD]
- * _flash_decode_combine_kernel writes zeros there).
- * Only sequences b in [b_lo, b_hi) are computed and written.
+ * An empty window (ctx[b] == 0 in plain decode) gives a zero row (the reading
+ * taken for the empty context; [FD] _flash_decode_combine_kernel writes zeros
+ * there).  Only sequences b in [b_lo, b_hi) are computed and written.
  * sbuf: caller scratch of at least max ctx doubles; acc: D doubles.
  */
 int oracle_decode(int B, int Hq, int Hkv, int D, int BS, int MBPS, int NB,
-                  int dtype, int layout, int x, int kv_dtype,
+                  int dtype, int layout, int x, int kv_dtype, int q_len,
                   const uint16_t* q, const void* k, const void* v,
                   const int32_t* table, const int32_t* ctx, double scale, double k_scale, double v_scale,
                   const double* alibi, int b_lo, int b_hi, double* out, double* sbuf, double* acc)
 {
-    decode_args a = {B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x, kv_dtype, q, k, v, table, ctx,
+    decode_args a = {B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x, kv_dtype, q_len, q, k, v, table, ctx,
                      scale, k_scale, v_scale, alibi};
     int st = check_decode(&a);
     if (st) return st;
@@ -255,11 +268,18 @@ int oracle_decode(int B, int Hq, int Hkv, int D, int BS, int MBPS, int NB,
     for (int b = b_lo; b < b_hi; ++b) {
         int n = seq_len(&a, b);
         if (n < 0) return OR_INVALID;
-        for (int h = 0; h < Hq; ++h) {
-            double m, l;
-            if (attend_range(&a, b, h, 0, n, &m, &l, acc, sbuf)) return OR_BAD_TABLE;
-            double* o = out + ((size_t)b * Hq + h) * D;
-            for (int d = 0; d < D; ++d) o[d] = (n == 0) ? 0.0 : acc[d] / l;
+        for (int i = 0; i < q_len; ++i) {
+            int end = window_end(n, q_len, i);
+            for (int h = 0; h < Hq; ++h) {
+                double m, l;
+                double* o = out + (((size_t)b * q_len + i) * Hq + h) * D;
+                if (end <= 0) {
+                    for (int d = 0; d < D; ++d) o[d] = 0.0;
+                    continue;
+                }
+                if (attend_range(&a, b, i, h, 0, end, &m, &l, acc, sbuf)) return OR_BAD_TABLE;
+                for (int d = 0; d < D; ++d) o[d] = acc[d] / l;
+            }
         }
     }
     return OR_OK;
@@ -267,19 +287,20 @@ int oracle_decode(int B, int Hq, int Hkv, int D, int BS, int MBPS, int NB,
 
 /*
  * Split mode ([V2] phase 1 with fixed partitions; [FD] partial kernel):
- * split s covers tokens [s*P, min((s+1)*P, ctx[b])).  For each (b, h, s) it
- * stores the unnormalised partial (m, l, acc) of attend_range, with the
- * (-inf, 0, 0) sentinel for empty splits.  Layouts: m, l [B][Hq][NS],
- * acc [B][Hq][NS][D].
+ * split s covers tokens [s*P, min((s+1)*P, ctx[b])), cut further at the end of
+ * each query's causal window.  For each (b, i, h, s) it stores the
+ * unnormalised partial (m, l, acc) of attend_range, with the (-inf, 0, 0)
+ * sentinel where that range is empty.  Layouts: m, l [B][q_len][Hq][NS],
+ * acc [B][q_len][Hq][NS][D].
  */
 int oracle_decode_partials(int B, int Hq, int Hkv, int D, int BS, int MBPS, int NB,
-                           int dtype, int layout, int x, int kv_dtype,
+                           int dtype, int layout, int x, int kv_dtype, int q_len,
                            const uint16_t* q, const void* k, const void* v,
                            const int32_t* table, const int32_t* ctx, double scale, double k_scale,
                            double v_scale, const double* alibi, int P, int NS, int b_lo, int b_hi,
                            double* pm, double* pl, double* pacc, double* sbuf)
 {
-    decode_args a = {B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x, kv_dtype, q, k, v, table, ctx,
+    decode_args a = {B, Hq, Hkv, D, BS, MBPS, NB, dtype, layout, x, kv_dtype, q_len, q, k, v, table, ctx,
                      scale, k_scale, v_scale, alibi};
     int st = check_decode(&a);
     if (st) return st;
@@ -288,14 +309,17 @@ int oracle_decode_partials(int B, int Hq, int Hkv, int D, int BS, int MBPS, int 
         int n = seq_len(&a, b);
         if (n < 0) return OR_INVALID;
         if ((long long)NS * P < n) return OR_INVALID;   /* splits must cover the context */
-        for (int h = 0; h < Hq; ++h) {
-            for (int s = 0; s < NS; ++s) {
-                long long t0 = (long long)s * P, t1 = t0 + P;
-                if (t1 > n) t1 = n;
-                if (t0 > n) t0 = n;
-                size_t i = ((size_t)b * Hq + h) * NS + s;
-                if (attend_range(&a, b, h, (int)t0, (int)t1, &pm[i], &pl[i], &pacc[i * D], sbuf))
-                    return OR_BAD_TABLE;
+        for (int i = 0; i < q_len; ++i) {
+            int end = window_end(n, q_len, i);
+            for (int h = 0; h < Hq; ++h) {
+                for (int s = 0; s < NS; ++s) {
+                    long long t0 = (long long)s * P, t1 = t0 + P;
+                    if (t1 > end) t1 = end;
+                    if (t0 > t1) t0 = t1;
+                    size_t r = (((size_t)b * q_len + i) * Hq + h) * NS + s;
+                    if (attend_range(&a, b, i, h, (int)t0, (int)t1, &pm[r], &pl[r], &pacc[r * D], sbuf))
+                        return OR_BAD_TABLE;
+                }
             }
         }
     }
@@ -306,21 +330,23 @@ int oracle_decode_partials(int B, int Hq, int Hkv, int D, int BS, int MBPS, int 
  * Cross-split combine ([FD] _flash_decode_combine_kernel; [V2]
  * _reduce_partitions_kernel docstring):  M = max_s m_s, f_s = exp(m_s - M),
  * out = sum_s f_s acc_s / sum_s f_s l_s.  Sentinel splits (m = -inf) get
- * f_s = 0.  ctx[b] == 0 gives zeros.
+ * f_s = 0.  Rows are (b, i, h), i < q_len; an empty causal window
+ * (ctx[b] == 0 in plain decode) gives zeros.
  */
-int oracle_combine(int B, int Hq, int D, int NS, const int32_t* ctx,
+int oracle_combine(int B, int q_len, int Hq, int D, int NS, const int32_t* ctx,
                    const double* pm, const double* pl, const double* pacc,
                    int b_lo, int b_hi, double* out)
 {
-    if (B < 0 || Hq <= 0 || D <= 0 || NS <= 0 || b_lo < 0 || b_hi > B || b_lo > b_hi)
+    if (B < 0 || q_len <= 0 || Hq <= 0 || D <= 0 || NS <= 0 || b_lo < 0 || b_hi > B || b_lo > b_hi)
         return OR_INVALID;
     for (int b = b_lo; b < b_hi; ++b) {
-        for (int h = 0; h < Hq; ++h) {
-            double* o = out + ((size_t)b * Hq + h) * D;
-            const double* m = pm + ((size_t)b * Hq + h) * NS;
-            const double* l = pl + ((size_t)b * Hq + h) * NS;
-            const double* acc = pacc + ((size_t)b * Hq + h) * NS * D;
-            if (ctx[b] == 0) {
+        for (long long r = (long long)b * q_len * Hq; r < (long long)(b + 1) * q_len * Hq; ++r) {
+            int i = (int)((r / Hq) % q_len);
+            double* o = out + (size_t)r * D;
+            const double* m = pm + (size_t)r * NS;
+            const double* l = pl + (size_t)r * NS;
+            const double* acc = pacc + (size_t)r * NS * D;
+            if (window_end(ctx[b], q_len, i) <= 0) {
                 for (int d = 0; d < D; ++d) o[d] = 0.0;
                 continue;
             }

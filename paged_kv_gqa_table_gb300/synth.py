@@ -109,8 +109,9 @@ def decode_case(seed: int, B: int, Hq: int, Hkv: int, D: int, block_size: int, d
                 layout: int = NHD, context_lens=None, ctx_range=None, max_blocks_per_seq=None,
                 slack_pages: int = 0, poison: bool = False, scale: float | None = None,
                 x: int = 8, kv_dtype: int | None = None, k_scale: float = 1.0 / 16,
-                v_scale: float = 1.0 / 16) -> dict:
-    """One paged GQA decode problem (a query token per sequence).
+                v_scale: float = 1.0 / 16, q_len: int = 1) -> dict:
+    """One paged GQA decode problem: q_len query tokens per sequence, the last
+    q_len of its context (q [B][Hq][D] for one, [B][q_len][Hq][D] for several).
 
     Layouts: NHD k/v_cache [num_blocks][Hkv][block_size][D]; VLLM key_cache
     [num_blocks][Hkv][D/x][block_size][x], value_cache [num_blocks][Hkv][D][block_size].
@@ -127,7 +128,8 @@ def decode_case(seed: int, B: int, Hq: int, Hkv: int, D: int, block_size: int, d
     pages = (ctx.astype(np.int64) + block_size - 1) // block_size
     mbps = int(max_blocks_per_seq) if max_blocks_per_seq is not None else int(max(1, pages.max(initial=1)))
     table, nb, unused = assign_pages(seed, pages, mbps, slack_pages)
-    q = normal_bits(seed, _STREAM_Q, B * Hq * D, dtype).reshape(B, Hq, D)
+    q = normal_bits(seed, _STREAM_Q, B * q_len * Hq * D, dtype)
+    q = q.reshape(B, Hq, D) if q_len == 1 else q.reshape(B, q_len, Hq, D)
     n_kv = nb * Hkv * block_size * D
     k = normal_bits(seed, _STREAM_K, n_kv, kv_dtype, fp8_scale=k_scale)
     v = normal_bits(seed, _STREAM_V, n_kv, kv_dtype, fp8_scale=v_scale)
@@ -142,6 +144,8 @@ def decode_case(seed: int, B: int, Hq: int, Hkv: int, D: int, block_size: int, d
                 scale=float(scale if scale is not None else 1.0 / math.sqrt(D)), unused_pages=unused)
     if kv_dtype != dtype:
         case.update(kv_dtype=kv_dtype, k_scale=float(k_scale), v_scale=float(v_scale))
+    if q_len != 1:
+        case["q_len"] = int(q_len)
     if poison:
         poison_decode_case(case)
     return case

@@ -371,6 +371,175 @@ def test_bad_table_and_bad_shapes_are_rejected():
     assert np.array_equal(oracle.decode(ok), oracle.decode(case))
 
 
+# ------------------------------------------------- multi-token decode ----
+#
+# q_len query tokens per sequence are its last q_len positions: query i sits at
+# pos = n - q_len + i and sees keys t <= pos (the MLA page's bottom-right causal
+# rule on the decode cache layouts); an empty window gives a zero row.
+
+MT_CASES = [
+    dict(B=4, Hq=4, Hkv=2, D=16, block_size=4, dtype=synth.F16, layout=synth.NHD, q_len=3,
+         context_lens=[0, 2, 3, 13], slack_pages=2),
+    dict(B=3, Hq=6, Hkv=2, D=16, block_size=4, dtype=synth.BF16, layout=synth.VLLM, q_len=5,
+         context_lens=[5, 12, 9]),
+    dict(B=2, Hq=3, Hkv=1, D=8, block_size=2, dtype=synth.BF16, layout=synth.NHD, q_len=2,
+         context_lens=[7, 1], kv_dtype=synth.FP8_E4M3),
+]
+
+
+def _dense_q(case):
+    """Queries as fp64 [B][q_len][Hq][D]."""
+    q = widen_np(case["q"], case["dtype"])
+    return q.reshape(case["B"], case.get("q_len", 1), case["Hq"], case["D"])
+
+
+def _dense_kv(case, b):
+    """Dense K, V [n][Hkv][D] of sequence b for 16-bit or FP8 caches (scales applied)."""
+    if case.get("kv_dtype", case["dtype"]) == synth.FP8_E4M3:
+        c = _fp8_as_bf16(case)
+        return depage_dense(c, b)
+    return depage_dense(case, b)
+
+
+def brute_force_multi_token(case, P=None, NS=None):
+    """numpy restatement: output [B][q_len][Hq][D]; with P, NS also the split
+    partials (m, l, acc) of each query's window cut into [s*P, (s+1)*P)."""
+    B, Hq, Hkv, D = case["B"], case["Hq"], case["Hkv"], case["D"]
+    ql, G = case.get("q_len", 1), Hq // Hkv
+    slopes = case.get("alibi_slopes")
+    q = _dense_q(case)
+    out = np.zeros((B, ql, Hq, D))
+    parts = None
+    if P is not None:
+        parts = (np.full((B, ql, Hq, NS), -np.inf), np.zeros((B, ql, Hq, NS)), np.zeros((B, ql, Hq, NS, D)))
+    for b in range(B):
+        n = int(case["context_lens"][b])
+        if n == 0:
+            continue
+        k, v = _dense_kv(case, b)
+        for i in range(ql):
+            pos = n - ql + i
+            if pos < 0:
+                continue
+            t = np.arange(pos + 1)
+            for h in range(Hq):
+                s = case["scale"] * (k[: pos + 1, h // G, :] @ q[b, i, h])
+                if slopes is not None:
+                    s = s + float(slopes[h]) * (t - pos)
+                w = np.exp(s - s.max())
+                out[b, i, h] = (w / w.sum()) @ v[: pos + 1, h // G, :]
+                if parts is not None:
+                    for sp in range(NS):
+                        sel = (t >= sp * P) & (t < (sp + 1) * P)
+                        if sel.any():
+                            m = s[sel].max()
+                            e = np.exp(s[sel] - m)
+                            parts[0][b, i, h, sp] = m
+                            parts[1][b, i, h, sp] = e.sum()
+                            parts[2][b, i, h, sp] = e @ v[: pos + 1][sel][:, h // G, :]
+    return out, parts
+
+
+@pytest.mark.parametrize("idx", range(len(MT_CASES)))
+def test_multi_token_decode_vs_numpy_brute_force(idx):
+    case = synth.decode_case(seed=300 + idx, **MT_CASES[idx])
+    assert case["q"].shape == (case["B"], case["q_len"], case["Hq"], case["D"])
+    np.testing.assert_allclose(oracle.decode(case), brute_force_multi_token(case)[0], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("idx", range(len(MT_CASES)))
+def test_multi_token_decode_vs_torch_sdpa_bottom_right_mask(idx):
+    # torch's is_causal is top-left aligned when q_len != n, so the mask is
+    # spelled out: query i may see key t iff t <= n - q_len + i.
+    torch = pytest.importorskip("torch")
+    case = synth.decode_case(seed=310 + idx, **MT_CASES[idx])
+    ql, G = case["q_len"], case["Hq"] // case["Hkv"]
+    q = _dense_q(case)
+    ref = np.zeros_like(q)
+    for b in range(case["B"]):
+        n = int(case["context_lens"][b])
+        if n == 0:
+            continue
+        k, v = _dense_kv(case, b)
+        kt = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(G, dim=0)     # [Hq][n][D]
+        vt = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        qt = torch.from_numpy(q[b]).permute(1, 0, 2)                              # [Hq][q_len][D]
+        allowed = torch.arange(n)[None, :] <= (n - ql + torch.arange(ql))[:, None]  # [q_len][n]
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=allowed, scale=case["scale"])
+        o = o.permute(1, 0, 2).numpy().copy()
+        o[~allowed.any(dim=1).numpy()] = 0.0                                       # empty windows: zero rows
+        ref[b] = o
+    np.testing.assert_allclose(oracle.decode(case), ref, rtol=1e-10, atol=1e-12)
+
+
+def test_multi_token_alibi_vs_torch_sdpa_with_additive_mask():
+    torch = pytest.importorskip("torch")
+    case = synth.decode_case(seed=320, **MT_CASES[1])
+    slopes = np.float32(2.0) ** -np.arange(1, case["Hq"] + 1, dtype=np.float32) * np.float32(5.0)
+    case["alibi_slopes"] = slopes
+    ql, G = case["q_len"], case["Hq"] // case["Hkv"]
+    q = _dense_q(case)
+    ref = np.zeros_like(q)
+    for b in range(case["B"]):
+        n = int(case["context_lens"][b])
+        k, v = _dense_kv(case, b)
+        kt = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        vt = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        qt = torch.from_numpy(q[b]).permute(1, 0, 2)
+        rel = torch.arange(n, dtype=torch.float64)[None, :] - (n - ql + torch.arange(ql, dtype=torch.float64))[:, None]
+        bias = torch.from_numpy(slopes.astype(np.float64))[:, None, None] * rel            # [Hq][q_len][n]
+        bias = bias.masked_fill(rel > 0, -math.inf)
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=bias, scale=case["scale"])
+        ref[b] = o.permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(oracle.decode(case), ref, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("idx", range(len(MT_CASES)))
+def test_each_query_token_equals_plain_decode_of_its_prefix(idx):
+    # Query i of a q_len case is the one-token decode of the first n - q_len + i + 1 tokens.
+    case = synth.decode_case(seed=330 + idx, **MT_CASES[idx])
+    out = oracle.decode(case)
+    ql = case["q_len"]
+    for i in range(ql):
+        single = dict(case, q=np.ascontiguousarray(case["q"][:, i]),
+                      context_lens=np.maximum(case["context_lens"] - ql + i + 1, 0).astype(np.int32))
+        single.pop("q_len")
+        assert np.array_equal(out[:, i], oracle.decode(single))
+
+
+@pytest.mark.parametrize("P", [2, 4, 8])
+def test_multi_token_partials_vs_numpy_brute_force(P):
+    # Fixes ALiBi's reference point in m: the bias is zero at each query's own position.
+    case = synth.decode_case(seed=340, **MT_CASES[0])
+    case["alibi_slopes"] = np.array([0.5, 0.25, 1.0, 2.0], np.float32)
+    NS = -(-13 // P) + 1
+    pm, pl, pacc = oracle.decode_partials(case, P, NS)
+    _, (bm, bl, bacc) = brute_force_multi_token(case, P, NS)
+    assert np.array_equal(pm == -np.inf, bm == -np.inf)
+    fin = bm > -np.inf
+    np.testing.assert_allclose(pm[fin], bm[fin], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(pl, bl, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(pacc, bacc, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("P", [2, 4, 8, 16])
+@pytest.mark.parametrize("idx", [0, 1])
+def test_multi_token_split_then_combine_equals_unsplit(P, idx):
+    # case 0 holds sequences shorter than q_len (empty windows, all-sentinel rows)
+    case = synth.decode_case(seed=350, **MT_CASES[idx])
+    NS = -(-int(case["context_lens"].max()) // P) + 1
+    pm, pl, pacc = oracle.decode_partials(case, P, NS)
+    np.testing.assert_allclose(oracle.combine(case["context_lens"], pm, pl, pacc), oracle.decode(case),
+                               rtol=1e-12, atol=1e-14)
+
+
+def test_multi_token_rejects_bad_q_len():
+    case = synth.decode_case(seed=360, **MT_CASES[0])
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.decode(dict(case, q_len=0, q=case["q"][:, :0]))
+    assert e.value.status == oracle.STATUS_INVALID
+
+
 # ---------------------------------------------------------------- MLA ----
 
 MLA_SMALL = [
@@ -507,8 +676,14 @@ MUTANTS = [
     ("fp8 k_scale dropped", "cache_value(a, a->k, k_index(a->layout, a->Hkv, a->BS, a->D, a->x, p, g, o, d), a->k_scale)",
      "cache_value(a, a->k, k_index(a->layout, a->Hkv, a->BS, a->D, a->x, p, g, o, d), 1.0)"),
     ("fp8 v_scale dropped", "a->v_scale);\n}", "1.0);\n}"),
-    ("alibi sign flipped", "a->alibi[h] * (double)(t - (n - 1));", "a->alibi[h] * (double)((n - 1) - t);"),
-    ("alibi dropped", "if (a->alibi) sbuf[t - t0] += a->alibi[h] * (double)(t - (n - 1));", "(void)n;"),
+    ("alibi sign flipped", "a->alibi[h] * (double)(t - pos);", "a->alibi[h] * (double)(pos - t);"),
+    ("alibi dropped", "if (a->alibi) sbuf[t - t0] += a->alibi[h] * (double)(t - pos);", "(void)pos;"),
+    ("alibi from the last position", "int pos = seq_len(a, b) - a->q_len + i;", "int pos = seq_len(a, b) - 1;"),
+    ("decode window one short", "return n - q_len + i + 1;", "return n - q_len + i;"),
+    ("decode window top-left", "return n - q_len + i + 1;", "return i + 1;"),
+    ("query token ignored", "(((size_t)b * a->q_len + i) * a->Hq + h) * a->D + d]",
+     "(((size_t)b * a->q_len + 0) * a->Hq + h) * a->D + d]"),
+    ("combine window ignored", "if (window_end(ctx[b], q_len, i) <= 0) {", "if (ctx[b] == 0) {"),
 ]
 
 
@@ -533,7 +708,9 @@ def test_planted_mistakes_are_caught(tmp_path, monkeypatch, name, old, new):
                lambda: test_split_then_combine_equals_unsplit(8), lambda: test_mla_vs_numpy_brute_force(0),
                test_widen_bf16_all_patterns, test_widen_e4m3_all_patterns,
                lambda: test_fp8_cache_decode_equals_bf16_decode_of_the_same_values(0),
-               test_alibi_geometric_closed_form):
+               test_alibi_geometric_closed_form, lambda: test_multi_token_decode_vs_numpy_brute_force(0),
+               lambda: test_multi_token_partials_vs_numpy_brute_force(4),
+               lambda: test_multi_token_split_then_combine_equals_unsplit(4, 0)):
         try:
             fn()
         except (AssertionError, oracle.OracleError):
