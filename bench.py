@@ -161,7 +161,7 @@ def barrier(world: int, device=None):
 def oracle_decode_timed(case, seqs, threads):
     """Runs the fp64 oracle over the given sequences on `threads` host threads; returns seconds."""
     import oracle
-    out = np.empty((case["B"], case["Hq"], case["D"]))
+    out = np.empty(case["q"].shape)
     t0 = time.perf_counter()
     with ThreadPoolExecutor(threads) as ex:
         list(ex.map(lambda b: oracle.decode(case, b, b + 1, out=out), seqs))
@@ -256,11 +256,12 @@ def tensors_fp8(case):
 def workload_config(case, name, flushed=True):
     from paged_kv_gqa_table_gb300 import synth
     ctx = case["context_lens"]
-    return {"workload": "%s: B=%d Hq=%d Hkv=%d D=%d block_size=%d %s %s layout, context_lens %d..%d (sum %d)" % (
-        name, case["B"], case["Hq"], case["Hkv"], case["D"], case["block_size"],
+    q_len = int(case.get("q_len", 1))
+    return {"workload": "%s: B=%d q_len=%d Hq=%d Hkv=%d D=%d block_size=%d %s %s layout, context_lens %d..%d (sum %d)" % (
+        name, case["B"], q_len, case["Hq"], case["Hkv"], case["D"], case["block_size"],
         dtype_label(case), {0: "NHD", 1: "vLLM x-packed"}[case["layout"]],
         int(ctx.min()), int(ctx.max()), int(ctx.sum())),
-        "seed": 0, "kv_bytes_per_step": synth.kv_bytes(case),
+        "seed": 0, "kv_bytes_per_step": synth.kv_bytes(case), "query_tokens_per_step": case["B"] * q_len,
         "l2": "flushed between steps (256 MiB write)" if flushed else "n/a (CPU)",
         "accumulate": "fp32"}
 
@@ -282,7 +283,7 @@ def run_gpu(args):
     dev = tensors.upload_decode_case(case, device)
     desc = tensors.decode_desc(case)
     ns, P = B.pkv_plan_splits(desc)
-    out = torch.empty((case["B"], case["Hq"], case["D"]), dtype=tensors.TORCH_DTYPE[case["dtype"]], device=device)
+    out = torch.empty(case["q"].shape, dtype=tensors.TORCH_DTYPE[case["dtype"]], device=device)
     ws = tensors.workspace_for(desc, device=device)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
@@ -549,7 +550,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b_decode",
                     choices=["llama3_8b_decode", "long_context_decode", "gqa6_d256_vllm_decode", "tiny",
-                             "llama3_8b_decode_fp8", "mla_prefill_h16"])
+                             "llama3_8b_decode_fp8", "llama3_8b_spec_decode_q4", "mla_prefill_h16"])
     ap.add_argument("--skip-e2e", action="store_true", help="omit the end-to-end leg (profiling runs)")
     ap.add_argument("--skip-cpu-baseline", action="store_true", help="omit the CPU oracle leg (profiling runs)")
     args = ap.parse_args(argv)

@@ -24,6 +24,12 @@
  *  [MLA] kernelindex.com "flashinfer gemini-2.5-pro triton xvhq2i"
  *        (mla_paged_prefill_causal_h16_ckv512_kpe64_ps1: run / _forward and
  *        the kernel's sections 2-4).
+ *
+ * Several query tokens per sequence (speculative / multi-token decode,
+ * pkv_decode_desc.q_len > 1) follow [MLA]'s bottom-right causal rule
+ * (section "3. Pass 1") on the decode cache layouts: the q_len tokens are the
+ * last q_len positions of the context, and token i attends keys up to its
+ * own position.
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -48,7 +54,7 @@ typedef struct CUstream_st* pkv_stream_t;  /* same type as cudaStream_t */
 typedef enum {
     PKV_OK = 0,
     PKV_INVALID_ARG = 1,          /* null pointer, bad shape, misaligned pointer, bad enum */
-    PKV_UNSUPPORTED = 2,          /* valid but not compiled: head_dim, group size, block size */
+    PKV_UNSUPPORTED = 2,          /* valid but not compiled: head_dim, block size, layout with FP8 */
     PKV_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the size query's answer */
     PKV_CUDA_ERROR = 4,           /* a CUDA runtime call or a launch failed */
     PKV_BAD_BLOCK_TABLE = 5       /* reported by pkv_validate_block_table only */
@@ -77,10 +83,10 @@ typedef enum {
     PKV_LAYOUT_VLLM = 1
 } pkv_layout;
 
-/* Problem description of one decode step (one query token per sequence). */
+/* Problem description of one decode step (q_len query tokens per sequence). */
 typedef struct {
     int B;                   /* sequences in the batch */
-    int Hq;                  /* query heads; Hq % Hkv == 0, group G = Hq / Hkv <= 16 */
+    int Hq;                  /* query heads; Hq % Hkv == 0, group G = Hq / Hkv */
     int Hkv;                 /* KV heads; query head h reads KV head h / G */
     int D;                   /* head dim: 64, 128 or 256 */
     int block_size;          /* tokens per page: 16 */
@@ -94,6 +100,12 @@ typedef struct {
     int kv_dtype;            /* PKV_KV_AS_Q, or PKV_FP8_E4M3 (NHD layout; q and out stay `dtype`) */
     float k_scale;           /* FP8 caches: K = k_scale * fp8 (finite, > 0); ignored otherwise */
     float v_scale;           /* FP8 caches: V = v_scale * fp8 (finite, > 0); ignored otherwise */
+    /* Query tokens per sequence, >= 1 (1 = plain decode).  q and out are
+     * [B][q_len][Hq][D]; context_lens[b] = n counts the q_len new tokens, whose
+     * K and V are already in the cache.  Query token i sits at position
+     * n - q_len + i and attends keys t <= n - q_len + i; where that window is
+     * empty (n < q_len - i) its rows are zero. */
+    int q_len;
 } pkv_decode_desc;
 
 /* Optional knobs; pass NULL for the defaults (all zero). */
@@ -107,16 +119,17 @@ typedef struct {
     void* phase1_event_start;
     void* phase1_event_stop;
     /* Optional ALiBi slopes, device fp32 [Hq] (4-byte aligned): the score of
-     * key position t of a sequence of length n gains alibi_slopes[h] * (t - (n - 1))
-     * before the softmax (ALiBi's linear bias, zero at the query's own position;
-     * [V2]'s launcher takes alibi_slopes and ignores them).  NULL = no bias. */
+     * key position t for a query at position pos (n - 1 for one token per
+     * sequence) gains alibi_slopes[h] * (t - pos) before the softmax (ALiBi's
+     * linear bias, zero at the query's own position; [V2]'s launcher takes
+     * alibi_slopes and ignores them).  NULL = no bias. */
     const float* alibi_slopes;
 } pkv_decode_opts;
 
 /* Text of a status code (static storage). */
 PKV_API const char* pkv_status_string(int status);
 
-/* ABI version of this header: 2 (1 had no kv_dtype / k_scale / v_scale). */
+/* ABI version of this header: 3 (2 had no q_len; 1 had no kv_dtype / k_scale / v_scale). */
 PKV_API int pkv_version(void);
 
 /*
@@ -127,8 +140,9 @@ PKV_API int pkv_version(void);
  * ceil(max_context_len / P) (at least 1) is the grid extent along splits.
  * num_sms <= 0 queries the current device.  The default picks P = 512 tokens
  * (or the longest context, if shorter), halved while the estimated number of
- * (sequence, KV head, split) work items stays below 6 * num_sms, down to
- * 4 * block_size.
+ * (sequence, KV head, row tile, split) work items stays below 6 * num_sms,
+ * down to 4 * block_size.  Row tiles: the G * q_len query rows of a
+ * (sequence, KV head) pair are covered 16 at a time (8 for D = 256).
  */
 PKV_API int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms,
                     int* num_splits, int* partition_tokens);
@@ -136,7 +150,8 @@ PKV_API int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* 
 /*
  * Bytes of scratch memory pkv_paged_decode_attention needs for this problem
  * and these options (256-byte header, then fp32 split partials m, l
- * [B][Hq][NS] and acc [B][Hq][NS][D] when the plan has more than one split).
+ * [B][q_len][Hq][NS] and acc [B][q_len][Hq][NS][D] when the plan has more
+ * than one split).
  * num_sms as for pkv_plan_splits.  The workspace must be 256-byte aligned.
  * Word 0 of the header collects device-side error bits (bit 0: a pipeline
  * wait timed out); zero it once after allocating.
@@ -147,10 +162,13 @@ PKV_API int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_dec
 /*
  * Paged GQA decode attention ([FD] paged_decode_attention; [V2]
  * paged_attention_v2_triton):
- *   out[b][h][:] = sum_t softmax_t(scale * q[b][h] . K_t) V_t,   t < context_lens[b],
+ *   out[b][i][h][:] = sum_t softmax_t(scale * q[b][i][h] . K_t) V_t,
+ *   t < context_lens[b] - q_len + i + 1   (t < context_lens[b] for q_len = 1),
  * with K_t, V_t the slot t % block_size of page block_table[b][t / block_size]
- * of KV head h / G.  context_lens[b] == 0 gives a zero row.
- *   q, out        [B][Hq][D] of dtype (4-byte aligned; out 8-byte aligned)
+ * of KV head h / G.  An empty window (context_lens[b] == 0 for q_len = 1)
+ * gives a zero row.  K and V inside the context must be finite: with
+ * q_len > 1 a masked key's V row still meets a zero weight.
+ *   q, out        [B][q_len][Hq][D] of dtype (4-byte aligned; out 8-byte aligned)
  *   k/v_cache     per layout (16-byte aligned)
  *   block_table   int32 [B][max_blocks_per_seq]; entries past a sequence's last
  *                 page are never used (-1 is the customary filler).  A live entry
@@ -159,8 +177,9 @@ PKV_API int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_dec
  *                 pkv_validate_block_table reports it.
  *   context_lens  int32 [B]; values are clamped to
  *                 [0, min(max_context_len, max_blocks_per_seq * block_size)].
- * Phase 1 runs one CTA per (sequence, KV head, split) of the pkv_plan_splits
- * plan, loading each page once for the whole group; sequences with more than
+ * Phase 1 runs one CTA per (sequence, KV head, row tile, split) of the
+ * pkv_plan_splits plan, loading each page once for all the query rows of a
+ * row tile (the whole group when G * q_len <= 16, or <= 8 for D = 256); sequences with more than
  * one split are merged by a log-sum-exp combine kernel launched as a
  * programmatic dependent of phase 1.  Calls sharing one workspace must be
  * ordered on the GPU (one stream).
@@ -173,12 +192,13 @@ PKV_API int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_de
 
 /*
  * Phase 1 alone, for layered testing ([FD] _flash_decode_partial_kernel):
- * writes, for every sequence b, query head h and split s < *num_splits_out,
- * the unnormalised fp32 partial of split s in natural-log units:
- *   part_m[b][h][s] = max_t s_t,  part_l[b][h][s] = sum_t exp(s_t - m),
- *   part_acc[b][h][s][:] = sum_t exp(s_t - m) V_t,
- * and the sentinel (-inf, 0, 0) for splits past the context.  The arrays
- * are [B][Hq][num_splits_capacity] (and [...][D]); the call fails with
+ * writes, for every sequence b, query token i, query head h and split
+ * s < *num_splits_out, the unnormalised fp32 partial of the tokens of split s
+ * inside query i's causal window, in natural-log units:
+ *   part_m[b][i][h][s] = max_t s_t,  part_l[b][i][h][s] = sum_t exp(s_t - m),
+ *   part_acc[b][i][h][s][:] = sum_t exp(s_t - m) V_t,
+ * and the sentinel (-inf, 0, 0) where that range is empty.  The arrays are
+ * [B][q_len][Hq][num_splits_capacity] (and [...][D]); the call fails with
  * PKV_WORKSPACE_TOO_SMALL if the plan needs more splits than the capacity.
  */
 PKV_API int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
@@ -189,11 +209,11 @@ PKV_API int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_op
 
 /*
  * Phase 2 alone ([FD] _flash_decode_combine_kernel; [V2]
- * _reduce_partitions_kernel): for every (b, h) with n = context_lens[b]
+ * _reduce_partitions_kernel): for every (b, i, h) with n = context_lens[b]
  * (clamped as above), NS_b = ceil(n / partition_tokens) splits are merged:
  *   M = max_s m_s,  out = sum_s e^{m_s - M} acc_s / sum_s e^{m_s - M} l_s,
- * and n == 0 gives zeros.  Partials are laid out as pkv_decode_partials
- * writes them with num_splits columns.
+ * and an empty causal window (n == 0 for q_len = 1) gives zeros.  Partials
+ * are laid out as pkv_decode_partials writes them with num_splits columns.
  */
 PKV_API int pkv_combine(const pkv_decode_desc* desc, int partition_tokens, int num_splits,
                 const int32_t* context_lens, const float* part_acc, const float* part_m,

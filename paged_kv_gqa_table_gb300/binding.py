@@ -31,7 +31,8 @@ class pkv_decode_desc(ctypes.Structure):
                 ("block_size", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int), ("num_blocks", ctypes.c_int),
                 ("max_context_len", ctypes.c_int), ("sum_context_len", ctypes.c_longlong),
                 ("dtype", ctypes.c_int), ("layout", ctypes.c_int), ("x_pack", ctypes.c_int),
-                ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+                ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
+                ("q_len", ctypes.c_int)]
 
 
 class pkv_decode_opts(ctypes.Structure):
@@ -111,10 +112,10 @@ def _stream(stream) -> int | None:
 
 def make_desc(B, Hq, Hkv, D, block_size, max_blocks_per_seq, num_blocks, max_context_len, sum_context_len,
               dtype, layout=PKV_LAYOUT_NHD, x_pack=8, kv_dtype=PKV_KV_AS_Q, k_scale=1.0,
-              v_scale=1.0) -> pkv_decode_desc:
+              v_scale=1.0, q_len=1) -> pkv_decode_desc:
     return pkv_decode_desc(int(B), int(Hq), int(Hkv), int(D), int(block_size), int(max_blocks_per_seq),
                            int(num_blocks), int(max_context_len), int(sum_context_len), int(dtype), int(layout),
-                           int(x_pack), int(kv_dtype), float(k_scale), float(v_scale))
+                           int(x_pack), int(kv_dtype), float(k_scale), float(v_scale), int(q_len))
 
 
 def make_opts(partition_tokens=0, num_splits=0, event_start=None, event_stop=None,

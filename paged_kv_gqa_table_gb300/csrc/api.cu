@@ -25,7 +25,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 int check_desc(const pkv_decode_desc* d) {
     if (!d) return PKV_INVALID_ARG;
     if (d->B < 0 || d->Hq <= 0 || d->Hkv <= 0 || d->D <= 0 || d->block_size <= 0 || d->max_blocks_per_seq < 0 ||
-        d->num_blocks < 0 || d->max_context_len < 0 || d->sum_context_len < 0)
+        d->num_blocks < 0 || d->max_context_len < 0 || d->sum_context_len < 0 || d->q_len <= 0)
         return PKV_INVALID_ARG;
     if (d->Hq % d->Hkv != 0) return PKV_INVALID_ARG;
     if (d->dtype != PKV_F16 && d->dtype != PKV_BF16) return PKV_INVALID_ARG;
@@ -41,11 +41,23 @@ int check_desc(const pkv_decode_desc* d) {
     if (d->max_context_len > 0 && d->num_blocks == 0) return PKV_INVALID_ARG;
     if (d->D != 64 && d->D != 128 && d->D != 256) return PKV_UNSUPPORTED;
     if (d->block_size != kBS) return PKV_UNSUPPORTED;
-    const int G = d->Hq / d->Hkv;
-    if (G > 16 || (G > 8 && d->D > 128)) return PKV_UNSUPPORTED;
     if ((long long)d->num_blocks * d->Hkv > INT_MAX) return PKV_UNSUPPORTED;
-    if ((long long)d->B * d->Hq > INT_MAX) return PKV_UNSUPPORTED;
+    if ((long long)d->q_len * d->Hq > INT_MAX || (long long)d->B * d->q_len * d->Hq > INT_MAX)
+        return PKV_UNSUPPORTED;
     return PKV_OK;
+}
+
+// Query-column tiling of phase 1: a (sequence, KV head) pair has R = G * q_len
+// query rows; a CTA holds 8 * nt of them as mma columns (nt = 2 when more than
+// 8 rows and D <= 128, else 1: D = 256 keeps its accumulators to one tile) and
+// rt = ceil(R / (8 * nt)) CTAs cover them.
+struct ColumnTiles {
+    int nt, rt, R;
+};
+ColumnTiles column_tiles(const pkv_decode_desc* d) {
+    const long long R = (long long)(d->Hq / d->Hkv) * d->q_len;   // <= q_len * Hq <= INT_MAX
+    const int nt = (R > 8 && d->D <= 128) ? 2 : 1;
+    return ColumnTiles{nt, (int)ceil_div(R, 8LL * nt), (int)R};
 }
 
 int current_sm_count(int* out) {
@@ -64,7 +76,8 @@ int current_sm_count(int* out) {
 
 // Default partition: 512 tokens (or the longest context rounded up to a
 // page, if shorter), halved while the estimated number of non-empty work
-// items Hkv * ceil(sum_n / P) stays below six per SM, down to four pages.
+// items Hkv * row_tiles * ceil(sum_n / P) stays below six per SM, down to
+// four pages.
 long long auto_partition(const pkv_decode_desc* d, int num_sms) {
     const long long BS = d->block_size;
     const long long maxn = d->max_context_len > 0 ? d->max_context_len : 1;
@@ -73,7 +86,7 @@ long long auto_partition(const pkv_decode_desc* d, int num_sms) {
     const long long target = 6LL * num_sms;
     const long long sum = d->sum_context_len > 0 ? d->sum_context_len : 1;
     while (P > min_p) {
-        const long long units = (long long)d->Hkv * ceil_div(sum, P);
+        const long long units = (long long)d->Hkv * column_tiles(d).rt * ceil_div(sum, P);
         if (units >= target) break;
         long long np = round_up(P / 2, BS);
         if (np < min_p) np = min_p;
@@ -105,14 +118,15 @@ int plan(const pkv_decode_desc* d, const pkv_decode_opts* o, int num_sms, int* n
     }
     long long n_splits = ceil_div(d->max_context_len, p);
     if (n_splits < 1) n_splits = 1;
-    if (p > INT_MAX || n_splits > INT_MAX || (long long)d->B * d->Hkv * n_splits > INT_MAX) return PKV_UNSUPPORTED;
+    if (p > INT_MAX || n_splits > INT_MAX || (long long)d->B * d->Hkv * column_tiles(d).rt * n_splits > INT_MAX)
+        return PKV_UNSUPPORTED;
     *P = (int)p;
     *ns = (int)n_splits;
     return PKV_OK;
 }
 
 size_t partial_bytes(const pkv_decode_desc* d, int ns) {
-    const size_t rows = (size_t)d->B * d->Hq * ns;
+    const size_t rows = (size_t)d->B * d->q_len * d->Hq * ns;
     return 2 * align256(rows * 4) + align256(rows * d->D * 4);
 }
 
@@ -199,9 +213,11 @@ int encode_rows_map(CUtensorMap* map, const void* base, cuuint64_t cols, cuuint6
     return r == CUDA_SUCCESS ? PKV_OK : PKV_INVALID_ARG;
 }
 
-cudaError_t dispatch_phase1(const pkv_decode_desc* d, const DecodeParams& p, long long grid, const CUtensorMap& k,
+// Launches phase 1 over the grid (sequence, KV head, row tile, split).
+cudaError_t dispatch_phase1(const pkv_decode_desc* d, const DecodeParams& p, const CUtensorMap& k,
                             const CUtensorMap& v, cudaStream_t s) {
-    const int nt = (d->Hq / d->Hkv) > 8 ? 2 : 1;
+    const int nt = column_tiles(d).nt;
+    const long long grid = (long long)p.B * p.Hkv * p.RT * p.NS;
     const bool bf = d->dtype == PKV_BF16;
     if (d->kv_dtype == PKV_FP8_E4M3)
         return bf ? launch_decode_nhd8_bf16(d->D, nt, p, grid, k, v, s)
@@ -234,6 +250,10 @@ int prepare_phase1(const pkv_decode_desc* d, int P, int NS, const void* q, const
     p->Hq = d->Hq;
     p->Hkv = d->Hkv;
     p->G = d->Hq / d->Hkv;
+    const ColumnTiles ct = column_tiles(d);
+    p->q_len = d->q_len;
+    p->R = ct.R;
+    p->RT = ct.rt;
     p->MBPS = d->max_blocks_per_seq;
     p->NB = d->num_blocks;
     p->P = P;
@@ -269,7 +289,7 @@ const char* pkv_status_string(int status) {
     }
 }
 
-int pkv_version(void) { return 2; }
+int pkv_version(void) { return 3; }
 
 int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms, int* num_splits,
                     int* partition_tokens) {
@@ -313,22 +333,23 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
     p.out = out;
     p.err = reinterpret_cast<uint32_t*>(ws);
     uint8_t* parts = ws + kHeaderBytes;
-    const size_t rows = (size_t)desc->B * desc->Hq * ns;
+    const size_t rows = (size_t)desc->B * desc->q_len * desc->Hq * ns;
     p.part_m = reinterpret_cast<float*>(parts);
     p.part_l = reinterpret_cast<float*>(parts + align256(rows * 4));
     p.part_acc = reinterpret_cast<float*>(parts + 2 * align256(rows * 4));
 
     if (desc->max_context_len == 0) {
         // Every context is empty: the combine kernel writes the zero rows.
-        CombineParams c{context_lens, nullptr, nullptr, nullptr, out, desc->B, desc->Hq, P, ns, 0, 0};
+        CombineParams c{context_lens, nullptr, nullptr, nullptr, out, desc->B, desc->Hq, P, ns, 0, 0, desc->q_len};
         return launch_combine(desc->dtype, desc->D, c, s, false) == cudaSuccess ? PKV_OK : PKV_CUDA_ERROR;
     }
     record(opts ? opts->phase1_event_start : nullptr, s);
-    if (dispatch_phase1(desc, p, (long long)desc->B * desc->Hkv * ns, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
+    if (dispatch_phase1(desc, p, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
     record(opts ? opts->phase1_event_stop : nullptr, s);
     if (ns > 1) {
         // Programmatic dependent of phase 1 (unless an event sits between them).
-        CombineParams c{context_lens, p.part_acc, p.part_m, p.part_l, out, desc->B, desc->Hq, P, ns, p.n_cap, 1};
+        CombineParams c{context_lens, p.part_acc, p.part_m, p.part_l, out, desc->B, desc->Hq, P, ns, p.n_cap, 1,
+                        desc->q_len};
         if (launch_combine(desc->dtype, desc->D, c, s, !(opts && opts->phase1_event_stop)) != cudaSuccess)
             return PKV_CUDA_ERROR;
     }
@@ -373,7 +394,7 @@ int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts
         mv = CUtensorMap{};
     }
     record(opts ? opts->phase1_event_start : nullptr, s);
-    if (dispatch_phase1(desc, p, (long long)desc->B * desc->Hkv * ns, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
+    if (dispatch_phase1(desc, p, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
     record(opts ? opts->phase1_event_stop : nullptr, s);
     return PKV_OK;
 }
@@ -387,7 +408,7 @@ int pkv_combine(const pkv_decode_desc* desc, int partition_tokens, int num_split
     if (desc->B == 0) return PKV_OK;
     if (!context_lens || !part_acc || !part_m || !part_l || !out || !aligned(part_acc, 16)) return PKV_INVALID_ARG;
     CombineParams c{context_lens, part_acc, part_m, part_l, out, desc->B, desc->Hq, partition_tokens, num_splits,
-                    desc->max_context_len, 0};
+                    desc->max_context_len, 0, desc->q_len};
     return launch_combine(desc->dtype, desc->D, c, reinterpret_cast<cudaStream_t>(stream), false) == cudaSuccess
                ? PKV_OK
                : PKV_CUDA_ERROR;

@@ -4,11 +4,23 @@
 // Combine ("koas-w.github.io flash-decode post", _flash_decode_combine_kernel;
 // "paged_attention_v2_triton.py", _reduce_partitions_kernel):
 //   M = max_s m_s,  f_s = e^{m_s - M},  out = sum_s f_s acc_s / sum_s f_s l_s.
+// Rows are (sequence b, query token i, head h), i < q_len; a row whose causal
+// window n - q_len + i + 1 is empty (n == 0 for one token) is zero.
 #include "internal.h"
 
 namespace pkv {
 
-// One warp per (sequence, query head); lane l owns elements [l*D/32, (l+1)*D/32).
+// Context length of row r's sequence (clamped) and whether its query token's
+// causal window is empty.
+__device__ __forceinline__ int row_context(const CombineParams& p, long long r, bool* empty) {
+    const long long bi = r / p.Hq;   // b * q_len + i
+    int n = p.ctx[bi / p.q_len];
+    n = n < 0 ? 0 : (n > p.n_cap ? p.n_cap : n);
+    *empty = n - p.q_len + (int)(bi % p.q_len) + 1 <= 0;
+    return n;
+}
+
+// One warp per row (sequence, query token, head); lane l owns elements [l*D/32, (l+1)*D/32).
 // Splits are merged a chunk at a time (32 / (D/32) splits): the chunk's m, l
 // and acc rows are all loaded before any is used, so a chunk costs one memory
 // round trip,
@@ -22,18 +34,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
     constexpr int CH = 32 / EPL;  // splits per chunk: 32 floats of acc in flight per lane
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long bh = (long long)blockIdx.x * 8 + warp;
-    const bool live = bh < (long long)p.B * p.Hq;
+    const bool live = bh < (long long)p.B * p.q_len * p.Hq;
     int n = 0;
-    if (live) {
-        n = p.ctx[bh / p.Hq];
-        n = n < 0 ? 0 : (n > p.n_cap ? p.n_cap : n);
-    }
+    bool empty = true;
+    if (live) n = row_context(p, bh, &empty);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!live) return;
     const int ns = (n + p.P - 1) / p.P;
     if (p.skip_single && ns <= 1) return;   // phase 1 wrote this row directly
     T* o = reinterpret_cast<T*>(p.out) + bh * D + lane * EPL;
-    if (n == 0) {
+    if (empty) {
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[e] = from_float<T>(0.f);
         return;
@@ -99,13 +109,13 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(const CombineParams p
     __shared__ float s_m[NW], s_l[NW];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long bh = blockIdx.x;
-    int n = p.ctx[bh / p.Hq];
-    n = n < 0 ? 0 : (n > p.n_cap ? p.n_cap : n);
+    bool empty = true;
+    const int n = row_context(p, bh, &empty);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int ns = (n + p.P - 1) / p.P;
     if (p.skip_single && ns <= 1) return;
     T* o = reinterpret_cast<T*>(p.out) + bh * D;
-    if (n == 0) {
+    if (empty) {
         for (int d = threadIdx.x; d < D; d += blockDim.x) o[d] = from_float<T>(0.f);
         return;
     }
@@ -181,7 +191,7 @@ constexpr int kWideCombineSplits = 32;
 
 template <typename T, int D>
 cudaError_t launch_combine_t(const CombineParams& p, cudaLaunchConfig_t& cfg) {
-    const long long rows = (long long)p.B * p.Hq;
+    const long long rows = (long long)p.B * p.q_len * p.Hq;
     if (p.ns_stride > kWideCombineSplits) {
         cfg.gridDim = dim3((unsigned)rows);
         return cudaLaunchKernelEx(&cfg, combine_wide_kernel<T, D>, p);
@@ -191,7 +201,7 @@ cudaError_t launch_combine_t(const CombineParams& p, cudaLaunchConfig_t& cfg) {
 }
 
 cudaError_t launch_combine(int dtype, int D, const CombineParams& p, cudaStream_t stream, bool after_phase1) {
-    if ((long long)p.B * p.Hq == 0) return cudaSuccess;
+    if ((long long)p.B * p.q_len * p.Hq == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(256);
     cfg.stream = stream;

@@ -1,9 +1,11 @@
 // decode.cuh -- phase 1 of paged GQA decode attention on sm_103a.
 //
-// One CTA per (sequence b, KV head, split s).  Split s covers tokens
+// One CTA per (sequence b, KV head, row tile, split s).  Split s covers tokens
 // [s*P, min((s+1)*P, n)) of the sequence (fixed partitions as in
 // "paged_attention_v2_triton.py", _partition_attn_kernel; page-granular
-// splits as in the flash-decode post's _flash_decode_partial_kernel).
+// splits as in the flash-decode post's _flash_decode_partial_kernel).  The
+// query rows of (b, KV head) -- q_len tokens x G heads -- are the mma N
+// columns, 8 * NT per CTA; more rows than that take several row tiles.
 //
 // Roles: warp NWC is the producer: it reads the split's block-table entries
 // (32 per coalesced load, one chunk ahead) and, per page, issues TMA tensor
@@ -13,7 +15,7 @@
 // own online-softmax state for all G query heads of the group:
 //
 //   S^T[t][h] = K[t][:] . Q[h][:]          mma.sync m16n8k16, tokens = M (16 per
-//                                           page), padded heads = N (8 per tile)
+//                                           page), query rows = N (8 per tile)
 //   m' = max(m, max_t S), alpha = 2^(m-m'), P = 2^(S-m'), l' = alpha*l + sum P
 //   O^T[d][h] = alpha*O^T[d][h] + V^T[d][t] P^T[t][h]   (P^T from movmatrix)
 //
@@ -37,15 +39,18 @@
 namespace pkv {
 
 struct DecodeParams {
-    const void* q;           // [B][Hq][D]
+    const void* q;           // [B][q_len][Hq][D]
     const int32_t* table;    // [B][MBPS]
     const int32_t* ctx;      // [B]
-    void* out;               // [B][Hq][D]
-    float* part_acc;         // [B][Hq][ns_stride][D]
-    float* part_m;           // [B][Hq][ns_stride]
-    float* part_l;           // [B][Hq][ns_stride]
+    void* out;               // [B][q_len][Hq][D]
+    float* part_acc;         // [B][q_len][Hq][ns_stride][D]
+    float* part_m;           // [B][q_len][Hq][ns_stride]
+    float* part_l;           // [B][q_len][Hq][ns_stride]
     uint32_t* err;           // device error word or nullptr
     int B, Hq, Hkv, G, MBPS, NB;
+    int q_len;               // query tokens per sequence (the last q_len positions)
+    int R;                   // query rows per (sequence, KV head): G * q_len
+    int RT;                  // row tiles: ceil(R / (8 * NT))
     int P;                   // tokens per split (multiple of BS)
     int NS;                  // splits in the grid
     int ns_stride;           // split extent of the partial arrays
@@ -69,13 +74,13 @@ struct DecodeTile {
     static constexpr int STAGING = (KVB == 1 && D < 128) ? NWC * 2 * BS * D * 2 : 0;
     static constexpr int RED_STRIDE = D + 4;                        // floats per reduction row
     static constexpr int smem_bytes(int nt) {
-        return 1024 + STAGES * 2 * SLICE + STAGING + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + nt * 8 * 4 + 16;
+        return 1024 + STAGES * 2 * SLICE + STAGING + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 16;
     }
 };
 
-// ALIBI: compiled separately so that kernels without the bias keep their
-// register allocation.
-template <typename T, int LAYOUT, int D, int NT, bool ALIBI>
+// GEN: the general kernel (several query tokens per sequence, ALiBi), compiled
+// separately so that the one-token kernel without bias keeps its registers.
+template <typename T, int LAYOUT, int D, int NT, bool GEN>
 __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     decode_phase1_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv) {
@@ -102,8 +107,7 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     uint64_t* empty = full + STAGES;
     float* st_m = reinterpret_cast<float*>(empty + STAGES);
     float* st_l = st_m + NWC * HP;
-    float* slopes = st_l + NWC * HP;   // [HP] ALiBi slopes of the group's heads, log2 units (0 without ALiBi)
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(slopes + HP);   // set on a wait timeout
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(st_l + NWC * HP);   // set on a wait timeout
 
     // Lets the combine kernel queued behind this one start its prologue as
     // soon as every CTA of this grid is running (it waits for our results).
@@ -112,9 +116,12 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     int item = blockIdx.x;
     const int s = item % p.NS;
     item /= p.NS;
+    const int rt = item % p.RT;
+    item /= p.RT;
     const int kvh = item % p.Hkv;
     const int b = item / p.Hkv;
-    const int h0 = kvh * p.G;
+    const QCols qc{b, kvh * p.G, rt * HP, p.R, p.G, p.q_len, p.Hq};
+    const int ncols = min(HP, p.R - qc.col0);   // live columns of this CTA
 
     const int n = clampi(p.ctx[b], 0, p.n_cap);
     const int ns_b = (n + p.P - 1) / p.P;
@@ -123,10 +130,10 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
 
     if (t0 >= t1) {
         // Split past the context.  Partials mode writes the (-inf, 0, 0)
-        // sentinel; an empty context (n == 0) writes a zero output row.
+        // sentinel; an empty context (n == 0) writes zero output rows.
         if (p.partials_only) {
-            for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) {
-                const size_t row = ((size_t)b * p.Hq + h0 + i / D) * p.ns_stride + s;
+            for (int i = threadIdx.x; i < ncols * D; i += blockDim.x) {
+                const size_t row = qc.row(i / D) * p.ns_stride + s;
                 p.part_acc[row * D + i % D] = 0.f;
                 if (i % D == 0) {
                     p.part_m[row] = -INFINITY;
@@ -134,8 +141,8 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
                 }
             }
         } else if (n == 0 && s == 0) {
-            T* o = reinterpret_cast<T*>(p.out) + ((size_t)b * p.Hq + h0) * D;
-            for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) o[i] = from_float<T>(0.f);
+            for (int i = threadIdx.x; i < ncols * D; i += blockDim.x)
+                reinterpret_cast<T*>(p.out)[qc.row(i / D) * D + i % D] = from_float<T>(0.f);
         }
         return;
     }
@@ -148,8 +155,6 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
         fence_barrier_init();
         *abort_flag = 0;
     }
-    for (int hh = threadIdx.x; hh < HP; hh += blockDim.x)
-        slopes[hh] = (p.alibi && hh < p.G) ? __ldg(p.alibi + h0 + hh) * 1.4426950408889634f : 0.f;
     __syncthreads();
 
     const int pg0 = t0 / BS;                        // first page of the split (sequence-relative)
@@ -201,11 +206,10 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     uint32_t qf[NT][KT][2];
     float scale_log2 = p.scale_log2;
     if constexpr (DIRECT8) {
-        const int qe = fp8_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + h0) * D,
-                                             p.G, lane);
+        const int qe = fp8_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q), qc, lane);
         scale_log2 *= exp2f((float)qe);
     } else {
-        load_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q) + ((size_t)b * p.Hq + h0) * D, p.G, lane);
+        load_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q), qc, lane);
     }
     if constexpr (KV8 && !DIRECT8 && std::is_same<T, __nv_bfloat16>::value) {
         // bf16 queries meet fp16 keys: convert them, scaled by 2^-e when
@@ -239,8 +243,20 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     }
     WarpState<D, NT> ws;
     ws.reset();
-    PageBias<NT> bias;
-    bias.slopes = slopes;
+    ColTerms<NT> ct;
+    if constexpr (GEN) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int c = nt * 8 + 2 * (lane & 3) + j;
+                const bool live = qc.live(c);
+                const int gc = qc.col0 + c;
+                ct.shift[nt][j] = live ? p.q_len - 1 - gc / p.G : 0;
+                ct.slope[nt][j] =
+                    (live && p.alibi) ? __ldg(p.alibi + qc.h0 + gc % p.G) * 1.4426950408889634f : 0.f;
+            }
+    }
 
     const int last_pg = (n - 1) / BS;
     bool ok = true;
@@ -255,9 +271,9 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
         }
         uint8_t* ks = ring + stg * 2 * SLICE;
         const int valid = (pg0 + i == last_pg) ? n - last_pg * BS : BS;
-        bias.pos0 = (pg0 + i) * BS - (n - 1);
+        ct.pos0 = (pg0 + i) * BS - (n - 1);
         if constexpr (DIRECT8) {
-            page_step_fp8<D, NT, ALIBI>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, bias);
+            page_step_fp8<D, NT, GEN>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, ct);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stg]);
         } else if constexpr (KV8) {
@@ -267,10 +283,10 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
             expand_fp8_slice<D>(ks + SLICE, sk + BS * D * 2, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stg]);
-            page_step<MT, kLayoutNHD, D, NT, ALIBI>(sk, sk + BS * D * 2, valid, scale_log2, qf, ws, lane, bias);
+            page_step<MT, kLayoutNHD, D, NT, GEN>(sk, sk + BS * D * 2, valid, scale_log2, qf, ws, lane, ct);
             __syncwarp();
         } else {
-            page_step<T, LAYOUT, D, NT, ALIBI>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, bias);
+            page_step<T, LAYOUT, D, NT, GEN>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, ct);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stg]);
         }
@@ -299,6 +315,7 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < NWC; ++w) M = fmaxf(M, st_m[w * HP + h]);
+            if (M == -INFINITY) M = 0.f;   // a column that saw no visible token: every f is 0
             const float f = ex2(ws.m[nt][j] - M);   // 0 for a warp that saw no page
             if constexpr (DIRECT8) {   // mma rows g, g+8 of d-tile dt hold d = 16dt + 2g, 16dt + 2g + 1
                 float* row = red + (warp * HP + h) * RS + 2 * (lane >> 2);
@@ -319,17 +336,18 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     named_bar_sync(1, NWC * 32);
 
     const bool direct = !p.partials_only && ns_b == 1;
-    for (int idx = threadIdx.x; idx < p.G * (D / 4); idx += NWC * 32) {
+    for (int idx = threadIdx.x; idx < ncols * (D / 4); idx += NWC * 32) {
         const int h = idx / (D / 4);
         const int d = (idx % (D / 4)) * 4;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NWC; ++w) M = fmaxf(M, st_m[w * HP + h]);
+        const float Mref = M == -INFINITY ? 0.f : M;   // no visible token: L = 0, sum = 0
         float L = 0.f;
         float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < NWC; ++w) {
-            L += st_l[w * HP + h] * ex2(st_m[w * HP + h] - M);
+            L += st_l[w * HP + h] * ex2(st_m[w * HP + h] - Mref);
             const float4 v = *reinterpret_cast<const float4*>(red + (w * HP + h) * RS + d);
             sum.x += v.x;
             sum.y += v.y;
@@ -340,9 +358,9 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
         sum.y *= p.v_scale;
         sum.z *= p.v_scale;
         sum.w *= p.v_scale;
-        const size_t bh = (size_t)b * p.Hq + h0 + h;
+        const size_t bh = qc.row(h);
         if (direct) {
-            const float inv = 1.f / L;
+            const float inv = L > 0.f ? 1.f / L : 0.f;   // an empty causal window gives a zero row
             T o4[4] = {from_float<T>(sum.x * inv), from_float<T>(sum.y * inv), from_float<T>(sum.z * inv),
                        from_float<T>(sum.w * inv)};
             *reinterpret_cast<uint2*>(reinterpret_cast<T*>(p.out) + bh * D + d) = *reinterpret_cast<uint2*>(o4);
@@ -357,12 +375,12 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     }
 }
 
-// Host-side launcher for one instantiation (with or without ALiBi).
-template <typename T, int LAYOUT, int D, int NT, bool ALIBI>
+// Host-side launcher for one instantiation (general or one-token without bias).
+template <typename T, int LAYOUT, int D, int NT, bool GEN>
 cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                          const CUtensorMap& tmv, cudaStream_t stream) {
     using Tile = DecodeTile<D, LAYOUT>;
-    auto kern = decode_phase1_kernel<T, LAYOUT, D, NT, ALIBI>;
+    auto kern = decode_phase1_kernel<T, LAYOUT, D, NT, GEN>;
     const int smem = Tile::smem_bytes(NT);
     static bool attr_set[64] = {};
     int dev = 0;
@@ -381,8 +399,8 @@ cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, 
 template <typename T, int LAYOUT, int D, int NT>
 cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                  const CUtensorMap& tmv, cudaStream_t stream) {
-    return p.alibi ? launch_decode_phase1_variant<T, LAYOUT, D, NT, true>(p, grid, tmk, tmv, stream)
-                   : launch_decode_phase1_variant<T, LAYOUT, D, NT, false>(p, grid, tmk, tmv, stream);
+    return (p.alibi || p.q_len > 1) ? launch_decode_phase1_variant<T, LAYOUT, D, NT, true>(p, grid, tmk, tmv, stream)
+                                    : launch_decode_phase1_variant<T, LAYOUT, D, NT, false>(p, grid, tmk, tmv, stream);
 }
 
 }  // namespace pkv

@@ -33,17 +33,34 @@ __device__ __forceinline__ uint32_t nhd_off(int t, int c) {
     return (uint32_t)((c >> 3) * (BS * 128) + t * 128 + (((c & 7) ^ (t & 7)) << 4));
 }
 
-// Q^T fragments (mma B operand) of heads [nt*8, nt*8+8) of the group; heads
-// at or past G are zero.  qb points at head 0 of the group.
+// The query columns of one CTA (the mma N dimension).  A (sequence b, KV
+// head) pair has R = G * q_len query rows: query token i (0 <= i < q_len) of
+// every head of the group.  Column c of the CTA is row gc = col0 + c, i.e.
+// token i = gc / G of head h0 + gc % G; columns at or past R are padding (zero
+// queries, never written).  row() is the row index of q, out and the partials,
+// all [B][q_len][Hq][...].
+struct QCols {
+    int b, h0, col0, R, G, q_len, Hq;
+    __device__ __forceinline__ bool live(int c) const { return col0 + c < R; }
+    __device__ __forceinline__ int token(int c) const { return (col0 + c) / G; }
+    __device__ __forceinline__ size_t row(int c) const {
+        const int gc = col0 + c;
+        return ((size_t)b * q_len + gc / G) * Hq + h0 + gc % G;
+    }
+};
+
+// Q^T fragments (mma B operand) of columns [nt*8, nt*8+8); padding columns are zero.
 template <typename T, int D, int NT>
-__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[NT][D / 16][2], const T* qb, int G, int lane) {
+__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[NT][D / 16][2], const T* q, const QCols& qc, int lane) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        const int hh = nt * 8 + (lane >> 2);
+        const int c = nt * 8 + (lane >> 2);
+        const bool live = qc.live(c);
+        const T* qb = q + (live ? qc.row(c) : 0) * D;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            if (hh < G) {
-                const uint32_t* qr = reinterpret_cast<const uint32_t*>(qb + hh * D + kk * 16 + 2 * (lane & 3));
+            if (live) {
+                const uint32_t* qr = reinterpret_cast<const uint32_t*>(qb + kk * 16 + 2 * (lane & 3));
                 qf[nt][kk][0] = qr[0];
                 qf[nt][kk][1] = qr[4];
             } else {
@@ -89,24 +106,31 @@ struct WarpState {
     }
 };
 
-// Folds one page (K slice ks, V slice vs in shared memory) into the warp's
-// state; `valid` = tokens of the page inside the context (1..16).  Tokens past
-// it are masked by select, and their V rows are zeroed first, so whatever the
-// unread slots hold (NaN included) cannot reach the result.
-// ALiBi bias of a page, in log2 units: score(t, h) += slopes[h] * (pos0 + t) for
-// page-relative token t and head h of the group; pos0 is the page's first
-// position minus (n - 1).  slopes (shared memory, padded heads included) are 0
-// without ALiBi.
+// Per-column terms of the general kernel (GEN), for the lane's accumulator
+// columns nt*8 + 2*(lane&3) + j:
+//   shift: q_len - 1 - i for query token i, which sits at pos_i = n - 1 - shift
+//          (bottom-right rule); page token t is at t_abs = page start + t, and
+//          rel = t_abs - pos_i = pos0 + t + shift with pos0 the page's first
+//          position minus (n - 1).  The key is visible iff rel <= 0;
+//   slope: its head's ALiBi slope in log2 units (0 without ALiBi): bias slope * rel.
 template <int NT>
-struct PageBias {
-    const float* slopes;
+struct ColTerms {
+    float slope[NT][2];
+    int shift[NT][2];
     int pos0;
 };
 
-template <typename T, int LAYOUT, int D, int NT, bool ALIBI>
+// Folds one page (K slice ks, V slice vs in shared memory) into the warp's
+// state; `valid` = tokens of the page inside the context (1..16).  Tokens past
+// it are masked by select, and their V rows are zeroed first, so whatever the
+// unread slots hold (NaN included) cannot reach the result.  With GEN, tokens
+// past a column's causal window are masked by select as well (their V rows lie
+// inside the context, so P = 0 multiplies finite cache values), and a column
+// that has seen no visible token keeps m = -inf with alpha = P = 0.
+template <typename T, int LAYOUT, int D, int NT, bool GEN>
 __device__ __forceinline__ void page_step(uint8_t* ks, uint8_t* vs, int valid, float scale_log2,
                                           const uint32_t (&qf)[NT][D / 16][2], WarpState<D, NT>& st, int lane,
-                                          const PageBias<NT>& bias) {
+                                          const ColTerms<NT>& ct) {
     constexpr int BS = kPageTokens, KT = D / 16;
     const int mi = lane >> 3, r8 = lane & 7;   // ldmatrix: matrix index and row within it
     const uint32_t ks_a = smem_u32(ks), vs_a = smem_u32(vs);
@@ -136,8 +160,13 @@ __device__ __forceinline__ void page_step(uint8_t* ks, uint8_t* vs, int valid, f
         for (int e = 0; e < 4; ++e) {
             const int t = tr + ((e >> 1) << 3);
             float v = sc[nt][e] * scale_log2;
-            if constexpr (ALIBI) v = fmaf(bias.slopes[nt * 8 + 2 * (lane & 3) + (e & 1)], (float)(bias.pos0 + t), v);
-            sc[nt][e] = t < valid ? v : -INFINITY;
+            if constexpr (GEN) {
+                const int rel = ct.pos0 + t + ct.shift[nt][e & 1];   // key position - query position
+                v = fmaf(ct.slope[nt][e & 1], (float)rel, v);
+                sc[nt][e] = rel <= 0 ? v : -INFINITY;   // also masks every token past the context
+            } else {
+                sc[nt][e] = t < valid ? v : -INFINITY;
+            }
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -146,10 +175,11 @@ __device__ __forceinline__ void page_step(uint8_t* ks, uint8_t* vs, int valid, f
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
             const float mnew = fmaxf(st.m[nt][j], mx);
-            const float alpha = ex2(st.m[nt][j] - mnew);
+            const float mref = (GEN && mnew == -INFINITY) ? 0.f : mnew;   // nothing visible yet
+            const float alpha = ex2(st.m[nt][j] - mref);
             st.m[nt][j] = mnew;
-            sc[nt][j] = ex2(sc[nt][j] - mnew);
-            sc[nt][j + 2] = ex2(sc[nt][j + 2] - mnew);
+            sc[nt][j] = ex2(sc[nt][j] - mref);
+            sc[nt][j + 2] = ex2(sc[nt][j + 2] - mref);
             st.l[nt][j] = st.l[nt][j] * alpha + (sc[nt][j] + sc[nt][j + 2]);
 #pragma unroll
             for (int dt = 0; dt < KT; ++dt) {
@@ -253,19 +283,21 @@ __device__ __forceinline__ uint32_t fp8_off(int t, int c) {   // chunk c (16 B) 
 }
 
 // Q fragments in the permuted k order above: qf[nt][kk][0] = (q[16kk+4q], q[16kk+4q+1]),
-// qf[nt][kk][1] = (q[16kk+4q+2], q[16kk+4q+3]) of head nt*8 + g, as fp16 pairs.
+// qf[nt][kk][1] = (q[16kk+4q+2], q[16kk+4q+3]) of column nt*8 + g, as fp16 pairs.
 // bf16 queries are scaled by 2^-e (returned) when |q| > 2^15 to fit fp16; e is
 // a warp-wide maximum, the same in every warp of the CTA.
 template <typename T, int D, int NT>
-__device__ __forceinline__ int fp8_q_frags(uint32_t (&qf)[NT][D / 16][2], const T* qb, int G, int lane) {
+__device__ __forceinline__ int fp8_q_frags(uint32_t (&qf)[NT][D / 16][2], const T* qv, const QCols& qc, int lane) {
     const int g = lane >> 2, q = lane & 3;
     uint2 raw[NT][D / 16];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        const int hh = nt * 8 + g;
+        const int c = nt * 8 + g;
+        const bool live = qc.live(c);
+        const T* qb = qv + (live ? qc.row(c) : 0) * D;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-            raw[nt][kk] = hh < G ? *reinterpret_cast<const uint2*>(qb + hh * D + kk * 16 + 4 * q) : make_uint2(0u, 0u);
+            raw[nt][kk] = live ? *reinterpret_cast<const uint2*>(qb + kk * 16 + 4 * q) : make_uint2(0u, 0u);
     }
     if constexpr (std::is_same<T, __half>::value) {
 #pragma unroll
@@ -307,10 +339,10 @@ __device__ __forceinline__ int fp8_q_frags(uint32_t (&qf)[NT][D / 16][2], const 
 // One FP8 page (swizzled K and V slices in the ring) into the warp's state, as
 // page_step; fp16 tensor-core arithmetic.  V rows past `valid` are zeroed in
 // the ring stage first (the caller fences before the stage is refilled).
-template <int D, int NT, bool ALIBI>
+template <int D, int NT, bool GEN>
 __device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int valid, float scale_log2,
                                               const uint32_t (&qf)[NT][D / 16][2], WarpState<D, NT>& st, int lane,
-                                              const PageBias<NT>& bias) {
+                                              const ColTerms<NT>& ct) {
     constexpr int BS = kPageTokens, KT = D / 16;
     const int mi = lane >> 3, r8 = lane & 7;
     const int t_l = r8 + ((mi & 1) << 3), c_l = mi >> 1;   // this lane's ldmatrix row and chunk offset
@@ -341,8 +373,13 @@ __device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int vali
         for (int e = 0; e < 4; ++e) {
             const int t = tr + ((e >> 1) << 3);
             float v = sc[nt][e] * scale_log2;
-            if constexpr (ALIBI) v = fmaf(bias.slopes[nt * 8 + 2 * (lane & 3) + (e & 1)], (float)(bias.pos0 + t), v);
-            sc[nt][e] = t < valid ? v : -INFINITY;
+            if constexpr (GEN) {
+                const int rel = ct.pos0 + t + ct.shift[nt][e & 1];   // key position - query position
+                v = fmaf(ct.slope[nt][e & 1], (float)rel, v);
+                sc[nt][e] = rel <= 0 ? v : -INFINITY;   // also masks every token past the context
+            } else {
+                sc[nt][e] = t < valid ? v : -INFINITY;
+            }
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -351,10 +388,11 @@ __device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int vali
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
             const float mnew = fmaxf(st.m[nt][j], mx);
-            const float alpha = ex2(st.m[nt][j] - mnew);
+            const float mref = (GEN && mnew == -INFINITY) ? 0.f : mnew;   // nothing visible yet
+            const float alpha = ex2(st.m[nt][j] - mref);
             st.m[nt][j] = mnew;
-            sc[nt][j] = ex2(sc[nt][j] - mnew);
-            sc[nt][j + 2] = ex2(sc[nt][j + 2] - mnew);
+            sc[nt][j] = ex2(sc[nt][j] - mref);
+            sc[nt][j + 2] = ex2(sc[nt][j + 2] - mref);
             st.l[nt][j] = st.l[nt][j] * alpha + (sc[nt][j] + sc[nt][j + 2]);
 #pragma unroll
             for (int dt = 0; dt < KT; ++dt) {

@@ -7,16 +7,17 @@ namespace pkv {
 
 struct CombineParams {
     const int32_t* ctx;        // [B]
-    const float* part_acc;     // [B][Hq][ns_stride][D]
-    const float* part_m;       // [B][Hq][ns_stride]
-    const float* part_l;       // [B][Hq][ns_stride]
-    void* out;                 // [B][Hq][D]
+    const float* part_acc;     // [B][q_len][Hq][ns_stride][D]
+    const float* part_m;       // [B][q_len][Hq][ns_stride]
+    const float* part_l;       // [B][q_len][Hq][ns_stride]
+    void* out;                 // [B][q_len][Hq][D]
     int B, Hq, P, ns_stride, n_cap;
     int skip_single;           // 1: rows whose sequence has <= 1 split were written by phase 1
+    int q_len;                 // query tokens per sequence
 };
 
 // Phase-1 dispatch, one function per (layout, dtype) translation unit.
-// D in {64, 128, 256}; nt = padded-head tiles of 8 (1, or 2 for D <= 128).
+// D in {64, 128, 256}; nt = query-column tiles of 8 per CTA (1, or 2 for D <= 128).
 cudaError_t launch_decode_nhd_f16(int D, int nt, const DecodeParams& p, long long grid, const CUtensorMap& k, const CUtensorMap& v,
                                   cudaStream_t s);
 cudaError_t launch_decode_nhd_bf16(int D, int nt, const DecodeParams& p, long long grid, const CUtensorMap& k, const CUtensorMap& v,

@@ -243,6 +243,10 @@ WORKLOADS = {
     # the Llama-3-8B-shaped step with an FP8 E4M3 KV cache (K, V = N(0,1) / 16 stored, scales 1/16)
     "llama3_8b_decode_fp8": dict(B=64, Hq=32, Hkv=8, D=128, block_size=16, dtype=BF16, layout=NHD,
                                  ctx_range=(1, 4096), max_blocks_per_seq=256, kv_dtype=FP8_E4M3),
+    # the Llama-3-8B-shaped step verifying 4 tokens per sequence (speculative decoding: the last
+    # 4 cached positions of each context are queries, bottom-right causal); same lengths and pages
+    "llama3_8b_spec_decode_q4": dict(B=64, Hq=32, Hkv=8, D=128, block_size=16, dtype=BF16, layout=NHD,
+                                     ctx_range=(1, 4096), max_blocks_per_seq=256, q_len=4),
 }
 MLA_WORKLOADS = {
     "mla_prefill_h16": dict(batch=8, q_len_range=(64, 512), prefix_range=(0, 2048)),

@@ -36,7 +36,8 @@ def decode_desc(case: dict) -> B.pkv_decode_desc:
     kv = dict(kv_dtype=B.PKV_FP8_E4M3, k_scale=case["k_scale"], v_scale=case["v_scale"]) if fp8_kv(case) else {}
     return B.make_desc(case["B"], case["Hq"], case["Hkv"], case["D"], case["block_size"],
                        case["block_table"].shape[1], case["num_blocks"], int(np.max(ctx, initial=0)),
-                       int(np.sum(ctx, dtype=np.int64)), case["dtype"], case["layout"], case.get("x", 8), **kv)
+                       int(np.sum(ctx, dtype=np.int64)), case["dtype"], case["layout"], case.get("x", 8), **kv,
+                       q_len=case.get("q_len", 1))
 
 
 def cache_to_torch(bits: np.ndarray, case: dict, device) -> torch.Tensor:
@@ -72,12 +73,12 @@ def mla_workspace_for(desc, device="cuda") -> torch.Tensor:
 
 def paged_decode_attention(case: dict, dev: dict | None = None, opts=None, out=None, workspace=None,
                            stream=None) -> torch.Tensor:
-    """Runs the full decode path on a synthetic case; returns out [B][Hq][D] on the device."""
+    """Runs the full decode path on a synthetic case; returns out shaped like q
+    ([B][Hq][D], or [B][q_len][Hq][D]) on the device."""
     dev = dev if dev is not None else upload_decode_case(case)
     desc = decode_desc(case)
     if out is None:
-        out = torch.empty((case["B"], case["Hq"], case["D"]), dtype=TORCH_DTYPE[case["dtype"]],
-                          device=dev["q"].device)
+        out = torch.empty(case["q"].shape, dtype=TORCH_DTYPE[case["dtype"]], device=dev["q"].device)
     if workspace is None:
         workspace = workspace_for(desc, opts, device=dev["q"].device)
     B.pkv_paged_decode_attention(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
@@ -86,16 +87,17 @@ def paged_decode_attention(case: dict, dev: dict | None = None, opts=None, out=N
 
 
 def decode_partials(case: dict, dev: dict | None = None, opts=None, capacity: int | None = None):
-    """Phase 1 alone; returns (P, NS, m, l, acc) as float64 numpy arrays with NS columns."""
+    """Phase 1 alone; returns (P, NS, m, l, acc) as float64 numpy arrays with NS columns
+    (leading dimensions those of q without D)."""
     dev = dev if dev is not None else upload_decode_case(case)
     desc = decode_desc(case)
     ns, P = B.pkv_plan_splits(desc, opts)
     cap = capacity if capacity is not None else ns
     d = dev["q"].device
-    Bn, Hq, D = case["B"], case["Hq"], case["D"]
-    acc = torch.full((Bn, Hq, cap, D), float("nan"), dtype=torch.float32, device=d)
-    m = torch.full((Bn, Hq, cap), float("nan"), dtype=torch.float32, device=d)
-    l = torch.full((Bn, Hq, cap), float("nan"), dtype=torch.float32, device=d)
+    lead, D = tuple(case["q"].shape[:-1]), case["D"]
+    acc = torch.full(lead + (cap, D), float("nan"), dtype=torch.float32, device=d)
+    m = torch.full(lead + (cap,), float("nan"), dtype=torch.float32, device=d)
+    l = torch.full(lead + (cap,), float("nan"), dtype=torch.float32, device=d)
     P2, ns2 = B.pkv_decode_partials(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
                                     dev["context_lens"], case["scale"], acc, m, l, cap, opts=opts)
     torch.cuda.synchronize()

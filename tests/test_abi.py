@@ -43,7 +43,7 @@ def test_library_exports_every_declared_function(B):
 
 
 def test_version_and_status_strings(B):
-    assert B.pkv_version() == 2
+    assert B.pkv_version() == 3
     assert B.status_string(0) == "ok"
     assert B.status_string(5) == "bad block table"
     assert B.status_string(99) == "unknown status"
@@ -56,6 +56,13 @@ def desc(lib, **kw):
     return lib.make_desc(**base)
 
 
+def ref_row_tiles(d):
+    """Row tiles of the documented column tiling: G * q_len rows, 16 per CTA (8 for D = 256 or <= 8 rows)."""
+    R = d.Hq // d.Hkv * d.q_len
+    per_cta = 16 if (R > 8 and d.D <= 128) else 8
+    return -(-R // per_cta)
+
+
 def ref_plan(d, num_sms, P_forced=0, ns_forced=0):
     """Independent restatement of the planner's documented rule."""
     bs = d.block_size
@@ -66,7 +73,7 @@ def ref_plan(d, num_sms, P_forced=0, ns_forced=0):
         P = up(-(-max(d.max_context_len, 1) // ns_forced))
     else:
         P = up(min(max(d.max_context_len, 1), 512))
-        while P > 4 * bs and d.Hkv * -(-max(d.sum_context_len, 1) // P) < 6 * num_sms:
+        while P > 4 * bs and d.Hkv * ref_row_tiles(d) * -(-max(d.sum_context_len, 1) // P) < 6 * num_sms:
             P = max(4 * bs, up(P // 2))
     return max(1, -(-d.max_context_len // P)), P
 
@@ -79,8 +86,9 @@ def test_plan_matches_the_documented_rule(B):
         mbps = rng.randint(1, 9000)
         maxn = rng.randint(0, mbps * 16)
         s = rng.randint(maxn, max(maxn, maxn * Bn))
-        d = desc(B, B=Bn, Hkv=Hkv, Hq=Hkv * rng.choice([1, 4, 6, 8]), D=rng.choice([64, 128]),
-                 max_blocks_per_seq=mbps, max_context_len=maxn, sum_context_len=s)
+        d = desc(B, B=Bn, Hkv=Hkv, Hq=Hkv * rng.choice([1, 4, 6, 8, 12, 32]), D=rng.choice([64, 128, 256]),
+                 max_blocks_per_seq=mbps, max_context_len=maxn, sum_context_len=s,
+                 q_len=rng.choice([1, 1, 2, 3, 4, 8]))
         sms = rng.choice([1, 76, 148, 152])
         mode = rng.randint(0, 2)
         if mode == 0:
@@ -112,11 +120,17 @@ def test_workspace_size(B):
     assert B.pkv_decode_workspace_size(d, None, 152) == 256 + 2 * al(rows * 4) + al(rows * 128 * 4)
     single = B.make_opts(num_splits=1)
     assert B.pkv_decode_workspace_size(d, single, 152) == 256
+    # several query tokens: m, l [B][q_len][Hq][NS], acc [B][q_len][Hq][NS][D]
+    d4 = desc(B, q_len=4)
+    ns, P = B.pkv_plan_splits(d4, None, 152)
+    rows = 64 * 4 * 32 * ns
+    assert ns > 1 and B.pkv_decode_workspace_size(d4, None, 152) == 256 + 2 * al(rows * 4) + al(rows * 128 * 4)
 
 
 @pytest.mark.parametrize("field,value,status", [
     ("Hkv", 3, 1), ("Hq", 0, 1), ("D", 96, 2), ("block_size", 32, 2), ("dtype", 7, 1), ("layout", 2, 1),
     ("max_context_len", 256 * 16 + 1, 1), ("B", -1, 1), ("num_blocks", 0, 1), ("sum_context_len", -5, 1),
+    ("q_len", 0, 1), ("q_len", -2, 1), ("q_len", 1 << 27, 2),
 ])
 def test_bad_descriptions_are_rejected(B, field, value, status):
     d = desc(B, **{field: value})
@@ -125,13 +139,12 @@ def test_bad_descriptions_are_rejected(B, field, value, status):
     assert e.value.status == status
 
 
-def test_unsupported_group_sizes(B):
-    with pytest.raises(B.PkvError) as e:
-        B.pkv_plan_splits(desc(B, Hq=8 * 17), None, 152)
-    assert e.value.status == 2
-    with pytest.raises(B.PkvError) as e:
-        B.pkv_plan_splits(desc(B, Hq=8 * 12, D=256), None, 152)
-    assert e.value.status == 2
+def test_large_groups_take_row_tiles(B):
+    # Any group size plans: its query rows are covered by several CTAs.
+    assert B.pkv_plan_splits(desc(B, Hq=8 * 17), None, 152) == ref_plan(desc(B, Hq=8 * 17), 152)
+    assert B.pkv_plan_splits(desc(B, Hq=8 * 12, D=256), None, 152) == ref_plan(desc(B, Hq=8 * 12, D=256), 152)
+    mqa = desc(B, Hq=64, Hkv=1, q_len=3)
+    assert ref_row_tiles(mqa) == 12 and B.pkv_plan_splits(mqa, None, 152) == ref_plan(mqa, 152)
     with pytest.raises(B.PkvError) as e:
         B.pkv_plan_splits(desc(B, layout=1, x_pack=4), None, 152)
     assert e.value.status == 1
