@@ -73,17 +73,21 @@ struct DecodeTile {
     // slice pair; D >= 128 goes straight from the ring into mma fragments.
     static constexpr int STAGING = (KVB == 1 && D < 128) ? NWC * 2 * BS * D * 2 : 0;
     static constexpr int RED_STRIDE = D + 4;                        // floats per reduction row
-    static constexpr int smem_bytes(int nt) {
-        return 1024 + STAGES * 2 * SLICE + STAGING + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 16;
+    // Two column tiles at D = 128 keep the CTA's Q fragments in shared memory
+    // (one 16-row tile) instead of 32 registers per thread, so that three CTAs
+    // fit on an SM (the kernel is then compiled for 3 blocks per SM).
+    __host__ __device__ static constexpr bool q_shared(int nt) { return nt == 2 && D == 128; }
+    __host__ __device__ static constexpr int qtile_bytes(int nt) { return q_shared(nt) ? 16 * D * 2 : 0; }
+    __host__ __device__ static constexpr int smem_bytes(int nt) {
+        return 1024 + STAGES * 2 * SLICE + STAGING + qtile_bytes(nt) + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 16;
     }
 };
 
 // GEN: the general kernel (several query tokens per sequence, ALiBi), compiled
 // separately so that the one-token kernel without bias keeps its registers.
 template <typename T, int LAYOUT, int D, int NT, bool GEN>
-__global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
-    decode_phase1_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
-                         const __grid_constant__ CUtensorMap tmv) {
+__device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const CUtensorMap& tmk,
+                                                   const CUtensorMap& tmv) {
     using Tile = DecodeTile<D, LAYOUT>;
     constexpr bool KV8 = LAYOUT == kLayoutNHD8;
     constexpr bool DIRECT8 = KV8 && D >= 128;   // page_step_fp8, no staging
@@ -103,7 +107,9 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
     uint8_t* staging = smem + STAGES * 2 * SLICE;   // FP8 only: [NWC][K, V][BS][D] fp16
-    uint64_t* full = reinterpret_cast<uint64_t*>(staging + Tile::STAGING);
+    constexpr bool QS = Tile::q_shared(NT);
+    uint8_t* qtile = staging + Tile::STAGING;       // QS: the CTA's Q fragments, 16 rows of D
+    uint64_t* full = reinterpret_cast<uint64_t*>(qtile + Tile::qtile_bytes(NT));
     uint64_t* empty = full + STAGES;
     float* st_m = reinterpret_cast<float*>(empty + STAGES);
     float* st_l = st_m + NWC * HP;
@@ -241,6 +247,11 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
                     qf[nt][kk][j] = *reinterpret_cast<const uint32_t*>(&h);
                 }
     }
+    if constexpr (QS) {   // one copy for the CTA; the page steps reload it per k-step
+        if (warp == 0) store_q_frags<D>(qtile, qf, lane);
+        named_bar_sync(1, NWC * 32);
+    }
+    const uint32_t qs_a = smem_u32(qtile);
     WarpState<D, NT> ws;
     ws.reset();
     ColTerms<NT> ct;
@@ -273,7 +284,7 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
         const int valid = (pg0 + i == last_pg) ? n - last_pg * BS : BS;
         ct.pos0 = (pg0 + i) * BS - (n - 1);
         if constexpr (DIRECT8) {
-            page_step_fp8<D, NT, GEN>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, ct);
+            page_step_fp8<D, NT, GEN, QS>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, ct, qs_a);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stg]);
         } else if constexpr (KV8) {
@@ -286,7 +297,7 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
             page_step<MT, kLayoutNHD, D, NT, GEN>(sk, sk + BS * D * 2, valid, scale_log2, qf, ws, lane, ct);
             __syncwarp();
         } else {
-            page_step<T, LAYOUT, D, NT, GEN>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, ct);
+            page_step<T, LAYOUT, D, NT, GEN, QS>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, ct, qs_a);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stg]);
         }
@@ -375,12 +386,32 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     }
 }
 
+template <typename T, int LAYOUT, int D, int NT, bool GEN>
+__global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
+    decode_phase1_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                         const __grid_constant__ CUtensorMap tmv) {
+    decode_phase1_body<T, LAYOUT, D, NT, GEN>(p, tmk, tmv);
+}
+
+// The same for the shared-Q tiles, compiled for three CTAs per SM.
+template <typename T, int LAYOUT, int D, int NT, bool GEN>
+__global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32, 3)
+    decode_phase1_kernel_qs(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                            const __grid_constant__ CUtensorMap tmv) {
+    decode_phase1_body<T, LAYOUT, D, NT, GEN>(p, tmk, tmv);
+}
+
 // Host-side launcher for one instantiation (general or one-token without bias).
 template <typename T, int LAYOUT, int D, int NT, bool GEN>
 cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                          const CUtensorMap& tmv, cudaStream_t stream) {
     using Tile = DecodeTile<D, LAYOUT>;
-    auto kern = decode_phase1_kernel<T, LAYOUT, D, NT, GEN>;
+    auto kern = [] {   // only the entry this instantiation uses is compiled
+        if constexpr (Tile::q_shared(NT))
+            return decode_phase1_kernel_qs<T, LAYOUT, D, NT, GEN>;
+        else
+            return decode_phase1_kernel<T, LAYOUT, D, NT, GEN>;
+    }();
     const int smem = Tile::smem_bytes(NT);
     static bool attr_set[64] = {};
     int dev = 0;

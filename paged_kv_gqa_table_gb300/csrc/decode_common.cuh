@@ -127,10 +127,34 @@ struct ColTerms {
 // past a column's causal window are masked by select as well (their V rows lie
 // inside the context, so P = 0 multiplies finite cache values), and a column
 // that has seen no visible token keeps m = -inf with alpha = P = 0.
-template <typename T, int LAYOUT, int D, int NT, bool GEN>
+// Q^T fragments of k-step kk for both column tiles (NT = 2) from the CTA's
+// shared copy (qs_a: its shared address; rows of D 16-bit values, 16-byte
+// chunks XOR-swizzled by row & 7, holding each lane's fragments as stored by
+// store_q_frags).
+template <int D>
+__device__ __forceinline__ void load_q_smem(uint32_t qs_a, int kk, int lane, uint32_t (&b)[4]) {
+    const int mi = lane >> 3, r8 = lane & 7;
+    const int row = ((mi >> 1) << 3) + r8;
+    ldsm_x4(qs_a + (uint32_t)(row * D * 2 + (((2 * kk + (mi & 1)) ^ r8) << 4)), b);
+}
+template <int D>
+__device__ __forceinline__ void store_q_frags(uint8_t* qs, const uint32_t (&qf)[2][D / 16][2], int lane) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int row = nt * 8 + (lane >> 2);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                *reinterpret_cast<uint32_t*>(qs + row * D * 2 + (((2 * kk + j) ^ (row & 7)) << 4) + 4 * (lane & 3)) =
+                    qf[nt][kk][j];
+    }
+}
+
+template <typename T, int LAYOUT, int D, int NT, bool GEN, bool QS = false>
 __device__ __forceinline__ void page_step(uint8_t* ks, uint8_t* vs, int valid, float scale_log2,
                                           const uint32_t (&qf)[NT][D / 16][2], WarpState<D, NT>& st, int lane,
-                                          const ColTerms<NT>& ct) {
+                                          const ColTerms<NT>& ct, uint32_t qs_a = 0) {
     constexpr int BS = kPageTokens, KT = D / 16;
     const int mi = lane >> 3, r8 = lane & 7;   // ldmatrix: matrix index and row within it
     const uint32_t ks_a = smem_u32(ks), vs_a = smem_u32(vs);
@@ -148,8 +172,16 @@ __device__ __forceinline__ void page_step(uint8_t* ks, uint8_t* vs, int valid, f
             ldsm_x4(ks_a + nhd_off<BS>(t, c), a);
         else
             ldsm_x4(ks_a + (uint32_t)(c * BS * 16 + t * 16), a);
+        if constexpr (QS) {
+            static_assert(NT == 2, "the shared Q copy holds two column tiles");
+            uint32_t b[4];
+            load_q_smem<D>(qs_a, kk, lane, b);
+            Mma<T>::run(sc[0], a, b[0], b[1]);
+            Mma<T>::run(sc[1], a, b[2], b[3]);
+        } else {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) Mma<T>::run(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+            for (int nt = 0; nt < NT; ++nt) Mma<T>::run(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+        }
     }
 
     // scale to log2 units, mask, online-softmax update
@@ -339,10 +371,10 @@ __device__ __forceinline__ int fp8_q_frags(uint32_t (&qf)[NT][D / 16][2], const 
 // One FP8 page (swizzled K and V slices in the ring) into the warp's state, as
 // page_step; fp16 tensor-core arithmetic.  V rows past `valid` are zeroed in
 // the ring stage first (the caller fences before the stage is refilled).
-template <int D, int NT, bool GEN>
+template <int D, int NT, bool GEN, bool QS = false>
 __device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int valid, float scale_log2,
                                               const uint32_t (&qf)[NT][D / 16][2], WarpState<D, NT>& st, int lane,
-                                              const ColTerms<NT>& ct) {
+                                              const ColTerms<NT>& ct, uint32_t qs_a = 0) {
     constexpr int BS = kPageTokens, KT = D / 16;
     const int mi = lane >> 3, r8 = lane & 7;
     const int t_l = r8 + ((mi & 1) << 3), c_l = mi >> 1;   // this lane's ldmatrix row and chunk offset
@@ -360,8 +392,17 @@ __device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int vali
             const uint32_t* rr = r + 2 * h;
             const uint32_t a[4] = {e4m3x2_to_f16x2((uint16_t)(rr[0] & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(rr[1] & 0xFFFFu)),
                                    e4m3x2_to_f16x2((uint16_t)(rr[0] >> 16)), e4m3x2_to_f16x2((uint16_t)(rr[1] >> 16))};
+            if constexpr (QS) {
+                static_assert(NT == 2, "the shared Q copy holds two column tiles");
+                uint32_t b[4];
+                load_q_smem<D>(qs_a, 2 * c2 + h, lane, b);
+                Mma<__half>::run(sc[0], a, b[0], b[1]);
+                Mma<__half>::run(sc[1], a, b[2], b[3]);
+            } else {
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) Mma<__half>::run(sc[nt], a, qf[nt][2 * c2 + h][0], qf[nt][2 * c2 + h][1]);
+                for (int nt = 0; nt < NT; ++nt)
+                    Mma<__half>::run(sc[nt], a, qf[nt][2 * c2 + h][0], qf[nt][2 * c2 + h][1]);
+            }
         }
     }
 
