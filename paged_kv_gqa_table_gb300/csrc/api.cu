@@ -74,14 +74,17 @@ int current_sm_count(int* out) {
     return PKV_OK;
 }
 
-// Default partition: 512 tokens (or the longest context rounded up to a
-// page, if shorter), halved while the estimated number of non-empty work
+// Default partition: 512 tokens per column tile of the CTA (512 or 1024; a
+// CTA's fixed costs -- loading Q, merging its warps' columns, writing the
+// partials -- grow with its columns), or the longest context rounded up to a
+// page, if shorter; halved while the estimated number of non-empty work
 // items Hkv * row_tiles * ceil(sum_n / P) stays below six per SM, down to
 // four pages.
 long long auto_partition(const pkv_decode_desc* d, int num_sms) {
     const long long BS = d->block_size;
     const long long maxn = d->max_context_len > 0 ? d->max_context_len : 1;
-    long long P = round_up(maxn < 512 ? maxn : 512, BS);
+    const long long P0 = 512LL * column_tiles(d).nt;
+    long long P = round_up(maxn < P0 ? maxn : P0, BS);
     const long long min_p = 4 * BS;
     const long long target = 6LL * num_sms;
     const long long sum = d->sum_context_len > 0 ? d->sum_context_len : 1;

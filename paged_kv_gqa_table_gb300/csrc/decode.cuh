@@ -122,8 +122,11 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
     int item = blockIdx.x;
     const int s = item % p.NS;
     item /= p.NS;
-    const int rt = item % p.RT;
-    item /= p.RT;
+    int rt = 0;
+    if (p.RT > 1) {   // several row tiles (keeps the division off the one-tile critical path)
+        rt = item % p.RT;
+        item /= p.RT;
+    }
     const int kvh = item % p.Hkv;
     const int b = item / p.Hkv;
     const QCols qc{b, kvh * p.G, rt * HP, p.R, p.G, p.q_len, p.Hq};

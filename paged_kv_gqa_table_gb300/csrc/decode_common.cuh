@@ -45,6 +45,7 @@ struct QCols {
     __device__ __forceinline__ int token(int c) const { return (col0 + c) / G; }
     __device__ __forceinline__ size_t row(int c) const {
         const int gc = col0 + c;
+        if (q_len == 1) return (size_t)b * Hq + h0 + gc;   // no division on the one-token path
         return ((size_t)b * q_len + gc / G) * Hq + h0 + gc % G;
     }
 };

@@ -56,11 +56,14 @@ def desc(lib, **kw):
     return lib.make_desc(**base)
 
 
-def ref_row_tiles(d):
-    """Row tiles of the documented column tiling: G * q_len rows, 16 per CTA (8 for D = 256 or <= 8 rows)."""
+def ref_rows_per_cta(d):
+    """Query rows per CTA of the documented column tiling: 16, or 8 for D = 256 or <= 8 rows."""
     R = d.Hq // d.Hkv * d.q_len
-    per_cta = 16 if (R > 8 and d.D <= 128) else 8
-    return -(-R // per_cta)
+    return 16 if (R > 8 and d.D <= 128) else 8
+
+
+def ref_row_tiles(d):
+    return -(-(d.Hq // d.Hkv * d.q_len) // ref_rows_per_cta(d))
 
 
 def ref_plan(d, num_sms, P_forced=0, ns_forced=0):
@@ -72,7 +75,7 @@ def ref_plan(d, num_sms, P_forced=0, ns_forced=0):
     elif ns_forced:
         P = up(-(-max(d.max_context_len, 1) // ns_forced))
     else:
-        P = up(min(max(d.max_context_len, 1), 512))
+        P = up(min(max(d.max_context_len, 1), 512 * ref_rows_per_cta(d) // 8))
         while P > 4 * bs and d.Hkv * ref_row_tiles(d) * -(-max(d.sum_context_len, 1) // P) < 6 * num_sms:
             P = max(4 * bs, up(P // 2))
     return max(1, -(-d.max_context_len // P)), P
@@ -145,6 +148,8 @@ def test_large_groups_take_row_tiles(B):
     assert B.pkv_plan_splits(desc(B, Hq=8 * 12, D=256), None, 152) == ref_plan(desc(B, Hq=8 * 12, D=256), 152)
     mqa = desc(B, Hq=64, Hkv=1, q_len=3)
     assert ref_row_tiles(mqa) == 12 and B.pkv_plan_splits(mqa, None, 152) == ref_plan(mqa, 152)
+    # 16 query rows per CTA start from 1024-token partitions: the 4-token Llama-3-shaped step
+    assert B.pkv_plan_splits(desc(B, q_len=4), None, 152) == (4, 1024)
     with pytest.raises(B.PkvError) as e:
         B.pkv_plan_splits(desc(B, layout=1, x_pack=4), None, 152)
     assert e.value.status == 1
