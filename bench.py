@@ -36,19 +36,25 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention: KV-cache GB/s and % of GB300 HBM peak; µs/step"
 FLUSH_BYTES = 256 << 20
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_phase1_llama3_8b_decode.md")
+# committed ncu summaries per workload (their traffic is used only while the sources match)
+PROFILE_SUMMARIES = {
+    "llama3_8b_decode": os.path.join(ROOT, "profiles", "decode_phase1_llama3_8b_decode.md"),
+    "llama3_8b_spec_decode_q4": os.path.join(ROOT, "profiles", "decode_phase1_llama3_8b_spec_decode_q4.md"),
+}
 MLA_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "mla_prefill_kernel_mla_prefill_h16.md")
 FALLBACK_HBM_GBS = 6800.0
 
 
-def kernel_source_hash() -> str:
-    """sha256 over the CUDA sources; a profile's counters are valid only for the sources they were taken on."""
+def kernel_source_hash(files=None) -> str:
+    """sha256 over CUDA sources (the named csrc files, else all of them); a
+    profile's counters are valid only for the sources they were taken on."""
     csrc = os.path.join(ROOT, "paged_kv_gqa_table_gb300", "csrc")
+    if not files:
+        files = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in files:
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -60,15 +66,18 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(summary=PROFILE_SUMMARY):
+def profiled_traffic(summary):
     """Per-launch DRAM bytes of the profiled kernel from a committed ncu
-    summary, if it was taken on the current kernel sources; else None."""
-    if not os.path.exists(summary):
+    summary, if it was taken on the current kernel sources (the summary's
+    `source_files`, else every csrc file); else None."""
+    if not summary or not os.path.exists(summary):
         return None
     text = open(summary).read()
     m_hash = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    m_files = re.search(r"source_files:\s*(.+)", text)
+    files = m_files.group(1).split() if m_files else None
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(files):
         return None
     return int(m_bytes.group(1))
 
@@ -376,7 +385,7 @@ def run_gpu(args):
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak,
-                         "traffic": profiled_traffic() if args.workload == "llama3_8b_decode" else None,
+                         "traffic": profiled_traffic(PROFILE_SUMMARIES.get(args.workload)),
                          "kernel": "decode_phase1_kernel", "peak_source": peak_kind,
                          "algorithmic_bytes_per_launch": kvb, "avg_launch_us": p1_avg * 1e6},
             "wall_s_timed_region": wall,
