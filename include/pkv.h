@@ -108,11 +108,14 @@ typedef struct {
     int q_len;
 } pkv_decode_desc;
 
+/* pkv_decode_opts.flags bit: plan on the device (see pkv_paged_decode_attention). */
+#define PKV_DECODE_DEVICE_PLAN 1
+
 /* Optional knobs; pass NULL for the defaults (all zero). */
 typedef struct {
     int partition_tokens;    /* tokens per split, a multiple of block_size; 0 = planner */
     int num_splits;          /* used when partition_tokens == 0: split the longest context this many ways */
-    int reserved;            /* must be 0 */
+    int flags;               /* 0, or PKV_DECODE_DEVICE_PLAN; other bits are invalid */
     /* Optional cudaEvent_t handles recorded on `stream` right before and right
      * after the phase-1 kernel, so a caller can time that kernel alone inside a
      * full call.  NULL = not recorded. */
@@ -129,7 +132,7 @@ typedef struct {
 /* Text of a status code (static storage). */
 PKV_API const char* pkv_status_string(int status);
 
-/* ABI version of this header: 3 (2 had no q_len; 1 had no kv_dtype / k_scale / v_scale). */
+/* ABI version of this header: 4 (3 had no device plan; 2 no q_len; 1 no kv_dtype / k_scale / v_scale). */
 PKV_API int pkv_version(void);
 
 /*
@@ -153,7 +156,9 @@ PKV_API int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* 
  * Bytes of scratch memory pkv_paged_decode_attention needs for this problem
  * and these options (256-byte header, then fp32 split partials m, l
  * [B][q_len][Hq][NS] and acc [B][q_len][Hq][NS][D] when the plan has more
- * than one split).
+ * than one split; with PKV_DECODE_DEVICE_PLAN, NS is the split count of the
+ * bounds and a work list of 16 bytes per (sequence, KV head, row tile, split)
+ * slot of the bounds follows).
  * num_sms as for pkv_plan_splits.  The workspace must be 256-byte aligned.
  * Word 0 of the header collects device-side error bits (bit 0: a pipeline
  * wait timed out); zero it once after allocating.
@@ -185,6 +190,17 @@ PKV_API int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_dec
  * one split are merged by a log-sum-exp combine kernel launched as a
  * programmatic dependent of phase 1.  Calls sharing one workspace must be
  * ordered on the GPU (one stream).
+ *
+ * flags & PKV_DECODE_DEVICE_PLAN: the split plan is made on the device from
+ * context_lens (a one-CTA schedule kernel applies the planner rule of
+ * pkv_plan_splits to the actual longest and total context, with the
+ * partition raised where needed so that the splits fit the bounds' split
+ * count, and lists the non-empty work items); max_context_len and
+ * sum_context_len are then only capacity bounds that size the workspace.
+ * Phase 1 runs a fixed grid of min(bound items, 24 per SM) CTAs that take
+ * the listed items in order, so a call captured into a CUDA graph with loose
+ * bounds launches no CTA per empty split.  pkv_decode_partials does not take
+ * this flag.
  */
 PKV_API int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
                                const void* q, const void* k_cache, const void* v_cache,

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libpkv (declared in include/pkv.h): argument
 // validation, the split planner, TMA descriptor set-up and kernel dispatch.
 // Host code only; nothing here touches device memory directly.
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cudaTypedefs.h>
@@ -102,7 +103,7 @@ long long auto_partition(const pkv_decode_desc* d, int num_sms) {
 int plan(const pkv_decode_desc* d, const pkv_decode_opts* o, int num_sms, int* ns, int* P) {
     int st = check_desc(d);
     if (st) return st;
-    if (o && o->reserved != 0) return PKV_INVALID_ARG;
+    if (o && (o->flags & ~PKV_DECODE_DEVICE_PLAN) != 0) return PKV_INVALID_ARG;
     if (num_sms <= 0) {
         st = current_sm_count(&num_sms);
         if (st) return st;
@@ -132,6 +133,27 @@ size_t partial_bytes(const pkv_decode_desc* d, int ns) {
     const size_t rows = (size_t)d->B * d->q_len * d->Hq * ns;
     return 2 * align256(rows * 4) + align256(rows * d->D * 4);
 }
+
+bool device_plan(const pkv_decode_opts* o) { return o && (o->flags & PKV_DECODE_DEVICE_PLAN); }
+
+// Work items of the bounds' plan: (sequence, KV head, row tile, split) slots.
+long long plan_items(const pkv_decode_desc* d, int ns) {
+    return (long long)d->B * d->Hkv * column_tiles(d).rt * ns;
+}
+
+// Workspace: 256-byte header | split partials (more than one split) | the
+// device plan's work list (16 bytes per item slot of the bounds).
+size_t required_workspace(const pkv_decode_desc* d, const pkv_decode_opts* o, int ns) {
+    size_t b = kHeaderBytes + (ns > 1 ? partial_bytes(d, ns) : 0);
+    if (device_plan(o)) b += align256((size_t)plan_items(d, ns) * 16);
+    return b;
+}
+
+// Header words of the device plan: {P, splits of the longest context, items}.
+constexpr int kSchedHeaderWord = 4;
+// Phase-1 CTAs of the device plan: enough to fill the GPU many times over;
+// more items than this are taken in turns.
+constexpr int kDevicePlanCtasPerSm = 24;
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -216,11 +238,12 @@ int encode_rows_map(CUtensorMap* map, const void* base, cuuint64_t cols, cuuint6
     return r == CUDA_SUCCESS ? PKV_OK : PKV_INVALID_ARG;
 }
 
-// Launches phase 1 over the grid (sequence, KV head, row tile, split).
+// Launches phase 1 over the grid (sequence, KV head, row tile, split), or
+// over `grid` CTAs that take the device plan's listed items.
 cudaError_t dispatch_phase1(const pkv_decode_desc* d, const DecodeParams& p, const CUtensorMap& k,
-                            const CUtensorMap& v, cudaStream_t s) {
+                            const CUtensorMap& v, cudaStream_t s, long long grid = 0) {
     const int nt = column_tiles(d).nt;
-    const long long grid = (long long)p.B * p.Hkv * p.RT * p.NS;
+    if (grid <= 0) grid = (long long)p.B * p.Hkv * p.RT * p.NS;
     const bool bf = d->dtype == PKV_BF16;
     if (d->kv_dtype == PKV_FP8_E4M3)
         return bf ? launch_decode_nhd8_bf16(d->D, nt, p, grid, k, v, s)
@@ -292,7 +315,7 @@ const char* pkv_status_string(int status) {
     }
 }
 
-int pkv_version(void) { return 3; }
+int pkv_version(void) { return 4; }
 
 int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms, int* num_splits,
                     int* partition_tokens) {
@@ -305,7 +328,7 @@ int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts
     int ns = 0, P = 0;
     int st = plan(desc, opts, num_sms, &ns, &P);
     if (st) return st;
-    *bytes = kHeaderBytes + (ns > 1 ? partial_bytes(desc, ns) : 0);
+    *bytes = required_workspace(desc, opts, ns);
     return PKV_OK;
 }
 
@@ -324,7 +347,7 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
     int ns = 0, P = 0;
     st = plan(desc, opts, 0, &ns, &P);
     if (st) return st;
-    if (workspace_bytes < kHeaderBytes + (ns > 1 ? partial_bytes(desc, ns) : 0)) return PKV_WORKSPACE_TOO_SMALL;
+    if (workspace_bytes < required_workspace(desc, opts, ns)) return PKV_WORKSPACE_TOO_SMALL;
 
     DecodeParams p;
     CUtensorMap mk{}, mv{};
@@ -343,16 +366,37 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
 
     if (desc->max_context_len == 0) {
         // Every context is empty: the combine kernel writes the zero rows.
-        CombineParams c{context_lens, nullptr, nullptr, nullptr, out, desc->B, desc->Hq, P, ns, 0, 0, desc->q_len};
+        CombineParams c{context_lens, nullptr, nullptr, nullptr, out, desc->B, desc->Hq, P, ns, 0, 0, desc->q_len,
+                        nullptr};
         return launch_combine(desc->dtype, desc->D, c, s, false) == cudaSuccess ? PKV_OK : PKV_CUDA_ERROR;
     }
+    long long grid = 0;
+    if (device_plan(opts)) {
+        // The schedule kernel plans from the device's context lengths; phase 1
+        // (its programmatic dependent) takes the listed items.
+        if (desc->Hkv > 0xFFFF || column_tiles(desc).rt > 0x7FFF) return PKV_UNSUPPORTED;   // list packing
+        int sms = 0;
+        st = current_sm_count(&sms);
+        if (st) return st;
+        int* hdr = reinterpret_cast<int*>(ws) + kSchedHeaderWord;
+        int4* list = reinterpret_cast<int4*>(parts + (ns > 1 ? partial_bytes(desc, ns) : 0));
+        const ColumnTiles ct = column_tiles(desc);
+        SchedParams sp{context_lens, hdr, list, desc->B, desc->Hkv, ct.rt, p.n_cap, ns, desc->block_size,
+                       opts->partition_tokens > 0 ? P : 0, opts->partition_tokens > 0 ? 0 : opts->num_splits,
+                       512 * ct.nt, sms};
+        p.sched_hdr = hdr;
+        p.sched_list = list;
+        p.sched_cap = (int)plan_items(desc, ns);
+        grid = std::min(plan_items(desc, ns), (long long)kDevicePlanCtasPerSm * sms);
+        if (launch_schedule(sp, s) != cudaSuccess) return PKV_CUDA_ERROR;
+    }
     record(opts ? opts->phase1_event_start : nullptr, s);
-    if (dispatch_phase1(desc, p, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
+    if (dispatch_phase1(desc, p, mk, mv, s, grid) != cudaSuccess) return PKV_CUDA_ERROR;
     record(opts ? opts->phase1_event_stop : nullptr, s);
     if (ns > 1) {
         // Programmatic dependent of phase 1 (unless an event sits between them).
         CombineParams c{context_lens, p.part_acc, p.part_m, p.part_l, out, desc->B, desc->Hq, P, ns, p.n_cap, 1,
-                        desc->q_len};
+                        desc->q_len, p.sched_hdr};
         if (launch_combine(desc->dtype, desc->D, c, s, !(opts && opts->phase1_event_stop)) != cudaSuccess)
             return PKV_CUDA_ERROR;
     }
@@ -365,6 +409,7 @@ int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts
                         int* partition_tokens_out, int* num_splits_out, pkv_stream_t stream) {
     int st = check_desc(desc);
     if (st) return st;
+    if (device_plan(opts)) return PKV_UNSUPPORTED;   // partials are laid out by the host plan
     if (desc->B > 0) {
         st = check_tensors(desc, q, k_cache, v_cache, block_table, context_lens);
         if (st) return st;
@@ -411,7 +456,7 @@ int pkv_combine(const pkv_decode_desc* desc, int partition_tokens, int num_split
     if (desc->B == 0) return PKV_OK;
     if (!context_lens || !part_acc || !part_m || !part_l || !out || !aligned(part_acc, 16)) return PKV_INVALID_ARG;
     CombineParams c{context_lens, part_acc, part_m, part_l, out, desc->B, desc->Hq, partition_tokens, num_splits,
-                    desc->max_context_len, 0, desc->q_len};
+                    desc->max_context_len, 0, desc->q_len, nullptr};
     return launch_combine(desc->dtype, desc->D, c, reinterpret_cast<cudaStream_t>(stream), false) == cudaSuccess
                ? PKV_OK
                : PKV_CUDA_ERROR;

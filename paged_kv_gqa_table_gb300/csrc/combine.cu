@@ -40,7 +40,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
     if (live) n = row_context(p, bh, &empty);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!live) return;
-    const int ns = (n + p.P - 1) / p.P;
+    const int P = p.sched_hdr ? p.sched_hdr[0] : p.P;   // the device plan's partition
+    const int ns = (n + P - 1) / P;
     if (p.skip_single && ns <= 1) return;   // phase 1 wrote this row directly
     T* o = reinterpret_cast<T*>(p.out) + bh * D + lane * EPL;
     if (empty) {
@@ -112,7 +113,8 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(const CombineParams p
     bool empty = true;
     const int n = row_context(p, bh, &empty);
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int ns = (n + p.P - 1) / p.P;
+    const int P = p.sched_hdr ? p.sched_hdr[0] : p.P;
+    const int ns = (n + P - 1) / P;
     if (p.skip_single && ns <= 1) return;
     T* o = reinterpret_cast<T*>(p.out) + bh * D;
     if (empty) {

@@ -59,6 +59,12 @@ struct DecodeParams {
     float v_scale;           // multiplies the output / partial acc (FP8 caches; 1 otherwise)
     const float* alibi;      // [Hq] ALiBi slopes (natural-log units) or nullptr
     int partials_only;       // 1: always write partials (+ sentinels), never out
+    // Device plan (else nullptr): the schedule kernel's header {P, splits of the
+    // longest context, items} and its list of items (b, kvh | rt << 16, s, n_b) in
+    // grid order; this grid's CTAs take items blockIdx.x, blockIdx.x + gridDim.x, ...
+    const int* sched_hdr;
+    const int4* sched_list;
+    int sched_cap;           // entries the list has room for (>= any item count)
 };
 
 template <int D, int LAYOUT>
@@ -85,9 +91,13 @@ struct DecodeTile {
 
 // GEN: the general kernel (several query tokens per sequence, ALiBi), compiled
 // separately so that the one-token kernel without bias keeps its registers.
-template <typename T, int LAYOUT, int D, int NT, bool GEN>
+// SCHED (with GEN): the CTA takes the device plan's listed items in turn
+// instead of its one grid-order item; compiled separately too, the item loop
+// costs registers.
+template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED>
 __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const CUtensorMap& tmk,
                                                    const CUtensorMap& tmv) {
+    static_assert(GEN || !SCHED, "the device plan runs the general kernel");
     using Tile = DecodeTile<D, LAYOUT>;
     constexpr bool KV8 = LAYOUT == kLayoutNHD8;
     constexpr bool DIRECT8 = KV8 && D >= 128;   // page_step_fp8, no staging
@@ -119,23 +129,19 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
     // soon as every CTA of this grid is running (it waits for our results).
     asm volatile("griddepcontrol.launch_dependents;");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int item = blockIdx.x;
-    const int s = item % p.NS;
-    item /= p.NS;
-    int rt = 0;
-    if (p.RT > 1) {   // several row tiles (keeps the division off the one-tile critical path)
-        rt = item % p.RT;
-        item /= p.RT;
-    }
-    const int kvh = item % p.Hkv;
-    const int b = item / p.Hkv;
+    bool inited = false;   // the ring's barriers have been initialised (uniform)
+
+    // One work item: split s of row tile rt of KV head kvh of sequence b, with
+    // P-token partitions (n_known: its clamped context length, or -1 to load
+    // it).  Every thread of the CTA runs it.
+    auto run_item = [&](const int b, const int kvh, const int rt, const int s, const int P, const int n_known) {
     const QCols qc{b, kvh * p.G, rt * HP, p.R, p.G, p.q_len, p.Hq};
     const int ncols = min(HP, p.R - qc.col0);   // live columns of this CTA
 
-    const int n = clampi(p.ctx[b], 0, p.n_cap);
-    const int ns_b = (n + p.P - 1) / p.P;
-    const int t0 = s * p.P;
-    const int t1 = min(t0 + p.P, n);
+    const int n = n_known >= 0 ? n_known : clampi(p.ctx[b], 0, p.n_cap);
+    const int ns_b = (n + P - 1) / P;
+    const int t0 = s * P;
+    const int t1 = min(t0 + P, n);
 
     if (t0 >= t1) {
         // Split past the context.  Partials mode writes the (-inf, 0, 0)
@@ -158,6 +164,10 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
+            if (inited) {   // a later item of this CTA: every phase of the previous one is complete
+                mbar_inval(&full[i]);
+                mbar_inval(&empty[i]);
+            }
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
@@ -165,6 +175,7 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
         *abort_flag = 0;
     }
     __syncthreads();
+    inited = true;
 
     const int pg0 = t0 / BS;                        // first page of the split (sequence-relative)
     const int npg = (t1 + BS - 1) / BS - pg0;       // pages in the split
@@ -387,33 +398,66 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
             }
         }
     }
+    };   // run_item
+
+    if constexpr (!SCHED) {   // grid order: this CTA's one item
+        int item = blockIdx.x;
+        const int s = item % p.NS;
+        item /= p.NS;
+        int rt = 0;
+        if (p.RT > 1) {   // several row tiles (keeps the division off the one-tile critical path)
+            rt = item % p.RT;
+            item /= p.RT;
+        }
+        run_item(item / p.Hkv, item % p.Hkv, rt, s, p.P, -1);
+        return;
+    }
+    // Device plan: the schedule kernel (this grid's programmatic prerequisite)
+    // has written the partition size and the list of non-empty items.
+    if (threadIdx.x == 0) *abort_flag = 0;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __syncthreads();
+    // The header is re-read per item rather than held in registers across it,
+    // with plain loads: a read-only (non-coherent) load may be hoisted above
+    // the wait and see the header before the schedule kernel wrote it.  The
+    // list entry is loaded with the item count (one round trip): every slot
+    // below sched_cap is inside the list.
+    for (int it = blockIdx.x; it < p.sched_cap; it += gridDim.x) {
+        const int4 e = p.sched_list[it];
+        if (it >= p.sched_hdr[2]) break;
+        run_item(e.x, e.y & 0xFFFF, e.y >> 16, e.z, p.sched_hdr[0], e.w);
+        fence_proxy_async_smem();   // this item's generic writes to the ring before the next item's copies
+        __syncthreads();            // every role is done with the ring, the barriers and the Q tile
+        if (*abort_flag) break;     // a wait timed out (already reported): take no further item
+    }
 }
 
-template <typename T, int LAYOUT, int D, int NT, bool GEN>
+template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED>
 __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     decode_phase1_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv) {
-    decode_phase1_body<T, LAYOUT, D, NT, GEN>(p, tmk, tmv);
+    decode_phase1_body<T, LAYOUT, D, NT, GEN, SCHED>(p, tmk, tmv);
 }
 
 // The same for the shared-Q tiles, compiled for three CTAs per SM.
-template <typename T, int LAYOUT, int D, int NT, bool GEN>
+template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED>
 __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32, 3)
     decode_phase1_kernel_qs(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv) {
-    decode_phase1_body<T, LAYOUT, D, NT, GEN>(p, tmk, tmv);
+    decode_phase1_body<T, LAYOUT, D, NT, GEN, SCHED>(p, tmk, tmv);
 }
 
-// Host-side launcher for one instantiation (general or one-token without bias).
-template <typename T, int LAYOUT, int D, int NT, bool GEN>
+// Host-side launcher for one instantiation (one-token without bias, general,
+// or general over the device plan's items).
+template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED>
 cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                          const CUtensorMap& tmv, cudaStream_t stream) {
     using Tile = DecodeTile<D, LAYOUT>;
     auto kern = [] {   // only the entry this instantiation uses is compiled
         if constexpr (Tile::q_shared(NT))
-            return decode_phase1_kernel_qs<T, LAYOUT, D, NT, GEN>;
+            return decode_phase1_kernel_qs<T, LAYOUT, D, NT, GEN, SCHED>;
         else
-            return decode_phase1_kernel<T, LAYOUT, D, NT, GEN>;
+            return decode_phase1_kernel<T, LAYOUT, D, NT, GEN, SCHED>;
     }();
     const int smem = Tile::smem_bytes(NT);
     static bool attr_set[64] = {};
@@ -426,6 +470,19 @@ cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, 
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
+    if (SCHED) {   // programmatic dependent of the schedule kernel just enqueued
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3((Tile::NWC + 1) * 32);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv);
+    }
     kern<<<(unsigned)grid, (Tile::NWC + 1) * 32, smem, stream>>>(p, tmk, tmv);
     return cudaGetLastError();
 }
@@ -433,8 +490,9 @@ cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, 
 template <typename T, int LAYOUT, int D, int NT>
 cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                  const CUtensorMap& tmv, cudaStream_t stream) {
-    return (p.alibi || p.q_len > 1) ? launch_decode_phase1_variant<T, LAYOUT, D, NT, true>(p, grid, tmk, tmv, stream)
-                                    : launch_decode_phase1_variant<T, LAYOUT, D, NT, false>(p, grid, tmk, tmv, stream);
+    if (p.sched_hdr) return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, true>(p, grid, tmk, tmv, stream);
+    return (p.alibi || p.q_len > 1) ? launch_decode_phase1_variant<T, LAYOUT, D, NT, true, false>(p, grid, tmk, tmv, stream)
+                                    : launch_decode_phase1_variant<T, LAYOUT, D, NT, false, false>(p, grid, tmk, tmv, stream);
 }
 
 }  // namespace pkv

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_function(B):
 
 
 def test_version_and_status_strings(B):
-    assert B.pkv_version() == 3
+    assert B.pkv_version() == 4
     assert B.status_string(0) == "ok"
     assert B.status_string(5) == "bad block table"
     assert B.status_string(99) == "unknown status"
@@ -140,6 +140,25 @@ def test_bad_descriptions_are_rejected(B, field, value, status):
     with pytest.raises(B.PkvError) as e:
         B.pkv_plan_splits(d, None, 152)
     assert e.value.status == status
+
+
+def test_device_plan_options(B):
+    al = lambda x: (x + 255) // 256 * 256
+    d = desc(B)
+    ns, P = B.pkv_plan_splits(d, None, 152)
+    plain = B.pkv_decode_workspace_size(d, None, 152)
+    # the work list adds 16 bytes per (sequence, KV head, row tile, split) slot of the bounds
+    dev = B.pkv_decode_workspace_size(d, B.make_opts(device_plan=True), 152)
+    assert dev == plain + al(64 * 8 * 1 * ns * 16)
+    assert B.pkv_plan_splits(d, B.make_opts(device_plan=True), 152) == (ns, P)
+    for bad in (2, 4, 1 << 30, -1):
+        with pytest.raises(B.PkvError) as e:
+            B.pkv_plan_splits(d, B.make_opts(flags=bad), 152)
+        assert e.value.status == B.PKV_INVALID_ARG
+    # phase 1 alone keeps the host plan's partial layout
+    st = B.raw_status("pkv_decode_partials", ctypes.byref(d), ctypes.byref(B.make_opts(device_plan=True)),
+                      None, None, None, None, None, ctypes.c_float(0.1), None, None, None, 8, None, None, None)
+    assert st == B.PKV_UNSUPPORTED
 
 
 def test_large_groups_take_row_tiles(B):
