@@ -135,269 +135,269 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
     // P-token partitions (n_known: its clamped context length, or -1 to load
     // it).  Every thread of the CTA runs it.
     auto run_item = [&](const int b, const int kvh, const int rt, const int s, const int P, const int n_known) {
-    const QCols qc{b, kvh * p.G, rt * HP, p.R, p.G, p.q_len, p.Hq};
-    const int ncols = min(HP, p.R - qc.col0);   // live columns of this CTA
+        const QCols qc{b, kvh * p.G, rt * HP, p.R, p.G, p.q_len, p.Hq};
+        const int ncols = min(HP, p.R - qc.col0);   // live columns of this CTA
 
-    const int n = n_known >= 0 ? n_known : clampi(p.ctx[b], 0, p.n_cap);
-    const int ns_b = (n + P - 1) / P;
-    const int t0 = s * P;
-    const int t1 = min(t0 + P, n);
+        const int n = n_known >= 0 ? n_known : clampi(p.ctx[b], 0, p.n_cap);
+        const int ns_b = (n + P - 1) / P;
+        const int t0 = s * P;
+        const int t1 = min(t0 + P, n);
 
-    if (t0 >= t1) {
-        // Split past the context.  Partials mode writes the (-inf, 0, 0)
-        // sentinel; an empty context (n == 0) writes zero output rows.
-        if (p.partials_only) {
-            for (int i = threadIdx.x; i < ncols * D; i += blockDim.x) {
-                const size_t row = qc.row(i / D) * p.ns_stride + s;
-                p.part_acc[row * D + i % D] = 0.f;
-                if (i % D == 0) {
-                    p.part_m[row] = -INFINITY;
-                    p.part_l[row] = 0.f;
+        if (t0 >= t1) {
+            // Split past the context.  Partials mode writes the (-inf, 0, 0)
+            // sentinel; an empty context (n == 0) writes zero output rows.
+            if (p.partials_only) {
+                for (int i = threadIdx.x; i < ncols * D; i += blockDim.x) {
+                    const size_t row = qc.row(i / D) * p.ns_stride + s;
+                    p.part_acc[row * D + i % D] = 0.f;
+                    if (i % D == 0) {
+                        p.part_m[row] = -INFINITY;
+                        p.part_l[row] = 0.f;
+                    }
                 }
+            } else if (n == 0 && s == 0) {
+                for (int i = threadIdx.x; i < ncols * D; i += blockDim.x)
+                    reinterpret_cast<T*>(p.out)[qc.row(i / D) * D + i % D] = from_float<T>(0.f);
             }
-        } else if (n == 0 && s == 0) {
-            for (int i = threadIdx.x; i < ncols * D; i += blockDim.x)
-                reinterpret_cast<T*>(p.out)[qc.row(i / D) * D + i % D] = from_float<T>(0.f);
+            return;
         }
-        return;
-    }
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; ++i) {
-            if (inited) {   // a later item of this CTA: every phase of the previous one is complete
-                mbar_inval(&full[i]);
-                mbar_inval(&empty[i]);
-            }
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
-        }
-        fence_barrier_init();
-        *abort_flag = 0;
-    }
-    __syncthreads();
-    inited = true;
-
-    const int pg0 = t0 / BS;                        // first page of the split (sequence-relative)
-    const int npg = (t1 + BS - 1) / BS - pg0;       // pages in the split
-    const int32_t* trow = p.table + (size_t)b * p.MBPS + pg0;
-
-    if (warp == NWC) {
-        // ------------------------------------------------------------ producer
-        const uint64_t pol = policy_evict_first();
-        if (lane == 0) {
-            prefetch_tensormap(&tmk);
-            prefetch_tensormap(&tmv);
-        }
-        int id_cur = lane < npg ? trow[lane] : 0;
-        int id_nxt = 32 + lane < npg ? trow[32 + lane] : 0;
-        bool ok = true;
-        int issued = 0;
-        for (int i = 0; i < npg; ++i) {
-            const int stg = i % STAGES;
-            if (i >= STAGES) {
-                const bool got = mbar_wait(&empty[stg], ((i / STAGES) - 1) & 1);
-                if (!__all_sync(0xffffffffu, got && *abort_flag == 0)) {
-                    ok = false;
-                    *abort_flag = 1;
-                    break;
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < STAGES; ++i) {
+                if (inited) {   // a later item of this CTA: every phase of the previous one is complete
+                    mbar_inval(&full[i]);
+                    mbar_inval(&empty[i]);
                 }
+                mbar_init(&full[i], 1);
+                mbar_init(&empty[i], 1);
             }
-            int phys = __shfl_sync(0xffffffffu, id_cur, i & 31);
-            phys = (phys < 0 || phys >= p.NB) ? 0 : phys;   // bad entries never leave the pool
+            fence_barrier_init();
+            *abort_flag = 0;
+        }
+        __syncthreads();
+        inited = true;
+
+        const int pg0 = t0 / BS;                        // first page of the split (sequence-relative)
+        const int npg = (t1 + BS - 1) / BS - pg0;       // pages in the split
+        const int32_t* trow = p.table + (size_t)b * p.MBPS + pg0;
+
+        if (warp == NWC) {
+            // ------------------------------------------------------------ producer
+            const uint64_t pol = policy_evict_first();
             if (lane == 0) {
-                uint8_t* kd = ring + stg * 2 * SLICE;
-                issue_page_loads<LAYOUT, D>(kd, kd + SLICE, &tmk, &tmv, &full[stg], phys * p.Hkv + kvh, pol);
+                prefetch_tensormap(&tmk);
+                prefetch_tensormap(&tmv);
             }
-            issued = i + 1;
-            if ((i & 31) == 31) {
-                id_cur = id_nxt;
-                const int j = i + 33 + lane;
-                id_nxt = j < npg ? trow[j] : 0;
+            int id_cur = lane < npg ? trow[lane] : 0;
+            int id_nxt = 32 + lane < npg ? trow[32 + lane] : 0;
+            bool ok = true;
+            int issued = 0;
+            for (int i = 0; i < npg; ++i) {
+                const int stg = i % STAGES;
+                if (i >= STAGES) {
+                    const bool got = mbar_wait(&empty[stg], ((i / STAGES) - 1) & 1);
+                    if (!__all_sync(0xffffffffu, got && *abort_flag == 0)) {
+                        ok = false;
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
+                int phys = __shfl_sync(0xffffffffu, id_cur, i & 31);
+                phys = (phys < 0 || phys >= p.NB) ? 0 : phys;   // bad entries never leave the pool
+                if (lane == 0) {
+                    uint8_t* kd = ring + stg * 2 * SLICE;
+                    issue_page_loads<LAYOUT, D>(kd, kd + SLICE, &tmk, &tmv, &full[stg], phys * p.Hkv + kvh, pol);
+                }
+                issued = i + 1;
+                if ((i & 31) == 31) {
+                    id_cur = id_nxt;
+                    const int j = i + 33 + lane;
+                    id_nxt = j < npg ? trow[j] : 0;
+                }
             }
+            // Never leave with copies in flight into this CTA's shared memory.
+            for (int i = max(0, issued - STAGES); i < issued; ++i)
+                if (!mbar_wait(&full[i % STAGES], (i / STAGES) & 1)) ok = false;
+            if (!ok && lane == 0 && p.err) atomicOr(p.err, kErrTimeout);
+            return;
         }
-        // Never leave with copies in flight into this CTA's shared memory.
-        for (int i = max(0, issued - STAGES); i < issued; ++i)
-            if (!mbar_wait(&full[i % STAGES], (i / STAGES) & 1)) ok = false;
-        if (!ok && lane == 0 && p.err) atomicOr(p.err, kErrTimeout);
-        return;
-    }
 
-    // ---------------------------------------------------------------- consumers
-    uint32_t qf[NT][KT][2];
-    float scale_log2 = p.scale_log2;
-    if constexpr (DIRECT8) {
-        const int qe = fp8_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q), qc, lane);
-        scale_log2 *= exp2f((float)qe);
-    } else {
-        load_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q), qc, lane);
-    }
-    if constexpr (KV8 && !DIRECT8 && std::is_same<T, __nv_bfloat16>::value) {
-        // bf16 queries meet fp16 keys: convert them, scaled by 2^-e when
-        // |q| > 2^15 so that they stay inside the fp16 range (e is the same
-        // in every warp: each holds the whole group's Q); 2^e goes into the
-        // score scale.
-        uint32_t mx = 0;
+        // ---------------------------------------------------------------- consumers
+        uint32_t qf[NT][KT][2];
+        float scale_log2 = p.scale_log2;
+        if constexpr (DIRECT8) {
+            const int qe = fp8_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q), qc, lane);
+            scale_log2 *= exp2f((float)qe);
+        } else {
+            load_q_frags<T, D, NT>(qf, reinterpret_cast<const T*>(p.q), qc, lane);
+        }
+        if constexpr (KV8 && !DIRECT8 && std::is_same<T, __nv_bfloat16>::value) {
+            // bf16 queries meet fp16 keys: convert them, scaled by 2^-e when
+            // |q| > 2^15 so that they stay inside the fp16 range (e is the same
+            // in every warp: each holds the whole group's Q); 2^e goes into the
+            // score scale.
+            uint32_t mx = 0;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int kk = 0; kk < KT; ++kk)
+                for (int kk = 0; kk < KT; ++kk)
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    mx = max(mx, max((qf[nt][kk][j] << 16) & 0x7FFFFFFFu, qf[nt][kk][j] & 0x7FFF0000u));
-        mx = __reduce_max_sync(0xffffffffu, mx);
-        const int ex = (int)((mx >> 23) & 0xFF) - 127;   // floor(log2 max|q|) for normal values
-        const int e = min(max(ex - 14, 0), 120);
-        const float down = exp2f((float)-e);
-        scale_log2 *= exp2f((float)e);
+                    for (int j = 0; j < 2; ++j)
+                        mx = max(mx, max((qf[nt][kk][j] << 16) & 0x7FFFFFFFu, qf[nt][kk][j] & 0x7FFF0000u));
+            mx = __reduce_max_sync(0xffffffffu, mx);
+            const int ex = (int)((mx >> 23) & 0xFF) - 127;   // floor(log2 max|q|) for normal values
+            const int e = min(max(ex - 14, 0), 120);
+            const float down = exp2f((float)-e);
+            scale_log2 *= exp2f((float)e);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int kk = 0; kk < KT; ++kk)
+                for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const uint32_t w = qf[nt][kk][j];
+                        const __half2 h = __floats2half2_rn(__uint_as_float(w << 16) * down,
+                                                            __uint_as_float(w & 0xFFFF0000u) * down);
+                        qf[nt][kk][j] = *reinterpret_cast<const uint32_t*>(&h);
+                    }
+        }
+        if constexpr (QS) {   // one copy for the CTA; the page steps reload it per k-step
+            if (warp == 0) store_q_frags<D>(qtile, qf, lane);
+            named_bar_sync(1, NWC * 32);
+        }
+        const uint32_t qs_a = smem_u32(qtile);
+        WarpState<D, NT> ws;
+        ws.reset();
+        ColTerms<NT> ct;
+        if constexpr (GEN) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const uint32_t w = qf[nt][kk][j];
-                    const __half2 h = __floats2half2_rn(__uint_as_float(w << 16) * down,
-                                                        __uint_as_float(w & 0xFFFF0000u) * down);
-                    qf[nt][kk][j] = *reinterpret_cast<const uint32_t*>(&h);
+                    const int c = nt * 8 + 2 * (lane & 3) + j;
+                    const bool live = qc.live(c);
+                    const int gc = qc.col0 + c;
+                    ct.shift[nt][j] = live ? p.q_len - 1 - gc / p.G : 0;
+                    ct.slope[nt][j] =
+                        (live && p.alibi) ? __ldg(p.alibi + qc.h0 + gc % p.G) * 1.4426950408889634f : 0.f;
                 }
-    }
-    if constexpr (QS) {   // one copy for the CTA; the page steps reload it per k-step
-        if (warp == 0) store_q_frags<D>(qtile, qf, lane);
+        }
+
+        const int last_pg = (n - 1) / BS;
+        bool ok = true;
+
+        for (int i = warp; i < npg; i += NWC) {
+            const int stg = i % STAGES;
+            const bool got = mbar_wait(&full[stg], (i / STAGES) & 1);
+            if (!__all_sync(0xffffffffu, got && *abort_flag == 0)) {
+                ok = false;
+                *abort_flag = 1;
+                break;
+            }
+            uint8_t* ks = ring + stg * 2 * SLICE;
+            const int valid = (pg0 + i == last_pg) ? n - last_pg * BS : BS;
+            ct.pos0 = (pg0 + i) * BS - (n - 1);
+            if constexpr (DIRECT8) {
+                page_step_fp8<D, NT, GEN, QS>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, ct, qs_a);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stg]);
+            } else if constexpr (KV8) {
+                // expand into this warp's fp16 slices; the ring stage is free again at once
+                uint8_t* sk = staging + warp * 2 * (BS * D * 2);
+                expand_fp8_slice<D>(ks, sk, lane);
+                expand_fp8_slice<D>(ks + SLICE, sk + BS * D * 2, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stg]);
+                page_step<MT, kLayoutNHD, D, NT, GEN>(sk, sk + BS * D * 2, valid, scale_log2, qf, ws, lane, ct);
+                __syncwarp();
+            } else {
+                page_step<T, LAYOUT, D, NT, GEN, QS>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, ct, qs_a);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stg]);
+            }
+        }
+        if (!ok && lane == 0 && p.err) atomicOr(p.err, kErrTimeout);
+
+        // ------------------------------------------------- merge the warps' states
+        ws.finish_l();
+        if (lane < 4) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    st_m[warp * HP + nt * 8 + 2 * lane + j] = ws.m[nt][j];
+                    st_l[warp * HP + nt * 8 + 2 * lane + j] = ws.l[nt][j];
+                }
+        }
+        named_bar_sync(1, NWC * 32);   // every consumer is past its last page
+
+        float* red = reinterpret_cast<float*>(ring);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int h = nt * 8 + 2 * (lane & 3) + j;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < NWC; ++w) M = fmaxf(M, st_m[w * HP + h]);
+                if (M == -INFINITY) M = 0.f;   // a column that saw no visible token: every f is 0
+                const float f = ex2(ws.m[nt][j] - M);   // 0 for a warp that saw no page
+                if constexpr (DIRECT8) {   // mma rows g, g+8 of d-tile dt hold d = 16dt + 2g, 16dt + 2g + 1
+                    float* row = red + (warp * HP + h) * RS + 2 * (lane >> 2);
+#pragma unroll
+                    for (int dt = 0; dt < KT; ++dt) {
+                        row[dt * 16] = ws.acc[dt][nt][j] * f;
+                        row[dt * 16 + 1] = ws.acc[dt][nt][j + 2] * f;
+                    }
+                } else {
+                    float* row = red + (warp * HP + h) * RS + (lane >> 2);
+#pragma unroll
+                    for (int dt = 0; dt < KT; ++dt) {
+                        row[dt * 16] = ws.acc[dt][nt][j] * f;
+                        row[dt * 16 + 8] = ws.acc[dt][nt][j + 2] * f;
+                    }
+                }
+            }
         named_bar_sync(1, NWC * 32);
-    }
-    const uint32_t qs_a = smem_u32(qtile);
-    WarpState<D, NT> ws;
-    ws.reset();
-    ColTerms<NT> ct;
-    if constexpr (GEN) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int c = nt * 8 + 2 * (lane & 3) + j;
-                const bool live = qc.live(c);
-                const int gc = qc.col0 + c;
-                ct.shift[nt][j] = live ? p.q_len - 1 - gc / p.G : 0;
-                ct.slope[nt][j] =
-                    (live && p.alibi) ? __ldg(p.alibi + qc.h0 + gc % p.G) * 1.4426950408889634f : 0.f;
-            }
-    }
 
-    const int last_pg = (n - 1) / BS;
-    bool ok = true;
-
-    for (int i = warp; i < npg; i += NWC) {
-        const int stg = i % STAGES;
-        const bool got = mbar_wait(&full[stg], (i / STAGES) & 1);
-        if (!__all_sync(0xffffffffu, got && *abort_flag == 0)) {
-            ok = false;
-            *abort_flag = 1;
-            break;
-        }
-        uint8_t* ks = ring + stg * 2 * SLICE;
-        const int valid = (pg0 + i == last_pg) ? n - last_pg * BS : BS;
-        ct.pos0 = (pg0 + i) * BS - (n - 1);
-        if constexpr (DIRECT8) {
-            page_step_fp8<D, NT, GEN, QS>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, ct, qs_a);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stg]);
-        } else if constexpr (KV8) {
-            // expand into this warp's fp16 slices; the ring stage is free again at once
-            uint8_t* sk = staging + warp * 2 * (BS * D * 2);
-            expand_fp8_slice<D>(ks, sk, lane);
-            expand_fp8_slice<D>(ks + SLICE, sk + BS * D * 2, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stg]);
-            page_step<MT, kLayoutNHD, D, NT, GEN>(sk, sk + BS * D * 2, valid, scale_log2, qf, ws, lane, ct);
-            __syncwarp();
-        } else {
-            page_step<T, LAYOUT, D, NT, GEN, QS>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, ct, qs_a);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stg]);
-        }
-    }
-    if (!ok && lane == 0 && p.err) atomicOr(p.err, kErrTimeout);
-
-    // ------------------------------------------------- merge the warps' states
-    ws.finish_l();
-    if (lane < 4) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                st_m[warp * HP + nt * 8 + 2 * lane + j] = ws.m[nt][j];
-                st_l[warp * HP + nt * 8 + 2 * lane + j] = ws.l[nt][j];
-            }
-    }
-    named_bar_sync(1, NWC * 32);   // every consumer is past its last page
-
-    float* red = reinterpret_cast<float*>(ring);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int h = nt * 8 + 2 * (lane & 3) + j;
+        const bool direct = !p.partials_only && ns_b == 1;
+        for (int idx = threadIdx.x; idx < ncols * (D / 4); idx += NWC * 32) {
+            const int h = idx / (D / 4);
+            const int d = (idx % (D / 4)) * 4;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < NWC; ++w) M = fmaxf(M, st_m[w * HP + h]);
-            if (M == -INFINITY) M = 0.f;   // a column that saw no visible token: every f is 0
-            const float f = ex2(ws.m[nt][j] - M);   // 0 for a warp that saw no page
-            if constexpr (DIRECT8) {   // mma rows g, g+8 of d-tile dt hold d = 16dt + 2g, 16dt + 2g + 1
-                float* row = red + (warp * HP + h) * RS + 2 * (lane >> 2);
+            const float Mref = M == -INFINITY ? 0.f : M;   // no visible token: L = 0, sum = 0
+            float L = 0.f;
+            float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int dt = 0; dt < KT; ++dt) {
-                    row[dt * 16] = ws.acc[dt][nt][j] * f;
-                    row[dt * 16 + 1] = ws.acc[dt][nt][j + 2] * f;
-                }
+            for (int w = 0; w < NWC; ++w) {
+                L += st_l[w * HP + h] * ex2(st_m[w * HP + h] - Mref);
+                const float4 v = *reinterpret_cast<const float4*>(red + (w * HP + h) * RS + d);
+                sum.x += v.x;
+                sum.y += v.y;
+                sum.z += v.z;
+                sum.w += v.w;
+            }
+            sum.x *= p.v_scale;
+            sum.y *= p.v_scale;
+            sum.z *= p.v_scale;
+            sum.w *= p.v_scale;
+            const size_t bh = qc.row(h);
+            if (direct) {
+                const float inv = L > 0.f ? 1.f / L : 0.f;   // an empty causal window gives a zero row
+                T o4[4] = {from_float<T>(sum.x * inv), from_float<T>(sum.y * inv), from_float<T>(sum.z * inv),
+                           from_float<T>(sum.w * inv)};
+                *reinterpret_cast<uint2*>(reinterpret_cast<T*>(p.out) + bh * D + d) = *reinterpret_cast<uint2*>(o4);
             } else {
-                float* row = red + (warp * HP + h) * RS + (lane >> 2);
-#pragma unroll
-                for (int dt = 0; dt < KT; ++dt) {
-                    row[dt * 16] = ws.acc[dt][nt][j] * f;
-                    row[dt * 16 + 8] = ws.acc[dt][nt][j + 2] * f;
+                const size_t row = bh * p.ns_stride + s;
+                *reinterpret_cast<float4*>(p.part_acc + row * D + d) = sum;
+                if (d == 0) {
+                    p.part_m[row] = M * 0.69314718055994531f;   // log2 units -> natural-log units
+                    p.part_l[row] = L;
                 }
             }
         }
-    named_bar_sync(1, NWC * 32);
-
-    const bool direct = !p.partials_only && ns_b == 1;
-    for (int idx = threadIdx.x; idx < ncols * (D / 4); idx += NWC * 32) {
-        const int h = idx / (D / 4);
-        const int d = (idx % (D / 4)) * 4;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NWC; ++w) M = fmaxf(M, st_m[w * HP + h]);
-        const float Mref = M == -INFINITY ? 0.f : M;   // no visible token: L = 0, sum = 0
-        float L = 0.f;
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < NWC; ++w) {
-            L += st_l[w * HP + h] * ex2(st_m[w * HP + h] - Mref);
-            const float4 v = *reinterpret_cast<const float4*>(red + (w * HP + h) * RS + d);
-            sum.x += v.x;
-            sum.y += v.y;
-            sum.z += v.z;
-            sum.w += v.w;
-        }
-        sum.x *= p.v_scale;
-        sum.y *= p.v_scale;
-        sum.z *= p.v_scale;
-        sum.w *= p.v_scale;
-        const size_t bh = qc.row(h);
-        if (direct) {
-            const float inv = L > 0.f ? 1.f / L : 0.f;   // an empty causal window gives a zero row
-            T o4[4] = {from_float<T>(sum.x * inv), from_float<T>(sum.y * inv), from_float<T>(sum.z * inv),
-                       from_float<T>(sum.w * inv)};
-            *reinterpret_cast<uint2*>(reinterpret_cast<T*>(p.out) + bh * D + d) = *reinterpret_cast<uint2*>(o4);
-        } else {
-            const size_t row = bh * p.ns_stride + s;
-            *reinterpret_cast<float4*>(p.part_acc + row * D + d) = sum;
-            if (d == 0) {
-                p.part_m[row] = M * 0.69314718055994531f;   // log2 units -> natural-log units
-                p.part_l[row] = L;
-            }
-        }
-    }
     };   // run_item
 
     if constexpr (!SCHED) {   // grid order: this CTA's one item
@@ -491,8 +491,9 @@ template <typename T, int LAYOUT, int D, int NT>
 cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                  const CUtensorMap& tmv, cudaStream_t stream) {
     if (p.sched_hdr) return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, true>(p, grid, tmk, tmv, stream);
-    return (p.alibi || p.q_len > 1) ? launch_decode_phase1_variant<T, LAYOUT, D, NT, true, false>(p, grid, tmk, tmv, stream)
-                                    : launch_decode_phase1_variant<T, LAYOUT, D, NT, false, false>(p, grid, tmk, tmv, stream);
+    if (p.alibi || p.q_len > 1)
+        return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, false>(p, grid, tmk, tmv, stream);
+    return launch_decode_phase1_variant<T, LAYOUT, D, NT, false, false>(p, grid, tmk, tmv, stream);
 }
 
 }  // namespace pkv
