@@ -177,6 +177,14 @@ def oracle_decode_timed(case, seqs, threads):
     return time.perf_counter() - t0
 
 
+def kv_bytes_page_rounded(case):
+    """KV bytes of whole pages: every live token's page read in full (the last page's unused slots too)."""
+    e = 1 if tensors_fp8(case) else 2
+    bs = case["block_size"]
+    pages = (case["context_lens"].astype(np.int64) + bs - 1) // bs
+    return int(pages.sum()) * bs * case["Hkv"] * case["D"] * 2 * e
+
+
 def seq_kv_bytes(case, seqs):
     """KV bytes of the given sequences (K and V, the cache's element size)."""
     e = 1 if tensors_fp8(case) else 2
@@ -184,7 +192,8 @@ def seq_kv_bytes(case, seqs):
 
 
 def cpu_baseline(case, budget_s: float = 15.0):
-    """The oracle as it stands on all host cores over a bounded sample of the workload."""
+    """The oracle as it stands on all host cores over a bounded sample of the workload, and
+    on one core over a smaller sample."""
     import oracle
     oracle.build()
     threads = os.cpu_count() or 1
@@ -201,8 +210,15 @@ def cpu_baseline(case, budget_s: float = 15.0):
         secs = oracle_decode_timed(case, order[:m], threads)
         n = m
     gbs = seq_kv_bytes(case, order[:n]) / secs / 1e9
+    # one core: sequences in the same order until ~2 s
+    m1, secs1 = 0, 0.0
+    while m1 < len(order) and secs1 < 2.0:
+        secs1 += oracle_decode_timed(case, [order[m1]], 1)
+        m1 += 1
     return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": "%d of %d sequences (all heads), one pass, %.1f s" % (n, case["B"], secs)}
+            "sample": "%d of %d sequences (all heads), one pass, %.1f s" % (n, case["B"], secs),
+            "single_core": {"value": seq_kv_bytes(case, order[:m1]) / secs1 / 1e9, "unit": "GB/s",
+                            "sample": "%d sequences, %.1f s" % (m1, secs1)}}
 
 
 # ----------------------------------------------------------------- arms ----
@@ -271,6 +287,7 @@ def workload_config(case, name, flushed=True):
         dtype_label(case), {0: "NHD", 1: "vLLM x-packed"}[case["layout"]],
         int(ctx.min()), int(ctx.max()), int(ctx.sum())),
         "seed": 0, "kv_bytes_per_step": synth.kv_bytes(case), "query_tokens_per_step": case["B"] * q_len,
+        "kv_bytes_per_step_page_rounded": kv_bytes_page_rounded(case),
         "l2": "flushed between steps (256 MiB write)" if flushed else "n/a (CPU)",
         "accumulate": "fp32"}
 
