@@ -161,3 +161,23 @@ def test_device_plan_header():
     splits = [max(1, -(-n // 512)) for n in lens]
     assert hdr == [512, 3, 2 * sum(splits)]
     check(case, out)
+
+
+def test_more_sequences_than_one_scan_chunk():
+    # 2500 sequences: the schedule kernel scans them 1024 at a time (later chunks reload their
+    # lengths from global memory); many empty and one-page contexts.
+    B, T = _binding(), _tensors()
+    case = synth.decode_case(seed=650, B=2500, Hq=8, Hkv=2, D=64, block_size=16, dtype=synth.F16,
+                             layout=synth.NHD, ctx_range=(0, 90), max_blocks_per_seq=8)
+    dev = T.upload_decode_case(case)
+    desc = T.decode_desc(case)
+    for opt in (dict(), dict(partition_tokens=32)):
+        host = run(case, desc, B.make_opts(**opt), dev)
+        devp = run(case, desc, B.make_opts(device_plan=True, **opt), dev)
+        assert torch.equal(host, devp)
+    rows = [0, 1023, 1024, 1500, 2047, 2048, 2499]
+    ref = np.full(case["q"].shape, np.nan)
+    for b in rows:
+        oracle.decode(case, b, b + 1, out=ref)
+    got = run(case, loose(case, T.decode_desc(case)), B.make_opts(device_plan=True), dev).double().cpu().numpy()
+    assert np.max(np.abs(got[rows] - ref[rows])) <= TOL[synth.F16]
