@@ -71,22 +71,25 @@ template <int D, int LAYOUT>
 struct DecodeTile {
     static constexpr int BS = kPageTokens;
     static constexpr int KVB = LAYOUT == kLayoutNHD8 ? 1 : 2;       // bytes per cache element
-    static constexpr int NWC = 4;                                   // consumer warps
+    // Consumer warps and ring stages.  The CTAs of a launch are short (a split),
+    // and each spends its start-up (context length, table, first page) with its
+    // ring empty, so more CTAs per SM with the same bytes in flight per SM keep
+    // the SM streaming: at D = 128 three consumers with 6 stages (16-bit, 48 KB)
+    // or 9 stages (FP8, 36 KB) give four or five CTAs per SM instead of three.
+    // FP8 pages at D = 256 keep twice the 16-bit stages (the same bytes).
+    static constexpr int NWC = D == 128 ? 3 : 4;
     static constexpr int SLICE = BS * D * KVB;                      // bytes of one page slice
-    // FP8 pages with D >= 128 keep more stages: at D = 256 twice (the same bytes in flight
-    // as 16-bit pages), at D = 128 1.5 times (48 KB, so that four CTAs fit on an SM)
-    static constexpr int STAGES = (D == 64 ? 12 : (D == 128 ? 8 : 4)) * ((KVB == 1 && D >= 128) ? 2 : 1) * 3 /
-                                  ((KVB == 1 && D == 128) ? 4 : 3);
+    static constexpr int STAGES = D == 64 ? 12 : (D == 128 ? (KVB == 1 ? 9 : 6) : (KVB == 1 ? 8 : 4));
     // FP8 pages with D = 64 are expanded to fp16 in a per-consumer-warp K/V
     // slice pair; D >= 128 goes straight from the ring into mma fragments.
     static constexpr int STAGING = (KVB == 1 && D < 128) ? NWC * 2 * BS * D * 2 : 0;
     static constexpr int RED_STRIDE = D + 4;                        // floats per reduction row
     // Two column tiles at D = 128 keep the CTA's Q fragments in shared memory
-    // (one 16-row tile) instead of 32 registers per thread, so that three CTAs
-    // fit on an SM (the kernel is then compiled for 3 blocks per SM).
+    // (one 16-row tile) instead of 32 registers per thread, so that four CTAs
+    // fit on an SM (the kernel is then compiled for 4 blocks per SM).
     __host__ __device__ static constexpr bool q_shared(int nt) { return nt == 2 && D == 128; }
-    // CTAs per SM the shared-Q kernels are compiled for (their register budget)
-    static constexpr int QS_MIN_BLOCKS = 3;
+    // CTAs per SM the shared-Q kernels (D = 128) are compiled for (their register budget)
+    static constexpr int QS_MIN_BLOCKS = 4;
     __host__ __device__ static constexpr int qtile_bytes(int nt) { return q_shared(nt) ? 16 * D * 2 : 0; }
     __host__ __device__ static constexpr int smem_bytes(int nt) {
         return 1024 + STAGES * 2 * SLICE + STAGING + qtile_bytes(nt) + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 16;
@@ -443,7 +446,7 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     decode_phase1_body<T, LAYOUT, D, NT, GEN, SCHED>(p, tmk, tmv);
 }
 
-// The same for the shared-Q tiles, compiled for three CTAs per SM.
+// The same for the shared-Q tiles, compiled for four CTAs per SM.
 template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED>
 __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32, DecodeTile<D, LAYOUT>::QS_MIN_BLOCKS)
     decode_phase1_kernel_qs(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
