@@ -273,3 +273,21 @@ def test_misaligned_alibi_slopes_are_rejected(B):
     st = B.raw_status("pkv_paged_decode_attention", ctypes.byref(d), ctypes.byref(opts), good, good, good, good, good,
                       ctypes.c_float(0.1), good, good, 1 << 30, None)
     assert st == B.PKV_INVALID_ARG
+
+
+def test_device_planner_condition_equals_the_host_rule():
+    # The schedule kernel tests "enough work items" as sum > (ceil(target / (Hkv*RT)) - 1) * P
+    # instead of the host's Hkv * RT * ceil(sum / P) >= target (no 64-bit division on the
+    # device); the two must agree for every operand, and so must its overflow-safe ceilings.
+    rng = random.Random(1)
+    cdiv = lambda a, b: (a - 1) // b + 1 if a > 0 else 0
+    for _ in range(200000):
+        hr = rng.choice([1, 2, 4, 8, 12, 64, 1000]) * rng.randint(1, 3)
+        P = 16 * rng.randint(4, 4096)
+        target = 6 * rng.choice([1, 76, 148, 152, 160])
+        s = rng.choice([rng.randint(1, 10 ** 4), rng.randint(1, 10 ** 8), rng.randint(1, 10 ** 12)])
+        host = hr * -(-s // P) >= target
+        need = -(-target // hr)
+        assert host == (s > (need - 1) * P), (hr, P, target, s)
+        n, k = rng.randint(0, 2 ** 31 - 1), rng.randint(1, 2 ** 20)
+        assert cdiv(n, k) == -(-n // k)
