@@ -176,8 +176,9 @@ PKV_API int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_dec
  * gives a zero row.  K and V inside the context must be finite: with
  * q_len > 1 a masked key's V row still meets a zero weight.
  *   q, out        [B][q_len][Hq][D] of dtype (4-byte aligned; out 8-byte aligned)
- *   k/v_cache     per layout (16-byte aligned)
- *   block_table   int32 [B][max_blocks_per_seq]; entries past a sequence's last
+ *   k/v_cache     per layout (16-byte aligned); may be NULL when num_blocks == 0
+ *   block_table   int32 [B][max_blocks_per_seq] (may be NULL when max_blocks_per_seq
+ *                 == 0); entries past a sequence's last
  *                 page are never used (-1 is the customary filler).  A live entry
  *                 outside [0, num_blocks) is a caller error: it is clamped to a
  *                 valid page (no out-of-bounds access, result unspecified);

@@ -200,6 +200,15 @@ def test_pointer_checks_happen_before_any_launch(B):
     assert st == B.PKV_INVALID_ARG       # 7 splits of 512 cannot cover 4096 tokens
     st = B.raw_status("pkv_validate_block_table", ctypes.byref(d), good, good, None, None)
     assert st == B.PKV_INVALID_ARG
+    # an empty pool (every context empty) may come without caches, a column-less table without a table
+    empty = desc(B, num_blocks=0, max_context_len=0, sum_context_len=0, max_blocks_per_seq=0)
+    st = B.raw_status("pkv_paged_decode_attention", ctypes.byref(empty), None, good, None, None, None, good,
+                      ctypes.c_float(0.1), good, good, 1 << 30, None)
+    assert st != B.PKV_INVALID_ARG       # (no GPU here: the launch itself reports a CUDA error)
+    with_pool = desc(B, max_context_len=0, sum_context_len=0)
+    st = B.raw_status("pkv_paged_decode_attention", ctypes.byref(with_pool), None, good, None, good, good, good,
+                      ctypes.c_float(0.1), good, good, 1 << 30, None)
+    assert st == B.PKV_INVALID_ARG       # a pool was described: its caches are required
 
 
 def test_empty_batch_is_a_no_op(B):

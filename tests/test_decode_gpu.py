@@ -92,6 +92,21 @@ def test_forced_splits(opts, layout):
     check_rows(case, got, list(range(case["B"])))
 
 
+def test_all_contexts_empty_with_an_empty_pool():
+    # no page in the pool: null caches are accepted and every row is zero
+    B, T = _binding(), _tensors()
+    case = _case(6, B=3, Hq=8, Hkv=2, D=128, block_size=16, dtype=synth.BF16, layout=synth.NHD,
+                 context_lens=[0, 0, 0], max_blocks_per_seq=4)
+    assert case["num_blocks"] == 0
+    dev = T.upload_decode_case(case)
+    out = torch.full(case["q"].shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    desc = T.decode_desc(case)
+    B.pkv_paged_decode_attention(desc, dev["q"], None, None, dev["block_table"], dev["context_lens"],
+                                 case["scale"], out, T.workspace_for(desc))
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
+
+
 def test_all_contexts_empty():
     case = _case(5, B=3, Hq=4, Hkv=1, D=64, block_size=16, dtype=synth.F16, layout=synth.NHD,
                  context_lens=[0, 0, 0], max_blocks_per_seq=2, slack_pages=2)
