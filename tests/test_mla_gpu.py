@@ -147,3 +147,19 @@ def test_mla_short_nnz_is_reported():
     out, lse, err = _run_with(case, nnz=int(case["kv_indptr"][-1]) // 2)
     assert err == 2
     assert out.shape == (case["total_q"], 16, 512)
+
+
+@pytest.mark.parametrize("i", range(30))
+def test_mla_random_case_matches_oracle(i):
+    """Seeded random batches: empty and single-token queries, row tiles cut at 8
+    tokens, prefixes around the 128-key block edge, slack pages poisoned."""
+    import random
+    r = random.Random(9000 + i)
+    batch = r.randint(1, 5)
+    q_lens = [r.choice([0, 1, r.randint(1, 70), 8, 9, 16]) for _ in range(batch)]
+    prefixes = [r.choice([0, r.randint(0, 300), 127, 128, 129]) for _ in range(batch)]
+    case = synth.mla_case(seed=i, batch=batch, q_len_range=(1, 1), prefix_range=(0, 0), q_lens=q_lens,
+                          prefixes=prefixes, slack_pages=r.randint(0, 5), poison=True)
+    if case["total_q"] == 0:
+        pytest.skip("no query token")
+    check(case, *gpu_mla(case))
