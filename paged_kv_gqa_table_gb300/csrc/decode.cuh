@@ -11,8 +11,8 @@
 // (32 per coalesced load, one chunk ahead) and, per page, issues TMA tensor
 // loads of that page's K and V slices for this KV head into a STAGES-deep
 // shared-memory ring (full/empty mbarriers).  Each page is loaded ONCE for the
-// whole GQA group.  Warps 0..NWC-1 consume pages round-robin, each keeping its
-// own online-softmax state for all G query heads of the group:
+// CTA's query rows.  Warps 0..NWC-1 consume pages round-robin, each keeping its
+// own online-softmax state for all of them:
 //
 //   S^T[t][h] = K[t][:] . Q[h][:]          mma.sync m16n8k16, tokens = M (16 per
 //                                           page), query rows = N (8 per tile)

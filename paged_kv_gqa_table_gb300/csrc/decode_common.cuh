@@ -1,10 +1,11 @@
-// decode_common.cuh -- the per-page arithmetic of paged GQA decode, shared by
-// the fixed-partition kernel (decode.cuh) and the balanced persistent kernel
-// (decode_streamk.cuh).
+// decode_common.cuh -- the per-page arithmetic of paged GQA decode phase 1
+// (decode.cuh): query-column maps, the page steps for 16-bit and FP8 pages,
+// and the TMA page loads.
 //
-// One consumer warp handles one 16-token page of one KV head for all G query
-// heads of its group (padded to NT tiles of 8):
-//   S^T[t][h] = K[t][:] . Q[h][:]           mma.sync m16n8k16, tokens = M, heads = N
+// One consumer warp handles one 16-token page of one KV head for all the
+// query rows of its CTA (heads of the group x query tokens, padded to NT tiles
+// of 8):
+//   S^T[t][h] = K[t][:] . Q[h][:]           mma.sync m16n8k16, tokens = M, query rows = N
 //   m' = max(m, max_t S), alpha = 2^(m - m'), P = 2^(S - m'), l' = alpha l + sum_t P
 //   O^T[d][h] = alpha O^T[d][h] + V^T[d][t] P^T[t][h]   (P^T via movmatrix)
 // ("paged_attention_v2_triton.py", _partition_attn_kernel docstring steps 1-4;
