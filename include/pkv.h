@@ -108,14 +108,16 @@ typedef struct {
     int q_len;
 } pkv_decode_desc;
 
-/* pkv_decode_opts.flags bit: plan on the device (see pkv_paged_decode_attention). */
+/* pkv_decode_opts.flags bits (see pkv_paged_decode_attention): plan on the
+ * device; with it, reuse the plan an earlier call left in the workspace. */
 #define PKV_DECODE_DEVICE_PLAN 1
+#define PKV_DECODE_PLAN_READY 2
 
 /* Optional knobs; pass NULL for the defaults (all zero). */
 typedef struct {
     int partition_tokens;    /* tokens per split, a multiple of block_size; 0 = planner */
     int num_splits;          /* used when partition_tokens == 0: split the longest context this many ways */
-    int flags;               /* 0, or PKV_DECODE_DEVICE_PLAN; other bits are invalid */
+    int flags;               /* 0, PKV_DECODE_DEVICE_PLAN, or that | PKV_DECODE_PLAN_READY; other bits are invalid */
     /* Optional cudaEvent_t handles recorded on `stream` right before and right
      * after the phase-1 kernel, so a caller can time that kernel alone inside a
      * full call.  NULL = not recorded. */
@@ -132,7 +134,7 @@ typedef struct {
 /* Text of a status code (static storage). */
 PKV_API const char* pkv_status_string(int status);
 
-/* ABI version of this header: 4 (3 had no device plan; 2 no q_len; 1 no kv_dtype / k_scale / v_scale). */
+/* ABI version of this header: 5 (4 had no plan reuse; 3 no device plan; 2 no q_len; 1 no kv_dtype / k_scale / v_scale). */
 PKV_API int pkv_version(void);
 
 /*
@@ -202,6 +204,13 @@ PKV_API int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_dec
  * the listed items in order, so a call captured into a CUDA graph with loose
  * bounds launches no CTA per empty split.  pkv_decode_partials does not take
  * this flag.
+ *
+ * flags & PKV_DECODE_PLAN_READY (with PKV_DECODE_DEVICE_PLAN): the workspace
+ * already holds the plan of an earlier device-planned call with the same
+ * desc, the same partition options and the same context_lens values, ordered
+ * before this call on the GPU; the schedule kernel is not launched.  For the
+ * layers of one decode step, which share context_lens: the first layer plans,
+ * the others reuse the plan (each with its own q, caches and out).
  */
 PKV_API int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
                                const void* q, const void* k_cache, const void* v_cache,

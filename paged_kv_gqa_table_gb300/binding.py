@@ -17,6 +17,7 @@ PKV_OK, PKV_INVALID_ARG, PKV_UNSUPPORTED, PKV_WORKSPACE_TOO_SMALL, PKV_CUDA_ERRO
 PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 PKV_KV_AS_Q = 0
 PKV_DECODE_DEVICE_PLAN = 1
+PKV_DECODE_PLAN_READY = 2
 PKV_LAYOUT_NHD, PKV_LAYOUT_VLLM = 0, 1
 
 FUNCTIONS = [
@@ -120,12 +121,13 @@ def make_desc(B, Hq, Hkv, D, block_size, max_blocks_per_seq, num_blocks, max_con
 
 
 def make_opts(partition_tokens=0, num_splits=0, event_start=None, event_stop=None,
-              alibi_slopes=None, device_plan=False, flags=None) -> pkv_decode_opts:
+              alibi_slopes=None, device_plan=False, plan_ready=False, flags=None) -> pkv_decode_opts:
     """alibi_slopes: a device fp32 tensor [Hq] (kept alive by the caller) or None.
-    device_plan: plan the splits on the device (PKV_DECODE_DEVICE_PLAN); flags: raw flag word."""
+    device_plan: plan the splits on the device (PKV_DECODE_DEVICE_PLAN); plan_ready: reuse the
+    plan an earlier device-planned call left in the workspace; flags: raw flag word."""
     ev = lambda e: None if e is None else (e if isinstance(e, int) else e.cuda_event)
     if flags is None:
-        flags = PKV_DECODE_DEVICE_PLAN if device_plan else 0
+        flags = (PKV_DECODE_DEVICE_PLAN if device_plan or plan_ready else 0) | (PKV_DECODE_PLAN_READY if plan_ready else 0)
     return pkv_decode_opts(int(partition_tokens), int(num_splits), int(flags), ev(event_start), ev(event_stop),
                            _ptr(alibi_slopes))
 

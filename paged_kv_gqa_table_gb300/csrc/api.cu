@@ -103,7 +103,8 @@ long long auto_partition(const pkv_decode_desc* d, int num_sms) {
 int plan(const pkv_decode_desc* d, const pkv_decode_opts* o, int num_sms, int* ns, int* P) {
     int st = check_desc(d);
     if (st) return st;
-    if (o && (o->flags & ~PKV_DECODE_DEVICE_PLAN) != 0) return PKV_INVALID_ARG;
+    if (o && (o->flags & ~(PKV_DECODE_DEVICE_PLAN | PKV_DECODE_PLAN_READY)) != 0) return PKV_INVALID_ARG;
+    if (o && (o->flags & PKV_DECODE_PLAN_READY) && !(o->flags & PKV_DECODE_DEVICE_PLAN)) return PKV_INVALID_ARG;
     if (num_sms <= 0) {
         st = current_sm_count(&num_sms);
         if (st) return st;
@@ -318,7 +319,7 @@ const char* pkv_status_string(int status) {
     }
 }
 
-int pkv_version(void) { return 4; }
+int pkv_version(void) { return 5; }
 
 int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms, int* num_splits,
                     int* partition_tokens) {
@@ -391,7 +392,8 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
         p.sched_list = list;
         p.sched_cap = (int)plan_items(desc, ns);
         grid = std::min(plan_items(desc, ns), (long long)kDevicePlanCtasPerSm * sms);
-        if (launch_schedule(sp, s) != cudaSuccess) return PKV_CUDA_ERROR;
+        // An earlier call left the same plan in this workspace: reuse it.
+        if (!(opts->flags & PKV_DECODE_PLAN_READY) && launch_schedule(sp, s) != cudaSuccess) return PKV_CUDA_ERROR;
     }
     record(opts ? opts->phase1_event_start : nullptr, s);
     if (dispatch_phase1(desc, p, mk, mv, s, grid) != cudaSuccess) return PKV_CUDA_ERROR;

@@ -16,7 +16,6 @@
 namespace {
 
 constexpr size_t kStaticScratchBytes = PKV_STATIC_SCRATCH_BYTES;   // 32 MiB
-constexpr size_t kHeaderBytes = 256;                        // error word + padding, zeroed per call
 
 static __device__ __align__(256) unsigned char g_scratch[kStaticScratchBytes];
 
@@ -55,9 +54,10 @@ int pkv_paged_decode_attention_static(const pkv_decode_desc* desc, const pkv_dec
     void* scratch = nullptr;
     st = scratch_address(&scratch);
     if (st) return st;
-    // The header's error word must start at zero; the partials are fully
-    // written by phase 1 before phase 2 reads them, so they need no clearing.
-    if (cudaMemsetAsync(scratch, 0, kHeaderBytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // The header's error word must start at zero (the rest of the header may
+    // hold a device plan an earlier call made for reuse); the partials are
+    // fully written by phase 1 before phase 2 reads them, so they need no clearing.
+    if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PKV_CUDA_ERROR;
     return pkv_paged_decode_attention(desc, opts, q, k_cache, v_cache, block_table, context_lens, scale, out,
                                       scratch, kStaticScratchBytes, stream);

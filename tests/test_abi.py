@@ -43,7 +43,7 @@ def test_library_exports_every_declared_function(B):
 
 
 def test_version_and_status_strings(B):
-    assert B.pkv_version() == 4
+    assert B.pkv_version() == 5
     assert B.status_string(0) == "ok"
     assert B.status_string(5) == "bad block table"
     assert B.status_string(99) == "unknown status"
@@ -151,7 +151,9 @@ def test_device_plan_options(B):
     dev = B.pkv_decode_workspace_size(d, B.make_opts(device_plan=True), 152)
     assert dev == plain + al(64 * 8 * 1 * ns * 16)
     assert B.pkv_plan_splits(d, B.make_opts(device_plan=True), 152) == (ns, P)
-    for bad in (2, 4, 1 << 30, -1):
+    assert B.pkv_plan_splits(d, B.make_opts(plan_ready=True), 152) == (ns, P)   # flags 3
+    assert B.make_opts(plan_ready=True).flags == B.PKV_DECODE_DEVICE_PLAN | B.PKV_DECODE_PLAN_READY
+    for bad in (2, 4, 6, 1 << 30, -1):   # 2: plan reuse without the device plan
         with pytest.raises(B.PkvError) as e:
             B.pkv_plan_splits(d, B.make_opts(flags=bad), 152)
         assert e.value.status == B.PKV_INVALID_ARG

@@ -181,3 +181,32 @@ def test_more_sequences_than_one_scan_chunk():
         oracle.decode(case, b, b + 1, out=ref)
     got = run(case, loose(case, T.decode_desc(case)), B.make_opts(device_plan=True), dev).double().cpu().numpy()
     assert np.max(np.abs(got[rows] - ref[rows])) <= TOL[synth.F16]
+
+
+@pytest.mark.parametrize("q_len", [1, 4])
+def test_plan_made_once_reused_by_later_layers(q_len):
+    # Three "layers" of one decode step share context_lens and the block table: the first call
+    # plans on the device, the next two reuse its plan (PKV_DECODE_PLAN_READY) with their own
+    # queries and caches.
+    B, T = _binding(), _tensors()
+    base = synth.decode_case(seed=660, B=20, Hq=16, Hkv=4, D=128, block_size=16, dtype=synth.BF16,
+                             layout=synth.NHD, ctx_range=(0, 1500), max_blocks_per_seq=100, q_len=q_len)
+    layers = [base]
+    for i in (1, 2):
+        new = lambda stream, a: synth.normal_bits(661 + i, stream, a.size, synth.BF16).reshape(a.shape)
+        layers.append(dict(base, q=new(3, base["q"]), k_cache=new(4, base["k_cache"]),
+                           v_cache=new(5, base["v_cache"])))
+    desc = loose(base, T.decode_desc(base))
+    plan, reuse = B.make_opts(device_plan=True), B.make_opts(plan_ready=True)
+    ws = T.workspace_for(desc, plan)
+    outs = []
+    for i, c in enumerate(layers):
+        dev = T.upload_decode_case(c)
+        out = torch.full(c["q"].shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+        B.pkv_paged_decode_attention(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
+                                     dev["context_lens"], c["scale"], out, ws, opts=plan if i == 0 else reuse)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    for c, out in zip(layers, outs):
+        check(c, out)

@@ -60,3 +60,24 @@ def test_static_scratch_refuses_problems_that_do_not_fit():
     with pytest.raises(B.PkvError) as e:
         B.pkv_paged_decode_attention_static(desc, dummy, dummy, dummy, dummy, dummy, 0.1, dummy, opts=opts)
     assert e.value.status == B.PKV_WORKSPACE_TOO_SMALL
+
+
+def test_static_scratch_keeps_a_device_plan_for_reuse():
+    # The static entry point clears only the error word, so a device plan made by one call
+    # (PKV_DECODE_DEVICE_PLAN) is reused by the next (PKV_DECODE_PLAN_READY) with new queries.
+    from paged_kv_gqa_table_gb300 import binding as B
+    from paged_kv_gqa_table_gb300 import tensors as T
+    import oracle
+    case = synth.decode_case(seed=3, B=12, Hq=16, Hkv=4, D=128, block_size=16, dtype=synth.BF16,
+                             layout=synth.NHD, ctx_range=(1, 2000), max_blocks_per_seq=128)
+    second = dict(case, q=synth.normal_bits(4, 3, case["q"].size, synth.BF16).reshape(case["q"].shape))
+    desc = T.decode_desc(case)
+    for c, opts in ((case, B.make_opts(device_plan=True)), (second, B.make_opts(plan_ready=True))):
+        dev = T.upload_decode_case(c)
+        out = torch.full(c["q"].shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+        B.pkv_paged_decode_attention_static(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
+                                            dev["context_lens"], c["scale"], out, opts=opts)
+        torch.cuda.synchronize()
+        got = out.double().cpu().numpy()
+        assert np.all(np.isfinite(got))
+        assert float(np.max(np.abs(got - oracle.decode(c)))) <= TOL[synth.BF16]
