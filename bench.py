@@ -4,10 +4,12 @@
 
 One step = one full decode step of the workload (phase 1 + cross-split
 combine) on synthetic inputs already resident in HBM.  Between timed steps a
-256 MiB buffer is written to flush the 129 MB L2; each step is timed with CUDA
-events on the launching stream, the K step times are summed, and the maximum
-over ranks is taken.  The metric is KV-cache bytes per second: live tokens x
-KV heads x head_dim x (K and V) x 2 bytes per step, divided by the step time.
+256 MiB buffer is written to flush the 129 MB L2 and a second 256 MiB buffer is
+read, so that the write's dirty lines reach HBM before the step instead of
+during it; each step is timed with CUDA events on the launching stream, the K
+step times are summed, and the maximum over ranks is taken.  The metric is
+KV-cache bytes per second: live tokens x KV heads x head_dim x (K and V) x 2
+bytes per step, divided by the step time.
 
 N > 1 runs independent replicas (one process per GPU, launched by torchrun):
 the decode step has no exchange between GPUs, so there is no collective on the
@@ -36,6 +38,26 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention: KV-cache GB/s and % of GB300 HBM peak; µs/step"
 FLUSH_BYTES = 256 << 20
+L2_NOTE = "cold between steps: 256 MiB written, then another 256 MiB read (the write's dirty lines reach HBM first)"
+
+
+class ColdL2:
+    """Leaves the L2 cold and clean before a timed step.  Writing a buffer twice the
+    L2's size evicts every line of the step's inputs but leaves the L2 full of that
+    buffer's dirty lines, whose write-back would otherwise run during the step and
+    take HBM bandwidth from it; reading a second buffer of the same size writes
+    them back first."""
+
+    def __init__(self, torch, device):
+        self.torch = torch
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.ones(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.torch.amax(self.r)
+
+
 # committed ncu summaries per workload (their traffic is used only while the sources match)
 PROFILE_SUMMARIES = {
     "llama3_8b_decode": os.path.join(ROOT, "profiles", "decode_phase1_llama3_8b_decode.md"),
@@ -288,7 +310,7 @@ def workload_config(case, name, flushed=True):
         int(ctx.min()), int(ctx.max()), int(ctx.sum())),
         "seed": 0, "kv_bytes_per_step": synth.kv_bytes(case), "query_tokens_per_step": case["B"] * q_len,
         "kv_bytes_per_step_page_rounded": kv_bytes_page_rounded(case),
-        "l2": "flushed between steps (256 MiB write)" if flushed else "n/a (CPU)",
+        "l2": L2_NOTE if flushed else "n/a (CPU)",
         "accumulate": "fp32"}
 
 
@@ -311,7 +333,7 @@ def run_gpu(args):
     ns, P = B.pkv_plan_splits(desc)
     out = torch.empty(case["q"].shape, dtype=tensors.TORCH_DTYPE[case["dtype"]], device=device)
     ws = tensors.workspace_for(desc, device=device)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = ColdL2(torch, device)
     stream = torch.cuda.current_stream(device)
     ev = lambda: torch.cuda.Event(enable_timing=True)
     p_start, p_stop = [ev() for _ in range(args.steps)], [ev() for _ in range(args.steps)]
@@ -331,14 +353,14 @@ def run_gpu(args):
         pass
     sampler = ClockSampler(uuid) if rank == 0 else None
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize(device)
     barrier(world, device)
     torch.cuda.synchronize(device)
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         s_start[i].record(stream)
         step()
         s_stop[i].record(stream)
@@ -351,7 +373,7 @@ def run_gpu(args):
     # kernels stops the combine from overlapping phase 1, so these steps are
     # not the timed ones).
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         step(B.make_opts(event_start=p_start[i], event_stop=p_stop[i]))
     torch.cuda.synchronize(device)
     clocks = sampler.stop() if sampler else None
@@ -444,7 +466,7 @@ def mla_workload_config(case, name):
                             name, case["batch"], int(np.diff(qo).min()), int(np.diff(qo).max()),
                             int(np.diff(kvp).min()), int(np.diff(kvp).max()), case["total_q"], int(kvp[-1])),
             "seed": 0, "flops_per_step": int(mla_flops(case)), "pairs": int(mla_pairs(case)),
-            "sm_scale": case["sm_scale"], "l2": "flushed between steps (256 MiB write)", "accumulate": "fp32"}
+            "sm_scale": case["sm_scale"], "l2": L2_NOTE, "accumulate": "fp32"}
 
 
 def mla_cpu_baseline(case, budget_s: float = 15.0):
@@ -497,7 +519,7 @@ def run_mla(args):
     lse = torch.empty((T, H), dtype=torch.float32, device=device)
     desc = tensors.mla_desc(case)
     ws = tensors.mla_workspace_for(desc, device=device)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = ColdL2(torch, device)
     stream = torch.cuda.current_stream(device)
     ev = lambda: torch.cuda.Event(enable_timing=True)
     starts, stops = [ev() for _ in range(args.steps)], [ev() for _ in range(args.steps)]
@@ -509,12 +531,12 @@ def run_mla(args):
         pass
     sampler = ClockSampler(uuid)
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize(device)
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         starts[i].record(stream)
         step()
         stops[i].record(stream)
