@@ -62,6 +62,9 @@ class ColdL2:
 PROFILE_SUMMARIES = {
     "llama3_8b_decode": os.path.join(ROOT, "profiles", "decode_phase1_llama3_8b_decode.md"),
     "llama3_8b_spec_decode_q4": os.path.join(ROOT, "profiles", "decode_phase1_llama3_8b_spec_decode_q4.md"),
+    "llama3_8b_decode_fp8": os.path.join(ROOT, "profiles", "decode_phase1_llama3_8b_decode_fp8.md"),
+    "long_context_decode": os.path.join(ROOT, "profiles", "decode_phase1_long_context_decode.md"),
+    "gqa6_d256_vllm_decode": os.path.join(ROOT, "profiles", "decode_phase1_gqa6_d256_vllm_decode.md"),
 }
 MLA_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "mla_prefill_kernel_mla_prefill_h16.md")
 FALLBACK_HBM_GBS = 6800.0
