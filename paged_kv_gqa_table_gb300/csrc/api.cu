@@ -175,7 +175,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 //   NHD : {D, BS, NB*Hkv}, box {64, BS, 1}, 128-byte swizzle.
 //   VLLM: the contiguous D*BS-element slice viewed as {256, D*BS/256, NB*Hkv},
 //         box {256, D*BS/256, 1}, no swizzle.
-int encode_cache_map(CUtensorMap* map, const void* base, const pkv_decode_desc* d) {
+int encode_cache_map(CUtensorMap* map, const void* base, const pkv_decode_desc* d, int heads) {
     auto fn = encode_fn();
     if (!fn) return PKV_CUDA_ERROR;
     const cuuint64_t slices = (cuuint64_t)d->num_blocks * d->Hkv;
@@ -184,7 +184,8 @@ int encode_cache_map(CUtensorMap* map, const void* base, const pkv_decode_desc* 
     CUtensorMapSwizzle swz;
     CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_UINT16;
     if (d->kv_dtype == PKV_FP8_E4M3) {
-        // {D, BS, NB*Hkv} bytes, one unswizzled {D, BS} box per page slice
+        // {D, BS, NB*Hkv} bytes, one {D, BS} box per page slice (per two
+        // adjacent slices, {D, BS, 2}, for head pairs)
         type = CU_TENSOR_MAP_DATA_TYPE_UINT8;
         dims[0] = d->D;
         dims[1] = d->block_size;
@@ -195,7 +196,7 @@ int encode_cache_map(CUtensorMap* map, const void* base, const pkv_decode_desc* 
         // fragments); D = 64: one unswizzled {64, BS} box (expanded in shared memory)
         box[0] = d->D >= 128 ? 128 : d->D;
         box[1] = d->block_size;
-        box[2] = 1;
+        box[2] = (cuuint32_t)heads;
         swz = d->D >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
     } else if (d->layout == PKV_LAYOUT_NHD) {
         dims[0] = d->D;
@@ -268,10 +269,20 @@ int check_tensors(const pkv_decode_desc* d, const void* q, const void* k, const 
     return PKV_OK;
 }
 
-// Common set-up of phase 1: parameters and the two tensor maps.
+// FP8 caches at D = 128 whose query rows per KV head (G * q_len) fill at most
+// half a column tile run one CTA per pair of adjacent KV heads: both heads'
+// page slices are contiguous, so each ring stage moves 4 KB boxes instead of
+// 2 KB ones, with the same tensor-core work per byte.
+bool head_pairs(const pkv_decode_desc* d) {
+    return d->kv_dtype == PKV_FP8_E4M3 && d->D == 128 && d->Hkv % 2 == 0 &&
+           2LL * (d->Hq / d->Hkv) * d->q_len <= 8;
+}
+
+// Common set-up of phase 1: parameters and the two tensor maps (pairs: one
+// CTA per pair of KV heads, see head_pairs).
 int prepare_phase1(const pkv_decode_desc* d, int P, int NS, const void* q, const void* k, const void* v,
-                   const int32_t* table, const int32_t* ctx, float scale, DecodeParams* p, CUtensorMap* mk,
-                   CUtensorMap* mv) {
+                   const int32_t* table, const int32_t* ctx, float scale, bool pairs, DecodeParams* p,
+                   CUtensorMap* mk, CUtensorMap* mv) {
     *p = DecodeParams{};
     p->q = q;
     p->table = table;
@@ -284,6 +295,14 @@ int prepare_phase1(const pkv_decode_desc* d, int P, int NS, const void* q, const
     p->q_len = d->q_len;
     p->R = ct.R;
     p->RT = ct.rt;
+    p->Hc = p->Hkv;
+    p->Gc = p->G;
+    if (pairs) {
+        p->Hkv = d->Hkv / 2;
+        p->G = 2 * p->Gc;
+        p->R = p->G * d->q_len;   // <= 8: one column tile
+        p->RT = 1;
+    }
     p->MBPS = d->max_blocks_per_seq;
     p->NB = d->num_blocks;
     p->P = P;
@@ -294,9 +313,9 @@ int prepare_phase1(const pkv_decode_desc* d, int P, int NS, const void* q, const
     p->scale_log2 = (float)((double)scale * (fp8 ? (double)d->k_scale : 1.0) * 1.4426950408889634);
     p->v_scale = fp8 ? d->v_scale : 1.f;
     if (d->max_context_len == 0) return PKV_OK;   // maps unused: every split is empty
-    int st = encode_cache_map(mk, k, d);
+    int st = encode_cache_map(mk, k, d, pairs ? 2 : 1);
     if (st) return st;
-    return encode_cache_map(mv, v, d);
+    return encode_cache_map(mv, v, d, pairs ? 2 : 1);
 }
 
 void record(void* ev, cudaStream_t s) {
@@ -355,7 +374,8 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
 
     DecodeParams p;
     CUtensorMap mk{}, mv{};
-    st = prepare_phase1(desc, P, ns, q, k_cache, v_cache, block_table, context_lens, scale, &p, &mk, &mv);
+    st = prepare_phase1(desc, P, ns, q, k_cache, v_cache, block_table, context_lens, scale,
+                        head_pairs(desc) && !device_plan(opts), &p, &mk, &mv);
     if (st) return st;
     if (opts) p.alibi = opts->alibi_slopes;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -431,7 +451,8 @@ int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts
     if (desc->B == 0) return PKV_OK;
     DecodeParams p;
     CUtensorMap mk, mv;
-    st = prepare_phase1(desc, P, ns, q, k_cache, v_cache, block_table, context_lens, scale, &p, &mk, &mv);
+    st = prepare_phase1(desc, P, ns, q, k_cache, v_cache, block_table, context_lens, scale, head_pairs(desc), &p,
+                        &mk, &mv);
     if (st) return st;
     if (opts) p.alibi = opts->alibi_slopes;
     p.partials_only = 1;

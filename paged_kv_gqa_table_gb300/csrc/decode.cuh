@@ -1,6 +1,8 @@
 // decode.cuh -- phase 1 of paged GQA decode attention on sm_103a.
 //
-// One CTA per (sequence b, KV head, row tile, split s).  Split s covers tokens
+// One CTA per (sequence b, KV head, row tile, split s) -- for FP8 caches with
+// few query rows per KV head, per pair of adjacent KV heads (kLayoutNHD8x2).
+// Split s covers tokens
 // [s*P, min((s+1)*P, n)) of the sequence (fixed partitions as in
 // "paged_attention_v2_triton.py", _partition_attn_kernel; page-granular
 // splits as in the flash-decode post's _flash_decode_partial_kernel).  The
@@ -47,7 +49,9 @@ struct DecodeParams {
     float* part_m;           // [B][q_len][Hq][ns_stride]
     float* part_l;           // [B][q_len][Hq][ns_stride]
     uint32_t* err;           // device error word or nullptr
-    int B, Hq, Hkv, G, MBPS, NB;
+    int B, Hq, Hkv, G, MBPS, NB;   // Hkv, G: the grid's KV heads and query heads per grid KV head
+    int Hc, Gc;              // the cache's KV heads and query heads per cache KV head (Hkv = Hc / 2,
+                             // G = 2 Gc for kLayoutNHD8x2, else Hc = Hkv, Gc = G)
     int q_len;               // query tokens per sequence (the last q_len positions)
     int R;                   // query rows per (sequence, KV head): G * q_len
     int RT;                  // row tiles: ceil(R / (8 * NT))
@@ -70,16 +74,18 @@ struct DecodeParams {
 template <int D, int LAYOUT>
 struct DecodeTile {
     static constexpr int BS = kPageTokens;
-    static constexpr int KVB = LAYOUT == kLayoutNHD8 ? 1 : 2;       // bytes per cache element
+    static constexpr int KVB = (LAYOUT == kLayoutNHD8 || LAYOUT == kLayoutNHD8x2) ? 1 : 2;   // bytes per element
+    static constexpr int HEADS = LAYOUT == kLayoutNHD8x2 ? 2 : 1;   // KV heads per CTA
     // Consumer warps and ring stages.  The CTAs of a launch are short (a split),
     // and each spends its start-up (context length, table, first page) with its
     // ring empty, so more CTAs per SM with the same bytes in flight per SM keep
     // the SM streaming: at D = 128 three consumers with 6 stages (16-bit, 48 KB)
     // or 9 stages (FP8, 36 KB) give four or five CTAs per SM instead of three.
-    // FP8 pages at D = 256 keep twice the 16-bit stages (the same bytes).
+    // FP8 pages at D = 256 keep twice the 16-bit stages (the same bytes).  Head
+    // pairs (8 KB stages) keep the 16-bit depth: 6 stages, four CTAs per SM.
     static constexpr int NWC = D == 128 ? 3 : 4;
-    static constexpr int SLICE = BS * D * KVB;                      // bytes of one page slice
-    static constexpr int STAGES = D == 64 ? 12 : (D == 128 ? (KVB == 1 ? 9 : 6) : (KVB == 1 ? 8 : 4));
+    static constexpr int SLICE = BS * D * KVB * HEADS;              // bytes of one page's K (or V) in a stage
+    static constexpr int STAGES = HEADS == 2 ? 6 : (D == 64 ? 12 : (D == 128 ? (KVB == 1 ? 9 : 6) : (KVB == 1 ? 8 : 4)));
     // FP8 pages with D = 64 are expanded to fp16 in a per-consumer-warp K/V
     // slice pair; D >= 128 goes straight from the ring into mma fragments.
     static constexpr int STAGING = (KVB == 1 && D < 128) ? NWC * 2 * BS * D * 2 : 0;
@@ -106,7 +112,8 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
                                                    const CUtensorMap& tmv) {
     static_assert(GEN || !SCHED, "the device plan runs the general kernel");
     using Tile = DecodeTile<D, LAYOUT>;
-    constexpr bool KV8 = LAYOUT == kLayoutNHD8;
+    constexpr bool KV8 = LAYOUT == kLayoutNHD8 || LAYOUT == kLayoutNHD8x2;
+    constexpr int HEADS = Tile::HEADS;
     constexpr bool DIRECT8 = KV8 && D >= 128;   // page_step_fp8, no staging
     using MT = typename std::conditional<KV8, __half, T>::type;   // tensor-core operand type
     constexpr int BS = Tile::BS, NWC = Tile::NWC, SLICE = Tile::SLICE, STAGES = Tile::STAGES;
@@ -213,7 +220,8 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
                 phys = (phys < 0 || phys >= p.NB) ? 0 : phys;   // bad entries never leave the pool
                 if (lane == 0) {
                     uint8_t* kd = ring + stg * 2 * SLICE;
-                    issue_page_loads<LAYOUT, D>(kd, kd + SLICE, &tmk, &tmv, &full[stg], phys * p.Hkv + kvh, pol);
+                    issue_page_loads<LAYOUT, D>(kd, kd + SLICE, &tmk, &tmv, &full[stg], phys * p.Hc + HEADS * kvh,
+                                                pol);
                 }
                 issued = i + 1;
                 if ((i & 31) == 31) {
@@ -276,6 +284,10 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
         WarpState<D, NT> ws;
         ws.reset();
         ColTerms<NT> ct;
+        if constexpr (HEADS == 2) {   // the pair's columns: Gc query heads of each KV head per query token
+#pragma unroll
+            for (int j = 0; j < 2; ++j) ct.second[0][j] = (qc.col0 + 2 * (lane & 3) + j) % p.G >= p.Gc;
+        }
         if constexpr (GEN) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -305,7 +317,7 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
             const int valid = (pg0 + i == last_pg) ? n - last_pg * BS : BS;
             ct.pos0 = (pg0 + i) * BS - (n - 1);
             if constexpr (DIRECT8) {
-                page_step_fp8<D, NT, GEN, QS>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, ct, qs_a);
+                page_step_fp8<D, NT, GEN, QS, HEADS>(ks, ks + SLICE, valid, scale_log2, qf, ws, lane, ct, qs_a);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[stg]);
             } else if constexpr (KV8) {
@@ -501,6 +513,17 @@ cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CU
     if (p.alibi || p.q_len > 1)
         return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, false>(p, grid, tmk, tmv, stream);
     return launch_decode_phase1_variant<T, LAYOUT, D, NT, false, false>(p, grid, tmk, tmv, stream);
+}
+
+// Head pairs (kLayoutNHD8x2, D = 128, one column tile) under the host plan
+// only: the device plan's item list counts single KV heads.
+template <typename T>
+cudaError_t launch_decode_phase1_pairs(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
+                                       const CUtensorMap& tmv, cudaStream_t stream) {
+    if (p.sched_hdr) return cudaErrorInvalidValue;
+    if (p.alibi || p.q_len > 1)
+        return launch_decode_phase1_variant<T, kLayoutNHD8x2, 128, 1, true, false>(p, grid, tmk, tmv, stream);
+    return launch_decode_phase1_variant<T, kLayoutNHD8x2, 128, 1, false, false>(p, grid, tmk, tmv, stream);
 }
 
 }  // namespace pkv

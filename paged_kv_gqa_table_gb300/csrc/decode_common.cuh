@@ -20,9 +20,15 @@
 namespace pkv {
 
 // kLayoutNHD8: the NHD layout with FP8 E4M3 elements (K = k_scale * fp8,
-// V = v_scale * fp8).  Its pages are expanded to fp16 in shared memory and
-// then take the kLayoutNHD path with fp16 tensor-core arithmetic.
-enum { kLayoutNHD = 0, kLayoutVLLM = 1, kLayoutNHD8 = 2 };
+// V = v_scale * fp8), fp16 tensor-core arithmetic: at D = 64 its pages are
+// expanded to fp16 in shared memory and take the kLayoutNHD path; at D >= 128
+// they go from the ring straight into mma fragments (page_step_fp8).
+// kLayoutNHD8x2: the same cache with one CTA per pair of adjacent KV heads
+// (D = 128, at most 4 query rows per KV head, so that both heads' rows fill
+// one 8-column tile): the two heads' slices of a page are contiguous in the
+// NHD layout, so one ring stage takes both with one 4 KB box for K and one for
+// V instead of two 2 KB stages.
+enum { kLayoutNHD = 0, kLayoutVLLM = 1, kLayoutNHD8 = 2, kLayoutNHD8x2 = 3 };
 constexpr int kPageTokens = 16;
 
 __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
@@ -115,11 +121,14 @@ struct WarpState {
 //          rel = t_abs - pos_i = pos0 + t + shift with pos0 the page's first
 //          position minus (n - 1).  The key is visible iff rel <= 0;
 //   slope: its head's ALiBi slope in log2 units (0 without ALiBi): bias slope * rel.
+// second (kLayoutNHD8x2, any kernel): the column's query head belongs to the
+// second KV head of the CTA's pair.
 template <int NT>
 struct ColTerms {
     float slope[NT][2];
     int shift[NT][2];
     int pos0;
+    bool second[NT][2];
 };
 
 // Folds one page (K slice ks, V slice vs in shared memory) into the warp's
@@ -370,31 +379,59 @@ __device__ __forceinline__ int fp8_q_frags(uint32_t (&qf)[NT][D / 16][2], const 
     }
 }
 
+// A-operand fragment of one 16-byte FP8 chunk pair of a K slice (ldmatrix
+// registers rr[0..1]: tokens t and t + 8), as fp16 pairs.
+__device__ __forceinline__ void fp8_k_frag(const uint32_t* rr, uint32_t (&a)[4]) {
+    a[0] = e4m3x2_to_f16x2((uint16_t)(rr[0] & 0xFFFFu));
+    a[1] = e4m3x2_to_f16x2((uint16_t)(rr[1] & 0xFFFFu));
+    a[2] = e4m3x2_to_f16x2((uint16_t)(rr[0] >> 16));
+    a[3] = e4m3x2_to_f16x2((uint16_t)(rr[1] >> 16));
+}
+// The same for a transposed V chunk pair (k = token order restored by a byte permute).
+__device__ __forceinline__ void fp8_v_frag(const uint32_t* rr, uint32_t (&a)[4]) {
+    const uint32_t lo = __byte_perm(rr[0], 0u, 0x3120), hi = __byte_perm(rr[1], 0u, 0x3120);
+    a[0] = e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu));
+    a[1] = e4m3x2_to_f16x2((uint16_t)(lo >> 16));
+    a[2] = e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu));
+    a[3] = e4m3x2_to_f16x2((uint16_t)(hi >> 16));
+}
+
 // One FP8 page (swizzled K and V slices in the ring) into the warp's state, as
 // page_step; fp16 tensor-core arithmetic.  V rows past `valid` are zeroed in
 // the ring stage first (the caller fences before the stage is refilled).
-template <int D, int NT, bool GEN, bool QS = false>
+// HEADS = 2 (kLayoutNHD8x2): ks and vs hold two KV heads' slices, BS * D bytes
+// apart, and the column tile holds both heads' query rows (ct.second marks the
+// second head's).  Each column takes its scores from its own head's keys, and
+// P goes into each head's P.V product with the other head's columns zeroed,
+// so a column sees exactly the arithmetic of the one-head kernel.
+template <int D, int NT, bool GEN, bool QS = false, int HEADS = 1>
 __device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int valid, float scale_log2,
                                               const uint32_t (&qf)[NT][D / 16][2], WarpState<D, NT>& st, int lane,
                                               const ColTerms<NT>& ct, uint32_t qs_a = 0) {
-    constexpr int BS = kPageTokens, KT = D / 16;
+    static_assert(HEADS == 1 || (HEADS == 2 && NT == 1 && !QS && D == 128), "head pairs: one column tile, D = 128");
+    constexpr int BS = kPageTokens, KT = D / 16, HOFF = BS * D;   // HOFF: bytes between the heads' slices
     const int mi = lane >> 3, r8 = lane & 7;
     const int t_l = r8 + ((mi & 1) << 3), c_l = mi >> 1;   // this lane's ldmatrix row and chunk offset
     const uint32_t ks_a = smem_u32(ks), vs_a = smem_u32(vs);
 
-    float sc[NT][4];
+    float sc[NT][4], sc2[4] = {0.f, 0.f, 0.f, 0.f};   // sc2: the second head's scores
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
     for (int c2 = 0; c2 < KT / 2; ++c2) {
-        uint32_t r[4];
+        uint32_t r[4], r2[4];
         ldsm_x4(ks_a + fp8_off(t_l, 2 * c2 + c_l), r);
+        if constexpr (HEADS == 2) ldsm_x4(ks_a + HOFF + fp8_off(t_l, 2 * c2 + c_l), r2);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {   // chunk 2*c2 + h: k-step kk
-            const uint32_t* rr = r + 2 * h;
-            const uint32_t a[4] = {e4m3x2_to_f16x2((uint16_t)(rr[0] & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(rr[1] & 0xFFFFu)),
-                                   e4m3x2_to_f16x2((uint16_t)(rr[0] >> 16)), e4m3x2_to_f16x2((uint16_t)(rr[1] >> 16))};
-            if constexpr (QS) {
+            uint32_t a[4];
+            fp8_k_frag(r + 2 * h, a);
+            if constexpr (HEADS == 2) {
+                uint32_t a2[4];
+                fp8_k_frag(r2 + 2 * h, a2);
+                Mma<__half>::run(sc[0], a, qf[0][2 * c2 + h][0], qf[0][2 * c2 + h][1]);
+                Mma<__half>::run(sc2, a2, qf[0][2 * c2 + h][0], qf[0][2 * c2 + h][1]);
+            } else if constexpr (QS) {
                 static_assert(NT == 2, "the shared Q copy holds two column tiles");
                 uint32_t b[4];
                 load_q_smem<D>(qs_a, 2 * c2 + h, lane, b);
@@ -406,6 +443,11 @@ __device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int vali
                     Mma<__half>::run(sc[nt], a, qf[nt][2 * c2 + h][0], qf[nt][2 * c2 + h][1]);
             }
         }
+    }
+    if constexpr (HEADS == 2) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (ct.second[0][e & 1]) sc[0][e] = sc2[e];
     }
 
     // scale to log2 units, mask, online-softmax update (as page_step)
@@ -444,19 +486,33 @@ __device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int vali
             }
         }
     }
-    uint32_t pb[NT][2];
+    uint32_t pb[NT][2], pb2[2];   // pb2: the second head's P (HEADS = 2; then pb holds the first's)
+    if constexpr (HEADS == 2) {
+        float p1[4], p2[4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        pb[nt][0] = movmatrix_trans(Mma<__half>::pack(sc[nt][0], sc[nt][1]));
-        pb[nt][1] = movmatrix_trans(Mma<__half>::pack(sc[nt][2], sc[nt][3]));
+        for (int e = 0; e < 4; ++e) {
+            p1[e] = ct.second[0][e & 1] ? 0.f : sc[0][e];
+            p2[e] = ct.second[0][e & 1] ? sc[0][e] : 0.f;
+        }
+        pb[0][0] = movmatrix_trans(Mma<__half>::pack(p1[0], p1[1]));
+        pb[0][1] = movmatrix_trans(Mma<__half>::pack(p1[2], p1[3]));
+        pb2[0] = movmatrix_trans(Mma<__half>::pack(p2[0], p2[1]));
+        pb2[1] = movmatrix_trans(Mma<__half>::pack(p2[2], p2[3]));
+    } else {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            pb[nt][0] = movmatrix_trans(Mma<__half>::pack(sc[nt][0], sc[nt][1]));
+            pb[nt][1] = movmatrix_trans(Mma<__half>::pack(sc[nt][2], sc[nt][3]));
+        }
     }
 
     if (valid < BS) {   // zero whole V rows past the context (layout-agnostic within a row)
         constexpr int ROWB = 128 / 16;   // 16-byte pieces per 128-byte row
-        const int pieces = (BS - valid) * ROWB * (D / 128);
-        for (int i = lane; i < pieces; i += 32) {
-            const int blk = i / ((BS - valid) * ROWB), rem = i % ((BS - valid) * ROWB);
-            *reinterpret_cast<uint4*>(vs + blk * (BS * 128) + (valid + rem / ROWB) * 128 + (rem % ROWB) * 16) =
+        const int per_head = (BS - valid) * ROWB * (D / 128);
+        for (int i = lane; i < HEADS * per_head; i += 32) {
+            const int hh = i / per_head, k = i % per_head;
+            const int blk = k / ((BS - valid) * ROWB), rem = k % ((BS - valid) * ROWB);
+            *reinterpret_cast<uint4*>(vs + hh * HOFF + blk * (BS * 128) + (valid + rem / ROWB) * 128 + (rem % ROWB) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
@@ -465,25 +521,36 @@ __device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int vali
 
 #pragma unroll
     for (int c2 = 0; c2 < KT / 2; ++c2) {
-        uint32_t r[4];
+        uint32_t r[4], r2[4];
         ldsm_x4_trans(vs_a + fp8_off(t_l, 2 * c2 + c_l), r);
+        if constexpr (HEADS == 2) ldsm_x4_trans(vs_a + HOFF + fp8_off(t_l, 2 * c2 + c_l), r2);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {   // chunk 2*c2 + h: output rows dt = 2*c2 + h
-            const uint32_t lo = __byte_perm(r[2 * h], 0u, 0x3120), hi = __byte_perm(r[2 * h + 1], 0u, 0x3120);
-            const uint32_t a[4] = {e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(lo >> 16)),
-                                   e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(hi >> 16))};
+            uint32_t a[4];
+            fp8_v_frag(r + 2 * h, a);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) Mma<__half>::run(st.acc[2 * c2 + h][nt], a, pb[nt][0], pb[nt][1]);
+            if constexpr (HEADS == 2) {
+                uint32_t a2[4];
+                fp8_v_frag(r2 + 2 * h, a2);
+                Mma<__half>::run(st.acc[2 * c2 + h][0], a2, pb2[0], pb2[1]);
+            }
         }
     }
 }
 
-// Issues the TMA loads of one page slice pair (K and V of one KV head) into a
-// ring stage, completing on `bar` (2 * BS * D * element-size bytes).
+// Issues the TMA loads of one page slice pair (K and V of one KV head, or of
+// two adjacent ones for kLayoutNHD8x2) into a ring stage, completing on `bar`.
 template <int LAYOUT, int D>
 __device__ __forceinline__ void issue_page_loads(uint8_t* kd, uint8_t* vd, const CUtensorMap* tmk,
                                                  const CUtensorMap* tmv, uint64_t* bar, int slice, uint64_t pol) {
     constexpr int BS = kPageTokens;
+    if (LAYOUT == kLayoutNHD8x2) {   // `slice` is the pair's first: one {128, BS, 2} box each (D = 128)
+        mbar_arrive_expect_tx(bar, 4 * BS * D);
+        tma_load_3d(kd, tmk, bar, 0, 0, slice, pol);
+        tma_load_3d(vd, tmv, bar, 0, 0, slice, pol);
+        return;
+    }
     if (LAYOUT == kLayoutNHD8) {
         mbar_arrive_expect_tx(bar, 2 * BS * D);
         if (D >= 128) {   // 128-byte-wide swizzled boxes (page_step_fp8)
