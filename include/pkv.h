@@ -144,10 +144,12 @@ PKV_API int pkv_version(void);
  * 512-token partitions; [FD] page-granular splits).  *num_splits =
  * ceil(max_context_len / P) (at least 1) is the grid extent along splits.
  * num_sms <= 0 queries the current device.  The default picks P = 512 tokens
- * per column tile of a CTA (1024 when a CTA holds 16 query rows, else 512; or
- * the longest context, if shorter), halved while the estimated number of
- * (sequence, KV head, row tile, split) work items stays below 6 * num_sms,
- * down to 4 * block_size.  Row tiles: the G * q_len query rows of a
+ * per column tile of a CTA and per KV head it holds -- 1024 when a CTA holds
+ * 16 query rows, or when an FP8 cache at D = 128 with an even Hkv has at most
+ * 4 query rows (G * q_len) per KV head, so that a CTA takes a pair of KV
+ * heads; else 512 -- or the longest context, if shorter, halved while the
+ * estimated number of (sequence, KV head, row tile, split) work items stays
+ * below 6 * num_sms, down to 4 * block_size.  Row tiles: the G * q_len query rows of a
  * (sequence, KV head) pair are covered 16 at a time (8 for D = 256 or for at
  * most 8 rows).
  */

@@ -75,16 +75,31 @@ int current_sm_count(int* out) {
     return PKV_OK;
 }
 
-// Default partition: 512 tokens per column tile of the CTA (512 or 1024; a
-// CTA's fixed costs -- loading Q, merging its warps' columns, writing the
-// partials -- grow with its columns), or the longest context rounded up to a
-// page, if shorter; halved while the estimated number of non-empty work
+// FP8 caches at D = 128 whose query rows per KV head (G * q_len) fill at most
+// half a column tile run one CTA per pair of adjacent KV heads: both heads'
+// page slices are contiguous, so each ring stage moves 4 KB boxes instead of
+// 2 KB ones, with the same tensor-core work per byte.
+bool head_pairs(const pkv_decode_desc* d) {
+    return d->kv_dtype == PKV_FP8_E4M3 && d->D == 128 && d->Hkv % 2 == 0 &&
+           2LL * (d->Hq / d->Hkv) * d->q_len <= 8;
+}
+
+// Base partition: 512 tokens per column tile of the CTA and per KV head it
+// holds (512, or 1024 for two column tiles or a pair of KV heads: a CTA's
+// fixed costs -- loading Q, merging its warps' columns, writing the partials
+// -- grow with its columns, and fewer splits shorten the combine).
+long long base_partition(const pkv_decode_desc* d) {
+    return 512LL * column_tiles(d).nt * (head_pairs(d) ? 2 : 1);
+}
+
+// Default partition: the base partition, or the longest context rounded up to
+// a page, if shorter; halved while the estimated number of non-empty work
 // items Hkv * row_tiles * ceil(sum_n / P) stays below six per SM, down to
-// four pages.
+// four pages.  The device plan applies the same rule to the actual lengths.
 long long auto_partition(const pkv_decode_desc* d, int num_sms) {
     const long long BS = d->block_size;
     const long long maxn = d->max_context_len > 0 ? d->max_context_len : 1;
-    const long long P0 = 512LL * column_tiles(d).nt;
+    const long long P0 = base_partition(d);
     long long P = round_up(maxn < P0 ? maxn : P0, BS);
     const long long min_p = 4 * BS;
     const long long target = 6LL * num_sms;
@@ -269,15 +284,6 @@ int check_tensors(const pkv_decode_desc* d, const void* q, const void* k, const 
     return PKV_OK;
 }
 
-// FP8 caches at D = 128 whose query rows per KV head (G * q_len) fill at most
-// half a column tile run one CTA per pair of adjacent KV heads: both heads'
-// page slices are contiguous, so each ring stage moves 4 KB boxes instead of
-// 2 KB ones, with the same tensor-core work per byte.
-bool head_pairs(const pkv_decode_desc* d) {
-    return d->kv_dtype == PKV_FP8_E4M3 && d->D == 128 && d->Hkv % 2 == 0 &&
-           2LL * (d->Hq / d->Hkv) * d->q_len <= 8;
-}
-
 // Common set-up of phase 1: parameters and the two tensor maps (pairs: one
 // CTA per pair of KV heads, see head_pairs).
 int prepare_phase1(const pkv_decode_desc* d, int P, int NS, const void* q, const void* k, const void* v,
@@ -407,7 +413,7 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
         const ColumnTiles ct = column_tiles(desc);
         SchedParams sp{context_lens, hdr, list, desc->B, desc->Hkv, ct.rt, p.n_cap, ns, desc->block_size,
                        opts->partition_tokens > 0 ? P : 0, opts->partition_tokens > 0 ? 0 : opts->num_splits,
-                       512 * ct.nt, sms};
+                       (int)base_partition(desc), sms};
         p.sched_hdr = hdr;
         p.sched_list = list;
         p.sched_cap = (int)plan_items(desc, ns);

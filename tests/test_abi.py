@@ -66,6 +66,12 @@ def ref_row_tiles(d):
     return -(-(d.Hq // d.Hkv * d.q_len) // ref_rows_per_cta(d))
 
 
+def ref_heads_per_cta(d):
+    """2 for the documented head pairs (FP8, D = 128, even Hkv, <= 4 query rows per KV head), else 1."""
+    pair = d.kv_dtype == 2 and d.D == 128 and d.Hkv % 2 == 0 and 2 * (d.Hq // d.Hkv) * d.q_len <= 8
+    return 2 if pair else 1
+
+
 def ref_plan(d, num_sms, P_forced=0, ns_forced=0):
     """Independent restatement of the planner's documented rule."""
     bs = d.block_size
@@ -75,7 +81,7 @@ def ref_plan(d, num_sms, P_forced=0, ns_forced=0):
     elif ns_forced:
         P = up(-(-max(d.max_context_len, 1) // ns_forced))
     else:
-        P = up(min(max(d.max_context_len, 1), 512 * ref_rows_per_cta(d) // 8))
+        P = up(min(max(d.max_context_len, 1), 512 * ref_rows_per_cta(d) // 8 * ref_heads_per_cta(d)))
         while P > 4 * bs and d.Hkv * ref_row_tiles(d) * -(-max(d.sum_context_len, 1) // P) < 6 * num_sms:
             P = max(4 * bs, up(P // 2))
     return max(1, -(-d.max_context_len // P)), P
@@ -89,9 +95,9 @@ def test_plan_matches_the_documented_rule(B):
         mbps = rng.randint(1, 9000)
         maxn = rng.randint(0, mbps * 16)
         s = rng.randint(maxn, max(maxn, maxn * Bn))
-        d = desc(B, B=Bn, Hkv=Hkv, Hq=Hkv * rng.choice([1, 4, 6, 8, 12, 32]), D=rng.choice([64, 128, 256]),
+        d = desc(B, B=Bn, Hkv=Hkv, Hq=Hkv * rng.choice([1, 2, 4, 6, 8, 12, 32]), D=rng.choice([64, 128, 256]),
                  max_blocks_per_seq=mbps, max_context_len=maxn, sum_context_len=s,
-                 q_len=rng.choice([1, 1, 2, 3, 4, 8]))
+                 q_len=rng.choice([1, 1, 2, 3, 4, 8]), kv_dtype=rng.choice([0, 2]))
         sms = rng.choice([1, 76, 148, 152])
         mode = rng.randint(0, 2)
         if mode == 0:
@@ -109,6 +115,11 @@ def test_named_workload_plans(B):
     assert B.pkv_plan_splits(desc(B), None, 152) == (8, 512)
     long_ctx = desc(B, B=4, max_blocks_per_seq=8192, max_context_len=131072, sum_context_len=4 * 81920)
     assert B.pkv_plan_splits(long_ctx, None, 152) == (256, 512)
+    # the FP8 variant of the default runs head pairs: 512 tokens per KV head of the CTA
+    assert B.pkv_plan_splits(desc(B, kv_dtype=2), None, 152) == (4, 1024)
+    # ... but not with an odd KV head count or a full column tile per KV head
+    assert B.pkv_plan_splits(desc(B, kv_dtype=2, Hkv=1, Hq=4), None, 152)[1] < 1024
+    assert B.pkv_plan_splits(desc(B, kv_dtype=2, q_len=2), None, 152) == (8, 512)
     tiny = desc(B, B=2, Hq=4, Hkv=2, D=64, max_blocks_per_seq=8, num_blocks=16, max_context_len=100,
                 sum_context_len=137, dtype=0)
     assert B.pkv_plan_splits(tiny, None, 152) == (2, 64)
