@@ -1,11 +1,11 @@
 // decode.cuh -- phase 1 of paged GQA decode attention on sm_103a.
 //
-// One CTA per (sequence b, KV head, row tile, split s) -- for FP8 caches with
+// One CTA per (sequence b, KV head, row tile, split s); for FP8 caches with
 // few query rows per KV head, per pair of adjacent KV heads (kLayoutNHD8x2).
-// Split s covers tokens
-// [s*P, min((s+1)*P, n)) of the sequence (fixed partitions as in
-// "paged_attention_v2_triton.py", _partition_attn_kernel; page-granular
-// splits as in the flash-decode post's _flash_decode_partial_kernel).  The
+// Split s covers tokens [s*P, min((s+1)*P, n)) of the sequence (fixed
+// partitions as in "paged_attention_v2_triton.py", _partition_attn_kernel;
+// page-granular splits as in the flash-decode post's
+// _flash_decode_partial_kernel).  The
 // query rows of (b, KV head) -- q_len tokens x G heads -- are the mma N
 // columns, 8 * NT per CTA; more rows than that take several row tiles.
 //
@@ -85,7 +85,8 @@ struct DecodeTile {
     // pairs (8 KB stages) keep the 16-bit depth: 6 stages, four CTAs per SM.
     static constexpr int NWC = D == 128 ? 3 : 4;
     static constexpr int SLICE = BS * D * KVB * HEADS;              // bytes of one page's K (or V) in a stage
-    static constexpr int STAGES = HEADS == 2 ? 6 : (D == 64 ? 12 : (D == 128 ? (KVB == 1 ? 9 : 6) : (KVB == 1 ? 8 : 4)));
+    static constexpr int STAGES =
+        HEADS == 2 ? 6 : (D == 64 ? 12 : (D == 128 ? (KVB == 1 ? 9 : 6) : (KVB == 1 ? 8 : 4)));
     // FP8 pages with D = 64 are expanded to fp16 in a per-consumer-warp K/V
     // slice pair; D >= 128 goes straight from the ring into mma fragments.
     static constexpr int STAGING = (KVB == 1 && D < 128) ? NWC * 2 * BS * D * 2 : 0;

@@ -512,8 +512,8 @@ __device__ __forceinline__ void page_step_fp8(uint8_t* ks, uint8_t* vs, int vali
         for (int i = lane; i < HEADS * per_head; i += 32) {
             const int hh = i / per_head, k = i % per_head;
             const int blk = k / ((BS - valid) * ROWB), rem = k % ((BS - valid) * ROWB);
-            *reinterpret_cast<uint4*>(vs + hh * HOFF + blk * (BS * 128) + (valid + rem / ROWB) * 128 + (rem % ROWB) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+            uint8_t* row = vs + hh * HOFF + blk * (BS * 128) + (valid + rem / ROWB) * 128;
+            *reinterpret_cast<uint4*>(row + (rem % ROWB) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
         __syncwarp();
