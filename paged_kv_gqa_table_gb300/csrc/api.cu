@@ -380,8 +380,8 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
 
     DecodeParams p;
     CUtensorMap mk{}, mv{};
-    st = prepare_phase1(desc, P, ns, q, k_cache, v_cache, block_table, context_lens, scale,
-                        head_pairs(desc) && !device_plan(opts), &p, &mk, &mv);
+    st = prepare_phase1(desc, P, ns, q, k_cache, v_cache, block_table, context_lens, scale, head_pairs(desc), &p,
+                        &mk, &mv);
     if (st) return st;
     if (opts) p.alibi = opts->alibi_slopes;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -411,9 +411,11 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
         int* hdr = reinterpret_cast<int*>(ws) + kSchedHeaderWord;
         int4* list = reinterpret_cast<int4*>(parts + (ns > 1 ? partial_bytes(desc, ns) : 0));
         const ColumnTiles ct = column_tiles(desc);
-        SchedParams sp{context_lens, hdr, list, desc->B, desc->Hkv, ct.rt, p.n_cap, ns, desc->block_size,
-                       opts->partition_tokens > 0 ? P : 0, opts->partition_tokens > 0 ? 0 : opts->num_splits,
-                       (int)base_partition(desc), sms};
+        // Items per grid KV head (a pair under head pairs); the planner rule
+        // counts the description's KV heads, as the host planner does.
+        SchedParams sp{context_lens, hdr, list, desc->B, p.Hkv, p.RT, p.n_cap, ns, desc->block_size,
+                       desc->Hkv * ct.rt, opts->partition_tokens > 0 ? P : 0,
+                       opts->partition_tokens > 0 ? 0 : opts->num_splits, (int)base_partition(desc), sms};
         p.sched_hdr = hdr;
         p.sched_list = list;
         p.sched_cap = (int)plan_items(desc, ns);

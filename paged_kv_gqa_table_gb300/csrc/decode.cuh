@@ -516,12 +516,13 @@ cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CU
     return launch_decode_phase1_variant<T, LAYOUT, D, NT, false, false>(p, grid, tmk, tmv, stream);
 }
 
-// Head pairs (kLayoutNHD8x2, D = 128, one column tile) under the host plan
-// only: the device plan's item list counts single KV heads.
+// Head pairs (kLayoutNHD8x2, D = 128, one column tile); under the device plan
+// the schedule kernel lists the items per KV-head pair.
 template <typename T>
 cudaError_t launch_decode_phase1_pairs(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                        const CUtensorMap& tmv, cudaStream_t stream) {
-    if (p.sched_hdr) return cudaErrorInvalidValue;
+    if (p.sched_hdr)
+        return launch_decode_phase1_variant<T, kLayoutNHD8x2, 128, 1, true, true>(p, grid, tmk, tmv, stream);
     if (p.alibi || p.q_len > 1)
         return launch_decode_phase1_variant<T, kLayoutNHD8x2, 128, 1, true, false>(p, grid, tmk, tmv, stream);
     return launch_decode_phase1_variant<T, kLayoutNHD8x2, 128, 1, false, false>(p, grid, tmk, tmv, stream);

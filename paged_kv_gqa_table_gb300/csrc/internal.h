@@ -24,10 +24,11 @@ struct SchedParams {
     const int32_t* ctx;        // [B]
     int* hdr;                  // out: [0] P, [1] splits of the longest context, [2] items listed
     int4* list;                // out: up to B * Hkv * RT * NS_cap items (b, kvh | rt << 16, s, n_b)
-    int B, Hkv, RT, n_cap, NS_cap, BS;
+    int B, Hkv, RT, n_cap, NS_cap, BS;   // Hkv, RT: the grid's (KV-head pairs under head pairs)
+    int HR_rule;               // (KV head, row tile) pairs the planner rule counts: the description's
     int P_fixed;               // > 0: this partition (caller option)
     int num_splits;            // > 0 (without P_fixed): split the longest context this many ways
-    int P0;                    // planner start: 512 tokens per column tile
+    int P0;                    // planner start: 512 tokens per column tile and KV head of the CTA
     int num_sms;               // the planner's work-item target is 6 per SM
 };
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream);

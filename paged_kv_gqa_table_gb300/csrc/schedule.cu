@@ -5,12 +5,14 @@
 //
 // Plan: the rule of the host planner (api.cu, auto_partition) applied to the
 // actual longest context max_n and total sum_n -- P starts at P0 (or max_n
-// rounded up to a page, if shorter) and halves while Hkv * RT * ceil(sum_n / P)
-// is below six items per SM, down to four pages -- then raised, if needed, to
+// rounded up to a page, if shorter) and halves while HR_rule * ceil(sum_n / P)
+// (the description's KV heads x row tiles) is below six items per SM, down to
+// four pages -- then raised, if needed, to
 // ceil(max_n / NS_cap) rounded up to a page so that no sequence has more splits
 // than the workspace holds.  Items: sequence b has ns_b = max(1, ceil(n_b / P))
 // splits (one item writes the zero rows of an empty context) for each of its
-// Hkv * RT (KV head, row tile) pairs, listed as (b, kvh | rt << 16, s, n_b)
+// Hkv * RT (grid KV head, row tile) pairs -- a grid KV head is a pair of KV
+// heads when the CTAs take two -- listed as (b, kvh | rt << 16, s, n_b)
 // with s fastest: the grid order of the host plan without its empty splits
 // (n_b rides along so that a CTA needs one load to start its item).
 #include "internal.h"
@@ -55,8 +57,8 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const SchedParams
         }
         if (lane == 0) {
             // The rule in 32-bit arithmetic (64-bit integer division is slow
-            // here): Hkv * RT * ceil(sum / P) >= target  <=>
-            // ceil(sum / P) >= need = ceil(target / (Hkv * RT))  <=>  sum > (need - 1) * P.
+            // here): HR * ceil(sum / P) >= target  <=>
+            // ceil(sum / P) >= need = ceil(target / HR)  <=>  sum > (need - 1) * P.
             const int BS = p.BS;
             auto cdiv = [](int a, int b) { return a > 0 ? (a - 1) / b + 1 : 0; };   // no overflow near INT_MAX
             auto round_up = [&](int a) { return cdiv(a, BS) * BS; };
@@ -68,7 +70,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const SchedParams
                 P = round_up(cdiv(maxn, p.num_splits));
             } else {
                 P = round_up(maxn < p.P0 ? maxn : p.P0);
-                const int min_p = 4 * BS, HR = p.Hkv * p.RT;
+                const int min_p = 4 * BS, HR = p.HR_rule;
                 const long long target = 6LL * p.num_sms;
                 const long long need = (target + HR - 1) / HR;   // once
                 const long long s1 = sum > 0 ? sum : 1;
