@@ -284,7 +284,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(case, args.workload, flushed=False),
+            "data": "synthetic", "config": workload_config(case, args.workload, flushed=False, accumulate="fp64"),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -303,7 +303,7 @@ def tensors_fp8(case):
     return case.get("kv_dtype", case["dtype"]) == synth.FP8_E4M3
 
 
-def workload_config(case, name, flushed=True):
+def workload_config(case, name, flushed=True, accumulate="fp32"):
     from paged_kv_gqa_table_gb300 import synth
     ctx = case["context_lens"]
     q_len = int(case.get("q_len", 1))
@@ -314,7 +314,7 @@ def workload_config(case, name, flushed=True):
         "seed": 0, "kv_bytes_per_step": synth.kv_bytes(case), "query_tokens_per_step": case["B"] * q_len,
         "kv_bytes_per_step_page_rounded": kv_bytes_page_rounded(case),
         "l2": L2_NOTE if flushed else "n/a (CPU)",
-        "accumulate": "fp32"}
+        "accumulate": accumulate}
 
 
 def run_gpu(args):
@@ -472,38 +472,85 @@ def mla_workload_config(case, name):
             "sm_scale": case["sm_scale"], "l2": L2_NOTE, "accumulate": "fp32"}
 
 
+def mla_oracle_timed(case, tokens, threads):
+    """The oracle on the given query tokens (all heads) on `threads` host threads:
+    (algorithmic flops of those tokens, seconds)."""
+    import oracle
+    out = np.empty((case["total_q"], case["H"], case["Dc"]))
+    lse = np.empty((case["total_q"], case["H"]))
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda t: oracle.mla(case, int(t), int(t) + 1, out=out, lse=lse), tokens))
+    secs = time.perf_counter() - t0
+    qo, kvp = case["qo_indptr"], case["kv_indptr"]
+    b_of = np.searchsorted(qo, tokens, side="right") - 1
+    pairs = 0
+    for t, b in zip(tokens, b_of):
+        q_len, kv_len = qo[b + 1] - qo[b], kvp[b + 1] - kvp[b]
+        pairs += (kv_len - q_len) + (t - qo[b]) + 1
+    return pairs * case["H"] * 2 * (2 * case["Dc"] + case["Dr"]), secs
+
+
 def mla_cpu_baseline(case, budget_s: float = 15.0):
     import oracle
     oracle.build()
     threads = os.cpu_count() or 1
     T = case["total_q"]
     order = np.random.default_rng(3).permutation(T)
-    out = np.empty((T, case["H"], case["Dc"]))
-    lse = np.empty((T, case["H"]))
-
-    def run(tokens):
-        t0 = time.perf_counter()
-        with ThreadPoolExecutor(threads) as ex:
-            list(ex.map(lambda t: oracle.mla(case, int(t), int(t) + 1, out=out, lse=lse), tokens))
-        return time.perf_counter() - t0
-
     n = min(T, threads * 2)
-    secs = run(order[:n])
+    flops, secs = mla_oracle_timed(case, order[:n], threads)
     m = min(T, max(n, int(n * budget_s / 4 / max(secs, 1e-3))))
     if m > n:
-        secs = run(order[:m])
         n = m
-    sub = dict(case)
-    qo, kvp = case["qo_indptr"], case["kv_indptr"]
-    # flops of the sampled tokens
-    b_of = np.searchsorted(qo, order[:n], side="right") - 1
-    pairs = 0
-    for t, b in zip(order[:n], b_of):
-        q_len, kv_len = qo[b + 1] - qo[b], kvp[b + 1] - kvp[b]
-        pairs += (kv_len - q_len) + (t - qo[b]) + 1
-    flops = pairs * case["H"] * 2 * (2 * case["Dc"] + case["Dr"])
+        flops, secs = mla_oracle_timed(case, order[:n], threads)
     return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": "%d of %d query tokens (all heads), %.1f s" % (n, T, secs)}
+
+
+def run_mla_reference(args):
+    """--impl reference on the MLA workload: the CPU oracle timed on bounded samples of query
+    tokens (a different sample each step), same metric and workload as run_mla."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from paged_kv_gqa_table_gb300 import synth
+    import oracle
+    oracle.build()
+    case = synth.mla_case(seed=0, **synth.MLA_WORKLOADS[args.workload])
+    threads = os.cpu_count() or 1
+    T = case["total_q"]
+    order = np.random.default_rng(3).permutation(T)
+    # step size: as many tokens as keep K + W steps within ~60 s
+    n0 = min(T, threads * 2)
+    _, secs0 = mla_oracle_timed(case, order[:n0], threads)
+    per_step = int(min(T, max(n0, n0 * 60.0 / (args.steps + args.warmup) / max(secs0, 1e-3))))
+    cursor = 0
+
+    def step():
+        nonlocal cursor
+        toks = order[np.arange(cursor, cursor + per_step) % T]
+        cursor += per_step
+        return mla_oracle_timed(case, toks, threads)
+
+    for _ in range(args.warmup):
+        step()
+    tot_f, tot_t = 0, 0.0
+    for _ in range(args.steps):
+        f, t = step()
+        tot_f += f
+        tot_t += t
+    value = tot_f / tot_t / 1e12
+    sample = "%d of %d query tokens (all heads) per step" % (per_step, T)
+    line = {"impl": "reference", "metric": MLA_METRIC, "value": value,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(mla_workload_config(case, args.workload), l2="n/a (CPU)", accumulate="fp64"),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def run_mla(args):
@@ -608,9 +655,7 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.workload == "mla_prefill_h16":
-        if args.impl == "reference":
-            ap.error("the reference arm covers the decode workloads")
-        return run_mla(args)
+        return run_mla_reference(args) if args.impl == "reference" else run_mla(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
