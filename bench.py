@@ -2,6 +2,11 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
+The default workload is the largest single-GPU decode configuration
+(gqa6_d256_vllm_decode: 128 sequences, GQA-6, D = 256, vLLM layout); the same
+run measures the other configurations (Llama-3-8B-shaped, long-context, FP8,
+4-token and the MLA prefill) and reports them under "per_config".
+
 One step = one full decode step of the workload (phase 1 + cross-split
 combine) on synthetic inputs already resident in HBM.  Between timed steps a
 256 MiB buffer is written to flush the 129 MB L2 and a second 256 MiB buffer is
@@ -68,6 +73,8 @@ PROFILE_SUMMARIES = {
 }
 MLA_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "mla_prefill_kernel_mla_prefill_h16.md")
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e nominal (context for the measured copy peak)
 
 
 def kernel_source_hash(files=None) -> str:
@@ -105,6 +112,15 @@ def profiled_traffic(summary):
     if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(files):
         return None
     return int(m_bytes.group(1))
+
+
+def profiled_field(summary, key):
+    """A number `key: value` from a committed ncu summary taken on the current
+    kernel sources (as profiled_traffic), else None."""
+    if not summary or not os.path.exists(summary) or profiled_traffic(summary) is None:
+        return None
+    m = re.search(r"^%s:\s*([0-9.]+)" % re.escape(key), open(summary).read(), flags=re.M)
+    return float(m.group(1)) if m else None
 
 
 # ----------------------------------------------------------------- clocks ----
@@ -317,19 +333,16 @@ def workload_config(case, name, flushed=True, accumulate="fp32"):
         "accumulate": accumulate}
 
 
-def run_gpu(args):
+def measure_decode(name, device, steps, warmup, world=1, rank=0, e2e_leg=True, cpu_leg=True, cpu_budget_s=15.0,
+                   sample_clocks=False):
+    """One decode workload: `warmup` untimed steps, then `steps` timed steps (cold L2
+    before each), then the same steps again with events around the phase-1 kernel
+    (the roofline's launch duration).  Returns (fields of the JSON line, case)."""
     import torch
-    world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
     from paged_kv_gqa_table_gb300 import binding as B
     from paged_kv_gqa_table_gb300 import synth, tensors
 
-    B.load()
-    case = synth.decode_case(seed=0, **synth.WORKLOADS[args.workload])
+    case = synth.decode_case(seed=0, **synth.WORKLOADS[name])
     kvb = synth.kv_bytes(case)
     dev = tensors.upload_decode_case(case, device)
     desc = tensors.decode_desc(case)
@@ -339,8 +352,8 @@ def run_gpu(args):
     flush = ColdL2(torch, device)
     stream = torch.cuda.current_stream(device)
     ev = lambda: torch.cuda.Event(enable_timing=True)
-    p_start, p_stop = [ev() for _ in range(args.steps)], [ev() for _ in range(args.steps)]
-    s_start, s_stop = [ev() for _ in range(args.steps)], [ev() for _ in range(args.steps)]
+    p_start, p_stop = [ev() for _ in range(steps)], [ev() for _ in range(steps)]
+    s_start, s_stop = [ev() for _ in range(steps)], [ev() for _ in range(steps)]
     for e in p_start + p_stop:
         e.record(stream)       # materialise the CUDA events before the library records them
     torch.cuda.synchronize(device)
@@ -349,20 +362,22 @@ def run_gpu(args):
         B.pkv_paged_decode_attention(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
                                      dev["context_lens"], case["scale"], out, ws, opts=opts, stream=stream)
 
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
-    except Exception:
-        pass
-    sampler = ClockSampler(uuid) if rank == 0 else None
-    for _ in range(args.warmup):
+    sampler = None
+    if sample_clocks:
+        uuid = None
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            pass
+        sampler = ClockSampler(uuid)
+    for _ in range(warmup):
         flush()
         step()
     torch.cuda.synchronize(device)
     barrier(world, device)
     torch.cuda.synchronize(device)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(steps):
         flush()
         s_start[i].record(stream)
         step()
@@ -375,7 +390,7 @@ def run_gpu(args):
     # library records around the phase-1 kernel (an event between the two
     # kernels stops the combine from overlapping phase 1, so these steps are
     # not the timed ones).
-    for i in range(args.steps):
+    for i in range(steps):
         flush()
         step(B.make_opts(event_start=p_start[i], event_stop=p_stop[i]))
     torch.cuda.synchronize(device)
@@ -384,17 +399,16 @@ def run_gpu(args):
     p1_ms = [a.elapsed_time(b) for a, b in zip(p_start, p_stop)]
     t_total = sum(step_ms) * 1e-3
     t_max = max_over_ranks(t_total, world, device)
-    value = world * kvb * args.steps / t_max / 1e9
-    launches = args.steps * (1 + (1 if ns > 1 else 0))
+    value = world * kvb * steps / t_max / 1e9
 
     # end to end: pinned host inputs -> device, the C-ABI call, result -> pinned host
     e2e = None
-    if not args.skip_e2e:
+    if e2e_leg:
         host = {k: v.cpu().pin_memory() for k, v in dev.items()}
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = out.numel() * out.element_size()
-        n_e2e = max(3, min(args.steps, 30))
+        n_e2e = max(3, min(steps, 30))
         for i in range(n_e2e + 2):
             if i == 2:
                 torch.cuda.synchronize(device)
@@ -410,30 +424,75 @@ def run_gpu(args):
         torch.cuda.synchronize(device)
         t_e2e = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world, device)
         e2e = {"value": world * kvb * n_e2e / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": n_e2e}
+               "d2h_bytes_per_step": int(d2h), "steps": n_e2e, "copies_declared": True}
 
+    peak, peak_kind = measured_peaks()
+    p1_avg = float(np.mean(p1_ms)) * 1e-3
+    achieved = kvb / p1_avg / 1e9
+    summary = PROFILE_SUMMARIES.get(name)
+    fields = {
+        "value": value, "unit": "GB/s", "ms_per_step": t_max / steps * 1e3, "us_per_step": t_max / steps * 1e6,
+        "steps": steps, "warmup": warmup, "dtype": dtype_label(case),
+        "config": dict(workload_config(case, name), partition_tokens=P, num_splits=ns),
+        "hbm_frac_of_measured_peak": value / peak, "hbm_frac_of_nominal_peak": value / NOMINAL_HBM_GBS,
+        "gpu_launches": steps * (1 + (1 if ns > 1 else 0)),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "traffic": profiled_traffic(summary),
+                     "ncu_dram_throughput_pct": profiled_field(summary, "dram_throughput_pct"),
+                     "kernel": "decode_phase1_kernel", "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": kvb, "avg_launch_us": p1_avg * 1e6},
+        "clocks": clocks, "e2e": e2e, "wall_s_timed_region": wall,
+    }
+    if cpu_leg and world == 1 and rank == 0:
+        fields["cpu_baseline"] = cpu_baseline(case, budget_s=cpu_budget_s)
+    return fields, case
+
+
+# The headline workload is the largest single-GPU configuration; the others are
+# measured in the same run and reported under "per_config".
+HEADLINE = "gqa6_d256_vllm_decode"
+PER_CONFIG = ["llama3_8b_decode", "long_context_decode", "llama3_8b_decode_fp8", "llama3_8b_spec_decode_q4",
+              "mla_prefill_h16"]
+PER_CONFIG_STEPS = 300
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from paged_kv_gqa_table_gb300 import binding as B
+    B.load()
+    fields, case = measure_decode(args.workload, device, args.steps, args.warmup, world, rank,
+                                  e2e_leg=not args.skip_e2e, cpu_leg=not args.skip_cpu_baseline,
+                                  sample_clocks=rank == 0)
+    per_config = None
+    if world == 1 and not args.skip_per_config and args.workload == HEADLINE:
+        per_config = {}
+        steps = min(args.steps, PER_CONFIG_STEPS)
+        for name in PER_CONFIG:
+            if name == "mla_prefill_h16":
+                f = measure_mla(name, device, steps, args.warmup, e2e_leg=False,
+                                cpu_leg=not args.skip_cpu_baseline, cpu_budget_s=8.0)
+            else:
+                f, _ = measure_decode(name, device, steps, args.warmup, e2e_leg=False,
+                                      cpu_leg=not args.skip_cpu_baseline, cpu_budget_s=8.0)
+            per_config[name] = {k: f[k] for k in ("value", "unit", "us_per_step", "steps", "dtype", "roofline",
+                                                  "cpu_baseline", "gpu_launches", "config") if k in f}
+            if "hbm_frac_of_measured_peak" in f:
+                per_config[name]["hbm_frac_of_measured_peak"] = f["hbm_frac_of_measured_peak"]
     if rank == 0:
-        peak, peak_kind = measured_peaks()
-        p1_avg = float(np.mean(p1_ms)) * 1e-3
-        achieved = kvb / p1_avg / 1e9
-        line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(case),
-            "data": "synthetic (seeded N(0,1) K/V/q, uniform context lengths, random page permutation)",
-            "config": dict(workload_config(case, args.workload), parallelism="replicas" if world > 1 else "1 GPU",
-                           partition_tokens=P, num_splits=ns),
-            "us_per_step": t_max / args.steps * 1e6, "hbm_frac_of_measured_peak": value / peak,
-            "clocks": clocks, "e2e": e2e, "gpu_launches": launches,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak,
-                         "traffic": profiled_traffic(PROFILE_SUMMARIES.get(args.workload)),
-                         "kernel": "decode_phase1_kernel", "peak_source": peak_kind,
-                         "algorithmic_bytes_per_launch": kvb, "avg_launch_us": p1_avg * 1e6},
-            "wall_s_timed_region": wall,
-        }
-        if world == 1 and not args.skip_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(case)
+        line = {"metric": METRIC, "n_gpus": world, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None,
+                "data": "synthetic (seeded N(0,1) K/V/q, uniform context lengths, random page permutation)"}
+        line.update(fields)
+        line["config"] = dict(fields["config"], parallelism="replicas" if world > 1 else "1 GPU")
+        if per_config is not None:
+            line["per_config"] = per_config
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -553,15 +612,11 @@ def run_mla_reference(args):
     return 0
 
 
-def run_mla(args):
+def measure_mla(name, device, steps, warmup, e2e_leg=True, cpu_leg=True, cpu_budget_s=15.0, sample_clocks=False):
     """The MLA prefill workload (one call per step), same timing rules as the decode arm."""
     import torch
-    torch.cuda.set_device(0)
-    device = torch.device("cuda", 0)
-    from paged_kv_gqa_table_gb300 import binding as B
     from paged_kv_gqa_table_gb300 import synth, tensors
-    B.load()
-    case = synth.mla_case(seed=0, **synth.MLA_WORKLOADS[args.workload])
+    case = synth.mla_case(seed=0, **synth.MLA_WORKLOADS[name])
     flops = mla_flops(case)
     dev = tensors.upload_mla_case(case, device)
     T, H, Dc = case["total_q"], case["H"], case["Dc"]
@@ -572,36 +627,38 @@ def run_mla(args):
     flush = ColdL2(torch, device)
     stream = torch.cuda.current_stream(device)
     ev = lambda: torch.cuda.Event(enable_timing=True)
-    starts, stops = [ev() for _ in range(args.steps)], [ev() for _ in range(args.steps)]
+    starts, stops = [ev() for _ in range(steps)], [ev() for _ in range(steps)]
     step = lambda: tensors.mla_paged_prefill(case, dev, out, lse, workspace=ws, stream=stream, desc=desc)
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
-    except Exception:
-        pass
-    sampler = ClockSampler(uuid)
-    for _ in range(args.warmup):
+    sampler = None
+    if sample_clocks:
+        uuid = None
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            pass
+        sampler = ClockSampler(uuid)
+    for _ in range(warmup):
         flush()
         step()
     torch.cuda.synchronize(device)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(steps):
         flush()
         starts[i].record(stream)
         step()
         stops[i].record(stream)
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - wall0
-    clocks = sampler.stop()
+    clocks = sampler.stop() if sampler else None
     t = sum(a.elapsed_time(b) for a, b in zip(starts, stops)) * 1e-3
     e2e = None
-    if not args.skip_e2e:
+    if e2e_leg:
         host = {k: v.cpu().pin_memory() for k, v in dev.items()}
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         h2d = sum(x.numel() * x.element_size() for x in host.values())
         d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
-        n_e2e = max(3, min(args.steps, 30))
+        n_e2e = max(3, min(steps, 30))
         for i in range(n_e2e + 2):
             if i == 2:
                 torch.cuda.synchronize(device)
@@ -617,25 +674,38 @@ def run_mla(args):
         torch.cuda.synchronize(device)
         t_e2e = e0.elapsed_time(e1) * 1e-3
         e2e = {"value": flops * n_e2e / t_e2e / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": n_e2e}
+               "d2h_bytes_per_step": int(d2h), "steps": n_e2e, "copies_declared": True}
     pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
-    peak = float(pk.get("bf16_tflops", 1900.0))
-    achieved = flops / (t / args.steps) / 1e12
-    line = {"metric": MLA_METRIC, "value": achieved, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
-            "config": mla_workload_config(case, args.workload), "us_per_step": t / args.steps * 1e6,
-            "clocks": clocks, "e2e": e2e, "gpu_launches": 2 * args.steps,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": profiled_traffic(MLA_PROFILE_SUMMARY),
-                         "kernel": "mla_prefill_kernel",
-                         "timed": "whole step: mla_stage_kernel + mla_prefill_kernel (its programmatic dependent)",
-                         "peak_source": "measured" if pk else "fallback",
-                         "algorithmic_flops_per_launch": int(flops), "avg_launch_us": t / args.steps * 1e6},
-            "wall_s_timed_region": wall}
-    if not args.skip_cpu_baseline:
-        line["cpu_baseline"] = mla_cpu_baseline(case)
+    peak = float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    achieved = flops / (t / steps) / 1e12
+    fields = {"value": achieved, "unit": "TFLOP/s", "steps": steps, "warmup": warmup, "ms_per_step": t / steps * 1e3,
+              "us_per_step": t / steps * 1e6, "dtype": "bf16", "config": mla_workload_config(case, name),
+              "clocks": clocks, "e2e": e2e, "gpu_launches": 2 * steps,
+              "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                           "frac": achieved / peak, "traffic": profiled_traffic(MLA_PROFILE_SUMMARY),
+                           "ncu_tensor_pipe_pct": profiled_field(MLA_PROFILE_SUMMARY, "tensor_pipe_pct"),
+                           "kernel": "mla_prefill_kernel",
+                           "timed": "whole step: mla_stage_kernel + mla_prefill_kernel (its programmatic dependent)",
+                           "peak_source": "measured" if pk else "fallback",
+                           "algorithmic_flops_per_launch": int(flops), "avg_launch_us": t / steps * 1e6},
+              "wall_s_timed_region": wall}
+    if cpu_leg:
+        fields["cpu_baseline"] = mla_cpu_baseline(case, budget_s=cpu_budget_s)
+    return fields
+
+
+def run_mla(args):
+    import torch
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    from paged_kv_gqa_table_gb300 import binding as B
+    B.load()
+    fields = measure_mla(args.workload, device, args.steps, args.warmup, e2e_leg=not args.skip_e2e,
+                         cpu_leg=not args.skip_cpu_baseline, sample_clocks=True)
+    line = {"metric": MLA_METRIC, "n_gpus": 1, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "data": "synthetic (seeded N(0,1) bf16)"}
+    line.update(fields)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -646,11 +716,13 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama3_8b_decode",
+    ap.add_argument("--workload", default=HEADLINE,
                     choices=["llama3_8b_decode", "long_context_decode", "gqa6_d256_vllm_decode", "tiny",
                              "llama3_8b_decode_fp8", "llama3_8b_spec_decode_q4", "mla_prefill_h16"])
     ap.add_argument("--skip-e2e", action="store_true", help="omit the end-to-end leg (profiling runs)")
     ap.add_argument("--skip-cpu-baseline", action="store_true", help="omit the CPU oracle leg (profiling runs)")
+    ap.add_argument("--skip-per-config", action="store_true",
+                    help="measure the headline workload only (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -134,7 +134,8 @@ typedef struct {
 /* Text of a status code (static storage). */
 PKV_API const char* pkv_status_string(int status);
 
-/* ABI version of this header: 5 (4 had no plan reuse; 3 no device plan; 2 no q_len; 1 no kv_dtype / k_scale / v_scale). */
+/* ABI version of this header: 6 (5 had no pkv_static_scratch_error and staged MLA keys unpadded; 4 no plan
+ * reuse; 3 no device plan; 2 no q_len; 1 no kv_dtype / k_scale / v_scale). */
 PKV_API int pkv_version(void);
 
 /*
@@ -212,7 +213,10 @@ PKV_API int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_dec
  * desc, the same partition options and the same context_lens values, ordered
  * before this call on the GPU; the schedule kernel is not launched.  For the
  * layers of one decode step, which share context_lens: the first layer plans,
- * the others reuse the plan (each with its own q, caches and out).
+ * the others reuse the plan (each with its own q, caches and out).  The
+ * kernels check every reused work item against this call's extents, so a
+ * workspace holding anything else gives wrong output rows but no access
+ * outside this call's tensors and workspace.
  */
 PKV_API int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
                                const void* q, const void* k_cache, const void* v_cache,
@@ -273,11 +277,13 @@ typedef struct {
 
 /*
  * Bytes of scratch memory pkv_mla_paged_prefill needs: a 256-byte header,
- * then nnz staged key rows of 1152 bytes (ckv 512 + kpe 64 bf16), rounded
- * up to 256 bytes.  The workspace must be 256-byte aligned.  Word 0 of the
- * header collects device-side error bits (bit 0: a pipeline wait timed out;
- * bit 1: kv_indptr[batch] > nnz, so keys past nnz were not staged and the
- * result is unspecified); zero it once after allocating.
+ * then nnz + 128 * batch staged key rows of 1152 bytes (ckv 512 + kpe 64
+ * bf16; every sequence's keys start on a multiple of 128 rows, the rows in
+ * between are zero), rounded up to 256 bytes; no rows when nnz == 0.  The
+ * workspace must be 256-byte aligned.  Word 0 of the header collects
+ * device-side error bits (bit 0: a pipeline wait timed out; bit 1:
+ * kv_indptr[batch] > nnz, so keys past nnz were not staged and the result is
+ * unspecified); zero it once after allocating.
  */
 PKV_API int pkv_mla_workspace_size(const pkv_mla_desc* desc, size_t* bytes);
 
@@ -298,8 +304,11 @@ PKV_API int pkv_mla_workspace_size(const pkv_mla_desc* desc, size_t* bytes);
  * Tensors 16-byte aligned (lse 4-byte).  kv_len < q_len is a caller error
  * (rows with no visible key get out = 0, lse = -inf); page ids outside
  * [0, num_pages) are clamped to page 0 (no out-of-bounds access, result
- * unspecified).  Rows that kv_indices references must be finite: a row a
- * query does not see still enters the tensor-core products with weight 0.
+ * unspecified).  A sequence's own cached rows must be finite: a row one of
+ * its queries does not see still enters the tensor-core products with weight
+ * 0.  No other sequence's rows enter them ([MLA] loads a sequence's keys
+ * only, section "3. Pass 1"): a non-finite row in one sequence leaves the
+ * other sequences' outputs unchanged.
  * The q -> sequence map of [MLA]'s host loop is computed on the device from
  * qo_indptr.
  * Two kernels run: the first copies every referenced key row, in kv_indptr
@@ -328,11 +337,18 @@ PKV_API int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, 
  * The step's scratch (error word and split partials) lives in one
  * file-scope device array of PKV_STATIC_SCRATCH_BYTES (32 MiB), which
  * every GPU that loads libpkv reserves until the process exits.  This call
- * allocates nothing: no cudaMalloc, cudaFree or allocating library routine;
- * it clears the array's 256-byte error header with cudaMemsetAsync on
- * `stream` and then runs the regular entry point on the array.
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * Once every argument has passed the regular entry point's checks, it clears
+ * the array's 4-byte error word (word 0 of the header) with cudaMemsetAsync
+ * on `stream` and runs the regular entry point on the array; the rest of the
+ * header, including a device plan an earlier call left there, keeps the
+ * previous call's contents.  pkv_static_scratch_error reads the error word.
  *  - A problem whose workspace (pkv_decode_workspace_size) exceeds the array
  *    is refused with PKV_WORKSPACE_TOO_SMALL before anything is launched.
+ *  - PKV_DECODE_PLAN_READY is refused (PKV_INVALID_ARG) unless the previous
+ *    successful call of this entry point on the device was device-planned
+ *    (PKV_DECODE_DEVICE_PLAN) with the same desc and partition options; the
+ *    caller still keeps context_lens unchanged between the two.
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
  *  - Every call on a device shares the one array and it keeps the last call's
@@ -347,6 +363,16 @@ PKV_API int pkv_paged_decode_attention_static(const pkv_decode_desc* desc, const
                                       const void* q, const void* k_cache, const void* v_cache,
                                       const int32_t* block_table, const int32_t* context_lens,
                                       float scale, void* out, pkv_stream_t stream);
+
+/*
+ * Copies the static array's error word (the device-side error bits of the
+ * last pkv_paged_decode_attention_static call on the current device; bit 0:
+ * a pipeline wait timed out and the output is unspecified) into *dst, with
+ * cudaMemcpyAsync on `stream`, ordered after the work already on it.  dst is
+ * 4 bytes of device or host memory (pinned host memory keeps the copy
+ * asynchronous).  Allocates nothing.
+ */
+PKV_API int pkv_static_scratch_error(uint32_t* dst, pkv_stream_t stream);
 
 #ifdef __cplusplus
 }

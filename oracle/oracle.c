@@ -15,15 +15,16 @@
  *   [V2]  "paged_attention_v2_triton.py -- CCCL-derived Triton PagedAttention V2":
  *         _partition_attn_kernel (docstring "Algorithm"), _reduce_partitions_kernel,
  *         the key/value cache layout comments of its argument list.
+ *         Its launcher, paged_attention_v2_triton, also takes kv_cache_dtype,
+ *         k_scale and v_scale (and ignores them); the fp8 KV cache here reads
+ *         them the plainest way: cache bytes are OCP FP8 E4M3 values and
+ *         K = k_scale * fp8, V = v_scale * fp8.  The same launcher takes
+ *         alibi_slopes (ignored too); read as ALiBi's additive bias: the score
+ *         of key position t for query head h gains slopes[h] * (t - pos), pos
+ *         the query's own position -- zero there, decreasing linearly with
+ *         distance.
  *   [FD]  "koas-w.github.io flash-decode post": Decode_Paged_GQAAttention_Kernel,
  *         _flash_decode_partial_kernel, _flash_decode_combine_kernel.
- *         Its launcher also takes kv_cache_dtype, k_scale and v_scale (and ignores
- *         them); the fp8 KV cache here reads them the plainest way: cache bytes
- *         are OCP FP8 E4M3 values and K = k_scale * fp8, V = v_scale * fp8.
- *         It also takes alibi_slopes (ignored too); read as ALiBi's additive
- *         bias: the score of key position t for query head h gains
- *         slopes[h] * (t - pos), pos the query's own position -- zero there,
- *         decreasing linearly with distance.
  *   [MTD] Several query tokens per sequence (speculative / multi-token decode):
  *         the bottom-right causal rule of [MLA] section "3. Pass 1" applied to
  *         the [FD] cache layouts.  A sequence of context length n carries q_len

@@ -23,7 +23,8 @@ PKV_LAYOUT_NHD, PKV_LAYOUT_VLLM = 0, 1
 FUNCTIONS = [
     "pkv_status_string", "pkv_version", "pkv_plan_splits", "pkv_decode_workspace_size",
     "pkv_paged_decode_attention", "pkv_decode_partials", "pkv_combine", "pkv_validate_block_table",
-    "pkv_paged_decode_attention_static", "pkv_mla_workspace_size", "pkv_mla_paged_prefill",
+    "pkv_paged_decode_attention_static", "pkv_static_scratch_error", "pkv_mla_workspace_size",
+    "pkv_mla_paged_prefill",
 ]
 PKV_STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -77,6 +78,7 @@ def load():
     lib.pkv_combine.argtypes = [D, I, I, P, P, P, P, P, P]
     lib.pkv_validate_block_table.argtypes = [D, P, P, P, P]
     lib.pkv_paged_decode_attention_static.argtypes = [D, O, P, P, P, P, P, ctypes.c_float, P, P]
+    lib.pkv_static_scratch_error.argtypes = [P, P]
     lib.pkv_mla_workspace_size.argtypes = [ctypes.POINTER(pkv_mla_desc), ctypes.POINTER(SZ)]
     lib.pkv_mla_paged_prefill.argtypes = [ctypes.POINTER(pkv_mla_desc), P, P, P, P, P, P, P, ctypes.c_float,
                                           P, P, P, SZ, P]
@@ -188,6 +190,11 @@ def pkv_paged_decode_attention_static(desc, q, k_cache, v_cache, block_table, co
     _check("pkv_paged_decode_attention_static", load().pkv_paged_decode_attention_static(
         ctypes.byref(desc), _opt_ref(opts), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
         _ptr(context_lens), float(scale), _ptr(out), _stream(stream)))
+
+
+def pkv_static_scratch_error(dst, stream=None) -> None:
+    """Copies the static scratch's error word into dst (4 bytes, device or host memory)."""
+    _check("pkv_static_scratch_error", load().pkv_static_scratch_error(_ptr(dst), _stream(stream)))
 
 
 def make_mla_desc(total_q, batch, num_pages, nnz, num_heads=16, d_ckv=512, d_kpe=64) -> pkv_mla_desc:

@@ -10,6 +10,7 @@
 
 #include "internal.h"
 #include "pkv.h"
+#include "trace.h"
 
 using namespace pkv;
 
@@ -62,17 +63,7 @@ ColumnTiles column_tiles(const pkv_decode_desc* d) {
 }
 
 int current_sm_count(int* out) {
-    static int cache[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_CUDA_ERROR;
-    if (cache[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            return PKV_CUDA_ERROR;
-        cache[dev] = n;
-    }
-    *out = cache[dev];
-    return PKV_OK;
+    return current_device_sm_count(out) == cudaSuccess ? PKV_OK : PKV_CUDA_ERROR;
 }
 
 // FP8 caches at D = 128 whose query rows per KV head (G * q_len) fill at most
@@ -344,7 +335,7 @@ const char* pkv_status_string(int status) {
     }
 }
 
-int pkv_version(void) { return 5; }
+int pkv_version(void) { return 6; }
 
 int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms, int* num_splits,
                     int* partition_tokens) {
@@ -365,6 +356,19 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
                                const void* k_cache, const void* v_cache, const int32_t* block_table,
                                const int32_t* context_lens, float scale, void* out, void* workspace,
                                size_t workspace_bytes, pkv_stream_t stream) {
+    return pkv::paged_decode_impl(desc, opts, q, k_cache, v_cache, block_table, context_lens, scale, out, workspace,
+                                  workspace_bytes, stream, false);
+}
+
+}  // extern "C"
+
+// The decode step behind both decode entry points.  Every argument is checked
+// before anything is enqueued; with clear_err_word the workspace's error word
+// is then zeroed on `stream` ahead of the kernels.
+int pkv::paged_decode_impl(const pkv_decode_desc* desc, const pkv_decode_opts* opts, const void* q,
+                           const void* k_cache, const void* v_cache, const int32_t* block_table,
+                           const int32_t* context_lens, float scale, void* out, void* workspace,
+                           size_t workspace_bytes, pkv_stream_t stream, bool clear_err_word) {
     int st = check_desc(desc);
     if (st) return st;
     if (desc->B == 0) return PKV_OK;
@@ -386,6 +390,7 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
     if (opts) p.alibi = opts->alibi_slopes;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (clear_err_word && cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return PKV_CUDA_ERROR;
     p.out = out;
     p.err = reinterpret_cast<uint32_t*>(ws);
     uint8_t* parts = ws + kHeaderBytes;
@@ -398,6 +403,7 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
         // Every context is empty: the combine kernel writes the zero rows.
         CombineParams c{context_lens, nullptr, nullptr, nullptr, out, desc->B, desc->Hq, P, ns, 0, 0, desc->q_len,
                         nullptr};
+        TraceRange r("pkv::decode.combine");
         return launch_combine(desc->dtype, desc->D, c, s, false) == cudaSuccess ? PKV_OK : PKV_CUDA_ERROR;
     }
     long long grid = 0;
@@ -421,13 +427,20 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
         p.sched_cap = (int)plan_items(desc, ns);
         grid = std::min(plan_items(desc, ns), (long long)kDevicePlanCtasPerSm * sms);
         // An earlier call left the same plan in this workspace: reuse it.
-        if (!(opts->flags & PKV_DECODE_PLAN_READY) && launch_schedule(sp, s) != cudaSuccess) return PKV_CUDA_ERROR;
+        if (!(opts->flags & PKV_DECODE_PLAN_READY)) {
+            TraceRange r("pkv::decode.schedule");
+            if (launch_schedule(sp, s) != cudaSuccess) return PKV_CUDA_ERROR;
+        }
     }
     record(opts ? opts->phase1_event_start : nullptr, s);
-    if (dispatch_phase1(desc, p, mk, mv, s, grid) != cudaSuccess) return PKV_CUDA_ERROR;
+    {
+        TraceRange r("pkv::decode.phase1");
+        if (dispatch_phase1(desc, p, mk, mv, s, grid) != cudaSuccess) return PKV_CUDA_ERROR;
+    }
     record(opts ? opts->phase1_event_stop : nullptr, s);
     if (ns > 1) {
         // Programmatic dependent of phase 1 (unless an event sits between them).
+        TraceRange r("pkv::decode.combine");
         CombineParams c{context_lens, p.part_acc, p.part_m, p.part_l, out, desc->B, desc->Hq, P, ns, p.n_cap, 1,
                         desc->q_len, p.sched_hdr};
         if (launch_combine(desc->dtype, desc->D, c, s, !(opts && opts->phase1_event_stop)) != cudaSuccess)
@@ -435,6 +448,8 @@ int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opt
     }
     return PKV_OK;
 }
+
+extern "C" {
 
 int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts, const void* q, const void* k_cache,
                         const void* v_cache, const int32_t* block_table, const int32_t* context_lens, float scale,
@@ -476,7 +491,10 @@ int pkv_decode_partials(const pkv_decode_desc* desc, const pkv_decode_opts* opts
         mv = CUtensorMap{};
     }
     record(opts ? opts->phase1_event_start : nullptr, s);
-    if (dispatch_phase1(desc, p, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
+    {
+        TraceRange r("pkv::decode.phase1");
+        if (dispatch_phase1(desc, p, mk, mv, s) != cudaSuccess) return PKV_CUDA_ERROR;
+    }
     record(opts ? opts->phase1_event_stop : nullptr, s);
     return PKV_OK;
 }
@@ -491,6 +509,7 @@ int pkv_combine(const pkv_decode_desc* desc, int partition_tokens, int num_split
     if (!context_lens || !part_acc || !part_m || !part_l || !out || !aligned(part_acc, 16)) return PKV_INVALID_ARG;
     CombineParams c{context_lens, part_acc, part_m, part_l, out, desc->B, desc->Hq, partition_tokens, num_splits,
                     desc->max_context_len, 0, desc->q_len, nullptr};
+    TraceRange r("pkv::decode.combine");
     return launch_combine(desc->dtype, desc->D, c, reinterpret_cast<cudaStream_t>(stream), false) == cudaSuccess
                ? PKV_OK
                : PKV_CUDA_ERROR;
@@ -509,6 +528,12 @@ int pkv_validate_block_table(const pkv_decode_desc* desc, const int32_t* block_t
                : PKV_CUDA_ERROR;
 }
 
+// Staged key rows: every key once, each sequence padded to a multiple of
+// kMlaSeqAlign rows (at most kMlaSeqAlign - 1 zero rows per sequence).
+static long long mla_stage_rows(const pkv_mla_desc& d) {
+    return d.nnz > 0 ? (long long)d.nnz + (long long)kMlaSeqAlign * d.batch : 0;
+}
+
 static int check_mla_desc(const pkv_mla_desc* desc) {
     if (!desc) return PKV_INVALID_ARG;
     const pkv_mla_desc& d = *desc;
@@ -518,11 +543,12 @@ static int check_mla_desc(const pkv_mla_desc* desc) {
     if (d.total_q > 0 && d.batch == 0) return PKV_INVALID_ARG;
     if (d.num_heads != 16 || d.d_ckv != 512 || d.d_kpe != 64) return PKV_UNSUPPORTED;
     if ((long long)d.total_q * d.num_heads * d.d_ckv > (long long)1 << 40) return PKV_UNSUPPORTED;
+    if (mla_stage_rows(d) > INT_MAX) return PKV_UNSUPPORTED;
     return PKV_OK;
 }
 
 static size_t mla_workspace_bytes(const pkv_mla_desc& d) {
-    return kHeaderBytes + align256((size_t)d.nnz * kMlaStageRowBytes);
+    return kHeaderBytes + align256((size_t)mla_stage_rows(d) * kMlaStageRowBytes);
 }
 
 int pkv_mla_workspace_size(const pkv_mla_desc* desc, size_t* bytes) {
@@ -566,15 +592,18 @@ int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const vo
     p.batch = d.batch;
     p.num_pages = d.num_pages;
     p.nnz = d.nnz;
+    p.stage_rows = (int)mla_stage_rows(d);
     p.scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
     MlaMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     const cuuint64_t q_rows = (cuuint64_t)d.total_q * 16;
     st = encode_rows_map(&maps.q_nope, q_nope, 512, q_rows, 64, 128);
     if (st == PKV_OK) st = encode_rows_map(&maps.q_pe, q_pe, 64, q_rows, 64, 128);
-    if (st == PKV_OK && d.num_pages > 0 && d.nnz > 0) st = encode_rows_map(&maps.kv, p.stage, 576, (cuuint64_t)d.nnz, 64, 128);
-    if (st == PKV_OK && d.num_pages > 0 && d.nnz > 0) st = encode_rows_map(&maps.v, p.stage, 576, (cuuint64_t)d.nnz, 64, 32);
+    const cuuint64_t stage_rows = (cuuint64_t)p.stage_rows;
+    if (st == PKV_OK && d.num_pages > 0 && stage_rows > 0) st = encode_rows_map(&maps.kv, p.stage, 576, stage_rows, 64, 128);
+    if (st == PKV_OK && d.num_pages > 0 && stage_rows > 0) st = encode_rows_map(&maps.v, p.stage, 576, stage_rows, 64, 32);
     if (st != PKV_OK) return st;
+    TraceRange r("pkv::mla.prefill");
     return launch_mla_prefill(p, maps, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK
                                                                                               : PKV_CUDA_ERROR;
 }

@@ -40,8 +40,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
     if (live) n = row_context(p, bh, &empty);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!live) return;
-    const int P = p.sched_hdr ? p.sched_hdr[0] : p.P;   // the device plan's partition
-    const int ns = (n + P - 1) / P;
+    // the device plan's partition (checked: the header may be another problem's)
+    const int P = p.sched_hdr ? device_plan_partition(p.sched_hdr[0]) : p.P;
+    const int ns = (int)min(((long long)n + P - 1) / P, (long long)p.ns_stride);
     if (p.skip_single && ns <= 1) return;   // phase 1 wrote this row directly
     T* o = reinterpret_cast<T*>(p.out) + bh * D + lane * EPL;
     if (empty) {
@@ -113,8 +114,8 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(const CombineParams p
     bool empty = true;
     const int n = row_context(p, bh, &empty);
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int P = p.sched_hdr ? p.sched_hdr[0] : p.P;
-    const int ns = (n + P - 1) / P;
+    const int P = p.sched_hdr ? device_plan_partition(p.sched_hdr[0]) : p.P;
+    const int ns = (int)min(((long long)n + P - 1) / P, (long long)p.ns_stride);
     if (p.skip_single && ns <= 1) return;
     T* o = reinterpret_cast<T*>(p.out) + bh * D;
     if (empty) {

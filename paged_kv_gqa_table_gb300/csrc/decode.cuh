@@ -37,6 +37,7 @@
 #include <type_traits>
 
 #include "decode_common.cuh"
+#include "once.h"
 
 namespace pkv {
 
@@ -442,10 +443,23 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
     // the wait and see the header before the schedule kernel wrote it.  The
     // list entry is loaded with the item count (one round trip): every slot
     // below sched_cap is inside the list.
+    //
+    // With PKV_DECODE_PLAN_READY the list is whatever an earlier call left in
+    // the workspace.  Each item is checked against this launch's extents
+    // before it is used, so a plan of another problem can give wrong rows but
+    // never an access outside this call's tensors: P is kept a positive page
+    // multiple, sequence, KV head, row tile and split must lie inside the grid,
+    // the context length inside [0, n_cap], and a split must start inside it.
+    // A plan the schedule kernel made for this problem passes every check.
+    const int P = device_plan_partition(p.sched_hdr[0]);
     for (int it = blockIdx.x; it < p.sched_cap; it += gridDim.x) {
         const int4 e = p.sched_list[it];
         if (it >= p.sched_hdr[2]) break;
-        run_item(e.x, e.y & 0xFFFF, e.y >> 16, e.z, p.sched_hdr[0], e.w);
+        const int kvh = e.y & 0xFFFF, rt = e.y >> 16, n = clampi(e.w, 0, p.n_cap);
+        if (e.x < 0 || e.x >= p.B || kvh >= p.Hkv || rt >= p.RT || e.z < 0 || e.z >= p.NS ||
+            (e.z > 0 && (long long)e.z * P >= n))
+            continue;
+        run_item(e.x, kvh, rt, e.z, P, n);
         fence_proxy_async_smem();   // this item's generic writes to the ring before the next item's copies
         __syncthreads();            // every role is done with the ring, the barriers and the Q tile
         if (*abort_flag) break;     // a wait timed out (already reported): take no further item
@@ -480,16 +494,15 @@ cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, 
             return decode_phase1_kernel<T, LAYOUT, D, NT, GEN, SCHED>;
     }();
     const int smem = Tile::smem_bytes(NT);
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[kMaxDevices];
+    static std::mutex attr_mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
+    e = once_per_device(attr_set, attr_mu, dev, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
+    if (e != cudaSuccess) return e;
     if (SCHED) {   // programmatic dependent of the schedule kernel just enqueued
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);

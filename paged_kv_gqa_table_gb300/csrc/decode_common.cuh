@@ -33,6 +33,14 @@ constexpr int kPageTokens = 16;
 
 __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
+// Partition of a device plan read back from a workspace header, kept a page
+// multiple in [one page, 2^30]: a valid plan is unchanged (its partition is a
+// page multiple of at least four pages), and a header another problem left
+// behind cannot make a split count or a token index overflow.
+__device__ __forceinline__ int device_plan_partition(int P) {
+    return clampi(P, kPageTokens, 1 << 30) / kPageTokens * kPageTokens;
+}
+
 // Byte offset of 16-byte chunk c (c < D/8) of token row t in an NHD slice
 // written by 64-element TMA boxes with 128-byte swizzle.
 template <int BS>

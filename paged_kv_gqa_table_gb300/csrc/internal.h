@@ -2,6 +2,7 @@
 #pragma once
 
 #include "decode.cuh"
+#include "pkv.h"
 
 namespace pkv {
 
@@ -60,16 +61,21 @@ struct MlaParams {
     const int32_t* kv_indices;     // [kv_indptr[batch]]
     __nv_bfloat16* out;            // [total_q][16][512]
     float* lse;                    // [total_q][16]
-    uint8_t* stage;                // [nnz][1152]: ckv row | kpe row of key r in kv_indptr order
+    uint8_t* stage;                // [stage_rows][1152]: ckv row | kpe row of each key, per sequence
+                                   // padded with zero rows to a multiple of 128 rows
     uint32_t* err;                 // header word 0
     int total_q, batch, num_pages, nnz;
+    int stage_rows;                // rows of `stage`: nnz + 128 * batch (0 without keys)
     float scale_log2;              // sm_scale * log2(e)
 };
 
 constexpr int kMlaStageRowBytes = (512 + 64) * 2;
+// Each sequence's staged keys start on a multiple of this many rows, so no
+// 128-row key block of one sequence reaches another's rows.
+constexpr int kMlaSeqAlign = 128;
 
 // TMA descriptors of the MLA operands: q_nope / q_pe as 2-D {512 | 64,
-// total_q * 16} tensors and the staged keys as {576, nnz}, with {64, 128}
+// total_q * 16} tensors and the staged keys as {576, stage_rows}, with {64, 128}
 // boxes (kv: K chunks) or {64, 32} boxes (v: V chunk blocks), all with
 // 128-byte swizzle.  kv and v are unused (zero) when the pool is empty.
 struct MlaMaps {
@@ -77,6 +83,13 @@ struct MlaMaps {
 };
 
 cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStream_t stream);
+
+// The decode step of pkv_paged_decode_attention (api.cu); with clear_err_word
+// it zeroes the workspace's error word on the stream once every argument has
+// passed its checks, before the first kernel.
+int paged_decode_impl(const pkv_decode_desc* desc, const pkv_decode_opts* opts, const void* q, const void* k_cache,
+                      const void* v_cache, const int32_t* block_table, const int32_t* context_lens, float scale,
+                      void* out, void* workspace, size_t workspace_bytes, pkv_stream_t stream, bool clear_err_word);
 
 // after_phase1: launched as a programmatic dependent of the phase-1 kernel just
 // enqueued on the same stream (its prologue overlaps phase 1's tail).

@@ -28,11 +28,13 @@
 // Page size 1 makes every key its own page.  Gathering 128-byte row pieces
 // per tile (up to ~100 tiles read each key) keeps too few bytes in flight
 // per TMA operation, so mla_stage_kernel first copies each referenced row
-// (ckv | kpe, 1152 bytes) once into a workspace in kv_indptr order; the
-// attention kernel then loads 128 consecutive staged rows per 16 KB box.
-// Rows of a box past the tile's keys are the next sequence's keys (finite
-// by contract), zero rows the stage kernel wrote past the last key, or
-// out-of-range rows TMA fills with zeros; they are masked in the softmax.
+// (ckv | kpe, 1152 bytes) once into a workspace, sequence by sequence, each
+// sequence padded with zero rows to a multiple of 128 rows; the attention
+// kernel then loads 128 consecutive staged rows per 16 KB box.  A box never
+// leaves its sequence's staged rows, as the page's kernel never loads a key
+// outside [kv_pages_start, kv_pages_end): rows of a box past the tile's
+// keys are the sequence's own later keys or zero rows, masked in the
+// softmax, so another sequence's cache rows cannot reach this output.
 //
 // Warps: 0 = producer (one thread issues the Q boxes and then, after the
 // staging grid has completed, the key boxes); 1 = TMEM allocator and
@@ -65,33 +67,53 @@ constexpr float kLazyRescale = 8.f;     // log2 units
 }  // namespace mla
 
 
-// staged[r] = ckv[kv_indices[r]] | kpe[kv_indices[r]] for r < min(kv_indptr[batch], nnz),
-// then zeros for the next 128 rows (within nnz), which a box that starts at a
-// sequence's last keys can reach.  One warp per row.
+// Staged rows of sequence b: its kv_len keys rounded up to kMlaSeqAlign rows.
+__device__ __forceinline__ int mla_padded_len(const MlaParams& p, int b) {
+    const int kv_len = max(0, p.kv_indptr[b + 1] - p.kv_indptr[b]);
+    return (kv_len + kMlaSeqAlign - 1) / kMlaSeqAlign * kMlaSeqAlign;
+}
+
+// Sequence b's keys are staged at rows [off_b, off_b + kv_len_b), off_b the
+// sum of the earlier sequences' padded lengths: staged[off_b + j] =
+// ckv[kv_indices[kv_indptr[b] + j]] | kpe[...], then zero rows up to the next
+// multiple of kMlaSeqAlign, so a 128-row box of one sequence never reaches the
+// next sequence's keys.  Keys whose kv_indices entry lies past nnz are staged
+// as zero rows (and reported); rows past stage_rows are not written (their
+// boxes read the tensor map's zero fill).  One warp per row; each warp walks
+// the sequences forward as its rows advance.
 __global__ void __launch_bounds__(256) mla_stage_kernel(const MlaParams p) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int total = p.kv_indptr[p.batch];
-    const int rows = min(total, p.nnz);
-    const int zero_end = total > p.nnz ? rows : (rows > p.nnz - 128 ? p.nnz : max(rows, 0) + 128);
-    if (blockIdx.x == 0 && threadIdx.x == 0 && total > p.nnz) atomicOr(p.err, 2u);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.kv_indptr[p.batch] > p.nnz) atomicOr(p.err, 2u);
     const int lane = threadIdx.x & 31;
-    const int warps = gridDim.x * (blockDim.x >> 5);
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < zero_end; r += warps) {
+    int b = 0;
+    long long off = 0;   // first staged row of sequence b
+    int pad = p.batch > 0 ? mla_padded_len(p, 0) : 0;
+    for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < p.stage_rows;
+         r += warps) {
+        while (b < p.batch && r >= off + pad) {
+            off += pad;
+            if (++b < p.batch) pad = mla_padded_len(p, b);
+        }
+        if (b >= p.batch) break;
+        const int j = (int)(r - off);
+        const int kv0 = p.kv_indptr[b];
+        const int kv_len = p.kv_indptr[b + 1] - kv0;
         uint4* dst = reinterpret_cast<uint4*>(p.stage + (size_t)r * kMlaStageRowBytes);
-        uint4 a = zero, b = zero, c = zero;
-        if (r < rows) {
-            int pg = p.kv_indices[r];
+        uint4 a = zero, c = zero, d = zero;
+        if (j < kv_len && kv0 + j >= 0 && kv0 + j < p.nnz) {
+            int pg = p.kv_indices[kv0 + j];
             pg = (pg < 0 || pg >= p.num_pages) ? 0 : pg;
             const uint4* ck = reinterpret_cast<const uint4*>(p.ckv + (size_t)pg * mla::kDc);
             const uint4* kp = reinterpret_cast<const uint4*>(p.kpe + (size_t)pg * mla::kDr);
             a = __ldg(ck + lane);
-            b = __ldg(ck + 32 + lane);
-            if (lane < 8) c = __ldg(kp + lane);
+            c = __ldg(ck + 32 + lane);
+            if (lane < 8) d = __ldg(kp + lane);
         }
         dst[lane] = a;
-        dst[32 + lane] = b;
-        if (lane < 8) dst[64 + lane] = c;
+        dst[32 + lane] = c;
+        if (lane < 8) dst[64 + lane] = d;
     }
 }
 
@@ -122,7 +144,9 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
     // Row tile -> (sequence, first token).  Within a sequence the tiles are
     // visited last-token-first so the tiles with the most keys start first.
-    int b = -1, i0 = 0;
+    // kv0 = the sequence's first staged row (the padded offsets of the earlier
+    // sequences).
+    int b = -1, i0 = 0, kv0 = 0;
     for (int bb = 0, acc = 0; bb < p.batch; ++bb) {
         const int nt = (p.qo_indptr[bb + 1] - p.qo_indptr[bb] + kTok - 1) / kTok;
         if (tile < acc + nt) {
@@ -131,14 +155,15 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
             break;
         }
         acc += nt;
+        kv0 += mla_padded_len(p, bb);
     }
     if (b < 0) return;
     const int q0 = p.qo_indptr[b], q_len = p.qo_indptr[b + 1] - q0;
-    const int kv0 = p.kv_indptr[b], kv_len = p.kv_indptr[b + 1] - kv0;
+    const int kv_len = p.kv_indptr[b + 1] - p.kv_indptr[b];
     const int prefix = kv_len - q_len;
     const int ntok = min(kTok, q_len - i0);
     // keys any row of the tile may see (none when the pool or the staging area is empty)
-    const int n_keys = (p.num_pages > 0 && p.nnz > 0) ? max(0, min(kv_len, prefix + i0 + ntok)) : 0;
+    const int n_keys = (p.num_pages > 0 && p.stage_rows > 0) ? max(0, min(kv_len, prefix + i0 + ntok)) : 0;
     const int J = (n_keys + kKeys - 1) / kKeys;
 
     if (J == 0) {   // no visible key (empty KV): out = 0, lse = -inf
@@ -418,23 +443,26 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 }
 
 cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStream_t stream) {
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[kMaxDevices];
+    static std::mutex attr_mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(mla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
+    e = once_per_device(attr_set, attr_mu, dev, [] {
+        return cudaFuncSetAttribute(mla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    mla::kSmemBytes);
+    });
+    if (e != cudaSuccess) return e;
     const long long tiles = (long long)(p.total_q + mla::kTok - 1) / mla::kTok + p.batch;
     if (tiles <= 0) return cudaSuccess;
-    const bool staged = p.num_pages > 0;
+    const bool staged = p.num_pages > 0 && p.stage_rows > 0;
     if (staged) {
-        // one warp per row of the nnz (+128 zero) rows, capped at 16 waves of 8-warp CTAs
-        const long long want = ((long long)p.nnz + 128 + 7) / 8;
-        mla_stage_kernel<<<(unsigned)std::min<long long>(want, 152LL * 8 * 16), 256, 0, stream>>>(p);
+        // one warp per staged row, capped at 16 waves of 8-warp CTAs per SM
+        int sms = 0;
+        e = device_sm_count(dev, &sms);
+        if (e != cudaSuccess) return e;
+        const long long want = ((long long)p.stage_rows + 7) / 8;
+        mla_stage_kernel<<<(unsigned)std::min<long long>(want, (long long)sms * 8 * 16), 256, 0, stream>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

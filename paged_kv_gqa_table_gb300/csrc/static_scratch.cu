@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "internal.h"
 #include "pkv.h"
 
 namespace {
@@ -19,21 +20,46 @@ constexpr size_t kStaticScratchBytes = PKV_STATIC_SCRATCH_BYTES;   // 32 MiB
 
 static __device__ __align__(256) unsigned char g_scratch[kStaticScratchBytes];
 
-// Device address of g_scratch, looked up once per device with that device
-// current.  The host symbol itself is only a stand-in and is never handed to
-// a kernel.
-int scratch_address(void** out) {
-    static std::mutex mu;
-    static void* addr[64] = {};
+// Host-side record of what the last call on each device left in the array:
+// whether it holds a device plan, and for which problem (description and
+// partition options).  A call that reuses a plan (PKV_DECODE_PLAN_READY) is
+// refused unless the previous call on the device made one for the same
+// problem; the record cannot see context_lens, which the caller keeps equal.
+struct LastCall {
+    bool device_plan = false;
+    pkv_decode_desc desc{};
+    int partition_tokens = 0, num_splits = 0;
+};
+
+struct DeviceState {
+    void* addr = nullptr;   // device address of g_scratch
+    LastCall last;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[pkv::kMaxDevices];
+
+bool same_problem(const pkv_decode_desc& a, const pkv_decode_desc& b) {
+    return a.B == b.B && a.Hq == b.Hq && a.Hkv == b.Hkv && a.D == b.D && a.block_size == b.block_size &&
+           a.max_blocks_per_seq == b.max_blocks_per_seq && a.num_blocks == b.num_blocks &&
+           a.max_context_len == b.max_context_len && a.sum_context_len == b.sum_context_len &&
+           a.dtype == b.dtype && a.layout == b.layout && a.x_pack == b.x_pack && a.kv_dtype == b.kv_dtype &&
+           a.k_scale == b.k_scale && a.v_scale == b.v_scale && a.q_len == b.q_len;
+}
+
+// The current device's state, with g_scratch's device address looked up
+// (once per device, with that device current).  The host symbol g_scratch is
+// only a stand-in and is never handed to a kernel.  Call with g_mu held.
+int device_state(DeviceState** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_CUDA_ERROR;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= pkv::kMaxDevices) return PKV_CUDA_ERROR;
+    DeviceState& d = g_dev[dev];
+    if (!d.addr) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return PKV_CUDA_ERROR;
-        addr[dev] = p;
+        d.addr = p;
     }
-    *out = addr[dev];
+    *out = &d;
     return PKV_OK;
 }
 
@@ -51,16 +77,42 @@ int pkv_paged_decode_attention_static(const pkv_decode_desc* desc, const pkv_dec
     if (st) return st;
     if (need > kStaticScratchBytes) return PKV_WORKSPACE_TOO_SMALL;
     if (desc->B == 0) return PKV_OK;
-    void* scratch = nullptr;
-    st = scratch_address(&scratch);
+    const int flags = opts ? opts->flags : 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* d = nullptr;
+    st = device_state(&d);
     if (st) return st;
-    // The header's error word must start at zero (the rest of the header may
-    // hold a device plan an earlier call made for reuse); the partials are
-    // fully written by phase 1 before phase 2 reads them, so they need no clearing.
-    if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return PKV_CUDA_ERROR;
-    return pkv_paged_decode_attention(desc, opts, q, k_cache, v_cache, block_table, context_lens, scale, out,
-                                      scratch, kStaticScratchBytes, stream);
+    if ((flags & PKV_DECODE_PLAN_READY) &&
+        !(d->last.device_plan && same_problem(d->last.desc, *desc) &&
+          d->last.partition_tokens == opts->partition_tokens && d->last.num_splits == opts->num_splits))
+        return PKV_INVALID_ARG;
+    // Every argument is checked before the array is touched; the error word is
+    // then cleared on the stream (the rest of the header may hold a device plan
+    // an earlier call made for reuse); the partials are fully written by phase
+    // 1 before phase 2 reads them, so they need no clearing.
+    st = pkv::paged_decode_impl(desc, opts, q, k_cache, v_cache, block_table, context_lens, scale, out, d->addr,
+                                kStaticScratchBytes, stream, true);
+    if (st == PKV_OK) {
+        d->last.device_plan = (flags & PKV_DECODE_DEVICE_PLAN) != 0;
+        d->last.desc = *desc;
+        d->last.partition_tokens = opts ? opts->partition_tokens : 0;
+        d->last.num_splits = opts ? opts->num_splits : 0;
+    } else if (st == PKV_CUDA_ERROR) {
+        d->last = LastCall{};   // something may have been enqueued: assume the plan is gone
+    }
+    return st;
+}
+
+int pkv_static_scratch_error(uint32_t* dst, pkv_stream_t stream) {
+    if (!dst) return PKV_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* d = nullptr;
+    const int st = device_state(&d);
+    if (st) return st;
+    return cudaMemcpyAsync(dst, d->addr, sizeof(uint32_t), cudaMemcpyDefault,
+                           reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_CUDA_ERROR;
 }
 
 }  // extern "C"

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_function(B):
 
 
 def test_version_and_status_strings(B):
-    assert B.pkv_version() == 5
+    assert B.pkv_version() == 6
     assert B.status_string(0) == "ok"
     assert B.status_string(5) == "bad block table"
     assert B.status_string(99) == "unknown status"
@@ -233,9 +233,12 @@ def test_empty_batch_is_a_no_op(B):
 
 def test_mla_workspace_size_and_argument_checks(B):
     al = lambda x: (x + 255) // 256 * 256
-    for nnz in (0, 1, 8070, 123457):
-        d = B.make_mla_desc(2866, 8, 9000, nnz)
-        assert B.pkv_mla_workspace_size(d) == 256 + al(nnz * 1152)
+    # every sequence's staged keys start on a multiple of 128 rows: room for
+    # nnz rows plus at most 127 zero rows per sequence (none without keys)
+    for nnz, batch in ((0, 8), (1, 1), (8070, 8), (123457, 300)):
+        d = B.make_mla_desc(2866, batch, 9000, nnz)
+        rows = nnz + 128 * batch if nnz > 0 else 0
+        assert B.pkv_mla_workspace_size(d) == 256 + al(rows * 1152)
     for bad in (dict(nnz=-1), dict(total_q=-1), dict(num_pages=-3)):
         kw = dict(total_q=100, batch=2, num_pages=50, nnz=40)
         kw.update(bad)

@@ -69,3 +69,27 @@ def test_l2_note_states_the_cold_clean_flush():
     cfg = bench.workload_config(case, "tiny")
     assert cfg["l2"] == bench.L2_NOTE and "256 MiB written" in cfg["l2"] and "read" in cfg["l2"]
     assert bench.workload_config(case, "tiny", flushed=False, accumulate="fp64")["accumulate"] == "fp64"
+
+
+def test_headline_is_the_largest_single_gpu_decode_configuration():
+    # The default workload (no --workload) is the GQA-6, D = 256 vLLM-layout
+    # step, the largest decode configuration; the others are per_config lines.
+    from paged_kv_gqa_table_gb300 import synth
+    assert bench.HEADLINE == "gqa6_d256_vllm_decode"
+    sizes = {n: synth.kv_bytes(synth.decode_case(seed=0, **synth.WORKLOADS[n]))
+             for n in ("llama3_8b_decode", "long_context_decode", "gqa6_d256_vllm_decode")}
+    assert max(sizes, key=sizes.get) == bench.HEADLINE
+    assert {"llama3_8b_decode", "long_context_decode", "mla_prefill_h16"} <= set(bench.PER_CONFIG)
+
+
+def test_profiled_field_follows_the_source_hash(tmp_path):
+    files = ["decode.cuh"]
+    good = tmp_path / "good.md"
+    good.write_text("source_files: %s\nsource_sha256: %s\ndram_bytes_per_launch: 1\ndram_throughput_pct: 87.5\n"
+                    % (" ".join(files), bench.kernel_source_hash(files)))
+    assert bench.profiled_field(str(good), "dram_throughput_pct") == 87.5
+    assert bench.profiled_field(str(good), "tensor_pipe_pct") is None
+    stale = tmp_path / "stale.md"
+    stale.write_text("source_files: decode.cuh\nsource_sha256: 0\ndram_bytes_per_launch: 1\n"
+                     "dram_throughput_pct: 87.5\n")
+    assert bench.profiled_field(str(stale), "dram_throughput_pct") is None
