@@ -143,6 +143,11 @@ class ClockSampler:
             self.t.start()
         except OSError:
             self.proc = None
+        # nvidia-smi's start-up (driver queries) can hold up kernel launches for
+        # milliseconds: let it reach its first sample before anything is timed.
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < 10.0 and self.proc.poll() is None:
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:

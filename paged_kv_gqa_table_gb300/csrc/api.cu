@@ -600,7 +600,7 @@ int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const vo
     st = encode_rows_map(&maps.q_nope, q_nope, 512, q_rows, 64, 128);
     if (st == PKV_OK) st = encode_rows_map(&maps.q_pe, q_pe, 64, q_rows, 64, 128);
     const cuuint64_t stage_rows = (cuuint64_t)p.stage_rows;
-    if (st == PKV_OK && d.num_pages > 0 && stage_rows > 0) st = encode_rows_map(&maps.kv, p.stage, 576, stage_rows, 64, 128);
+    if (st == PKV_OK && d.num_pages > 0 && stage_rows > 0) st = encode_rows_map(&maps.kv, p.stage, 576, stage_rows, 64, 64);
     if (st == PKV_OK && d.num_pages > 0 && stage_rows > 0) st = encode_rows_map(&maps.v, p.stage, 576, stage_rows, 64, 32);
     if (st != PKV_OK) return st;
     TraceRange r("pkv::mla.prefill");

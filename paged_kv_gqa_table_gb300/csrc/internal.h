@@ -75,9 +75,10 @@ constexpr int kMlaStageRowBytes = (512 + 64) * 2;
 constexpr int kMlaSeqAlign = 128;
 
 // TMA descriptors of the MLA operands: q_nope / q_pe as 2-D {512 | 64,
-// total_q * 16} tensors and the staged keys as {576, stage_rows}, with {64, 128}
-// boxes (kv: K chunks) or {64, 32} boxes (v: V chunk blocks), all with
-// 128-byte swizzle.  kv and v are unused (zero) when the pool is empty.
+// total_q * 16} tensors with {64, 128} boxes, and the staged keys as {576,
+// stage_rows}, with {64, 64} boxes (kv: K chunks, one CTA's half of a key
+// block) or {64, 32} boxes (v: V chunk blocks), all with 128-byte swizzle.
+// kv and v are unused (zero) when the pool is empty.
 struct MlaMaps {
     CUtensorMap q_nope, q_pe, kv, v;
 };

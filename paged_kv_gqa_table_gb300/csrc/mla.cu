@@ -1,4 +1,5 @@
-// mla.cu -- MLA paged causal prefill on sm_103a tensor cores (tcgen05 + TMEM).
+// mla.cu -- MLA paged causal prefill on sm_103a tensor cores (tcgen05 + TMEM),
+// one CTA pair (cta_group::2) per tile.
 //
 // Problem (kernelindex.com "flashinfer gemini-2.5-pro triton xvhq2i",
 // mla_paged_prefill_causal_h16_ckv512_kpe64_ps1, sections 2-4): for query
@@ -9,40 +10,54 @@
 //
 // The page computes this in two passes (an LSE pass, then a pass that
 // recomputes every logit); here it is one online-softmax pass on the tensor
-// cores, with the 16 heads of 8 query tokens stacked into one 128-row tile
+// cores, with the 16 heads of 16 query tokens stacked into one 256-row tile
 // that shares each gathered key row.
 //
-// CTA = (sequence, 8-token row tile, half of the 512 output columns).  TMEM
-// (512 columns x 128 lanes, fp32) holds the CTA's 256 output columns O, one
-// S tile of 128 keys and two bf16 P tiles (the A operand of O += P.V, read
-// from TMEM), which is why the output is split across two CTAs that each
-// recompute S.  Shared memory holds the whole Q tile (9 chunks of 128 rows x
-// 64 bf16 = 144 KB, one 2-D TMA box each) and a 5-stage ring of 16 KB
-// chunks, all in the 128-byte-swizzled layout the UMMA descriptors describe.
-// Per block of 128 keys the ring carries 9 K chunks (128 keys x 64 columns,
-// the K-major B operand of S = Q.K^T, N = 128) and 4 V chunks (32 keys x the
-// CTA's 256 output columns as four 64-column blocks 4 KB apart, the MN-major
-// B operand of O += P.V, N = 256).  Both are cut from the same staged ckv
-// rows.
+// Cluster = a CTA pair = (sequence, 16-token row tile, half of the 512 output
+// columns).  CTA r of the pair holds rows 128r .. 128r + 127 (tokens 8r ..
+// 8r + 7 of the tile): its Q rows in shared memory (9 chunks of 128 rows x 64
+// bf16 = 144 KB, one 2-D TMA box each) and, in its TMEM (512 columns), those
+// rows' 256 output columns O and two fp32 S buffers of 128 keys; a block's
+// bf16 P is written over its scores (the TMEM A operand of O += P.V), so the
+// tensor core computes the next block's scores into the other buffer while
+// the softmax warps work.  One thread of CTA 0 issues every MMA for both
+// (M = 256): B operands are split between the CTAs, so each SM loads half of
+// every key block -- per 128 keys, 9 K sub-chunks of 64 keys x 64 columns
+// (its half of the N = 128 keys of S = Q.K^T) and 4 V sub-chunks of 32 keys x
+// 128 output columns (its half of the N = 256 columns of O += P.V), 8 KB each,
+// two per 16 KB slot of a 5-slot ring, in the 128-byte-swizzled layout of the
+// UMMA descriptors.  A one-SM tile would read all of every chunk; the pair
+// halves the L2-to-SM bytes per MMA.  O in TMEM is why the two halves of the
+// output are separate pairs that each compute S (1.53x the algorithmic
+// tensor work).
 //
 // Page size 1 makes every key its own page.  Gathering 128-byte row pieces
 // per tile (up to ~100 tiles read each key) keeps too few bytes in flight
 // per TMA operation, so mla_stage_kernel first copies each referenced row
 // (ckv | kpe, 1152 bytes) once into a workspace, sequence by sequence, each
 // sequence padded with zero rows to a multiple of 128 rows; the attention
-// kernel then loads 128 consecutive staged rows per 16 KB box.  A box never
-// leaves its sequence's staged rows, as the page's kernel never loads a key
-// outside [kv_pages_start, kv_pages_end): rows of a box past the tile's
-// keys are the sequence's own later keys or zero rows, masked in the
-// softmax, so another sequence's cache rows cannot reach this output.
+// kernel then loads consecutive staged rows per box.  A box never leaves its
+// sequence's staged rows, as the page's kernel never loads a key outside
+// [kv_pages_start, kv_pages_end): rows of a box past the tile's keys are the
+// sequence's own later keys or zero rows, masked in the softmax, so another
+// sequence's cache rows cannot reach this output.
 //
-// Warps: 0 = producer (one thread issues the Q boxes and then, after the
-// staging grid has completed, the key boxes); 1 = TMEM allocator and
-// single-thread MMA issuer;
-// 2..5 = softmax (one thread per row / TMEM lane): online max/sum in log2
+// Synchronisation.  Both CTAs' TMA copies of a chunk complete on CTA 0's
+// `full` barrier (cta_group::2 loads; CTA 0's producer expects the bytes of
+// both), which CTA 0's MMA thread waits on.  Its commits arrive on the
+// barriers of both CTAs (multicast): `empty` (a ring slot is free),
+// `s_full` (scores of a block in an S buffer), `p_free` (O += P.V of a block
+// done), `mma_done`.  The softmax warps of both CTAs arrive on CTA 0's
+// `p_full` (P written over the scores), one elected lane per warp.
+//
+// Warps: 0 = producer (one thread issues the Q boxes and the key boxes, the
+// latter after the staging grid has completed); 1 = TMEM allocation, then
+// CTA 0's MMA issuer; 2..9 = softmax, two warps per TMEM lane quadrant, each
+// taking 64 of a block's 128 keys for its 32 rows: online max/sum in log2
 // units, lazy O rescaling (only when the running max grows by more than 8,
 // i.e. a factor 256), P stored to TMEM as bf16, final O / l and the base-2
-// LSE.
+// LSE.  Every wait is bounded; both CTAs meet at a cluster barrier before the
+// TMEM is freed.
 #include <algorithm>
 
 #include "internal.h"
@@ -52,18 +67,30 @@ namespace pkv {
 
 namespace mla {
 constexpr int kHeads = 16, kDc = 512, kDr = 64;
-constexpr int kTok = 8;                 // query tokens per row tile
-constexpr int kRows = kTok * kHeads;    // 128 TMEM lanes
-constexpr int kKeys = 128;              // keys per block
-constexpr int kChunk = kRows * 64 * 2;  // 16 KB: 128 rows x 64 bf16
-constexpr int kQChunks = 9;             // 8 x ckv + 1 x kpe
-constexpr int kVChunks = 4;             // 128 keys / 32 keys per V chunk
+constexpr int kTok = 8;                   // query tokens per CTA
+constexpr int kPairTok = 2 * kTok;        // query tokens per CTA pair (row tile)
+constexpr int kRows = kTok * kHeads;      // 128 TMEM lanes per CTA
+constexpr int kKeys = 128;                // keys per block: N of S over the pair
+constexpr int kHalfKeys = kKeys / 2;      // keys of a block each CTA loads for S
+constexpr int kQChunk = kRows * 64 * 2;   // 16 KB: 128 rows x 64 bf16
+constexpr int kQChunks = 9;               // 8 x ckv + 1 x kpe
+constexpr int kSub = 8192;                // K sub-chunk: 64 keys x 64 bf16; V sub-chunk: 32 keys x 128 bf16
+constexpr int kSlot = 2 * kSub;           // ring slot: two sub-chunks
+constexpr int kKSlots = 5;                // per block: K columns 0-127, ..., 384-511, then kpe 512-575 alone
+constexpr int kVSlots = 2;                // per block: keys 0-63, 64-127 of this CTA's 128 output columns
 constexpr int kStages = 5;
-constexpr int kThreads = 192;
-constexpr int kBars = 2 * kStages + 8;
-constexpr int kSmemBytes = 1024 + (kQChunks + kStages) * kChunk + kBars * 8 + 16;
-constexpr uint32_t kColS = 256, kColP = 384;   // TMEM columns: O [0,256), S [256,384), P x2 [384,512)
-constexpr float kLazyRescale = 8.f;     // log2 units
+constexpr int kSoftmaxWarps = 8;          // two per TMEM lane quadrant, each 64 of a block's 128 keys
+constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
+constexpr int kBars = 2 * kStages + kQChunks + 14;
+constexpr int kRedBytes = 2 * kRows * 4;   // row max / row sum exchange: [key half][row]
+constexpr int kSmemBytes = 1024 + kQChunks * kQChunk + kStages * kSlot + kRedBytes + kBars * 8 + 16;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+// TMEM columns: O [0,256), S buffers [256,384) and [384,512); block j's scores go
+// to buffer j % 2, and its bf16 P is written over them in place (key half h at
+// columns 64h .. 64h + 31 of the buffer, where that half's scores were).
+constexpr uint32_t kColS = 256;
+constexpr float kLazyRescale = 8.f;       // log2 units
+constexpr uint16_t kBothCtas = 3;         // multicast mask of the pair
 }  // namespace mla
 
 
@@ -117,59 +144,82 @@ __global__ void __launch_bounds__(256) mla_stage_kernel(const MlaParams p) {
     }
 }
 
-__global__ void __launch_bounds__(mla::kThreads, 1)
+// One value swapped between the two softmax warps of a TMEM quadrant through
+// shared memory: xa completes when both wrote, xb when both read (its wait
+// comes before the next write).  x counts the swaps done (the phase).  False
+// if a wait timed out.
+__device__ __forceinline__ bool mla_swap(uint64_t* xa, uint64_t* xb, int& x, float* mine_slot,
+                                         const float* peer_slot, float mine, float& theirs) {
+    if (x >= 1 && !mbar_wait(xb, (x - 1) & 1)) return false;   // the partner read the last value
+    *mine_slot = mine;
+    mbar_arrive(xa);
+    if (!mbar_wait(xa, x & 1)) return false;
+    theirs = *peer_slot;
+    mbar_arrive(xb);
+    ++x;
+    return true;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     mla_prefill_kernel(const MlaParams p, const __grid_constant__ CUtensorMap tm_qn,
-                       const __grid_constant__ CUtensorMap tm_qp, const __grid_constant__ CUtensorMap tm_kv,
+                       const __grid_constant__ CUtensorMap tm_qp, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v) {
     using namespace mla;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;
-    uint8_t* sRing = sQ + kQChunks * kChunk;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + kStages * kChunk);
-    uint64_t* ring_full = bars;
-    uint64_t* ring_empty = bars + kStages;
-    uint64_t* q_full = bars + 2 * kStages;
-    uint64_t* s_full = q_full + 1;
-    uint64_t* s_free = s_full + 1;
-    uint64_t* p_full = s_free + 1;     // [2]
-    uint64_t* p_free = p_full + 2;     // [2]
-    uint64_t* mma_done = p_free + 2;
+    uint8_t* sRing = sQ + kQChunks * kQChunk;
+    float* red = reinterpret_cast<float*>(sRing + kStages * kSlot);   // [2][kRows]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + kRedBytes);
+    uint64_t* full = bars;                     // [kStages] CTA 0: both CTAs' copies of a slot landed
+    uint64_t* empty = bars + kStages;          // [kStages] the MMAs read the slot (both CTAs)
+    uint64_t* q_full = bars + 2 * kStages;     // [kQChunks] CTA 0: both CTAs' Q chunk landed
+    uint64_t* s_full = q_full + kQChunks;      // [2] per S buffer: the scores are in TMEM (both CTAs)
+    uint64_t* p_full = s_full + 2;             // [2] per S buffer, CTA 0: both CTAs wrote P over them
+    uint64_t* p_free = p_full + 2;             // O += P.V of the last block done (both CTAs)
+    uint64_t* mma_done = p_free + 1;
+    uint64_t* xa = mma_done + 1;               // [4] per TMEM quadrant: both softmax warps wrote `red`
+    uint64_t* xb = xa + 4;                     // [4] per TMEM quadrant: both read the partner's value
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int half = blockIdx.x & 1;
-    const int tile = blockIdx.x >> 1;
+    const uint32_t rank = cluster_ctarank();   // 0 issues the MMAs
+    const int pair = blockIdx.x >> 1;
+    const int half = pair & 1;
+    const int tile = pair >> 1;
 
     // Row tile -> (sequence, first token).  Within a sequence the tiles are
     // visited last-token-first so the tiles with the most keys start first.
     // kv0 = the sequence's first staged row (the padded offsets of the earlier
-    // sequences).
+    // sequences).  Both CTAs of the pair compute the same values.
     int b = -1, i0 = 0, kv0 = 0;
     for (int bb = 0, acc = 0; bb < p.batch; ++bb) {
-        const int nt = (p.qo_indptr[bb + 1] - p.qo_indptr[bb] + kTok - 1) / kTok;
+        const int nt = (p.qo_indptr[bb + 1] - p.qo_indptr[bb] + kPairTok - 1) / kPairTok;
         if (tile < acc + nt) {
             b = bb;
-            i0 = (nt - 1 - (tile - acc)) * kTok;
+            i0 = (nt - 1 - (tile - acc)) * kPairTok;
             break;
         }
         acc += nt;
         kv0 += mla_padded_len(p, bb);
     }
-    if (b < 0) return;
+    if (b < 0) return;   // the whole pair: past the last tile
     const int q0 = p.qo_indptr[b], q_len = p.qo_indptr[b + 1] - q0;
     const int kv_len = p.kv_indptr[b + 1] - p.kv_indptr[b];
     const int prefix = kv_len - q_len;
-    const int ntok = min(kTok, q_len - i0);
-    // keys any row of the tile may see (none when the pool or the staging area is empty)
-    const int n_keys = (p.num_pages > 0 && p.stage_rows > 0) ? max(0, min(kv_len, prefix + i0 + ntok)) : 0;
+    const int ntok_pair = min(kPairTok, q_len - i0);
+    const int tok0 = i0 + (int)rank * kTok;          // this CTA's first token
+    const int ntok = max(0, min(kTok, q_len - tok0)); // its live tokens
+    // keys any row of the pair may see (none when the pool or the staging area is empty)
+    const int n_keys =
+        (p.num_pages > 0 && p.stage_rows > 0) ? max(0, min(kv_len, prefix + i0 + ntok_pair)) : 0;
     const int J = (n_keys + kKeys - 1) / kKeys;
 
-    if (J == 0) {   // no visible key (empty KV): out = 0, lse = -inf
+    if (J == 0) {   // no visible key (empty KV): out = 0, lse = -inf; the whole pair returns
         for (int i = threadIdx.x; i < ntok * kHeads * 32; i += blockDim.x) {
             const int r = i / 32, c = i % 32;
-            const size_t t = (size_t)(q0 + i0 + r / kHeads);
+            const size_t t = (size_t)(q0 + tok0 + r / kHeads);
             reinterpret_cast<uint4*>(p.out + (t * kHeads + r % kHeads) * kDc + half * 256)[c] =
                 make_uint4(0u, 0u, 0u, 0u);
             if (half == 0 && c == 0) p.lse[t * kHeads + r % kHeads] = -INFINITY;
@@ -179,241 +229,356 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&ring_full[i], 1);
-            mbar_init(&ring_empty[i], 1);
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
         }
-        mbar_init(q_full, 1);
-        mbar_init(s_full, 1);
-        mbar_init(s_free, 128);
+        for (int i = 0; i < kQChunks; ++i) mbar_init(&q_full[i], 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&p_full[i], 128);
-            mbar_init(&p_free[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 2 * kSoftmaxWarps);   // every softmax warp of both CTAs
         }
+        mbar_init(p_free, 1);
         mbar_init(mma_done, 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&xa[i], 64);
+            mbar_init(&xb[i], 64);
+        }
         fence_barrier_init();
         *abort_flag = 0;
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 512);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, 512);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();   // both CTAs: barriers initialised, TMEM allocated
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // Both CTAs load their halves; the copies complete on CTA 0's barriers,
+        // whose expected byte counts (set by CTA 0 alone) cover both halves.
+        // Per block: 5 K slots (columns 64c .. 64c + 127 of this CTA's 64 keys,
+        // c = 0, 2, 4, 6; then the kpe columns 512 .. 575 alone) and 2 V slots
+        // (this CTA's 128 output columns of keys 0-63, then 64-127), in the
+        // MMA thread's order: K(0), then K(j + 1) and V(j) for each block j.
+        // Q comes chunk by chunk, each just ahead of the first K slot that
+        // needs it, so the first MMAs wait for 32 KB of Q rather than 144 KB.
         if (lane == 0) {
-            prefetch_tensormap(&tm_kv);
-            const int y = (q0 + i0) * kHeads;   // rows past the tensor are zero-filled
-            mbar_arrive_expect_tx(q_full, kQChunks * kChunk);
-            for (int c = 0; c < kQChunks - 1; ++c) tma_load_2d(sQ + c * kChunk, &tm_qn, q_full, c * 64, y);
-            tma_load_2d(sQ + (kQChunks - 1) * kChunk, &tm_qp, q_full, 0, y);
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            const bool lead = rank == 0;
+            const int y = (q0 + tok0) * kHeads;   // rows past the tensor are zero-filled
+            auto load_q = [&](int c) {
+                if (lead) mbar_arrive_expect_tx(&q_full[c], 2 * kQChunk);
+                const uint32_t bar = mapa_shared(smem_u32(&q_full[c]), 0);
+                if (c < kQChunks - 1)
+                    tma_load_2d_pair(sQ + c * kQChunk, &tm_qn, bar, c * 64, y);
+                else
+                    tma_load_2d_pair(sQ + c * kQChunk, &tm_qp, bar, 0, y);
+            };
+            for (int c = 0; c < 4; ++c) load_q(c);   // before the staging grid ends
             // the staged keys are written by the preceding grid
             asm volatile("griddepcontrol.wait;" ::: "memory");
             bool ok = true;
-            int k = 0;   // running chunk index (same order as the MMA issuer consumes them)
-            // v < 0: K chunk (128 keys of block jb, columns [x, x + 64));
-            // v >= 0: V chunk v (keys 32v .. 32v + 31 of block jb, the CTA's 256 columns)
-            auto load_chunk = [&](int jb, int x, int v) -> bool {
-                const int stage = k % kStages;
-                if (k >= kStages && !(mbar_wait(&ring_empty[stage], ((k / kStages) - 1) & 1) && *abort_flag == 0))
-                    return false;
-                uint8_t* dst = sRing + stage * kChunk;
-                mbar_arrive_expect_tx(&ring_full[stage], kChunk);
+            int k = 0, stage = 0;
+            uint32_t phase = 0;
+            // v < 0: K slot c (c = 0..4); v >= 0: V slot v (v = 0, 1)
+            auto load_slot = [&](int jb, int c, int v) -> bool {
+                if (k >= kStages && !(mbar_wait(&empty[stage], phase ^ 1) && *abort_flag == 0)) return false;
+                uint8_t* dst = sRing + stage * kSlot;
+                const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+                const int row = kv0 + jb * kKeys;
                 if (v < 0) {
-                    tma_load_2d(dst, &tm_kv, &ring_full[stage], x, kv0 + jb * kKeys);
+                    const int subs = c < 4 ? 2 : 1;
+                    if (lead) mbar_arrive_expect_tx(&full[stage], 2 * subs * kSub);
+                    for (int s2 = 0; s2 < subs; ++s2)
+                        tma_load_2d_pair(dst + s2 * kSub, &tm_k, bar, (2 * c + s2) * 64,
+                                         row + (int)rank * kHalfKeys);
                 } else {
+                    if (lead) mbar_arrive_expect_tx(&full[stage], 2 * kSlot);
 #pragma unroll
-                    for (int n = 0; n < 4; ++n)
-                        tma_load_2d(dst + n * 4096, &tm_v, &ring_full[stage], (half * 4 + n) * 64,
-                                    kv0 + jb * kKeys + v * 32);
+                    for (int w = 0; w < 2; ++w)
+#pragma unroll
+                        for (int n = 0; n < 2; ++n)
+                            tma_load_2d_pair(dst + w * kSub + n * 4096, &tm_v, bar,
+                                             half * 256 + (int)rank * 128 + n * 64, row + v * 64 + w * 32);
                 }
                 ++k;
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
                 return true;
             };
-            for (int step = 0; step <= J && ok; ++step) {
-                if (step < J)
-                    for (int c = 0; c < kQChunks && ok; ++c) ok = load_chunk(step, c * 64, -1);
-                if (step >= 1)
-                    for (int v = 0; v < kVChunks && ok; ++v) ok = load_chunk(step - 1, 0, v);
+            for (int c = 0; c < kKSlots && ok; ++c) {   // K(0), with the rest of Q
+                if (c >= 2) load_q(2 * c);
+                if (c >= 2 && c < 4) load_q(2 * c + 1);
+                ok = load_slot(0, c, -1);
+            }
+            for (int jb = 0; jb < J && ok; ++jb) {
+                if (jb + 1 < J)
+                    for (int c = 0; c < kKSlots && ok; ++c) ok = load_slot(jb + 1, c, -1);
+                for (int v = 0; v < kVSlots && ok; ++v) ok = load_slot(jb, 0, v);
             }
             if (!ok) {
                 *abort_flag = 1;
                 atomicOr(p.err, kErrTimeout);
             }
-            // Never leave with copies in flight: wait for the last fill of
-            // every stage and for Q (immediate unless the pipeline aborted).
-            for (int kk = max(0, k - kStages); kk < k; ++kk) mbar_wait(&ring_full[kk % kStages], (kk / kStages) & 1);
-            mbar_wait(q_full, 0);
+            // CTA 0: never leave with copies in flight into either CTA's shared
+            // memory: wait for the last fill of every slot and for Q (immediate
+            // unless the pipeline aborted).  CTA 1 cannot observe its copies;
+            // it stays resident until CTA 0 is past this point (cluster barrier
+            // below).
+            if (lead) {
+                for (int kk = max(0, k - kStages); kk < k; ++kk)
+                    mbar_wait(&full[kk % kStages], (kk / kStages) & 1);
+                for (int c = 0; c < kQChunks; ++c) mbar_wait(&q_full[c], 0);
+            }
         }
         __syncwarp();
+    } else if (warp == 1 && rank == 1) {
+        // CTA 0's last commit also arrives here: no MMA of the pair still reads
+        // this CTA's shared memory or writes its TMEM after it.
+        if (lane == 0) mbar_wait(mma_done, 0);
+        __syncwarp();
     } else if (warp == 1) {
-        // ----------------------------------------------------------- MMA issuer
+        // ------------------------------------------------ CTA 0: the MMA issuer
+        // Order: S(0); then for each block j: S(j + 1) into the other S buffer
+        // (the tensor core works on it while the softmax warps turn S(j) into
+        // P(j)), then O += P(j).V(j).  S(j + 2) reuses P(j)'s columns only
+        // after O += P(j).V(j) was issued, and the MMAs of one thread run in
+        // issue order.  Kept lean: the thread waits ~70 cycles per issued MMA
+        // for the pipe anyway, so descriptors are formed once and advanced by
+        // adding the address step (16 bytes per unit; every operand address
+        // stays below 256 KB, so the 14-bit field never carries), and the ring
+        // index and phase are counters.
         if (lane == 0) {
-            const uint32_t idesc_qk = umma_idesc_bf16_f32(kRows, kKeys, false);
-            const uint32_t idesc_pv = umma_idesc_bf16_f32(kRows, 256, true);
-            const uint32_t q_addr = smem_u32(sQ), ring_addr = smem_u32(sRing);
-            bool ok = mbar_wait(q_full, 0);
-            tc_fence_after();
-            int k = 0;
-            for (int step = 0; step <= J && ok; ++step) {
-                if (step < J) {
-                    if (step >= 1) {   // softmax has read S(step - 1)
-                        ok = mbar_wait(s_free, (step - 1) & 1) && *abort_flag == 0;
+            const uint32_t idesc_qk = umma_idesc_bf16_f32(2 * kRows, kKeys, false);
+            const uint32_t idesc_pv = umma_idesc_bf16_f32(2 * kRows, 256, true);
+            const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dk = umma_desc_sw128(smem_u32(sRing), 16, 1024);
+            const uint64_t dv = umma_desc_sw128(smem_u32(sRing), 4096, 1024);
+            bool ok = true;
+            int stage = 0;
+            uint32_t phase = 0;
+            auto next = [&]() {
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            };
+            // S(j)[256 rows][128 keys] = Q . K(j)^T into buffer j % 2: A rows from each
+            // CTA's Q chunk, B keys 64 from each CTA's sub-chunk (K-major, 8-row groups
+            // 1 KB apart); 4 MMAs of 16 columns per sub-chunk
+            auto issue_s = [&](int j) -> bool {
+                const uint32_t d = tmem + kColS + (j & 1) * 128;
+                for (int c = 0; c < kKSlots; ++c) {
+                    if (j == 0) {   // Q arrives chunk by chunk with the first block
+                        if (!mbar_wait(&q_full[2 * c], 0) || (c < 4 && !mbar_wait(&q_full[2 * c + 1], 0)))
+                            return false;
                         tc_fence_after();
                     }
-                    for (int c = 0; c < kQChunks && ok; ++c, ++k) {
-                        // TMA data only: no tcgen05 fence, and no abort-flag load on this
-                        // path (the issue thread's extra latency stalls the tensor pipe; a
-                        // stalled pipeline ends in a timed-out wait anyway)
-                        const int stage = k % kStages;
-                        ok = mbar_wait(&ring_full[stage], (k / kStages) & 1);
-                        if (!ok) break;
+                    // TMA data only: no tcgen05 fence
+                    if (!mbar_wait(&full[stage], phase)) return false;
+                    const uint64_t a0 = dq + (uint64_t)((2 * c * kQChunk) >> 4);
+                    const uint64_t b0 = dk + (uint64_t)((stage * kSlot) >> 4);
+#pragma unroll
+                    for (int s2 = 0; s2 < 2; ++s2) {
+                        if (s2 == 1 && c == kKSlots - 1) break;   // the kpe slot holds one sub-chunk
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            umma_bf16(tmem + kColS, umma_desc_sw128(q_addr + c * kChunk + kk * 32, 16, 1024),
-                                      umma_desc_sw128(ring_addr + stage * kChunk + kk * 32, 16, 1024), idesc_qk,
-                                      (c | kk) != 0);
-                        umma_commit(&ring_empty[stage]);
+                            umma_bf16_pair(d, a0 + (uint64_t)((s2 * kQChunk + kk * 32) >> 4),
+                                           b0 + (uint64_t)((s2 * kSub + kk * 32) >> 4), idesc_qk, (c | s2 | kk) != 0);
                     }
-                    if (ok) umma_commit(s_full);
+                    umma_commit_pair_mc(&empty[stage], kBothCtas);
+                    next();
                 }
-                if (step >= 1 && ok) {
-                    const int jb = step - 1, pb = jb & 1;
-                    ok = mbar_wait(&p_full[pb], (jb >> 1) & 1) && *abort_flag == 0;
-                    tc_fence_after();
-                    for (int v = 0; v < kVChunks && ok; ++v, ++k) {
-                        const int stage = k % kStages;
-                        ok = mbar_wait(&ring_full[stage], (k / kStages) & 1);
-                        if (!ok) break;
-                        // keys 32v + 16kk .. +15: P columns (32v + 16kk) / 2; B = 16 key rows
-                        // of the four 64-column blocks (MN-major: blocks 4 KB apart, 8-row
-                        // groups 1 KB apart)
+                umma_commit_pair_mc(&s_full[j & 1], kBothCtas);
+                return true;
+            };
+            // O += P(j).V(j): keys 64v + 32w + 16kk .. +15 are P columns 64v + 16w + 8kk of
+            // buffer j % 2; B = 16 key rows of the 256 output columns, 128 from each CTA's
+            // sub-chunk w (MN-major: two 64-column blocks 4 KB apart, 8-row groups 1 KB apart)
+            auto issue_pv = [&](int j) -> bool {
+                if (!(mbar_wait(&p_full[j & 1], (j >> 1) & 1) && *abort_flag == 0)) return false;
+                tc_fence_after();
+                const uint32_t a_p = tmem + kColS + (j & 1) * 128;
+                for (int v = 0; v < kVSlots; ++v) {
+                    if (!mbar_wait(&full[stage], phase)) return false;
+                    const uint64_t b0 = dv + (uint64_t)((stage * kSlot) >> 4);
+#pragma unroll
+                    for (int w = 0; w < 2; ++w)
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk)
-                            umma_bf16_tmem_a(tmem, tmem + kColP + pb * 64 + v * 16 + kk * 8,
-                                             umma_desc_sw128(ring_addr + stage * kChunk + kk * 2048, 4096, 1024),
-                                             idesc_pv, (jb | v | kk) != 0);
-                        umma_commit(&ring_empty[stage]);
-                    }
-                    if (ok) umma_commit(&p_free[pb]);
+                            umma_bf16_tmem_a_pair(tmem, a_p + v * 64 + w * 16 + kk * 8,
+                                                  b0 + (uint64_t)((w * kSub + kk * 2048) >> 4), idesc_pv,
+                                                  (j | v | w | kk) != 0);
+                    umma_commit_pair_mc(&empty[stage], kBothCtas);
+                    next();
                 }
+                umma_commit_pair_mc(p_free, kBothCtas);
+                return true;
+            };
+            ok = issue_s(0);
+            for (int j = 0; j < J && ok; ++j) {
+                if (j + 1 < J) ok = issue_s(j + 1);
+                ok = ok && issue_pv(j);
             }
             if (!ok) {
                 *abort_flag = 1;
                 atomicOr(p.err, kErrTimeout);
             }
-            // never release TMEM with MMAs in flight
-            umma_commit(mma_done);
+            // never free TMEM with MMAs in flight (the commit reaches both CTAs)
+            umma_commit_pair_mc(mma_done, kBothCtas);
             mbar_wait(mma_done, 0);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------- softmax
+        // Two warps per TMEM lane quadrant (a warp reaches only the lanes
+        // 32 * (warp % 4) ..): warp group kh = 0 takes keys 0-63 of every
+        // block, kh = 1 keys 64-127.  A warp reads its 64 scores and releases
+        // the S tile at once (the next block's S = Q.K^T can start), then the
+        // two warps of a quadrant swap their row maxima through shared memory
+        // (mbarriers xa: both wrote, xb: both read; every wait bounded), so
+        // both apply the same running maximum and lazy-rescale decision.  Each
+        // keeps a partial row sum, rescales and writes 128 of the 256 output
+        // columns; the sums are merged at the end the same way.
         const int quad = warp & 3;
+        const int kh = (warp - 2) >> 2;   // key half of the block
         const int row = quad * 32 + lane;
-        const int tok = i0 + row / kHeads;
+        const int tok = tok0 + row / kHeads;
         const int lim = prefix + tok;   // last visible key of this row
         const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16);
+        const float sc = p.scale_log2;
+        // keys <= this are visible to every row of this CTA: blocks below it need no mask
+        const int unmasked_below = min(prefix + tok0, n_keys - 1);
+        float* my_red = red + kh * kRows + row;
+        const float* peer_red = red + (kh ^ 1) * kRows + row;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
+        int x = 0;   // exchanges done (phase of xa / xb)
         for (int j = 0; j < J; ++j) {
-            const bool got = mbar_wait(s_full, j & 1);
+            const bool got = mbar_wait(&s_full[j & 1], (j >> 1) & 1);
             if (!__all_sync(0xffffffffu, got && *abort_flag == 0)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float s[kKeys];
-#pragma unroll
-            for (int c = 0; c < kKeys / 32; ++c) {
-                float v[32];
-                tmem_ld32(t_row + kColS + c * 32, v);
+            const uint32_t t_s = t_row + kColS + (j & 1) * 128 + kh * 64;   // this warp's scores, then P
+            float s[kKeys / 2];   // this warp's 64 keys
+            {
+                float v0[32], v1[32];
+                tmem_ld32(t_s, v0);
+                tmem_ld32(t_s + 32, v1);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
+                for (int i = 0; i < 32; ++i) {
+                    s[i] = v0[i];
+                    s[32 + i] = v1[i];
+                }
             }
-            tc_fence_before();
-            mbar_arrive(s_free);
 
-            float mx = -INFINITY;
+            // scale to log2 units, mask, row maximum (8 independent chains)
+            float mx8[8];
 #pragma unroll
-            for (int c = 0; c < kKeys; ++c) {
-                const int key = j * kKeys + c;
-                s[c] = (key <= lim && key < n_keys) ? s[c] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[c]);
+            for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+            const int key0 = j * kKeys + kh * 64;
+            if (j * kKeys + kKeys - 1 <= unmasked_below) {
+#pragma unroll
+                for (int c = 0; c < kKeys / 2; ++c) {
+                    s[c] *= sc;
+                    mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kKeys / 2; ++c) {
+                    const int key = key0 + c;
+                    s[c] = (key <= lim && key < n_keys) ? s[c] * sc : -INFINITY;
+                    mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                }
             }
+            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            float mx_peer = -INFINITY;
+            if (!__all_sync(0xffffffffu, mla_swap(&xa[quad], &xb[quad], x, my_red, peer_red, mx, mx_peer))) {
+                ok = false;
+                break;
+            }
+            mx = fmaxf(mx, mx_peer);
             const float m_new = fmaxf(m, mx);
             float m_use = m, alpha = 1.f;
             if (m == -INFINITY || m_new > m + kLazyRescale) {
                 m_use = m_new == -INFINITY ? 0.f : m_new;
                 alpha = ex2(m - m_use);
             }
-            float ls = 0.f;
+            float ls8[8];
 #pragma unroll
-            for (int c = 0; c < kKeys; ++c) {
+            for (int i = 0; i < 8; ++i) ls8[i] = 0.f;
+#pragma unroll
+            for (int c = 0; c < kKeys / 2; ++c) {
                 s[c] = ex2(s[c] - m_use);
-                ls += s[c];
+                ls8[c & 7] += s[c];
             }
+            const float ls = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
             l = l * alpha + ls;
             m = m_use;
 
-            const int pb = j & 1;
             bool got2 = true;
             if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                // O holds P(j-1).V: wait for it, then rescale this warp's rows.
-                got2 = mbar_wait(&p_free[pb ^ 1], ((j - 1) >> 1) & 1);
+                // O holds P(j-1).V: wait for it, then rescale this warp's rows (its 128 columns).
+                got2 = mbar_wait(p_free, (j - 1) & 1);
                 if (__all_sync(0xffffffffu, got2 && *abort_flag == 0)) {
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < 256 / 32; ++c) {
+                    for (int c = 0; c < 128 / 32; ++c) {
                         float o[32];
-                        tmem_ld32(t_row + c * 32, o);
+                        tmem_ld32(t_row + kh * 128 + c * 32, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(t_row + c * 32, o);
+                        tmem_st32(t_row + kh * 128 + c * 32, o);
                     }
                     tmem_wait_st();
                 }
-            } else if (j >= 2) {
-                // P buffer pb was last read by P(j-2).V
-                got2 = mbar_wait(&p_free[pb], ((j - 2) >> 1) & 1);
-                tc_fence_after();
             }
             if (!__all_sync(0xffffffffu, got2 && *abort_flag == 0)) {
                 ok = false;
                 break;
             }
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
+            {
                 uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    pk[i] = Mma<__nv_bfloat16>::pack(s[h2 * 64 + 2 * i], s[h2 * 64 + 2 * i + 1]);
-                tmem_st32(t_row + kColP + pb * 64 + h2 * 32, pk);
+                for (int i = 0; i < 32; ++i) pk[i] = Mma<__nv_bfloat16>::pack(s[2 * i], s[2 * i + 1]);
+                tmem_st32(t_s, pk);   // over this warp's own scores, already read
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&p_full[pb]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&p_full[j & 1]), 0));
         }
         if (ok) {
-            const bool got = mbar_wait(&p_free[(J - 1) & 1], ((J - 1) >> 1) & 1);
+            const bool got = mbar_wait(p_free, (J - 1) & 1);
             ok = __all_sync(0xffffffffu, got && *abort_flag == 0);
             tc_fence_after();
         }
+        // the quadrant's two partial row sums (a partner that left the loop
+        // early never arrives; the bounded wait then ends with no output written)
+        float l_peer = 0.f;
+        ok = __all_sync(0xffffffffu, ok && mla_swap(&xa[quad], &xb[quad], x, my_red, peer_red, l, l_peer));
         if (ok) {
+            l += l_peer;
             const bool live = row / kHeads < ntok;
             const size_t t = (size_t)(q0 + tok);
             const int h = row % kHeads;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16* orow = p.out + (t * kHeads + h) * kDc + half * 256;
+            __nv_bfloat16* orow = p.out + (t * kHeads + h) * kDc + half * 256 + kh * 128;
 #pragma unroll 1
-            for (int c = 0; c < 256 / 32; ++c) {
+            for (int c = 0; c < 128 / 32; ++c) {
                 float o[32];
-                tmem_ld32(t_row + c * 32, o);
+                tmem_ld32(t_row + kh * 128 + c * 32, o);
                 tmem_wait_ld();
                 if (live) {
 #pragma unroll
@@ -427,19 +592,19 @@ __global__ void __launch_bounds__(mla::kThreads, 1)
                     }
                 }
             }
-            if (live && half == 0) p.lse[t * kHeads + h] = l > 0.f ? m + log2f(l) : -INFINITY;
+            if (live && half == 0 && kh == 0) p.lse[t * kHeads + h] = l > 0.f ? m + log2f(l) : -INFINITY;
         } else {
             *abort_flag = 1;
             if (lane == 0) atomicOr(p.err, kErrTimeout);
         }
     }
 
+    // Both CTAs: every role is done with the pair's barriers, shared memory
+    // and TMEM before either CTA frees its TMEM or exits.
     tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, 512);
-    }
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, 512);
 }
 
 cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStream_t stream) {
@@ -453,7 +618,8 @@ cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStre
                                     mla::kSmemBytes);
     });
     if (e != cudaSuccess) return e;
-    const long long tiles = (long long)(p.total_q + mla::kTok - 1) / mla::kTok + p.batch;
+    // pair tiles: an upper bound of sum_b ceil(q_len_b / 16) (excess pairs return at once)
+    const long long tiles = (long long)(p.total_q + mla::kPairTok - 1) / mla::kPairTok + p.batch;
     if (tiles <= 0) return cudaSuccess;
     const bool staged = p.num_pages > 0 && p.stage_rows > 0;
     if (staged) {
@@ -467,7 +633,7 @@ cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStre
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * tiles));
+    cfg.gridDim = dim3((unsigned)(4 * tiles));   // (tile, output half) pairs of 2 CTAs
     cfg.blockDim = dim3(mla::kThreads);
     cfg.dynamicSmemBytes = mla::kSmemBytes;
     cfg.stream = stream;
