@@ -276,14 +276,16 @@ typedef struct {
 } pkv_mla_desc;
 
 /*
- * Bytes of scratch memory pkv_mla_paged_prefill needs: a 256-byte header,
- * then nnz + 128 * batch staged key rows of 1152 bytes (ckv 512 + kpe 64
- * bf16; every sequence's keys start on a multiple of 128 rows, the rows in
- * between are zero), rounded up to 256 bytes; no rows when nnz == 0.  The
- * workspace must be 256-byte aligned.  Word 0 of the header collects
- * device-side error bits (bit 0: a pipeline wait timed out; bit 1:
- * kv_indptr[batch] > nnz, so keys past nnz were not staged and the result is
- * unspecified); zero it once after allocating.
+ * Bytes of scratch memory pkv_mla_paged_prefill needs: a 256-byte header;
+ * the work list of 16-byte entries, one per (16-token row tile, half of the
+ * output columns), 2 * (ceil(total_q / 16) + batch) of them; two ints per
+ * sequence (plus one); then nnz + 128 * batch staged key rows of 1152 bytes
+ * (ckv 512 + kpe 64 bf16; every sequence's keys start on a multiple of 128
+ * rows, the rows in between are zero; no rows when nnz == 0); each part
+ * rounded up to 256 bytes.  The workspace must be 256-byte aligned.  Word 0
+ * of the header collects device-side error bits (bit 0: a pipeline wait
+ * timed out; bit 1: kv_indptr[batch] > nnz, so keys past nnz were not staged
+ * and the result is unspecified); zero it once after allocating.
  */
 PKV_API int pkv_mla_workspace_size(const pkv_mla_desc* desc, size_t* bytes);
 
@@ -311,12 +313,13 @@ PKV_API int pkv_mla_workspace_size(const pkv_mla_desc* desc, size_t* bytes);
  * other sequences' outputs unchanged.
  * The q -> sequence map of [MLA]'s host loop is computed on the device from
  * qo_indptr.
- * Two kernels run: the first copies every referenced key row, in kv_indptr
- * order, into the workspace (one gather per call instead of one per query
- * tile); the second, launched as its programmatic dependent, streams those
- * rows with 16 KB tensor-memory-access boxes.  workspace / workspace_bytes as
- * pkv_mla_workspace_size describes; calls sharing one workspace must be
- * ordered on the GPU (one stream).
+ * Two kernels run: the first copies every referenced key row, sequence by
+ * sequence, into the workspace (one gather per call instead of one per query
+ * tile) and lists the work, longest row tiles first; the second, launched as
+ * its programmatic dependent, runs one pair of CTAs per two SMs that take the
+ * listed tiles in turns and stream the staged rows with tensor-memory-access
+ * boxes.  workspace / workspace_bytes as pkv_mla_workspace_size describes;
+ * calls sharing one workspace must be ordered on the GPU (one stream).
  */
 PKV_API int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const void* q_pe,
                           const void* ckv_cache, const void* kpe_cache, const int32_t* qo_indptr,

@@ -534,6 +534,12 @@ static long long mla_stage_rows(const pkv_mla_desc& d) {
     return d.nnz > 0 ? (long long)d.nnz + (long long)kMlaSeqAlign * d.batch : 0;
 }
 
+// Tasks of the persistent prefill kernel: (16-token row tile, output half)
+// pairs, at most 2 * (ceil(total_q / 16) + batch).
+static long long mla_max_tasks(const pkv_mla_desc& d) {
+    return 2 * (((long long)d.total_q + 15) / 16 + d.batch);
+}
+
 static int check_mla_desc(const pkv_mla_desc* desc) {
     if (!desc) return PKV_INVALID_ARG;
     const pkv_mla_desc& d = *desc;
@@ -543,13 +549,27 @@ static int check_mla_desc(const pkv_mla_desc* desc) {
     if (d.total_q > 0 && d.batch == 0) return PKV_INVALID_ARG;
     if (d.num_heads != 16 || d.d_ckv != 512 || d.d_kpe != 64) return PKV_UNSUPPORTED;
     if ((long long)d.total_q * d.num_heads * d.d_ckv > (long long)1 << 40) return PKV_UNSUPPORTED;
-    if (mla_stage_rows(d) > INT_MAX) return PKV_UNSUPPORTED;
+    if (mla_stage_rows(d) > INT_MAX || mla_max_tasks(d) > INT_MAX / 2) return PKV_UNSUPPORTED;
     return PKV_OK;
 }
 
-static size_t mla_workspace_bytes(const pkv_mla_desc& d) {
-    return kHeaderBytes + align256((size_t)mla_stage_rows(d) * kMlaStageRowBytes);
+// Workspace: 256-byte header | task list (16 bytes per task) | first row tile
+// of each sequence (batch + 1 ints) | first staged row of each sequence
+// (batch ints) | staged key rows.
+struct MlaLayout {
+    size_t tasks, seq_tile, seq_row, stage, total;
+};
+static MlaLayout mla_layout(const pkv_mla_desc& d) {
+    MlaLayout l;
+    l.tasks = kHeaderBytes;
+    l.seq_tile = l.tasks + align256((size_t)mla_max_tasks(d) * 16);
+    l.seq_row = l.seq_tile + align256((size_t)(d.batch + 1) * 4);
+    l.stage = l.seq_row + align256((size_t)d.batch * 4);
+    l.total = l.stage + align256((size_t)mla_stage_rows(d) * kMlaStageRowBytes);
+    return l;
 }
+
+static size_t mla_workspace_bytes(const pkv_mla_desc& d) { return mla_layout(d).total; }
 
 int pkv_mla_workspace_size(const pkv_mla_desc* desc, size_t* bytes) {
     const int st = check_mla_desc(desc);
@@ -586,8 +606,15 @@ int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const vo
     p.kv_indices = kv_indices;
     p.out = static_cast<__nv_bfloat16*>(out);
     p.lse = lse;
-    p.err = static_cast<uint32_t*>(workspace);
-    p.stage = static_cast<uint8_t*>(workspace) + kHeaderBytes;
+    const MlaLayout lay = mla_layout(d);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.err = reinterpret_cast<uint32_t*>(ws);
+    p.task_count = reinterpret_cast<int*>(ws) + 1;
+    p.tasks = reinterpret_cast<int4*>(ws + lay.tasks);
+    p.seq_tile = reinterpret_cast<int*>(ws + lay.seq_tile);
+    p.seq_row = reinterpret_cast<int*>(ws + lay.seq_row);
+    p.stage = ws + lay.stage;
+    p.max_tasks = (int)mla_max_tasks(d);
     p.total_q = d.total_q;
     p.batch = d.batch;
     p.num_pages = d.num_pages;

@@ -63,6 +63,13 @@ struct MlaParams {
     float* lse;                    // [total_q][16]
     uint8_t* stage;                // [stage_rows][1152]: ckv row | kpe row of each key, per sequence
                                    // padded with zero rows to a multiple of 128 rows
+    int4* tasks;                   // [max_tasks] (sequence, first token, first staged row, key blocks |
+                                   // output half << 30), most key blocks first (built on the device)
+    int* seq_tile;                 // [batch + 1] first 16-token row tile of each sequence
+    int* seq_row;                  // [batch] first staged row of each sequence
+    int* task_count;               // header words 1-3: tasks listed, of them with keys (listed
+                                   // first), next task with keys to hand out
+    int max_tasks;                 // 2 * (ceil(total_q / 16) + batch)
     uint32_t* err;                 // header word 0
     int total_q, batch, num_pages, nnz;
     int stage_rows;                // rows of `stage`: nnz + 128 * batch (0 without keys)

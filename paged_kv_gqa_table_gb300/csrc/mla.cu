@@ -81,9 +81,9 @@ constexpr int kVSlots = 2;                // per block: keys 0-63, 64-127 of thi
 constexpr int kStages = 5;
 constexpr int kSoftmaxWarps = 8;          // two per TMEM lane quadrant, each 64 of a block's 128 keys
 constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
-constexpr int kBars = 2 * kStages + kQChunks + 14;
+constexpr int kBars = 2 * kStages + kQChunks + 19;
 constexpr int kRedBytes = 2 * kRows * 4;   // row max / row sum exchange: [key half][row]
-constexpr int kSmemBytes = 1024 + kQChunks * kQChunk + kStages * kSlot + kRedBytes + kBars * 8 + 16;
+constexpr int kSmemBytes = 1024 + kQChunks * kQChunk + kStages * kSlot + kRedBytes + kBars * 8 + 32;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 // TMEM columns: O [0,256), S buffers [256,384) and [384,512); block j's scores go
 // to buffer j % 2, and its bf16 P is written over them in place (key half h at
@@ -100,17 +100,139 @@ __device__ __forceinline__ int mla_padded_len(const MlaParams& p, int b) {
     return (kv_len + kMlaSeqAlign - 1) / kMlaSeqAlign * kMlaSeqAlign;
 }
 
-// Sequence b's keys are staged at rows [off_b, off_b + kv_len_b), off_b the
-// sum of the earlier sequences' padded lengths: staged[off_b + j] =
-// ckv[kv_indices[kv_indptr[b] + j]] | kpe[...], then zero rows up to the next
-// multiple of kMlaSeqAlign, so a 128-row box of one sequence never reaches the
-// next sequence's keys.  Keys whose kv_indices entry lies past nnz are staged
-// as zero rows (and reported); rows past stage_rows are not written (their
-// boxes read the tensor map's zero fill).  One warp per row; each warp walks
-// the sequences forward as its rows advance.
+// Key blocks (128 keys) that the rows of 16-token tile t of sequence b may
+// see: the tile's last token sees prefix + its index + 1 keys (none without a
+// pool or staged keys).
+__device__ __forceinline__ int mla_tile_blocks(const MlaParams& p, int b, int t) {
+    const int q_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
+    const int kv_len = p.kv_indptr[b + 1] - p.kv_indptr[b];
+    const int i0 = t * mla::kPairTok;
+    const int n_keys = (p.num_pages > 0 && p.stage_rows > 0)
+                           ? max(0, min(kv_len, kv_len - q_len + i0 + min(mla::kPairTok, q_len - i0)))
+                           : 0;
+    return (n_keys + mla::kKeys - 1) / mla::kKeys;
+}
+
+// Exclusive scan of one int per thread over a 256-thread block; returns the
+// thread's prefix and sets *total.  Uses `sbuf` (8 ints).
+__device__ __forceinline__ int block_scan_256(int v, int* sbuf, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sbuf[warp] = x;
+    __syncthreads();
+    int wsum = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const int t = sbuf[w];
+        if (w < warp) wsum += t;
+        all += t;
+    }
+    __syncthreads();
+    *total = all;
+    return wsum + x - v;
+}
+
+// The task list (one block of 256 threads): every (16-token row tile, output
+// half) pair of the batch, tiles with the most key blocks first (a counting
+// sort on the block count), so that the persistent CTA pairs, which take the
+// list in turns, start the longest tiles first.  Also the first row tile and
+// the first staged row of every sequence.
+constexpr int kTaskBins = 2048;   // block counts at or above kTaskBins - 1 share the last bin
+__device__ void mla_build_tasks(const MlaParams& p) {
+    __shared__ int bins[kTaskBins];
+    __shared__ int sbuf[8];
+    const int tid = threadIdx.x;
+    // per-sequence first tile and first staged row (scans over the batch, 256 at a time)
+    int tile_carry = 0, row_carry = 0;
+    for (int base = 0; base < p.batch; base += 256) {
+        const int b = base + tid;
+        const int nt = b < p.batch ? max(0, (p.qo_indptr[b + 1] - p.qo_indptr[b] + mla::kPairTok - 1) / mla::kPairTok) : 0;
+        const int rows = b < p.batch ? mla_padded_len(p, b) : 0;
+        int t_total = 0, r_total = 0;
+        const int t_ex = block_scan_256(nt, sbuf, &t_total);
+        const int r_ex = block_scan_256(rows, sbuf, &r_total);
+        if (b < p.batch) {
+            p.seq_tile[b] = tile_carry + t_ex;
+            p.seq_row[b] = row_carry + r_ex;
+        }
+        tile_carry += t_total;
+        row_carry += r_total;
+    }
+    const int T = tile_carry;   // row tiles of the batch
+    if (tid == 0) p.seq_tile[p.batch] = T;
+    for (int i = tid; i < kTaskBins; i += 256) bins[i] = 0;
+    __syncthreads();   // seq_tile / seq_row written (global, same block) and bins cleared
+    // tile t -> (sequence, tile of the sequence): the last sequence whose first tile is <= t
+    auto seq_of = [&](int t) {
+        int lo = 0, hi = p.batch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.seq_tile[mid] <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    };
+    for (int t = tid; t < T; t += 256) {
+        const int b = seq_of(t);
+        atomicAdd(&bins[min(mla_tile_blocks(p, b, t - p.seq_tile[b]), kTaskBins - 1)], 1);
+    }
+    __syncthreads();
+    // bin starts in decreasing block count: thread tid owns bins kTaskBins - 8 tid - 1 .. - 8
+    int own[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        own[i] = bins[kTaskBins - 1 - (8 * tid + i)];
+        sum += own[i];
+    }
+    int total = 0;
+    int start = block_scan_256(sum, sbuf, &total);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        bins[kTaskBins - 1 - (8 * tid + i)] = start;
+        start += own[i];
+    }
+    __syncthreads();
+    // bin 0 starts after every tile with keys
+    if (tid == 0) {
+        p.task_count[1] = min(2 * bins[0], p.max_tasks);
+        p.task_count[2] = 0;   // next task with keys to hand out
+    }
+    __syncthreads();
+    for (int t = tid; t < T; t += 256) {
+        const int b = seq_of(t);
+        const int tt = t - p.seq_tile[b];
+        const int J = mla_tile_blocks(p, b, tt);
+        const int pos = atomicAdd(&bins[min(J, kTaskBins - 1)], 1);
+        if (2 * pos + 1 < p.max_tasks) {
+            const int4 e = make_int4(b, tt * mla::kPairTok, p.seq_row[b], J);
+            p.tasks[2 * pos] = e;
+            p.tasks[2 * pos + 1] = make_int4(e.x, e.y, e.z, e.w | (1 << 30));
+        }
+    }
+    if (tid == 0) p.task_count[0] = min(2 * T, p.max_tasks);
+}
+
+// Block 0 builds the task list; every block stages key rows: sequence b's keys
+// at rows [off_b, off_b + kv_len_b), off_b the sum of the earlier sequences'
+// padded lengths: staged[off_b + j] = ckv[kv_indices[kv_indptr[b] + j]] |
+// kpe[...], then zero rows up to the next multiple of kMlaSeqAlign, so a
+// 128-row box of one sequence never reaches the next sequence's keys.  Keys
+// whose kv_indices entry lies past nnz are staged as zero rows (and
+// reported); rows past stage_rows are not written (their boxes read the
+// tensor map's zero fill).  One warp per row; each warp walks the sequences
+// forward as its rows advance.
 __global__ void __launch_bounds__(256) mla_stage_kernel(const MlaParams p) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (blockIdx.x == 0 && threadIdx.x == 0 && p.kv_indptr[p.batch] > p.nnz) atomicOr(p.err, 2u);
+    if (blockIdx.x == 0) {
+        if (threadIdx.x == 0 && p.kv_indptr[p.batch] > p.nnz) atomicOr(p.err, 2u);
+        mla_build_tasks(p);
+    }
+    if (p.num_pages <= 0) return;
     const int lane = threadIdx.x & 31;
     const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
@@ -160,6 +282,29 @@ __device__ __forceinline__ bool mla_swap(uint64_t* xa, uint64_t* xb, int& x, flo
     return true;
 }
 
+// One task of the list, as every role of both CTAs of a pair decodes it.
+struct MlaTask {
+    int q0, q_len, kv0, prefix, tok0, ntok, n_keys, J, half;
+};
+
+__device__ __forceinline__ MlaTask mla_task(const MlaParams& p, int idx, uint32_t rank) {
+    const int4 e = p.tasks[idx];
+    MlaTask t;
+    const int b = e.x, i0 = e.y;
+    t.kv0 = e.z;
+    t.J = e.w & 0x3FFFFFFF;
+    t.half = (e.w >> 30) & 1;
+    t.q0 = p.qo_indptr[b];
+    t.q_len = p.qo_indptr[b + 1] - t.q0;
+    const int kv_len = p.kv_indptr[b + 1] - p.kv_indptr[b];
+    t.prefix = kv_len - t.q_len;
+    const int ntok_pair = min(mla::kPairTok, t.q_len - i0);
+    t.tok0 = i0 + (int)rank * mla::kTok;
+    t.ntok = max(0, min(mla::kTok, t.q_len - t.tok0));
+    t.n_keys = (p.num_pages > 0 && p.stage_rows > 0) ? max(0, min(kv_len, t.prefix + i0 + ntok_pair)) : 0;
+    return t;
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     mla_prefill_kernel(const MlaParams p, const __grid_constant__ CUtensorMap tm_qn,
                        const __grid_constant__ CUtensorMap tm_qp, const __grid_constant__ CUtensorMap tm_k,
@@ -173,59 +318,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + kRedBytes);
     uint64_t* full = bars;                     // [kStages] CTA 0: both CTAs' copies of a slot landed
     uint64_t* empty = bars + kStages;          // [kStages] the MMAs read the slot (both CTAs)
-    uint64_t* q_full = bars + 2 * kStages;     // [kQChunks] CTA 0: both CTAs' Q chunk landed
-    uint64_t* s_full = q_full + kQChunks;      // [2] per S buffer: the scores are in TMEM (both CTAs)
+    uint64_t* q_full = bars + 2 * kStages;     // [kQChunks] CTA 0: both CTAs' Q chunk landed (per task)
+    uint64_t* q_free = q_full + kQChunks;      // the task's last S MMAs done: Q may be replaced (both)
+    uint64_t* s_full = q_free + 1;             // [2] per S buffer: the scores are in TMEM (both CTAs)
     uint64_t* p_full = s_full + 2;             // [2] per S buffer, CTA 0: both CTAs wrote P over them
     uint64_t* p_free = p_full + 2;             // O += P.V of the last block done (both CTAs)
     uint64_t* mma_done = p_free + 1;
     uint64_t* xa = mma_done + 1;               // [4] per TMEM quadrant: both softmax warps wrote `red`
     uint64_t* xb = xa + 4;                     // [4] per TMEM quadrant: both read the partner's value
+    uint64_t* task_bar = xb + 4;               // [4] a task index handed out is in task_slot (both CTAs)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* task_slot = reinterpret_cast<int*>(tmem_slot + 2);   // [4]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();   // 0 issues the MMAs
-    const int pair = blockIdx.x >> 1;
-    const int half = pair & 1;
-    const int tile = pair >> 1;
-
-    // Row tile -> (sequence, first token).  Within a sequence the tiles are
-    // visited last-token-first so the tiles with the most keys start first.
-    // kv0 = the sequence's first staged row (the padded offsets of the earlier
-    // sequences).  Both CTAs of the pair compute the same values.
-    int b = -1, i0 = 0, kv0 = 0;
-    for (int bb = 0, acc = 0; bb < p.batch; ++bb) {
-        const int nt = (p.qo_indptr[bb + 1] - p.qo_indptr[bb] + kPairTok - 1) / kPairTok;
-        if (tile < acc + nt) {
-            b = bb;
-            i0 = (nt - 1 - (tile - acc)) * kPairTok;
-            break;
-        }
-        acc += nt;
-        kv0 += mla_padded_len(p, bb);
-    }
-    if (b < 0) return;   // the whole pair: past the last tile
-    const int q0 = p.qo_indptr[b], q_len = p.qo_indptr[b + 1] - q0;
-    const int kv_len = p.kv_indptr[b + 1] - p.kv_indptr[b];
-    const int prefix = kv_len - q_len;
-    const int ntok_pair = min(kPairTok, q_len - i0);
-    const int tok0 = i0 + (int)rank * kTok;          // this CTA's first token
-    const int ntok = max(0, min(kTok, q_len - tok0)); // its live tokens
-    // keys any row of the pair may see (none when the pool or the staging area is empty)
-    const int n_keys =
-        (p.num_pages > 0 && p.stage_rows > 0) ? max(0, min(kv_len, prefix + i0 + ntok_pair)) : 0;
-    const int J = (n_keys + kKeys - 1) / kKeys;
-
-    if (J == 0) {   // no visible key (empty KV): out = 0, lse = -inf; the whole pair returns
-        for (int i = threadIdx.x; i < ntok * kHeads * 32; i += blockDim.x) {
-            const int r = i / 32, c = i % 32;
-            const size_t t = (size_t)(q0 + tok0 + r / kHeads);
-            reinterpret_cast<uint4*>(p.out + (t * kHeads + r % kHeads) * kDc + half * 256)[c] =
-                make_uint4(0u, 0u, 0u, 0u);
-            if (half == 0 && c == 0) p.lse[t * kHeads + r % kHeads] = -INFINITY;
-        }
-        return;
-    }
+    const int pair = blockIdx.x >> 1, pairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -233,6 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < kQChunks; ++i) mbar_init(&q_full[i], 1);
+        mbar_init(q_free, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 2 * kSoftmaxWarps);   // every softmax warp of both CTAs
@@ -242,6 +351,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
         for (int i = 0; i < 4; ++i) {
             mbar_init(&xa[i], 64);
             mbar_init(&xb[i], 64);
+            mbar_init(&task_bar[i], 1);
         }
         fence_barrier_init();
         *abort_flag = 0;
@@ -250,60 +360,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
         tmem_alloc_pair(tmem_slot, 512);
         tmem_relinquish_pair();
     }
+    // the task list and the staged keys are written by the preceding grid
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int n_tasks = p.task_count[0], n_keyed = p.task_count[1];
     tc_fence_before();
     cluster_sync();   // both CTAs: barriers initialised, TMEM allocated
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Tasks with keys are handed out one at a time, in list order (longest
+    // first), by CTA 0's producer thread, which takes the next one from a
+    // counter in the workspace when it starts on it and passes its index to
+    // every role of both CTAs through task_slot / task_bar (4 entries, used in
+    // turn: task r in entry r % 4; index -1 ends the list).  An entry is
+    // reused only after every role has moved past the task it held: the
+    // producer starts task r + 4 after it has loaded every ring slot of task
+    // r + 3, which the MMA thread frees only while working on task r + 2 or
+    // later, and each of those needs the softmax warps' P of that task.
+    auto hand_out = [&](int r) -> int {
+        int idx = atomicAdd(&p.task_count[2], 1);
+        if (idx >= n_keyed) idx = -1;
+        task_slot[r & 3] = idx;
+        st_shared_cluster(mapa_shared(smem_u32(&task_slot[r & 3]), 1), idx);
+        mbar_arrive(&task_bar[r & 3]);
+        mbar_arrive_release_cluster(mapa_shared(smem_u32(&task_bar[r & 3]), 1));
+        return idx;
+    };
+    // -2: the wait timed out
+    auto next_task = [&](int r) -> int {
+        if (!mbar_wait_acq_cluster(&task_bar[r & 3], (r >> 2) & 1)) return -2;
+        return *reinterpret_cast<volatile int*>(&task_slot[r & 3]);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         // Both CTAs load their halves; the copies complete on CTA 0's barriers,
         // whose expected byte counts (set by CTA 0 alone) cover both halves.
-        // Per block: 5 K slots (columns 64c .. 64c + 127 of this CTA's 64 keys,
-        // c = 0, 2, 4, 6; then the kpe columns 512 .. 575 alone) and 2 V slots
-        // (this CTA's 128 output columns of keys 0-63, then 64-127), in the
-        // MMA thread's order: K(0), then K(j + 1) and V(j) for each block j.
-        // Q comes chunk by chunk, each just ahead of the first K slot that
-        // needs it, so the first MMAs wait for 32 KB of Q rather than 144 KB.
+        // Per key block: 5 K slots (columns 64c .. 64c + 127 of this CTA's 64
+        // keys, c = 0, 2, 4, 6; then the kpe columns 512 .. 575 alone) and 2 V
+        // slots (this CTA's 128 output columns of keys 0-63, then 64-127), in
+        // the MMA thread's order: per task K(0), then K(j + 1) and V(j) for
+        // each block j.  A task's Q comes chunk by chunk, each just ahead of
+        // the first K slot that needs it, once the previous task's last S
+        // MMAs have released the Q buffer.
         if (lane == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
             const bool lead = rank == 0;
-            const int y = (q0 + tok0) * kHeads;   // rows past the tensor are zero-filled
-            auto load_q = [&](int c) {
-                if (lead) mbar_arrive_expect_tx(&q_full[c], 2 * kQChunk);
-                const uint32_t bar = mapa_shared(smem_u32(&q_full[c]), 0);
-                if (c < kQChunks - 1)
-                    tma_load_2d_pair(sQ + c * kQChunk, &tm_qn, bar, c * 64, y);
-                else
-                    tma_load_2d_pair(sQ + c * kQChunk, &tm_qp, bar, 0, y);
-            };
-            for (int c = 0; c < 4; ++c) load_q(c);   // before the staging grid ends
-            // the staged keys are written by the preceding grid
-            asm volatile("griddepcontrol.wait;" ::: "memory");
             bool ok = true;
-            int k = 0, stage = 0;
+            int k = 0, stage = 0, n = 0;   // ring slots, ring index, tasks with keys
             uint32_t phase = 0;
-            // v < 0: K slot c (c = 0..4); v >= 0: V slot v (v = 0, 1)
-            auto load_slot = [&](int jb, int c, int v) -> bool {
+            auto load_slot = [&](int row, int c, int v, int half) -> bool {
                 if (k >= kStages && !(mbar_wait(&empty[stage], phase ^ 1) && *abort_flag == 0)) return false;
                 uint8_t* dst = sRing + stage * kSlot;
                 const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
-                const int row = kv0 + jb * kKeys;
                 if (v < 0) {
                     const int subs = c < 4 ? 2 : 1;
                     if (lead) mbar_arrive_expect_tx(&full[stage], 2 * subs * kSub);
                     for (int s2 = 0; s2 < subs; ++s2)
-                        tma_load_2d_pair(dst + s2 * kSub, &tm_k, bar, (2 * c + s2) * 64,
-                                         row + (int)rank * kHalfKeys);
+                        tma_load_2d_pair(dst + s2 * kSub, &tm_k, bar, (2 * c + s2) * 64, row + (int)rank * kHalfKeys);
                 } else {
                     if (lead) mbar_arrive_expect_tx(&full[stage], 2 * kSlot);
 #pragma unroll
                     for (int w = 0; w < 2; ++w)
 #pragma unroll
-                        for (int n = 0; n < 2; ++n)
-                            tma_load_2d_pair(dst + w * kSub + n * 4096, &tm_v, bar,
-                                             half * 256 + (int)rank * 128 + n * 64, row + v * 64 + w * 32);
+                        for (int nn = 0; nn < 2; ++nn)
+                            tma_load_2d_pair(dst + w * kSub + nn * 4096, &tm_v, bar,
+                                             half * 256 + (int)rank * 128 + nn * 64, row + v * 64 + w * 32);
                 }
                 ++k;
                 if (++stage == kStages) {
@@ -312,29 +434,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 }
                 return true;
             };
-            for (int c = 0; c < kKSlots && ok; ++c) {   // K(0), with the rest of Q
-                if (c >= 2) load_q(2 * c);
-                if (c >= 2 && c < 4) load_q(2 * c + 1);
-                ok = load_slot(0, c, -1);
-            }
-            for (int jb = 0; jb < J && ok; ++jb) {
-                if (jb + 1 < J)
-                    for (int c = 0; c < kKSlots && ok; ++c) ok = load_slot(jb + 1, c, -1);
-                for (int v = 0; v < kVSlots && ok; ++v) ok = load_slot(jb, 0, v);
+            for (int r = 0; ok; ++r) {
+                const int idx = lead ? hand_out(r) : next_task(r);
+                if (idx < 0) {
+                    ok = idx == -1;
+                    break;
+                }
+                const MlaTask t = mla_task(p, idx, rank);
+                const int y = (t.q0 + t.tok0) * kHeads;   // rows past the tensor are zero-filled
+                auto load_q = [&](int c) {
+                    if (lead) mbar_arrive_expect_tx(&q_full[c], 2 * kQChunk);
+                    const uint32_t bar = mapa_shared(smem_u32(&q_full[c]), 0);
+                    if (c < kQChunks - 1)
+                        tma_load_2d_pair(sQ + c * kQChunk, &tm_qn, bar, c * 64, y);
+                    else
+                        tma_load_2d_pair(sQ + c * kQChunk, &tm_qp, bar, 0, y);
+                };
+                // the previous task's S MMAs are done with Q
+                if (n >= 1 && !(mbar_wait(q_free, (n - 1) & 1) && *abort_flag == 0)) {
+                    ok = false;
+                    break;
+                }
+                for (int c = 0; c < kKSlots && ok; ++c) {   // K(0), with Q
+                    load_q(2 * c);
+                    if (c < 4) load_q(2 * c + 1);
+                    ok = load_slot(t.kv0, c, -1, t.half);
+                }
+                for (int jb = 0; jb < t.J && ok; ++jb) {
+                    if (jb + 1 < t.J)
+                        for (int c = 0; c < kKSlots && ok; ++c) ok = load_slot(t.kv0 + (jb + 1) * kKeys, c, -1, t.half);
+                    for (int v = 0; v < kVSlots && ok; ++v) ok = load_slot(t.kv0 + jb * kKeys, 0, v, t.half);
+                }
+                ++n;
             }
             if (!ok) {
                 *abort_flag = 1;
                 atomicOr(p.err, kErrTimeout);
             }
             // CTA 0: never leave with copies in flight into either CTA's shared
-            // memory: wait for the last fill of every slot and for Q (immediate
+            // memory: wait for the last fill of every slot and of Q (immediate
             // unless the pipeline aborted).  CTA 1 cannot observe its copies;
             // it stays resident until CTA 0 is past this point (cluster barrier
             // below).
             if (lead) {
                 for (int kk = max(0, k - kStages); kk < k; ++kk)
                     mbar_wait(&full[kk % kStages], (kk / kStages) & 1);
-                for (int c = 0; c < kQChunks; ++c) mbar_wait(&q_full[c], 0);
+                if (n >= 1)
+                    for (int c = 0; c < kQChunks; ++c) mbar_wait(&q_full[c], (n - 1) & 1);
             }
         }
         __syncwarp();
@@ -345,15 +491,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ CTA 0: the MMA issuer
-        // Order: S(0); then for each block j: S(j + 1) into the other S buffer
-        // (the tensor core works on it while the softmax warps turn S(j) into
-        // P(j)), then O += P(j).V(j).  S(j + 2) reuses P(j)'s columns only
-        // after O += P(j).V(j) was issued, and the MMAs of one thread run in
-        // issue order.  Kept lean: the thread waits ~70 cycles per issued MMA
-        // for the pipe anyway, so descriptors are formed once and advanced by
-        // adding the address step (16 bytes per unit; every operand address
-        // stays below 256 KB, so the 14-bit field never carries), and the ring
-        // index and phase are counters.
+        // Per task: S(0); then for each block j: S(j + 1) into the other S
+        // buffer (the tensor core works on it while the softmax warps turn
+        // S(j) into P(j)), then O += P(j).V(j).  S buffers alternate over the
+        // blocks of all tasks (G counts them).  S(j + 2) reuses P(j)'s columns
+        // only after O += P(j).V(j) was issued, and the MMAs of one thread run
+        // in issue order; a task's first O += P.V overwrites O, which the
+        // softmax warps have read out by then (they write that block's P
+        // after their epilogue).  Kept lean: the thread waits ~70 cycles per
+        // issued MMA for the pipe anyway, so descriptors are formed once and
+        // advanced by adding the address step (16 bytes per unit; every
+        // operand address stays below 256 KB, so the 14-bit field never
+        // carries), and the ring index and phase are counters.
         if (lane == 0) {
             const uint32_t idesc_qk = umma_idesc_bf16_f32(2 * kRows, kKeys, false);
             const uint32_t idesc_pv = umma_idesc_bf16_f32(2 * kRows, 256, true);
@@ -361,7 +510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
             const uint64_t dk = umma_desc_sw128(smem_u32(sRing), 16, 1024);
             const uint64_t dv = umma_desc_sw128(smem_u32(sRing), 4096, 1024);
             bool ok = true;
-            int stage = 0;
+            int stage = 0, n = 0, G = 0;   // ring index, tasks with keys, blocks issued before this task
             uint32_t phase = 0;
             auto next = [&]() {
                 if (++stage == kStages) {
@@ -369,14 +518,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                     phase ^= 1;
                 }
             };
-            // S(j)[256 rows][128 keys] = Q . K(j)^T into buffer j % 2: A rows from each
+            // S(block g)[256 rows][128 keys] = Q . K^T into buffer g % 2: A rows from each
             // CTA's Q chunk, B keys 64 from each CTA's sub-chunk (K-major, 8-row groups
             // 1 KB apart); 4 MMAs of 16 columns per sub-chunk
-            auto issue_s = [&](int j) -> bool {
-                const uint32_t d = tmem + kColS + (j & 1) * 128;
+            auto issue_s = [&](int g, bool first, bool last) -> bool {
+                const uint32_t d = tmem + kColS + (g & 1) * 128;
                 for (int c = 0; c < kKSlots; ++c) {
-                    if (j == 0) {   // Q arrives chunk by chunk with the first block
-                        if (!mbar_wait(&q_full[2 * c], 0) || (c < 4 && !mbar_wait(&q_full[2 * c + 1], 0)))
+                    if (first) {   // Q arrives chunk by chunk with the task's first block
+                        if (!mbar_wait(&q_full[2 * c], n & 1) || (c < 4 && !mbar_wait(&q_full[2 * c + 1], n & 1)))
                             return false;
                         tc_fence_after();
                     }
@@ -395,16 +544,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                     umma_commit_pair_mc(&empty[stage], kBothCtas);
                     next();
                 }
-                umma_commit_pair_mc(&s_full[j & 1], kBothCtas);
+                umma_commit_pair_mc(&s_full[g & 1], kBothCtas);
+                if (last) umma_commit_pair_mc(q_free, kBothCtas);   // Q no longer read
                 return true;
             };
-            // O += P(j).V(j): keys 64v + 32w + 16kk .. +15 are P columns 64v + 16w + 8kk of
-            // buffer j % 2; B = 16 key rows of the 256 output columns, 128 from each CTA's
+            // O += P(g).V(g): keys 64v + 32w + 16kk .. +15 are P columns 64v + 16w + 8kk of
+            // buffer g % 2; B = 16 key rows of the 256 output columns, 128 from each CTA's
             // sub-chunk w (MN-major: two 64-column blocks 4 KB apart, 8-row groups 1 KB apart)
-            auto issue_pv = [&](int j) -> bool {
-                if (!(mbar_wait(&p_full[j & 1], (j >> 1) & 1) && *abort_flag == 0)) return false;
+            auto issue_pv = [&](int g, bool first) -> bool {
+                if (!(mbar_wait(&p_full[g & 1], (g >> 1) & 1) && *abort_flag == 0)) return false;
                 tc_fence_after();
-                const uint32_t a_p = tmem + kColS + (j & 1) * 128;
+                const uint32_t a_p = tmem + kColS + (g & 1) * 128;
                 for (int v = 0; v < kVSlots; ++v) {
                     if (!mbar_wait(&full[stage], phase)) return false;
                     const uint64_t b0 = dv + (uint64_t)((stage * kSlot) >> 4);
@@ -414,17 +564,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                         for (int kk = 0; kk < 2; ++kk)
                             umma_bf16_tmem_a_pair(tmem, a_p + v * 64 + w * 16 + kk * 8,
                                                   b0 + (uint64_t)((w * kSub + kk * 2048) >> 4), idesc_pv,
-                                                  (j | v | w | kk) != 0);
+                                                  !first || (v | w | kk) != 0);
                     umma_commit_pair_mc(&empty[stage], kBothCtas);
                     next();
                 }
                 umma_commit_pair_mc(p_free, kBothCtas);
                 return true;
             };
-            ok = issue_s(0);
-            for (int j = 0; j < J && ok; ++j) {
-                if (j + 1 < J) ok = issue_s(j + 1);
-                ok = ok && issue_pv(j);
+            for (int r = 0; ok; ++r) {
+                const int idx = next_task(r);
+                if (idx < 0) {
+                    ok = idx == -1;
+                    break;
+                }
+                const int J = p.tasks[idx].w & 0x3FFFFFFF;
+                ok = issue_s(G, true, J == 1);
+                for (int j = 0; j < J && ok; ++j) {
+                    if (j + 1 < J) ok = issue_s(G + j + 1, false, j + 2 == J);
+                    ok = ok && issue_pv(G + j, j == 0);
+                }
+                G += J;
+                ++n;
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -439,142 +599,164 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
         // ------------------------------------------------------------- softmax
         // Two warps per TMEM lane quadrant (a warp reaches only the lanes
         // 32 * (warp % 4) ..): warp group kh = 0 takes keys 0-63 of every
-        // block, kh = 1 keys 64-127.  A warp reads its 64 scores and releases
-        // the S tile at once (the next block's S = Q.K^T can start), then the
+        // block, kh = 1 keys 64-127.  A warp reads its 64 scores, then the
         // two warps of a quadrant swap their row maxima through shared memory
         // (mbarriers xa: both wrote, xb: both read; every wait bounded), so
         // both apply the same running maximum and lazy-rescale decision.  Each
         // keeps a partial row sum, rescales and writes 128 of the 256 output
-        // columns; the sums are merged at the end the same way.
+        // columns; the sums are merged at the end of a task the same way.
         const int quad = warp & 3;
         const int kh = (warp - 2) >> 2;   // key half of the block
         const int row = quad * 32 + lane;
-        const int tok = tok0 + row / kHeads;
-        const int lim = prefix + tok;   // last visible key of this row
         const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16);
         const float sc = p.scale_log2;
-        // keys <= this are visible to every row of this CTA: blocks below it need no mask
-        const int unmasked_below = min(prefix + tok0, n_keys - 1);
         float* my_red = red + kh * kRows + row;
         const float* peer_red = red + (kh ^ 1) * kRows + row;
-        float m = -INFINITY, l = 0.f;
+        int x = 0;       // swaps done (phase of xa / xb)
+        int G = 0;       // blocks of the earlier tasks
         bool ok = true;
-        int x = 0;   // exchanges done (phase of xa / xb)
-        for (int j = 0; j < J; ++j) {
-            const bool got = mbar_wait(&s_full[j & 1], (j >> 1) & 1);
-            if (!__all_sync(0xffffffffu, got && *abort_flag == 0)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t t_s = t_row + kColS + (j & 1) * 128 + kh * 64;   // this warp's scores, then P
-            float s[kKeys / 2];   // this warp's 64 keys
-            {
-                float v0[32], v1[32];
-                tmem_ld32(t_s, v0);
-                tmem_ld32(t_s + 32, v1);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    s[i] = v0[i];
-                    s[32 + i] = v1[i];
-                }
-            }
-
-            // scale to log2 units, mask, row maximum (8 independent chains)
-            float mx8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-            const int key0 = j * kKeys + kh * 64;
-            if (j * kKeys + kKeys - 1 <= unmasked_below) {
-#pragma unroll
-                for (int c = 0; c < kKeys / 2; ++c) {
-                    s[c] *= sc;
-                    mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kKeys / 2; ++c) {
-                    const int key = key0 + c;
-                    s[c] = (key <= lim && key < n_keys) ? s[c] * sc : -INFINITY;
-                    mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-                }
-            }
-            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            float mx_peer = -INFINITY;
-            if (!__all_sync(0xffffffffu, mla_swap(&xa[quad], &xb[quad], x, my_red, peer_red, mx, mx_peer))) {
-                ok = false;
-                break;
-            }
-            mx = fmaxf(mx, mx_peer);
-            const float m_new = fmaxf(m, mx);
-            float m_use = m, alpha = 1.f;
-            if (m == -INFINITY || m_new > m + kLazyRescale) {
-                m_use = m_new == -INFINITY ? 0.f : m_new;
-                alpha = ex2(m - m_use);
-            }
-            float ls8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ls8[i] = 0.f;
-#pragma unroll
-            for (int c = 0; c < kKeys / 2; ++c) {
-                s[c] = ex2(s[c] - m_use);
-                ls8[c & 7] += s[c];
-            }
-            const float ls = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-            l = l * alpha + ls;
-            m = m_use;
-
-            bool got2 = true;
-            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                // O holds P(j-1).V: wait for it, then rescale this warp's rows (its 128 columns).
-                got2 = mbar_wait(p_free, (j - 1) & 1);
-                if (__all_sync(0xffffffffu, got2 && *abort_flag == 0)) {
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int c = 0; c < 128 / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(t_row + kh * 128 + c * 32, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(t_row + kh * 128 + c * 32, o);
-                    }
-                    tmem_wait_st();
-                }
-            }
-            if (!__all_sync(0xffffffffu, got2 && *abort_flag == 0)) {
-                ok = false;
-                break;
-            }
-            {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) pk[i] = Mma<__nv_bfloat16>::pack(s[2 * i], s[2 * i + 1]);
-                tmem_st32(t_s, pk);   // over this warp's own scores, already read
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&p_full[j & 1]), 0));
-        }
-        if (ok) {
-            const bool got = mbar_wait(p_free, (J - 1) & 1);
-            ok = __all_sync(0xffffffffu, got && *abort_flag == 0);
-            tc_fence_after();
-        }
-        // the quadrant's two partial row sums (a partner that left the loop
-        // early never arrives; the bounded wait then ends with no output written)
-        float l_peer = 0.f;
-        ok = __all_sync(0xffffffffu, ok && mla_swap(&xa[quad], &xb[quad], x, my_red, peer_red, l, l_peer));
-        if (ok) {
-            l += l_peer;
-            const bool live = row / kHeads < ntok;
-            const size_t t = (size_t)(q0 + tok);
+        // tasks without a visible key (empty KV), listed last: out = 0, lse = -inf
+        for (int idx = n_keyed + pair; idx < n_tasks; idx += pairs) {
+            const MlaTask t = mla_task(p, idx, rank);
+            const int tok = t.tok0 + row / kHeads;
+            const size_t tq = (size_t)(t.q0 + tok);
             const int h = row % kHeads;
+            if (row / kHeads < t.ntok) {
+                uint4* orow = reinterpret_cast<uint4*>(p.out + (tq * kHeads + h) * kDc + t.half * 256 + kh * 128);
+                for (int c = 0; c < 16; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+                if (t.half == 0 && kh == 0) p.lse[tq * kHeads + h] = -INFINITY;
+            }
+        }
+        for (int r = 0; ok; ++r) {
+            int idx = 0;
+            if (lane == 0) idx = next_task(r);
+            idx = __shfl_sync(0xffffffffu, idx, 0);   // warp-uniform
+            if (idx < 0) {
+                ok = idx == -1;
+                break;
+            }
+            const MlaTask t = mla_task(p, idx, rank);
+            const int tok = t.tok0 + row / kHeads;
+            const bool live = row / kHeads < t.ntok;
+            const size_t tq = (size_t)(t.q0 + tok);
+            const int h = row % kHeads;
+            __nv_bfloat16* orow = p.out + (tq * kHeads + h) * kDc + t.half * 256 + kh * 128;
+            const int lim = t.prefix + tok;   // last visible key of this row
+            // keys <= this are visible to every row of this CTA: blocks below it need no mask
+            const int unmasked_below = min(t.prefix + t.tok0, t.n_keys - 1);
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < t.J; ++j) {
+                const int g = G + j;
+                const bool got = mbar_wait(&s_full[g & 1], (g >> 1) & 1);
+                if (!__all_sync(0xffffffffu, got && *abort_flag == 0)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t t_s = t_row + kColS + (g & 1) * 128 + kh * 64;   // this warp's scores, then P
+                float s[kKeys / 2];   // this warp's 64 keys
+                {
+                    float v0[32], v1[32];
+                    tmem_ld32(t_s, v0);
+                    tmem_ld32(t_s + 32, v1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        s[i] = v0[i];
+                        s[32 + i] = v1[i];
+                    }
+                }
+
+                // scale to log2 units, mask, row maximum (8 independent chains)
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+                const int key0 = j * kKeys + kh * 64;
+                if (j * kKeys + kKeys - 1 <= unmasked_below) {
+#pragma unroll
+                    for (int c = 0; c < kKeys / 2; ++c) {
+                        s[c] *= sc;
+                        mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kKeys / 2; ++c) {
+                        const int key = key0 + c;
+                        s[c] = (key <= lim && key < t.n_keys) ? s[c] * sc : -INFINITY;
+                        mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                    }
+                }
+                float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                float mx_peer = -INFINITY;
+                if (!__all_sync(0xffffffffu, mla_swap(&xa[quad], &xb[quad], x, my_red, peer_red, mx, mx_peer))) {
+                    ok = false;
+                    break;
+                }
+                mx = fmaxf(mx, mx_peer);
+                const float m_new = fmaxf(m, mx);
+                float m_use = m, alpha = 1.f;
+                if (m == -INFINITY || m_new > m + kLazyRescale) {
+                    m_use = m_new == -INFINITY ? 0.f : m_new;
+                    alpha = ex2(m - m_use);
+                }
+                float ls8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ls8[i] = 0.f;
+#pragma unroll
+                for (int c = 0; c < kKeys / 2; ++c) {
+                    s[c] = ex2(s[c] - m_use);
+                    ls8[c & 7] += s[c];
+                }
+                const float ls = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+                l = l * alpha + ls;
+                m = m_use;
+
+                bool got2 = true;
+                if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    // O holds P(j-1).V: wait for it, then rescale this warp's rows (its 128 columns).
+                    got2 = mbar_wait(p_free, (g - 1) & 1);
+                    if (__all_sync(0xffffffffu, got2 && *abort_flag == 0)) {
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c = 0; c < 128 / 32; ++c) {
+                            float o[32];
+                            tmem_ld32(t_row + kh * 128 + c * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                            tmem_st32(t_row + kh * 128 + c * 32, o);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                if (!__all_sync(0xffffffffu, got2 && *abort_flag == 0)) {
+                    ok = false;
+                    break;
+                }
+                {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) pk[i] = Mma<__nv_bfloat16>::pack(s[2 * i], s[2 * i + 1]);
+                    tmem_st32(t_s, pk);   // over this warp's own scores, already read
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&p_full[g & 1]), 0));
+            }
+            if (!ok) break;
+            G += t.J;
+            // O complete after the task's last O += P.V
+            ok = __all_sync(0xffffffffu, mbar_wait(p_free, (G - 1) & 1) && *abort_flag == 0);
+            tc_fence_after();
+            // the quadrant's two partial row sums (a partner that left early never
+            // arrives; the bounded wait then ends with no output written)
+            float l_peer = 0.f;
+            ok = __all_sync(0xffffffffu, ok && mla_swap(&xa[quad], &xb[quad], x, my_red, peer_red, l, l_peer));
+            if (!ok) break;
+            l += l_peer;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16* orow = p.out + (t * kHeads + h) * kDc + half * 256 + kh * 128;
 #pragma unroll 1
             for (int c = 0; c < 128 / 32; ++c) {
                 float o[32];
@@ -592,8 +774,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                     }
                 }
             }
-            if (live && half == 0 && kh == 0) p.lse[t * kHeads + h] = l > 0.f ? m + log2f(l) : -INFINITY;
-        } else {
+            if (live && t.half == 0 && kh == 0) p.lse[tq * kHeads + h] = l > 0.f ? m + log2f(l) : -INFINITY;
+            tc_fence_before();   // O read out before this warp's next P store lets O be overwritten
+        }
+        if (!ok) {
             *abort_flag = 1;
             if (lane == 0) atomicOr(p.err, kErrTimeout);
         }
@@ -618,22 +802,20 @@ cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStre
                                     mla::kSmemBytes);
     });
     if (e != cudaSuccess) return e;
-    // pair tiles: an upper bound of sum_b ceil(q_len_b / 16) (excess pairs return at once)
-    const long long tiles = (long long)(p.total_q + mla::kPairTok - 1) / mla::kPairTok + p.batch;
-    if (tiles <= 0) return cudaSuccess;
-    const bool staged = p.num_pages > 0 && p.stage_rows > 0;
-    if (staged) {
-        // one warp per staged row, capped at 16 waves of 8-warp CTAs per SM
-        int sms = 0;
-        e = device_sm_count(dev, &sms);
-        if (e != cudaSuccess) return e;
-        const long long want = ((long long)p.stage_rows + 7) / 8;
-        mla_stage_kernel<<<(unsigned)std::min<long long>(want, (long long)sms * 8 * 16), 256, 0, stream>>>(p);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
+    if (p.max_tasks <= 0) return cudaSuccess;
+    int sms = 0;
+    e = device_sm_count(dev, &sms);
+    if (e != cudaSuccess) return e;
+    // task list (block 0) and staged keys: one warp per staged row, capped at
+    // 16 waves of 8-warp CTAs per SM
+    const long long want = std::max<long long>(1, ((long long)p.stage_rows + 7) / 8);
+    mla_stage_kernel<<<(unsigned)std::min<long long>(want, (long long)sms * 8 * 16), 256, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // persistent CTA pairs, one per two SMs (never more than the tasks)
+    const long long pairs = std::min<long long>(p.max_tasks, std::max(1, sms / 2));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(4 * tiles));   // (tile, output half) pairs of 2 CTAs
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
     cfg.blockDim = dim3(mla::kThreads);
     cfg.dynamicSmemBytes = mla::kSmemBytes;
     cfg.stream = stream;
@@ -641,7 +823,7 @@ cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStre
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = staged ? 1 : 0;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, mla_prefill_kernel, p, maps.q_nope, maps.q_pe, maps.kv, maps.v);
 }
 

@@ -233,12 +233,16 @@ def test_empty_batch_is_a_no_op(B):
 
 def test_mla_workspace_size_and_argument_checks(B):
     al = lambda x: (x + 255) // 256 * 256
-    # every sequence's staged keys start on a multiple of 128 rows: room for
-    # nnz rows plus at most 127 zero rows per sequence (none without keys)
+    # header | work list (one 16-byte entry per 16-token row tile and output
+    # half) | per-sequence first tile (batch + 1 ints) and first staged row |
+    # staged rows: every sequence's keys start on a multiple of 128 rows, so
+    # room for nnz rows plus at most 127 zero rows per sequence (none without keys)
     for nnz, batch in ((0, 8), (1, 1), (8070, 8), (123457, 300)):
         d = B.make_mla_desc(2866, batch, 9000, nnz)
         rows = nnz + 128 * batch if nnz > 0 else 0
-        assert B.pkv_mla_workspace_size(d) == 256 + al(rows * 1152)
+        tasks = 2 * ((2866 + 15) // 16 + batch)
+        want = 256 + al(tasks * 16) + al((batch + 1) * 4) + al(batch * 4) + al(rows * 1152)
+        assert B.pkv_mla_workspace_size(d) == want
     for bad in (dict(nnz=-1), dict(total_q=-1), dict(num_pages=-3)):
         kw = dict(total_q=100, batch=2, num_pages=50, nnz=40)
         kw.update(bad)
