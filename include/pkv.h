@@ -162,8 +162,7 @@ PKV_API int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* 
  * and these options (256-byte header, then fp32 split partials m, l
  * [B][q_len][Hq][NS] and acc [B][q_len][Hq][NS][D] when the plan has more
  * than one split; with PKV_DECODE_DEVICE_PLAN, NS is the split count of the
- * bounds and a work list of 16 bytes per (sequence, KV head, row tile, split)
- * slot of the bounds follows).
+ * bounds).
  * num_sms as for pkv_plan_splits.  The workspace must be 256-byte aligned.
  * Word 0 of the header collects device-side error bits (bit 0: a pipeline
  * wait timed out); zero it once after allocating.
@@ -198,25 +197,21 @@ PKV_API int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_dec
  * ordered on the GPU (one stream).
  *
  * flags & PKV_DECODE_DEVICE_PLAN: the split plan is made on the device from
- * context_lens (a one-CTA schedule kernel applies the planner rule of
- * pkv_plan_splits to the actual longest and total context, with the
+ * context_lens: every CTA of phase 1 applies the planner rule of
+ * pkv_plan_splits to the actual longest and total context (with the
  * partition raised where needed so that the splits fit the bounds' split
- * count, and lists the non-empty work items); max_context_len and
+ * count) and finds its own non-empty work items; max_context_len and
  * sum_context_len are then only capacity bounds that size the workspace.
  * Phase 1 runs a fixed grid of min(bound items, 24 per SM) CTAs that take
- * the listed items in order, so a call captured into a CUDA graph with loose
- * bounds launches no CTA per empty split.  pkv_decode_partials does not take
- * this flag.
+ * the items in order, so a call captured into a CUDA graph with loose bounds
+ * launches no CTA per empty split, and no planning kernel runs before it.
+ * pkv_decode_partials does not take this flag.
  *
- * flags & PKV_DECODE_PLAN_READY (with PKV_DECODE_DEVICE_PLAN): the workspace
- * already holds the plan of an earlier device-planned call with the same
- * desc, the same partition options and the same context_lens values, ordered
- * before this call on the GPU; the schedule kernel is not launched.  For the
- * layers of one decode step, which share context_lens: the first layer plans,
- * the others reuse the plan (each with its own q, caches and out).  The
- * kernels check every reused work item against this call's extents, so a
- * workspace holding anything else gives wrong output rows but no access
- * outside this call's tensors and workspace.
+ * flags & PKV_DECODE_PLAN_READY (with PKV_DECODE_DEVICE_PLAN): states that an
+ * earlier device-planned call with the same desc, partition options and
+ * context_lens values ran on this workspace before this call (the layers of
+ * one decode step).  Every device-planned call plans inside phase 1, so the
+ * flag changes nothing in this version; it stays valid.
  */
 PKV_API int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
                                const void* q, const void* k_cache, const void* v_cache,
@@ -344,14 +339,13 @@ PKV_API int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, 
  * Once every argument has passed the regular entry point's checks, it clears
  * the array's 4-byte error word (word 0 of the header) with cudaMemsetAsync
  * on `stream` and runs the regular entry point on the array; the rest of the
- * header, including a device plan an earlier call left there, keeps the
- * previous call's contents.  pkv_static_scratch_error reads the error word.
+ * header keeps the previous call's contents.  pkv_static_scratch_error reads the error word.
  *  - A problem whose workspace (pkv_decode_workspace_size) exceeds the array
  *    is refused with PKV_WORKSPACE_TOO_SMALL before anything is launched.
  *  - PKV_DECODE_PLAN_READY is refused (PKV_INVALID_ARG) unless the previous
  *    successful call of this entry point on the device was device-planned
- *    (PKV_DECODE_DEVICE_PLAN) with the same desc and partition options; the
- *    caller still keeps context_lens unchanged between the two.
+ *    (PKV_DECODE_DEVICE_PLAN) with the same desc and partition options, as
+ *    the flag states.
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
  *  - Every call on a device shares the one array and it keeps the last call's

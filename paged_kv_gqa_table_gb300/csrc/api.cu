@@ -148,15 +148,13 @@ long long plan_items(const pkv_decode_desc* d, int ns) {
     return (long long)d->B * d->Hkv * column_tiles(d).rt * ns;
 }
 
-// Workspace: 256-byte header | split partials (more than one split) | the
-// device plan's work list (16 bytes per item slot of the bounds).
+// Workspace: 256-byte header | split partials (more than one split).
 size_t required_workspace(const pkv_decode_desc* d, const pkv_decode_opts* o, int ns) {
-    size_t b = kHeaderBytes + (ns > 1 ? partial_bytes(d, ns) : 0);
-    if (device_plan(o)) b += align256((size_t)plan_items(d, ns) * 16);
-    return b;
+    (void)o;
+    return kHeaderBytes + (ns > 1 ? partial_bytes(d, ns) : 0);
 }
 
-// Header words of the device plan: {P, splits of the longest context, items}.
+// Header words of the device plan: {P, splits of the longest context}.
 constexpr int kSchedHeaderWord = 4;
 // Phase-1 CTAs of the device plan: enough to fill the GPU many times over;
 // more items than this are taken in turns.
@@ -408,29 +406,19 @@ int pkv::paged_decode_impl(const pkv_decode_desc* desc, const pkv_decode_opts* o
     }
     long long grid = 0;
     if (device_plan(opts)) {
-        // The schedule kernel plans from the device's context lengths; phase 1
-        // (its programmatic dependent) takes the listed items.
-        if (desc->Hkv > 0xFFFF || column_tiles(desc).rt > 0x7FFF) return PKV_UNSUPPORTED;   // list packing
+        // Phase 1 plans from the device's context lengths (every CTA of a fixed
+        // grid, device_plan.cuh) and takes the non-empty items in turns.
+        if (desc->Hkv > 0xFFFF || column_tiles(desc).rt > 0x7FFF) return PKV_UNSUPPORTED;
         int sms = 0;
         st = current_sm_count(&sms);
         if (st) return st;
-        int* hdr = reinterpret_cast<int*>(ws) + kSchedHeaderWord;
-        int4* list = reinterpret_cast<int4*>(parts + (ns > 1 ? partial_bytes(desc, ns) : 0));
         const ColumnTiles ct = column_tiles(desc);
-        // Items per grid KV head (a pair under head pairs); the planner rule
-        // counts the description's KV heads, as the host planner does.
-        SchedParams sp{context_lens, hdr, list, desc->B, p.Hkv, p.RT, p.n_cap, ns, desc->block_size,
-                       desc->Hkv * ct.rt, opts->partition_tokens > 0 ? P : 0,
-                       opts->partition_tokens > 0 ? 0 : opts->num_splits, (int)base_partition(desc), sms};
-        p.sched_hdr = hdr;
-        p.sched_list = list;
-        p.sched_cap = (int)plan_items(desc, ns);
+        // The rule counts the description's KV heads, as the host planner does;
+        // items are per grid KV head (a pair under head pairs).
+        p.plan_hdr = reinterpret_cast<int*>(ws) + kSchedHeaderWord;
+        p.rule = PlanRule{opts->partition_tokens > 0 ? P : 0, opts->partition_tokens > 0 ? 0 : opts->num_splits,
+                          (int)base_partition(desc), desc->Hkv * ct.rt, sms, ns};
         grid = std::min(plan_items(desc, ns), (long long)kDevicePlanCtasPerSm * sms);
-        // An earlier call left the same plan in this workspace: reuse it.
-        if (!(opts->flags & PKV_DECODE_PLAN_READY)) {
-            TraceRange r("pkv::decode.schedule");
-            if (launch_schedule(sp, s) != cudaSuccess) return PKV_CUDA_ERROR;
-        }
     }
     record(opts ? opts->phase1_event_start : nullptr, s);
     {
@@ -442,7 +430,7 @@ int pkv::paged_decode_impl(const pkv_decode_desc* desc, const pkv_decode_opts* o
         // Programmatic dependent of phase 1 (unless an event sits between them).
         TraceRange r("pkv::decode.combine");
         CombineParams c{context_lens, p.part_acc, p.part_m, p.part_l, out, desc->B, desc->Hq, P, ns, p.n_cap, 1,
-                        desc->q_len, p.sched_hdr};
+                        desc->q_len, p.plan_hdr};
         if (launch_combine(desc->dtype, desc->D, c, s, !(opts && opts->phase1_event_stop)) != cudaSuccess)
             return PKV_CUDA_ERROR;
     }

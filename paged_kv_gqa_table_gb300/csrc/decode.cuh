@@ -37,6 +37,7 @@
 #include <type_traits>
 
 #include "decode_common.cuh"
+#include "device_plan.cuh"
 #include "once.h"
 
 namespace pkv {
@@ -64,12 +65,11 @@ struct DecodeParams {
     float v_scale;           // multiplies the output / partial acc (FP8 caches; 1 otherwise)
     const float* alibi;      // [Hq] ALiBi slopes (natural-log units) or nullptr
     int partials_only;       // 1: always write partials (+ sentinels), never out
-    // Device plan (else nullptr): the schedule kernel's header {P, splits of the
-    // longest context, items} and its list of items (b, kvh | rt << 16, s, n_b) in
-    // grid order; this grid's CTAs take items blockIdx.x, blockIdx.x + gridDim.x, ...
-    const int* sched_hdr;
-    const int4* sched_list;
-    int sched_cap;           // entries the list has room for (>= any item count)
+    // Device plan (plan_hdr != nullptr): every CTA plans from ctx with `rule`
+    // and takes the non-empty items blockIdx.x, blockIdx.x + gridDim.x, ...;
+    // CTA 0 writes {P, splits of the longest context} to plan_hdr for the combine.
+    int* plan_hdr;
+    PlanRule rule;
 };
 
 template <int D, int LAYOUT>
@@ -100,7 +100,7 @@ struct DecodeTile {
     static constexpr int QS_MIN_BLOCKS = 4;
     __host__ __device__ static constexpr int qtile_bytes(int nt) { return q_shared(nt) ? 16 * D * 2 : 0; }
     __host__ __device__ static constexpr int smem_bytes(int nt) {
-        return 1024 + STAGES * 2 * SLICE + STAGING + qtile_bytes(nt) + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 16;
+        return 1024 + STAGES * 2 * SLICE + STAGING + qtile_bytes(nt) + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 48;
     }
 };
 
@@ -140,6 +140,7 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
     float* st_m = reinterpret_cast<float*>(empty + STAGES);
     float* st_l = st_m + NWC * HP;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(st_l + NWC * HP);   // set on a wait timeout
+    volatile int* plan_sm = abort_flag + 1;   // device plan: [0] P, [1] b (-1: done), [2] kvh, [3] rt, [4] s, [5] n
 
     // Lets the combine kernel queued behind this one start its prologue as
     // soon as every CTA of this grid is running (it waits for our results).
@@ -433,35 +434,46 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
         run_item(item / p.Hkv, item % p.Hkv, rt, s, p.P, -1);
         return;
     }
-    // Device plan: the schedule kernel (this grid's programmatic prerequisite)
-    // has written the partition size and the list of non-empty items.
+    // Device plan: consumer warp 0 plans from the context lengths and finds
+    // this CTA's items one by one (device_plan.cuh); CTA 0 publishes the
+    // partition for the combine kernel.
+    if (warp == 0) {
+        int mx = 0;
+        long long sum = 0;
+        warp_context_stats(p.ctx, p.B, p.n_cap, lane, &mx, &sum);
+        if (lane == 0) {
+            const int P = device_plan_partition_rule(p.rule, mx, sum);
+            plan_sm[0] = P;
+            if (blockIdx.x == 0) {
+                p.plan_hdr[0] = P;
+                p.plan_hdr[1] = mx > 0 ? (mx - 1) / P + 1 : 1;
+            }
+        }
+    }
     if (threadIdx.x == 0) *abort_flag = 0;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
-    // The header is re-read per item rather than held in registers across it,
-    // with plain loads: a read-only (non-coherent) load may be hoisted above
-    // the wait and see the header before the schedule kernel wrote it.  The
-    // list entry is loaded with the item count (one round trip): every slot
-    // below sched_cap is inside the list.
-    //
-    // With PKV_DECODE_PLAN_READY the list is whatever an earlier call left in
-    // the workspace.  Each item is checked against this launch's extents
-    // before it is used, so a plan of another problem can give wrong rows but
-    // never an access outside this call's tensors: P is kept a positive page
-    // multiple, sequence, KV head, row tile and split must lie inside the grid,
-    // the context length inside [0, n_cap], and a split must start inside it.
-    // A plan the schedule kernel made for this problem passes every check.
-    const int P = device_plan_partition(p.sched_hdr[0]);
-    for (int it = blockIdx.x; it < p.sched_cap; it += gridDim.x) {
-        const int4 e = p.sched_list[it];
-        if (it >= p.sched_hdr[2]) break;
-        const int kvh = e.y & 0xFFFF, rt = e.y >> 16, n = clampi(e.w, 0, p.n_cap);
-        if (e.x < 0 || e.x >= p.B || kvh >= p.Hkv || rt >= p.RT || e.z < 0 || e.z >= p.NS ||
-            (e.z > 0 && (long long)e.z * P >= n))
-            continue;
-        run_item(e.x, kvh, rt, e.z, P, n);
+    const int P = plan_sm[0];
+    const int HR = p.Hkv * p.RT;
+    PlanCursor cur{0, 0};
+    for (long long k = blockIdx.x;; k += gridDim.x) {
+        if (warp == 0) {
+            int b = 0, j = 0, n = 0, nsb = 1;
+            const bool found = warp_plan_item(p.ctx, p.B, p.n_cap, P, HR, k, cur, lane, &b, &j, &n, &nsb);
+            if (lane == 0) {
+                const int kr = j / nsb;
+                plan_sm[1] = found ? b : -1;
+                plan_sm[2] = kr / p.RT;
+                plan_sm[3] = kr % p.RT;
+                plan_sm[4] = j - kr * nsb;
+                plan_sm[5] = n;
+            }
+        }
+        __syncthreads();
+        const int b = plan_sm[1];
+        if (b < 0) break;
+        run_item(b, plan_sm[2], plan_sm[3], plan_sm[4], P, plan_sm[5]);
         fence_proxy_async_smem();   // this item's generic writes to the ring before the next item's copies
-        __syncthreads();            // every role is done with the ring, the barriers and the Q tile
+        __syncthreads();            // every role is done with the ring, the barriers, the Q tile and plan_sm
         if (*abort_flag) break;     // a wait timed out (already reported): take no further item
     }
 }
@@ -503,19 +515,6 @@ cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, 
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (e != cudaSuccess) return e;
-    if (SCHED) {   // programmatic dependent of the schedule kernel just enqueued
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3((Tile::NWC + 1) * 32);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv);
-    }
     kern<<<(unsigned)grid, (Tile::NWC + 1) * 32, smem, stream>>>(p, tmk, tmv);
     return cudaGetLastError();
 }
@@ -523,18 +522,18 @@ cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, 
 template <typename T, int LAYOUT, int D, int NT>
 cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                  const CUtensorMap& tmv, cudaStream_t stream) {
-    if (p.sched_hdr) return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, true>(p, grid, tmk, tmv, stream);
+    if (p.plan_hdr) return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, true>(p, grid, tmk, tmv, stream);
     if (p.alibi || p.q_len > 1)
         return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, false>(p, grid, tmk, tmv, stream);
     return launch_decode_phase1_variant<T, LAYOUT, D, NT, false, false>(p, grid, tmk, tmv, stream);
 }
 
 // Head pairs (kLayoutNHD8x2, D = 128, one column tile); under the device plan
-// the schedule kernel lists the items per KV-head pair.
+// the device plan lists the items per KV-head pair.
 template <typename T>
 cudaError_t launch_decode_phase1_pairs(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                        const CUtensorMap& tmv, cudaStream_t stream) {
-    if (p.sched_hdr)
+    if (p.plan_hdr)
         return launch_decode_phase1_variant<T, kLayoutNHD8x2, 128, 1, true, true>(p, grid, tmk, tmv, stream);
     if (p.alibi || p.q_len > 1)
         return launch_decode_phase1_variant<T, kLayoutNHD8x2, 128, 1, true, false>(p, grid, tmk, tmv, stream);

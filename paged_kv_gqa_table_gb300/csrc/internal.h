@@ -15,24 +15,9 @@ struct CombineParams {
     int B, Hq, P, ns_stride, n_cap;
     int skip_single;           // 1: rows whose sequence has <= 1 split were written by phase 1
     int q_len;                 // query tokens per sequence
-    const int* sched_hdr;      // device plan: header word 0 holds P (else nullptr: P above)
+    const int* sched_hdr;      // device plan: header word 0 holds P, written by phase 1 (else nullptr: P above)
 };
 
-// The device plan's schedule kernel (schedule.cu): reads context_lens, applies
-// the planner rule to the actual longest and total context and lists the
-// non-empty work items (b, kvh, rt, s) in grid order.
-struct SchedParams {
-    const int32_t* ctx;        // [B]
-    int* hdr;                  // out: [0] P, [1] splits of the longest context, [2] items listed
-    int4* list;                // out: up to B * Hkv * RT * NS_cap items (b, kvh | rt << 16, s, n_b)
-    int B, Hkv, RT, n_cap, NS_cap, BS;   // Hkv, RT: the grid's (KV-head pairs under head pairs)
-    int HR_rule;               // (KV head, row tile) pairs the planner rule counts: the description's
-    int P_fixed;               // > 0: this partition (caller option)
-    int num_splits;            // > 0 (without P_fixed): split the longest context this many ways
-    int P0;                    // planner start: 512 tokens per column tile and KV head of the CTA
-    int num_sms;               // the planner's work-item target is 6 per SM
-};
-cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream);
 
 // Phase-1 dispatch, one function per (layout, dtype) translation unit.
 // D in {64, 128, 256}; nt = query-column tiles of 8 per CTA (1, or 2 for D <= 128).

@@ -1,9 +1,9 @@
 """GPU tests of the device plan (PKV_DECODE_DEVICE_PLAN).
 
-A one-CTA schedule kernel reads context_lens on the device, applies the
-planner rule to the actual longest and total context and lists the non-empty
-(sequence, KV head, row tile, split) items; phase 1 runs a fixed grid whose
-CTAs take the listed items in turn.  With exact host bounds the device makes
+Every CTA of phase 1 reads context_lens on the device, applies the planner
+rule to the actual longest and total context and finds its own non-empty
+(sequence, KV head, row tile, split) items: the CTAs of a fixed grid take them
+in turn.  With exact host bounds the device makes
 the host's plan, so the outputs must be bit-identical to the host-planned call;
 with capacity bounds (what a captured CUDA graph needs) the outputs must match
 the oracle within the decode tolerances.
@@ -144,7 +144,7 @@ def test_graph_replay_with_capacity_bounds(q_len, kv8):
 
 
 def test_device_plan_header():
-    # The schedule kernel's header words 4..6: partition, splits of the longest context, items listed.
+    # Header words 4..5, written by phase 1: partition, splits of the longest context.
     B, T = _binding(), _tensors()
     lens = [0, 1, 700, 1024, 1025, 300]
     case = synth.decode_case(seed=640, B=6, Hq=8, Hkv=2, D=128, block_size=16, dtype=synth.BF16,
@@ -157,14 +157,13 @@ def test_device_plan_header():
     B.pkv_paged_decode_attention(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
                                  dev["context_lens"], case["scale"], out, ws, opts=opts)
     torch.cuda.synchronize()
-    hdr = ws[16:28].view(torch.int32).cpu().tolist()
-    splits = [max(1, -(-n // 512)) for n in lens]
-    assert hdr == [512, 3, 2 * sum(splits)]
+    hdr = ws[16:24].view(torch.int32).cpu().tolist()
+    assert hdr == [512, 3]
     check(case, out)
 
 
 def test_more_sequences_than_one_scan_chunk():
-    # 2500 sequences: the schedule kernel scans them 1024 at a time (later chunks reload their
+    # 2500 sequences: each phase-1 CTA walks them 32 at a time to its items (later chunks reload their
     # lengths from global memory); many empty and one-page contexts.
     B, T = _binding(), _tensors()
     case = synth.decode_case(seed=650, B=2500, Hq=8, Hkv=2, D=64, block_size=16, dtype=synth.F16,

@@ -77,8 +77,8 @@ def test_static_scratch_refuses_problems_that_do_not_fit():
 
 
 def test_static_scratch_keeps_a_device_plan_for_reuse():
-    # The static entry point clears only the error word, so a device plan made by one call
-    # (PKV_DECODE_DEVICE_PLAN) is reused by the next (PKV_DECODE_PLAN_READY) with new queries.
+    # A device-planned call (PKV_DECODE_DEVICE_PLAN), then one that states the plan is
+    # ready (PKV_DECODE_PLAN_READY) with new queries: both match the oracle.
     from paged_kv_gqa_table_gb300 import binding as B
     from paged_kv_gqa_table_gb300 import tensors as T
     import oracle
