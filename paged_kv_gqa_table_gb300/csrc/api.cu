@@ -416,8 +416,10 @@ int pkv::paged_decode_impl(const pkv_decode_desc* desc, const pkv_decode_opts* o
         // The rule counts the description's KV heads, as the host planner does;
         // items are per grid KV head (a pair under head pairs).
         p.plan_hdr = reinterpret_cast<int*>(ws) + kSchedHeaderWord;
+        const int hr_rule = desc->Hkv * ct.rt;
         p.rule = PlanRule{opts->partition_tokens > 0 ? P : 0, opts->partition_tokens > 0 ? 0 : opts->num_splits,
-                          (int)base_partition(desc), desc->Hkv * ct.rt, sms, ns};
+                          (int)base_partition(desc), (6 * sms + hr_rule - 1) / hr_rule, ns,
+                          (long long)desc->B * p.n_cap < (1LL << 31) ? 1 : 0};
         grid = std::min(plan_items(desc, ns), (long long)kDevicePlanCtasPerSm * sms);
     }
     record(opts ? opts->phase1_event_start : nullptr, s);

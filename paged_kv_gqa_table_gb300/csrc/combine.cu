@@ -40,15 +40,22 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
     if (live) n = row_context(p, bh, &empty);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!live) return;
-    // the device plan's partition (checked: the header may be another problem's)
-    const int P = p.sched_hdr ? device_plan_partition(p.sched_hdr[0]) : p.P;
-    const int ns = (int)min(((long long)n + P - 1) / P, (long long)p.ns_stride);
-    if (p.skip_single && ns <= 1) return;   // phase 1 wrote this row directly
     T* o = reinterpret_cast<T*>(p.out) + bh * D + lane * EPL;
     if (empty) {
+        if (p.skip_single) return;   // phase 1 wrote the zero row
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[e] = from_float<T>(0.f);
         return;
+    }
+    // Under the device plan the partition is read from the header phase 1
+    // wrote (checked: the header may be another problem's), and the first
+    // chunk's partials are loaded together with it, clamped to the row's
+    // ns_stride splits of the workspace and masked once the split count is
+    // known; under the host plan the split count comes first.
+    int ns = -1;
+    if (!p.sched_hdr) {
+        ns = (int)min(((long long)n + p.P - 1) / p.P, (long long)p.ns_stride);
+        if (p.skip_single && ns <= 1) return;   // phase 1 wrote this row directly
     }
     const float* pm = p.part_m + bh * p.ns_stride;
     const float* pl = p.part_l + bh * p.ns_stride;
@@ -57,13 +64,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
     float M = -INFINITY, L = 0.f, acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-    for (int c0 = 0; c0 < ns; c0 += CH) {
+    for (int c0 = 0;; c0 += CH) {
         // Unconditional loads (index clamped to the last split) so that all
-        // of the chunk's loads are in flight together; padding gets m = -inf.
+        // of the chunk's loads are in flight together; padding is masked.
+        const int lim = ns >= 0 ? ns : p.ns_stride;
         float m[CH], l[CH], a[CH][EPL];
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
-            const int sj = min(c0 + j, ns - 1);
+            const int sj = min(c0 + j, lim - 1);
             m[j] = __ldg(pm + sj);
             l[j] = __ldg(pl + sj);
 #pragma unroll
@@ -73,9 +81,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
                 a[j][e + 1] = v.y;
             }
         }
+        if (ns < 0) {
+            const int P = device_plan_partition(p.sched_hdr[0]);
+            ns = (int)min(((long long)n + P - 1) / P, (long long)p.ns_stride);
+            if (p.skip_single && ns <= 1) return;   // phase 1 wrote this row directly
+        }
+        // Splits past the row's last are padding: weight 0 and values 0 (a
+        // speculatively loaded one may hold anything).
 #pragma unroll
         for (int j = 0; j < CH; ++j)
-            if (c0 + j >= ns) m[j] = -INFINITY;
+            if (c0 + j >= ns) {
+                m[j] = -INFINITY;
+                l[j] = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) a[j][e] = 0.f;
+            }
         float Mc = M;
 #pragma unroll
         for (int j = 0; j < CH; ++j) Mc = fmaxf(Mc, m[j]);
@@ -91,6 +111,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
             for (int e = 0; e < EPL; ++e) acc[e] += f * a[j][e];
         }
         M = Mc;
+        if (c0 + CH >= ns) break;
     }
     const float inv = 1.f / L;
 #pragma unroll

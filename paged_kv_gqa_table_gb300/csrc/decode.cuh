@@ -100,7 +100,7 @@ struct DecodeTile {
     static constexpr int QS_MIN_BLOCKS = 4;
     __host__ __device__ static constexpr int qtile_bytes(int nt) { return q_shared(nt) ? 16 * D * 2 : 0; }
     __host__ __device__ static constexpr int smem_bytes(int nt) {
-        return 1024 + STAGES * 2 * SLICE + STAGING + qtile_bytes(nt) + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 48;
+        return 1024 + STAGES * 2 * SLICE + STAGING + qtile_bytes(nt) + STAGES * 2 * 8 + 2 * NWC * nt * 8 * 4 + 16;
     }
 };
 
@@ -140,7 +140,6 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
     float* st_m = reinterpret_cast<float*>(empty + STAGES);
     float* st_l = st_m + NWC * HP;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(st_l + NWC * HP);   // set on a wait timeout
-    volatile int* plan_sm = abort_flag + 1;   // device plan: [0] P, [1] b (-1: done), [2] kvh, [3] rt, [4] s, [5] n
 
     // Lets the combine kernel queued behind this one start its prologue as
     // soon as every CTA of this grid is running (it waits for our results).
@@ -434,46 +433,41 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
         run_item(item / p.Hkv, item % p.Hkv, rt, s, p.P, -1);
         return;
     }
-    // Device plan: consumer warp 0 plans from the context lengths and finds
-    // this CTA's items one by one (device_plan.cuh); CTA 0 publishes the
+    // Device plan (device_plan.cuh): every warp plans from the context lengths
+    // and finds this CTA's items one by one (the same in each warp, so no
+    // broadcast and no barrier precede the first item); CTA 0 publishes the
     // partition for the combine kernel.
-    if (warp == 0) {
-        int mx = 0;
-        long long sum = 0;
-        warp_context_stats(p.ctx, p.B, p.n_cap, lane, &mx, &sum);
-        if (lane == 0) {
-            const int P = device_plan_partition_rule(p.rule, mx, sum);
-            plan_sm[0] = P;
-            if (blockIdx.x == 0) {
-                p.plan_hdr[0] = P;
-                p.plan_hdr[1] = mx > 0 ? (mx - 1) / P + 1 : 1;
-            }
-        }
-    }
-    if (threadIdx.x == 0) *abort_flag = 0;
-    __syncthreads();
-    const int P = plan_sm[0];
     const int HR = p.Hkv * p.RT;
     PlanCursor cur{0, 0};
-    for (long long k = blockIdx.x;; k += gridDim.x) {
-        if (warp == 0) {
-            int b = 0, j = 0, n = 0, nsb = 1;
-            const bool found = warp_plan_item(p.ctx, p.B, p.n_cap, P, HR, k, cur, lane, &b, &j, &n, &nsb);
-            if (lane == 0) {
-                const int kr = j / nsb;
-                plan_sm[1] = found ? b : -1;
-                plan_sm[2] = kr / p.RT;
-                plan_sm[3] = kr % p.RT;
-                plan_sm[4] = j - kr * nsb;
-                plan_sm[5] = n;
-            }
+    int P = 0, b = 0, j = 0, n = 0;
+    bool found = false, only = false;
+    {
+        PlanRegs pr;
+        int mx = 0;
+        long long sum = 0, total = -1;
+        warp_context_stats(p.ctx, p.B, p.n_cap, p.rule.sum32 != 0, lane, pr, &mx, &sum);
+        P = device_plan_partition_rule(p.rule, mx, sum);
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            p.plan_hdr[0] = P;
+            p.plan_hdr[1] = mx > 0 ? (mx - 1) / P + 1 : 1;
         }
-        __syncthreads();
-        const int b = plan_sm[1];
-        if (b < 0) break;
-        run_item(b, plan_sm[2], plan_sm[3], plan_sm[4], P, plan_sm[5]);
+        const PlanDiv dv(P, HR);
+        found = warp_plan_first_item(pr, p.B, dv, blockIdx.x, cur, lane, &b, &j, &n, &total);
+        if (!found) found = warp_plan_item(p.ctx, p.B, p.n_cap, dv, blockIdx.x, cur, lane, &b, &j, &n);
+        only = total >= 0 && (long long)blockIdx.x + gridDim.x >= total;   // no second item
+    }
+    const PlanDiv dv(P, HR);
+    // Read after each item's closing barrier; an empty item does not set it.
+    if (threadIdx.x == 0) *abort_flag = 0;
+    for (long long k = blockIdx.x;; k += gridDim.x) {
+        if (k != blockIdx.x) found = warp_plan_item(p.ctx, p.B, p.n_cap, dv, k, cur, lane, &b, &j, &n);
+        if (!found) break;
+        const int s = dv.split_of(j);   // item j of a sequence: split s, then (grid KV head, row tile) kr
+        const int kr = j - s * HR;
+        run_item(b, p.RT == 1 ? kr : kr / p.RT, p.RT == 1 ? 0 : kr % p.RT, s, P, n);
+        if (only) return;           // leave at once, freeing the SM's slot for the next CTA
         fence_proxy_async_smem();   // this item's generic writes to the ring before the next item's copies
-        __syncthreads();            // every role is done with the ring, the barriers, the Q tile and plan_sm
+        __syncthreads();            // every role is done with the ring, the barriers and the Q tile
         if (*abort_flag) break;     // a wait timed out (already reported): take no further item
     }
 }
