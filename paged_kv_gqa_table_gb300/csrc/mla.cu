@@ -46,7 +46,7 @@
 // `full` barrier (cta_group::2 loads; CTA 0's producer expects the bytes of
 // both), which CTA 0's MMA thread waits on.  Its commits arrive on the
 // barriers of both CTAs (multicast): `empty` (a ring slot is free),
-// `s_full` (scores of a block in an S buffer), `p_free` (O += P.V of a block
+// `s_full` (scores of a block in an S buffer), `pv_buf` (O += P.V of a block
 // done), `mma_done`.  The softmax warps of both CTAs arrive on CTA 0's
 // `p_full` (P written over the scores), one elected lane per warp.
 //
@@ -81,7 +81,7 @@ constexpr int kVSlots = 2;                // per block: keys 0-63, 64-127 of thi
 constexpr int kStages = 5;
 constexpr int kSoftmaxWarps = 8;          // two per TMEM lane quadrant, each 64 of a block's 128 keys
 constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
-constexpr int kBars = 2 * kStages + kQChunks + 19;
+constexpr int kBars = 2 * kStages + kQChunks + 20;
 constexpr int kRedBytes = 2 * kRows * 4;   // row max / row sum exchange: [key half][row]
 constexpr int kSmemBytes = 1024 + kQChunks * kQChunk + kStages * kSlot + kRedBytes + kBars * 8 + 32;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -322,11 +322,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     uint64_t* q_free = q_full + kQChunks;      // the task's last S MMAs done: Q may be replaced (both)
     uint64_t* s_full = q_free + 1;             // [2] per S buffer: the scores are in TMEM (both CTAs)
     uint64_t* p_full = s_full + 2;             // [2] per S buffer, CTA 0: both CTAs wrote P over them
-    uint64_t* p_free = p_full + 2;             // O += P.V of the last block done (both CTAs)
-    uint64_t* mma_done = p_free + 1;
+    uint64_t* mma_done = p_full + 2;
     uint64_t* xa = mma_done + 1;               // [4] per TMEM quadrant: both softmax warps wrote `red`
     uint64_t* xb = xa + 4;                     // [4] per TMEM quadrant: both read the partner's value
     uint64_t* task_bar = xb + 4;               // [4] a task index handed out is in task_slot (both CTAs)
+    // [2] per S buffer: O += P.V of its latest block done (both CTAs).  One
+    // barrier per buffer, not one for all blocks: every wait on it then has
+    // exactly one such MMA outstanding, so the phase parity names it.  (With a
+    // single barrier, a softmax warp at the end of a task could find the P.V
+    // of its last two blocks both pending -- the last block's S completes
+    // before they are issued -- and a parity wait for the last one passed.)
+    uint64_t* pv_buf = task_bar + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* task_slot = reinterpret_cast<int*>(tmem_slot + 2);   // [4]
@@ -346,8 +352,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 2 * kSoftmaxWarps);   // every softmax warp of both CTAs
         }
-        mbar_init(p_free, 1);
         mbar_init(mma_done, 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&pv_buf[i], 1);
         for (int i = 0; i < 4; ++i) {
             mbar_init(&xa[i], 64);
             mbar_init(&xb[i], 64);
@@ -495,8 +501,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
         // buffer (the tensor core works on it while the softmax warps turn
         // S(j) into P(j)), then O += P(j).V(j).  S buffers alternate over the
         // blocks of all tasks (G counts them).  S(j + 2) reuses P(j)'s columns
-        // only after O += P(j).V(j) was issued, and the MMAs of one thread run
-        // in issue order; a task's first O += P.V overwrites O, which the
+        // only once O += P(j).V(j) has completed (pv_buf); a task's first
+        // O += P.V overwrites O, which the
         // softmax warps have read out by then (they write that block's P
         // after their epilogue).  Kept lean: the thread waits ~70 cycles per
         // issued MMA for the pipe anyway, so descriptors are formed once and
@@ -523,6 +529,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
             // 1 KB apart); 4 MMAs of 16 columns per sub-chunk
             auto issue_s = [&](int g, bool first, bool last) -> bool {
                 const uint32_t d = tmem + kColS + (g & 1) * 128;
+                // The buffer holds P(g - 2), the TMEM operand of O += P(g - 2).V:
+                // that MMA completes before these overwrite it.
+                if (g >= 2) {
+                    if (!mbar_wait(&pv_buf[g & 1], ((g - 2) >> 1) & 1)) return false;
+                    tc_fence_after();
+                }
                 for (int c = 0; c < kKSlots; ++c) {
                     if (first) {   // Q arrives chunk by chunk with the task's first block
                         if (!mbar_wait(&q_full[2 * c], n & 1) || (c < 4 && !mbar_wait(&q_full[2 * c + 1], n & 1)))
@@ -568,7 +580,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                     umma_commit_pair_mc(&empty[stage], kBothCtas);
                     next();
                 }
-                umma_commit_pair_mc(p_free, kBothCtas);
+                umma_commit_pair_mc(&pv_buf[g & 1], kBothCtas);
                 return true;
             };
             for (int r = 0; ok; ++r) {
@@ -715,7 +727,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 bool got2 = true;
                 if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
                     // O holds P(j-1).V: wait for it, then rescale this warp's rows (its 128 columns).
-                    got2 = mbar_wait(p_free, (g - 1) & 1);
+                    got2 = mbar_wait(&pv_buf[(g - 1) & 1], ((g - 1) >> 1) & 1);
                     if (__all_sync(0xffffffffu, got2 && *abort_flag == 0)) {
                         tc_fence_after();
 #pragma unroll 1
@@ -748,7 +760,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
             if (!ok) break;
             G += t.J;
             // O complete after the task's last O += P.V
-            ok = __all_sync(0xffffffffu, mbar_wait(p_free, (G - 1) & 1) && *abort_flag == 0);
+            // The S of the task's last block completing says nothing of the
+            // O += P.V of its last two blocks: wait for both.
+            bool done = t.J < 2 || mbar_wait(&pv_buf[(G - 2) & 1], ((G - 2) >> 1) & 1);
+            done = done && mbar_wait(&pv_buf[(G - 1) & 1], ((G - 1) >> 1) & 1);
+            ok = __all_sync(0xffffffffu, done && *abort_flag == 0);
             tc_fence_after();
             // the quadrant's two partial row sums (a partner that left early never
             // arrives; the bounded wait then ends with no output written)
