@@ -134,8 +134,8 @@ typedef struct {
 /* Text of a status code (static storage). */
 PKV_API const char* pkv_status_string(int status);
 
-/* ABI version of this header: 6 (5 had no pkv_static_scratch_error and staged MLA keys unpadded; 4 no plan
- * reuse; 3 no device plan; 2 no q_len; 1 no kv_dtype / k_scale / v_scale). */
+/* ABI version of this header: 7 (6 had no pkv_set_stress_delay; 5 no pkv_static_scratch_error and staged
+ * MLA keys unpadded; 4 no plan reuse; 3 no device plan; 2 no q_len; 1 no kv_dtype / k_scale / v_scale). */
 PKV_API int pkv_version(void);
 
 /*
@@ -370,6 +370,21 @@ PKV_API int pkv_paged_decode_attention_static(const pkv_decode_desc* desc, const
  * asynchronous).  Allocates nothing.
  */
 PKV_API int pkv_static_scratch_error(uint32_t* dst, pkv_stream_t stream);
+
+/*
+ * Timing perturbation for race testing.  From the next call on, the copy
+ * producer of every kernel launched by this library -- decode phase 1's page
+ * loads, the MLA prefill's Q and key loads -- pauses producer_delay_ns
+ * nanoseconds after each copy it issues (0, the default, turns it off).  The
+ * results must not change: the kernels order every consumer after its data by
+ * barriers, never by timing, and a parity test run under a delay checks that
+ * (a parity wait on a barrier two phases behind the expected one passes at
+ * once; slowing the producers is what shows such a wait).  Calls become
+ * slower; nothing else changes.  Process-wide and thread-safe; calls already
+ * enqueued keep the value they were launched with.
+ * Returns PKV_OK, or PKV_INVALID_ARG above 1,000,000 ns.
+ */
+PKV_API int pkv_set_stress_delay(uint32_t producer_delay_ns);
 
 #ifdef __cplusplus
 }

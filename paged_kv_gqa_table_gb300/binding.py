@@ -24,7 +24,7 @@ FUNCTIONS = [
     "pkv_status_string", "pkv_version", "pkv_plan_splits", "pkv_decode_workspace_size",
     "pkv_paged_decode_attention", "pkv_decode_partials", "pkv_combine", "pkv_validate_block_table",
     "pkv_paged_decode_attention_static", "pkv_static_scratch_error", "pkv_mla_workspace_size",
-    "pkv_mla_paged_prefill",
+    "pkv_mla_paged_prefill", "pkv_set_stress_delay",
 ]
 PKV_STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -79,6 +79,7 @@ def load():
     lib.pkv_validate_block_table.argtypes = [D, P, P, P, P]
     lib.pkv_paged_decode_attention_static.argtypes = [D, O, P, P, P, P, P, ctypes.c_float, P, P]
     lib.pkv_static_scratch_error.argtypes = [P, P]
+    lib.pkv_set_stress_delay.argtypes = [ctypes.c_uint32]
     lib.pkv_mla_workspace_size.argtypes = [ctypes.POINTER(pkv_mla_desc), ctypes.POINTER(SZ)]
     lib.pkv_mla_paged_prefill.argtypes = [ctypes.POINTER(pkv_mla_desc), P, P, P, P, P, P, P, ctypes.c_float,
                                           P, P, P, SZ, P]
@@ -195,6 +196,11 @@ def pkv_paged_decode_attention_static(desc, q, k_cache, v_cache, block_table, co
 def pkv_static_scratch_error(dst, stream=None) -> None:
     """Copies the static scratch's error word into dst (4 bytes, device or host memory)."""
     _check("pkv_static_scratch_error", load().pkv_static_scratch_error(_ptr(dst), _stream(stream)))
+
+
+def pkv_set_stress_delay(producer_delay_ns: int) -> None:
+    """Producer pause (ns) after each issued copy in later calls; 0 turns it off (race testing)."""
+    _check("pkv_set_stress_delay", load().pkv_set_stress_delay(int(producer_delay_ns)))
 
 
 def make_mla_desc(total_q, batch, num_pages, nnz, num_heads=16, d_ckv=512, d_kpe=64) -> pkv_mla_desc:

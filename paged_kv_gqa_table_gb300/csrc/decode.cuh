@@ -70,6 +70,7 @@ struct DecodeParams {
     // CTA 0 writes {P, splits of the longest context} to plan_hdr for the combine.
     int* plan_hdr;
     PlanRule rule;
+    uint32_t stress_ns;      // producer pause after each page's copies (pkv_set_stress_delay), 0: none
 };
 
 template <int D, int LAYOUT>
@@ -225,6 +226,7 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
                     issue_page_loads<LAYOUT, D>(kd, kd + SLICE, &tmk, &tmv, &full[stg], phys * p.Hc + HEADS * kvh,
                                                 pol);
                 }
+                if (p.stress_ns) __nanosleep(p.stress_ns);
                 issued = i + 1;
                 if ((i & 31) == 31) {
                     id_cur = id_nxt;

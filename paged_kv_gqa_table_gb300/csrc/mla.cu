@@ -433,6 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                             tma_load_2d_pair(dst + w * kSub + nn * 4096, &tm_v, bar,
                                              half * 256 + (int)rank * 128 + nn * 64, row + v * 64 + w * 32);
                 }
+                if (p.stress_ns) __nanosleep(p.stress_ns);
                 ++k;
                 if (++stage == kStages) {
                     stage = 0;
@@ -455,6 +456,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                         tma_load_2d_pair(sQ + c * kQChunk, &tm_qn, bar, c * 64, y);
                     else
                         tma_load_2d_pair(sQ + c * kQChunk, &tm_qp, bar, 0, y);
+                    if (p.stress_ns) __nanosleep(p.stress_ns);
                 };
                 // the previous task's S MMAs are done with Q
                 if (n >= 1 && !(mbar_wait(q_free, (n - 1) & 1) && *abort_flag == 0)) {

@@ -43,10 +43,19 @@ def test_library_exports_every_declared_function(B):
 
 
 def test_version_and_status_strings(B):
-    assert B.pkv_version() == 6
+    assert B.pkv_version() == 7
     assert B.status_string(0) == "ok"
     assert B.status_string(5) == "bad block table"
     assert B.status_string(99) == "unknown status"
+
+
+def test_stress_delay_accepts_its_range_on_the_host(B):
+    # a host setting only: no GPU is touched; the value is left at 0 (off)
+    B.pkv_set_stress_delay(1000000)
+    B.pkv_set_stress_delay(0)
+    with pytest.raises(B.PkvError) as e:
+        B.pkv_set_stress_delay(1000001)
+    assert e.value.status == B.PKV_INVALID_ARG
 
 
 def desc(lib, **kw):
