@@ -372,19 +372,22 @@ PKV_API int pkv_paged_decode_attention_static(const pkv_decode_desc* desc, const
 PKV_API int pkv_static_scratch_error(uint32_t* dst, pkv_stream_t stream);
 
 /*
- * Timing perturbation for race testing.  From the next call on, the copy
- * producer of every kernel launched by this library -- decode phase 1's page
- * loads, the MLA prefill's Q and key loads -- pauses producer_delay_ns
- * nanoseconds after each copy it issues (0, the default, turns it off).  The
- * results must not change: the kernels order every consumer after its data by
- * barriers, never by timing, and a parity test run under a delay checks that
- * (a parity wait on a barrier two phases behind the expected one passes at
- * once; slowing the producers is what shows such a wait).  Calls become
- * slower; nothing else changes.  Process-wide and thread-safe; calls already
- * enqueued keep the value they were launched with.
- * Returns PKV_OK, or PKV_INVALID_ARG above 1,000,000 ns.
+ * Timing perturbation for race testing.  From the next call on, in every
+ * kernel launched by this library, the copy producers -- decode phase 1's page
+ * loads, the MLA prefill's Q and key loads -- pause producer_delay_ns
+ * nanoseconds after each copy they issue, and the consumers -- decode phase
+ * 1's consumer warps after each page, the MLA prefill's MMA thread after each
+ * ring slot and its softmax warps after each key block -- pause
+ * consumer_delay_ns (0, the default, turns either off).  The results must not
+ * change: the kernels order every role after what it reads by barriers, never
+ * by timing, and a parity test run under a delay checks that (a parity wait on
+ * a barrier two phases behind the expected one passes at once; a slow role is
+ * what shows such a wait).  Calls become slower; nothing else changes.
+ * Process-wide and thread-safe; calls already enqueued keep the values they
+ * were launched with.
+ * Returns PKV_OK, or PKV_INVALID_ARG if either delay is above 1,000,000 ns.
  */
-PKV_API int pkv_set_stress_delay(uint32_t producer_delay_ns);
+PKV_API int pkv_set_stress_delay(uint32_t producer_delay_ns, uint32_t consumer_delay_ns);
 
 #ifdef __cplusplus
 }

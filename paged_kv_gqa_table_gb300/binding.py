@@ -79,7 +79,7 @@ def load():
     lib.pkv_validate_block_table.argtypes = [D, P, P, P, P]
     lib.pkv_paged_decode_attention_static.argtypes = [D, O, P, P, P, P, P, ctypes.c_float, P, P]
     lib.pkv_static_scratch_error.argtypes = [P, P]
-    lib.pkv_set_stress_delay.argtypes = [ctypes.c_uint32]
+    lib.pkv_set_stress_delay.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
     lib.pkv_mla_workspace_size.argtypes = [ctypes.POINTER(pkv_mla_desc), ctypes.POINTER(SZ)]
     lib.pkv_mla_paged_prefill.argtypes = [ctypes.POINTER(pkv_mla_desc), P, P, P, P, P, P, P, ctypes.c_float,
                                           P, P, P, SZ, P]
@@ -198,9 +198,9 @@ def pkv_static_scratch_error(dst, stream=None) -> None:
     _check("pkv_static_scratch_error", load().pkv_static_scratch_error(_ptr(dst), _stream(stream)))
 
 
-def pkv_set_stress_delay(producer_delay_ns: int) -> None:
-    """Producer pause (ns) after each issued copy in later calls; 0 turns it off (race testing)."""
-    _check("pkv_set_stress_delay", load().pkv_set_stress_delay(int(producer_delay_ns)))
+def pkv_set_stress_delay(producer_delay_ns: int, consumer_delay_ns: int = 0) -> None:
+    """Producer / consumer pauses (ns) in later calls; 0 turns each off (race testing)."""
+    _check("pkv_set_stress_delay", load().pkv_set_stress_delay(int(producer_delay_ns), int(consumer_delay_ns)))
 
 
 def make_mla_desc(total_q, batch, num_pages, nnz, num_heads=16, d_ckv=512, d_kpe=64) -> pkv_mla_desc:

@@ -20,8 +20,8 @@ namespace {
 constexpr int kBS = 16;          // compiled page size
 constexpr int kHeaderBytes = 256;
 
-// pkv_set_stress_delay: producer pause after each issued copy, read by every launch.
-std::atomic<uint32_t> g_stress_ns{0};
+// pkv_set_stress_delay: producer / consumer pauses, read by every launch.
+std::atomic<uint32_t> g_stress_ns{0}, g_stress_consumer_ns{0};
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 long long round_up(long long a, long long b) { return ceil_div(a, b) * b; }
@@ -311,6 +311,7 @@ int prepare_phase1(const pkv_decode_desc* d, int P, int NS, const void* q, const
     const bool fp8 = d->kv_dtype == PKV_FP8_E4M3;
     p->scale_log2 = (float)((double)scale * (fp8 ? (double)d->k_scale : 1.0) * 1.4426950408889634);
     p->stress_ns = g_stress_ns.load(std::memory_order_relaxed);
+    p->stress_consumer_ns = g_stress_consumer_ns.load(std::memory_order_relaxed);
     p->v_scale = fp8 ? d->v_scale : 1.f;
     if (d->max_context_len == 0) return PKV_OK;   // maps unused: every split is empty
     int st = encode_cache_map(mk, k, d, pairs ? 2 : 1);
@@ -340,9 +341,10 @@ const char* pkv_status_string(int status) {
 
 int pkv_version(void) { return 7; }
 
-int pkv_set_stress_delay(uint32_t producer_delay_ns) {
-    if (producer_delay_ns > 1000000u) return PKV_INVALID_ARG;
+int pkv_set_stress_delay(uint32_t producer_delay_ns, uint32_t consumer_delay_ns) {
+    if (producer_delay_ns > 1000000u || consumer_delay_ns > 1000000u) return PKV_INVALID_ARG;
     g_stress_ns.store(producer_delay_ns, std::memory_order_relaxed);
+    g_stress_consumer_ns.store(consumer_delay_ns, std::memory_order_relaxed);
     return PKV_OK;
 }
 
@@ -623,6 +625,7 @@ int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const vo
     p.stage_rows = (int)mla_stage_rows(d);
     p.scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
     p.stress_ns = g_stress_ns.load(std::memory_order_relaxed);
+    p.stress_consumer_ns = g_stress_consumer_ns.load(std::memory_order_relaxed);
     MlaMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     const cuuint64_t q_rows = (cuuint64_t)d.total_q * 16;

@@ -71,6 +71,7 @@ struct DecodeParams {
     int* plan_hdr;
     PlanRule rule;
     uint32_t stress_ns;      // producer pause after each page's copies (pkv_set_stress_delay), 0: none
+    uint32_t stress_consumer_ns;   // consumer warp pause after each page, 0: none
 };
 
 template <int D, int LAYOUT>
@@ -110,7 +111,9 @@ struct DecodeTile {
 // SCHED (with GEN): the CTA takes the device plan's listed items in turn
 // instead of its one grid-order item; compiled separately too, the item loop
 // costs registers.
-template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED>
+// STRESS: compiled with the pauses of pkv_set_stress_delay (race testing); the
+// ordinary instantiations have none, so the test facility costs them nothing.
+template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED, bool STRESS>
 __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const CUtensorMap& tmk,
                                                    const CUtensorMap& tmv) {
     static_assert(GEN || !SCHED, "the device plan runs the general kernel");
@@ -226,7 +229,7 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
                     issue_page_loads<LAYOUT, D>(kd, kd + SLICE, &tmk, &tmv, &full[stg], phys * p.Hc + HEADS * kvh,
                                                 pol);
                 }
-                if (p.stress_ns) __nanosleep(p.stress_ns);
+                if (STRESS && p.stress_ns) __nanosleep(p.stress_ns);
                 issued = i + 1;
                 if ((i & 31) == 31) {
                     id_cur = id_nxt;
@@ -338,6 +341,7 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[stg]);
             }
+            if (STRESS && p.stress_consumer_ns) __nanosleep(p.stress_consumer_ns);
         }
         if (!ok && lane == 0 && p.err) atomicOr(p.err, kErrTimeout);
 
@@ -474,32 +478,32 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
     }
 }
 
-template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED>
+template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED, bool STRESS>
 __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     decode_phase1_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv) {
-    decode_phase1_body<T, LAYOUT, D, NT, GEN, SCHED>(p, tmk, tmv);
+    decode_phase1_body<T, LAYOUT, D, NT, GEN, SCHED, STRESS>(p, tmk, tmv);
 }
 
 // The same for the shared-Q tiles, compiled for four CTAs per SM.
-template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED>
+template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED, bool STRESS>
 __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32, DecodeTile<D, LAYOUT>::QS_MIN_BLOCKS)
     decode_phase1_kernel_qs(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv) {
-    decode_phase1_body<T, LAYOUT, D, NT, GEN, SCHED>(p, tmk, tmv);
+    decode_phase1_body<T, LAYOUT, D, NT, GEN, SCHED, STRESS>(p, tmk, tmv);
 }
 
 // Host-side launcher for one instantiation (one-token without bias, general,
-// or general over the device plan's items).
-template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED>
+// or general over the device plan's items; STRESS: with the race-testing pauses).
+template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED, bool STRESS>
 cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                          const CUtensorMap& tmv, cudaStream_t stream) {
     using Tile = DecodeTile<D, LAYOUT>;
     auto kern = [] {   // only the entry this instantiation uses is compiled
         if constexpr (Tile::q_shared(NT))
-            return decode_phase1_kernel_qs<T, LAYOUT, D, NT, GEN, SCHED>;
+            return decode_phase1_kernel_qs<T, LAYOUT, D, NT, GEN, SCHED, STRESS>;
         else
-            return decode_phase1_kernel<T, LAYOUT, D, NT, GEN, SCHED>;
+            return decode_phase1_kernel<T, LAYOUT, D, NT, GEN, SCHED, STRESS>;
     }();
     const int smem = Tile::smem_bytes(NT);
     static std::atomic<bool> attr_set[kMaxDevices];
@@ -515,13 +519,22 @@ cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, 
     return cudaGetLastError();
 }
 
+template <typename T, int LAYOUT, int D, int NT, bool STRESS>
+cudaError_t launch_decode_phase1_kind(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
+                                      const CUtensorMap& tmv, cudaStream_t stream) {
+    if (p.plan_hdr)
+        return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, true, STRESS>(p, grid, tmk, tmv, stream);
+    if (p.alibi || p.q_len > 1)
+        return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, false, STRESS>(p, grid, tmk, tmv, stream);
+    return launch_decode_phase1_variant<T, LAYOUT, D, NT, false, false, STRESS>(p, grid, tmk, tmv, stream);
+}
+
 template <typename T, int LAYOUT, int D, int NT>
 cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                  const CUtensorMap& tmv, cudaStream_t stream) {
-    if (p.plan_hdr) return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, true>(p, grid, tmk, tmv, stream);
-    if (p.alibi || p.q_len > 1)
-        return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, false>(p, grid, tmk, tmv, stream);
-    return launch_decode_phase1_variant<T, LAYOUT, D, NT, false, false>(p, grid, tmk, tmv, stream);
+    if (p.stress_ns || p.stress_consumer_ns)
+        return launch_decode_phase1_kind<T, LAYOUT, D, NT, true>(p, grid, tmk, tmv, stream);
+    return launch_decode_phase1_kind<T, LAYOUT, D, NT, false>(p, grid, tmk, tmv, stream);
 }
 
 // Head pairs (kLayoutNHD8x2, D = 128, one column tile); under the device plan
@@ -529,11 +542,7 @@ cudaError_t launch_decode_phase1(const DecodeParams& p, long long grid, const CU
 template <typename T>
 cudaError_t launch_decode_phase1_pairs(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                        const CUtensorMap& tmv, cudaStream_t stream) {
-    if (p.plan_hdr)
-        return launch_decode_phase1_variant<T, kLayoutNHD8x2, 128, 1, true, true>(p, grid, tmk, tmv, stream);
-    if (p.alibi || p.q_len > 1)
-        return launch_decode_phase1_variant<T, kLayoutNHD8x2, 128, 1, true, false>(p, grid, tmk, tmv, stream);
-    return launch_decode_phase1_variant<T, kLayoutNHD8x2, 128, 1, false, false>(p, grid, tmk, tmv, stream);
+    return launch_decode_phase1<T, kLayoutNHD8x2, 128, 1>(p, grid, tmk, tmv, stream);
 }
 
 }  // namespace pkv

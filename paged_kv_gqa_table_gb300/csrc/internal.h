@@ -60,6 +60,7 @@ struct MlaParams {
     int stage_rows;                // rows of `stage`: nnz + 128 * batch (0 without keys)
     float scale_log2;              // sm_scale * log2(e)
     uint32_t stress_ns;            // producer pause after each issued copy (pkv_set_stress_delay), 0: none
+    uint32_t stress_consumer_ns;   // MMA thread / softmax warp pause after each slot / block, 0: none
 };
 
 constexpr int kMlaStageRowBytes = (512 + 64) * 2;

@@ -305,6 +305,9 @@ __device__ __forceinline__ MlaTask mla_task(const MlaParams& p, int idx, uint32_
     return t;
 }
 
+// STRESS: compiled with the pauses of pkv_set_stress_delay (race testing); the
+// ordinary instantiation has none, so the test facility costs it nothing.
+template <bool STRESS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     mla_prefill_kernel(const MlaParams p, const __grid_constant__ CUtensorMap tm_qn,
                        const __grid_constant__ CUtensorMap tm_qp, const __grid_constant__ CUtensorMap tm_k,
@@ -433,7 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                             tma_load_2d_pair(dst + w * kSub + nn * 4096, &tm_v, bar,
                                              half * 256 + (int)rank * 128 + nn * 64, row + v * 64 + w * 32);
                 }
-                if (p.stress_ns) __nanosleep(p.stress_ns);
+                if (STRESS && p.stress_ns) __nanosleep(p.stress_ns);
                 ++k;
                 if (++stage == kStages) {
                     stage = 0;
@@ -456,7 +459,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                         tma_load_2d_pair(sQ + c * kQChunk, &tm_qn, bar, c * 64, y);
                     else
                         tma_load_2d_pair(sQ + c * kQChunk, &tm_qp, bar, 0, y);
-                    if (p.stress_ns) __nanosleep(p.stress_ns);
+                    if (STRESS && p.stress_ns) __nanosleep(p.stress_ns);
                 };
                 // the previous task's S MMAs are done with Q
                 if (n >= 1 && !(mbar_wait(q_free, (n - 1) & 1) && *abort_flag == 0)) {
@@ -557,6 +560,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                     }
                     umma_commit_pair_mc(&empty[stage], kBothCtas);
                     next();
+                    if (STRESS && p.stress_consumer_ns) __nanosleep(p.stress_consumer_ns);
                 }
                 umma_commit_pair_mc(&s_full[g & 1], kBothCtas);
                 if (last) umma_commit_pair_mc(q_free, kBothCtas);   // Q no longer read
@@ -581,6 +585,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                                                   !first || (v | w | kk) != 0);
                     umma_commit_pair_mc(&empty[stage], kBothCtas);
                     next();
+                    if (STRESS && p.stress_consumer_ns) __nanosleep(p.stress_consumer_ns);
                 }
                 umma_commit_pair_mc(&pv_buf[g & 1], kBothCtas);
                 return true;
@@ -758,6 +763,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&p_full[g & 1]), 0));
+                if (STRESS && p.stress_consumer_ns) __nanosleep(p.stress_consumer_ns);
             }
             if (!ok) break;
             G += t.J;
@@ -816,8 +822,12 @@ cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStre
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     e = once_per_device(attr_set, attr_mu, dev, [] {
-        return cudaFuncSetAttribute(mla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    mla::kSmemBytes);
+        cudaError_t r = cudaFuncSetAttribute(mla_prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             mla::kSmemBytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(mla_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     mla::kSmemBytes);
+        return r;
     });
     if (e != cudaSuccess) return e;
     if (p.max_tasks <= 0) return cudaSuccess;
@@ -842,7 +852,9 @@ cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mla_prefill_kernel, p, maps.q_nope, maps.q_pe, maps.kv, maps.v);
+    if (p.stress_ns || p.stress_consumer_ns)
+        return cudaLaunchKernelEx(&cfg, mla_prefill_kernel<true>, p, maps.q_nope, maps.q_pe, maps.kv, maps.v);
+    return cudaLaunchKernelEx(&cfg, mla_prefill_kernel<false>, p, maps.q_nope, maps.q_pe, maps.kv, maps.v);
 }
 
 }  // namespace pkv

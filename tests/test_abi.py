@@ -51,11 +51,12 @@ def test_version_and_status_strings(B):
 
 def test_stress_delay_accepts_its_range_on_the_host(B):
     # a host setting only: no GPU is touched; the value is left at 0 (off)
-    B.pkv_set_stress_delay(1000000)
-    B.pkv_set_stress_delay(0)
-    with pytest.raises(B.PkvError) as e:
-        B.pkv_set_stress_delay(1000001)
-    assert e.value.status == B.PKV_INVALID_ARG
+    B.pkv_set_stress_delay(1000000, 1000000)
+    B.pkv_set_stress_delay(0, 0)
+    for bad in ((1000001, 0), (0, 1000001)):
+        with pytest.raises(B.PkvError) as e:
+            B.pkv_set_stress_delay(*bad)
+        assert e.value.status == B.PKV_INVALID_ARG
 
 
 def desc(lib, **kw):

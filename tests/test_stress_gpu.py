@@ -1,13 +1,15 @@
-"""Parity under perturbed producer timing (pkv_set_stress_delay).
+"""Parity under perturbed timing (pkv_set_stress_delay).
 
 Every kernel of the library orders its consumers after their data with
 barriers.  A wait that relies on timing instead -- for instance a parity wait
 on a barrier that can run two phases behind the expected one -- passes the
-ordinary parity tests as long as the producers are fast, and fails once they
-are slow.  These tests slow the copy producers (a pause after each issued
-page, Q chunk or key slot) and compare the results with the fp64 oracle: the
-MLA prefill kernel's task epilogue once had such a wait, and a run with a
-slowed producer made every small MLA case fail.
+ordinary parity tests as long as every role runs at its usual pace, and fails
+once one of them is slow.  These tests slow the copy producers (a pause after
+each issued page, Q chunk or key slot) or the consumers (decode consumer warps
+after each page; the MLA MMA thread after each ring slot and its softmax warps
+after each key block) and compare the results with the fp64 oracle: the MLA
+prefill kernel's task epilogue once had such a wait, and a run with a slowed
+producer made every small MLA case fail.
 """
 import numpy as np
 import pytest
@@ -24,10 +26,10 @@ TOL = {synth.F16: 4e-3, synth.BF16: 1.6e-2}
 @pytest.fixture
 def stress():
     from paged_kv_gqa_table_gb300 import binding as B
-    def set_delay(ns):
-        B.pkv_set_stress_delay(ns)
+    def set_delay(producer_ns, consumer_ns):
+        B.pkv_set_stress_delay(producer_ns, consumer_ns)
     yield set_delay
-    B.pkv_set_stress_delay(0)
+    B.pkv_set_stress_delay(0, 0)
 
 
 MLA_CASES = [
@@ -38,12 +40,12 @@ MLA_CASES = [
 ]
 
 
-@pytest.mark.parametrize("delay_ns", [300, 2000])
+@pytest.mark.parametrize("delays", [(300, 0), (2000, 0), (0, 1000)])
 @pytest.mark.parametrize("idx", range(len(MLA_CASES)))
-def test_mla_parity_with_slow_producers(stress, idx, delay_ns):
+def test_mla_parity_with_slow_roles(stress, idx, delays):
     from paged_kv_gqa_table_gb300 import tensors as T
     import oracle
-    stress(delay_ns)
+    stress(*delays)
     case = synth.mla_case(seed=40 + idx, poison=True, **MLA_CASES[idx])
     desc = T.mla_desc(case)
     ws = T.mla_workspace_for(desc)
@@ -67,13 +69,14 @@ DECODE_CASES = [
 ]
 
 
+@pytest.mark.parametrize("delays", [(1000, 0), (0, 1000)])
 @pytest.mark.parametrize("device_plan", [False, True])
 @pytest.mark.parametrize("idx", range(len(DECODE_CASES)))
-def test_decode_parity_with_slow_producers(stress, idx, device_plan):
+def test_decode_parity_with_slow_roles(stress, idx, device_plan, delays):
     from paged_kv_gqa_table_gb300 import binding as B
     from paged_kv_gqa_table_gb300 import tensors as T
     import oracle
-    stress(1000)
+    stress(*delays)
     case = synth.decode_case(seed=70 + idx, block_size=16, max_blocks_per_seq=200, poison=True,
                              **DECODE_CASES[idx])
     opts = B.make_opts(device_plan=True) if device_plan else None
