@@ -134,7 +134,7 @@ typedef struct {
 /* Text of a status code (static storage). */
 PKV_API const char* pkv_status_string(int status);
 
-/* ABI version of this header: 7 (6 had no pkv_set_stress_delay; 5 no pkv_static_scratch_error and staged
+/* ABI version of this header: 8 (7 had no pkv_mla_desc.max_kv_len; 6 no pkv_set_stress_delay; 5 no pkv_static_scratch_error and staged
  * MLA keys unpadded; 4 no plan reuse; 3 no device plan; 2 no q_len; 1 no kv_dtype / k_scale / v_scale). */
 PKV_API int pkv_version(void);
 
@@ -268,6 +268,13 @@ typedef struct {
     int batch;      /* sequences; qo_indptr and kv_indptr hold batch + 1 entries */
     int num_pages;  /* rows of ckv_cache and kpe_cache */
     int nnz;        /* kv_indptr[batch] (entries of kv_indices), or an upper bound of it */
+    int max_kv_len; /* an upper bound of every sequence's kv_len, or 0 (none given).  With a
+                     * bound, S = Q.K^T is computed once per 16-token row tile: the tasks of the
+                     * first 256 output columns export each key block's softmax weights P
+                     * (bf16) and rescale factors, and a second kernel computes the other 256
+                     * columns from them (bit-identical to computing S again); the workspace
+                     * grows accordingly (pkv_mla_workspace_size).  Without one, each half of
+                     * the output columns computes S itself. */
 } pkv_mla_desc;
 
 /*
@@ -277,10 +284,15 @@ typedef struct {
  * sequence (plus one); then nnz + 128 * batch staged key rows of 1152 bytes
  * (ckv 512 + kpe 64 bf16; every sequence's keys start on a multiple of 128
  * rows, the rows in between are zero; no rows when nnz == 0); each part
- * rounded up to 256 bytes.  The workspace must be 256-byte aligned.  Word 0
- * of the header collects device-side error bits (bit 0: a pipeline wait
- * timed out; bit 1: kv_indptr[batch] > nnz, so keys past nnz were not staged
- * and the result is unspecified); zero it once after allocating.
+ * rounded up to 256 bytes.  With max_kv_len > 0, also, for up to
+ * E = (ceil(total_q / 16) + batch) * ceil(max_kv_len / 128) exported key
+ * blocks, 66,576 bytes each (P 65,536, rescale factors 1,024, flags 16), and
+ * 1 KB of row sums plus 4 bytes per row tile.  The workspace must be 256-byte
+ * aligned.  Word 0 of the header collects device-side error bits (bit 0: a
+ * pipeline wait timed out; bit 1: kv_indptr[batch] > nnz, so keys past nnz
+ * were not staged and the result is unspecified; bit 2: some kv_len exceeds
+ * max_kv_len, the export did not fit and the second half of the output
+ * columns is unspecified); zero it once after allocating.
  */
 PKV_API int pkv_mla_workspace_size(const pkv_mla_desc* desc, size_t* bytes);
 

@@ -47,7 +47,7 @@ class pkv_decode_opts(ctypes.Structure):
 class pkv_mla_desc(ctypes.Structure):
     _fields_ = [("total_q", ctypes.c_int), ("num_heads", ctypes.c_int), ("d_ckv", ctypes.c_int),
                 ("d_kpe", ctypes.c_int), ("batch", ctypes.c_int), ("num_pages", ctypes.c_int),
-                ("nnz", ctypes.c_int)]
+                ("nnz", ctypes.c_int), ("max_kv_len", ctypes.c_int)]
 
 
 class PkvError(RuntimeError):
@@ -203,9 +203,9 @@ def pkv_set_stress_delay(producer_delay_ns: int, consumer_delay_ns: int = 0) -> 
     _check("pkv_set_stress_delay", load().pkv_set_stress_delay(int(producer_delay_ns), int(consumer_delay_ns)))
 
 
-def make_mla_desc(total_q, batch, num_pages, nnz, num_heads=16, d_ckv=512, d_kpe=64) -> pkv_mla_desc:
+def make_mla_desc(total_q, batch, num_pages, nnz, num_heads=16, d_ckv=512, d_kpe=64, max_kv_len=0) -> pkv_mla_desc:
     return pkv_mla_desc(int(total_q), int(num_heads), int(d_ckv), int(d_kpe), int(batch), int(num_pages),
-                        int(nnz))
+                        int(nnz), int(max_kv_len))
 
 
 def pkv_mla_workspace_size(desc) -> int:

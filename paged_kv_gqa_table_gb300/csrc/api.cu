@@ -235,15 +235,16 @@ int encode_cache_map(CUtensorMap* map, const void* base, const pkv_decode_desc* 
 }
 
 // Row-major 2-D bf16 tensor {cols, rows} with a {box_cols, box_rows} box and
-// 128-byte swizzle (box_cols * 2 <= 128).
+// 128-byte swizzle (box_cols * 2 <= 128), or none (the box copied as it is).
 int encode_rows_map(CUtensorMap* map, const void* base, cuuint64_t cols, cuuint64_t rows, cuuint32_t box_cols,
-                    cuuint32_t box_rows) {
+                    cuuint32_t box_rows, bool swizzle = true) {
     auto fn = encode_fn();
     if (!fn) return PKV_CUDA_ERROR;
     cuuint64_t dims[2] = {cols, rows}, strides[1] = {cols * 2};
     cuuint32_t box[2] = {box_cols, box_rows}, estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PKV_OK : PKV_INVALID_ARG;
 }
@@ -339,7 +340,7 @@ const char* pkv_status_string(int status) {
     }
 }
 
-int pkv_version(void) { return 7; }
+int pkv_version(void) { return 8; }
 
 int pkv_set_stress_delay(uint32_t producer_delay_ns, uint32_t consumer_delay_ns) {
     if (producer_delay_ns > 1000000u || consumer_delay_ns > 1000000u) return PKV_INVALID_ARG;
@@ -543,6 +544,12 @@ static long long mla_max_tasks(const pkv_mla_desc& d) {
     return 2 * (((long long)d.total_q + 15) / 16 + d.batch);
 }
 
+// Exported key blocks with a max_kv_len bound: every row tile sees at most
+// ceil(max_kv_len / 128) blocks.
+static long long mla_export_blocks(const pkv_mla_desc& d) {
+    return d.max_kv_len > 0 ? mla_max_tasks(d) / 2 * (((long long)d.max_kv_len + 127) / 128) : 0;
+}
+
 static int check_mla_desc(const pkv_mla_desc* desc) {
     if (!desc) return PKV_INVALID_ARG;
     const pkv_mla_desc& d = *desc;
@@ -552,15 +559,18 @@ static int check_mla_desc(const pkv_mla_desc* desc) {
     if (d.total_q > 0 && d.batch == 0) return PKV_INVALID_ARG;
     if (d.num_heads != 16 || d.d_ckv != 512 || d.d_kpe != 64) return PKV_UNSUPPORTED;
     if ((long long)d.total_q * d.num_heads * d.d_ckv > (long long)1 << 40) return PKV_UNSUPPORTED;
+    if (d.max_kv_len < 0) return PKV_INVALID_ARG;
     if (mla_stage_rows(d) > INT_MAX || mla_max_tasks(d) > INT_MAX / 2) return PKV_UNSUPPORTED;
+    if (mla_export_blocks(d) > INT_MAX / 512) return PKV_UNSUPPORTED;   // rows of the P tensor map
     return PKV_OK;
 }
 
 // Workspace: 256-byte header | task list (16 bytes per task) | first row tile
 // of each sequence (batch + 1 ints) | first staged row of each sequence
-// (batch ints) | staged key rows.
+// (batch ints) | staged key rows | with max_kv_len > 0: export base per row
+// tile | exported P | rescale factors | flags | row sums.
 struct MlaLayout {
-    size_t tasks, seq_tile, seq_row, stage, total;
+    size_t tasks, seq_tile, seq_row, stage, exp_base, exp_p, exp_alpha, exp_flag, exp_l, total;
 };
 static MlaLayout mla_layout(const pkv_mla_desc& d) {
     MlaLayout l;
@@ -568,7 +578,13 @@ static MlaLayout mla_layout(const pkv_mla_desc& d) {
     l.seq_tile = l.tasks + align256((size_t)mla_max_tasks(d) * 16);
     l.seq_row = l.seq_tile + align256((size_t)(d.batch + 1) * 4);
     l.stage = l.seq_row + align256((size_t)d.batch * 4);
-    l.total = l.stage + align256((size_t)mla_stage_rows(d) * kMlaStageRowBytes);
+    l.exp_base = l.stage + align256((size_t)mla_stage_rows(d) * kMlaStageRowBytes);
+    const size_t e = (size_t)mla_export_blocks(d), tiles = e > 0 ? (size_t)mla_max_tasks(d) / 2 : 0;
+    l.exp_p = l.exp_base + align256(tiles * 4);
+    l.exp_alpha = l.exp_p + align256(e * 65536);
+    l.exp_flag = l.exp_alpha + align256(e * 1024);
+    l.exp_l = l.exp_flag + align256(e * 16);
+    l.total = l.exp_l + align256(tiles * 1024);
     return l;
 }
 
@@ -617,6 +633,15 @@ int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const vo
     p.seq_tile = reinterpret_cast<int*>(ws + lay.seq_tile);
     p.seq_row = reinterpret_cast<int*>(ws + lay.seq_row);
     p.stage = ws + lay.stage;
+    p.exp_cap = (int)mla_export_blocks(d);
+    p.replay = p.exp_cap > 0 && d.num_pages > 0 && d.nnz > 0;
+    if (p.replay) {
+        p.exp_base = reinterpret_cast<int*>(ws + lay.exp_base);
+        p.exp_p = reinterpret_cast<__nv_bfloat16*>(ws + lay.exp_p);
+        p.exp_alpha = reinterpret_cast<float*>(ws + lay.exp_alpha);
+        p.exp_flag = ws + lay.exp_flag;
+        p.exp_l = reinterpret_cast<float*>(ws + lay.exp_l);
+    }
     p.max_tasks = (int)mla_max_tasks(d);
     p.total_q = d.total_q;
     p.batch = d.batch;
@@ -634,6 +659,8 @@ int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, const vo
     const cuuint64_t stage_rows = (cuuint64_t)p.stage_rows;
     if (st == PKV_OK && d.num_pages > 0 && stage_rows > 0) st = encode_rows_map(&maps.kv, p.stage, 576, stage_rows, 64, 64);
     if (st == PKV_OK && d.num_pages > 0 && stage_rows > 0) st = encode_rows_map(&maps.v, p.stage, 576, stage_rows, 64, 32);
+    if (st == PKV_OK && p.replay)
+        st = encode_rows_map(&maps.p_exp, p.exp_p, 64, (cuuint64_t)p.exp_cap * 512, 64, 128, false);
     if (st != PKV_OK) return st;
     TraceRange r("pkv::mla.prefill");
     return launch_mla_prefill(p, maps, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK

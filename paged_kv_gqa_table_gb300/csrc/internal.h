@@ -52,8 +52,20 @@ struct MlaParams {
                                    // output half << 30), most key blocks first (built on the device)
     int* seq_tile;                 // [batch + 1] first 16-token row tile of each sequence
     int* seq_row;                  // [batch] first staged row of each sequence
-    int* task_count;               // header words 1-3: tasks listed, of them with keys (listed
-                                   // first), next task with keys to hand out
+    int* task_count;               // header words 1-6: tasks listed, of them with keys (listed
+                                   // first), next task with keys to hand out; replay list: next
+                                   // task to hand out, tasks, first entry
+    // Replay (max_kv_len > 0): the tasks of the first output half export each key
+    // block's bf16 P, the factor O was rescaled by before it and the final row
+    // sums; mla_replay_kernel computes the second half from them (S once per tile).
+    int replay;                    // 1: export, and list the second half for the replay kernel
+    int* exp_base;                 // [tiles] first export block of the tile at each list position
+    __nv_bfloat16* exp_p;          // [exp_cap][2 CTAs][2 key halves][8][128 rows][8 keys]: key half
+                                   // chunk-major (keys 8q .. 8q + 7 of all rows, then q + 1)
+    float* exp_alpha;              // [exp_cap][2 CTAs][128 rows]
+    uint8_t* exp_flag;             // [exp_cap][2 CTAs][8 softmax warps]: some row of the warp rescaled
+    float* exp_l;                  // [tiles][2 CTAs][128 rows] final row sums
+    int exp_cap;                   // export blocks the workspace holds
     int max_tasks;                 // 2 * (ceil(total_q / 16) + batch)
     uint32_t* err;                 // header word 0
     int total_q, batch, num_pages, nnz;
@@ -74,7 +86,7 @@ constexpr int kMlaSeqAlign = 128;
 // block) or {64, 32} boxes (v: V chunk blocks), all with 128-byte swizzle.
 // kv and v are unused (zero) when the pool is empty.
 struct MlaMaps {
-    CUtensorMap q_nope, q_pe, kv, v;
+    CUtensorMap q_nope, q_pe, kv, v, p_exp;   // p_exp: exp_p as {64, exp_cap * 512}, {64, 128} boxes, no swizzle
 };
 
 cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStream_t stream);

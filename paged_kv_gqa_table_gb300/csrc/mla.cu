@@ -198,23 +198,57 @@ __device__ void mla_build_tasks(const MlaParams& p) {
     }
     __syncthreads();
     // bin 0 starts after every tile with keys
+    const int keyed = bins[0];
+    __syncthreads();   // every thread read bins[0] before the positions are taken
+    // Without replay: list position i holds both output halves of its tile,
+    // entries 2i and 2i + 1.  With replay: entry i holds the first half of the
+    // i-th tile with keys, the second half is entry L + i of the replay list
+    // (L = keyed + 2 * tiles without keys); tiles without keys keep both
+    // halves, entries keyed + 2 j and + 1.
+    const int L = p.replay ? T + (T - keyed) : 0;
     if (tid == 0) {
-        p.task_count[1] = min(2 * bins[0], p.max_tasks);
+        p.task_count[1] = p.replay ? keyed : min(2 * keyed, p.max_tasks);
         p.task_count[2] = 0;   // next task with keys to hand out
+        p.task_count[3] = 0;   // next replay task to hand out
+        p.task_count[4] = p.replay ? max(0, min(keyed, p.max_tasks - L)) : 0;
+        p.task_count[5] = L;
     }
-    __syncthreads();
     for (int t = tid; t < T; t += 256) {
         const int b = seq_of(t);
         const int tt = t - p.seq_tile[b];
         const int J = mla_tile_blocks(p, b, tt);
         const int pos = atomicAdd(&bins[min(J, kTaskBins - 1)], 1);
-        if (2 * pos + 1 < p.max_tasks) {
-            const int4 e = make_int4(b, tt * mla::kPairTok, p.seq_row[b], J);
-            p.tasks[2 * pos] = e;
-            p.tasks[2 * pos + 1] = make_int4(e.x, e.y, e.z, e.w | (1 << 30));
+        const int4 e = make_int4(b, tt * mla::kPairTok, p.seq_row[b], J);
+        const int4 e1 = make_int4(e.x, e.y, e.z, e.w | (1 << 30));
+        if (!p.replay) {
+            if (2 * pos + 1 < p.max_tasks) {
+                p.tasks[2 * pos] = e;
+                p.tasks[2 * pos + 1] = e1;
+            }
+        } else if (J > 0) {   // L + pos < 2 T <= max_tasks
+            if (L + pos < p.max_tasks) {
+                p.tasks[pos] = e;
+                p.tasks[L + pos] = e1;
+            }
+        } else if (pos + (pos - keyed) + 1 < p.max_tasks) {
+            p.tasks[keyed + 2 * (pos - keyed)] = e;
+            p.tasks[keyed + 2 * (pos - keyed) + 1] = e1;
         }
     }
-    if (tid == 0) p.task_count[0] = min(2 * T, p.max_tasks);
+    if (tid == 0) p.task_count[0] = min(p.replay ? L : 2 * T, p.max_tasks);
+    if (!p.replay) return;
+    // export blocks: the listed tiles' key blocks in list order
+    __syncthreads();   // the task entries are written (global, same block)
+    int carry = 0;
+    for (int base = 0; base < keyed; base += 256) {
+        const int i = base + tid;
+        const int J = i < keyed ? (p.tasks[i].w & 0x3FFFFFFF) : 0;
+        int total = 0;
+        const int ex = block_scan_256(J, sbuf, &total);
+        if (i < keyed) p.exp_base[i] = carry + ex;
+        carry += total;
+    }
+    if (tid == 0 && carry > p.exp_cap) atomicOr(p.err, 4u);   // a kv_len above max_kv_len
 }
 
 // Block 0 builds the task list; every block stages key rows: sequence b's keys
@@ -371,6 +405,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     }
     // the task list and the staged keys are written by the preceding grid
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the replay grid may start its set-up once every CTA of this one runs (it
+    // waits for this grid's completion before reading the export)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int n_tasks = p.task_count[0], n_keyed = p.task_count[1];
     tc_fence_before();
     cluster_sync();   // both CTAs: barriers initialised, TMEM allocated
@@ -663,6 +700,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
             const int lim = t.prefix + tok;   // last visible key of this row
             // keys <= this are visible to every row of this CTA: blocks below it need no mask
             const int unmasked_below = min(t.prefix + t.tok0, t.n_keys - 1);
+            // replay: the first half's tasks export their blocks for the second
+            const int xb0 = (p.replay && t.half == 0) ? p.exp_base[idx] : 0;
+            const bool xp = p.replay && t.half == 0 && xb0 + t.J <= p.exp_cap;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < t.J; ++j) {
                 const int g = G + j;
@@ -758,6 +798,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) pk[i] = Mma<__nv_bfloat16>::pack(s[2 * i], s[2 * i + 1]);
                     tmem_st32(t_s, pk);   // over this warp's own scores, already read
+                    if (xp) {   // P (keys 2i, 2i + 1 in word i), the factor O was rescaled by, the flag
+                        // P chunk-major: 16 bytes (8 keys) of each row, row after row, so that
+                        // each store of the warp writes 512 contiguous bytes
+                        const size_t eb = (size_t)(xb0 + j) * 2 + rank;
+                        uint4* dst = reinterpret_cast<uint4*>(p.exp_p + (eb * 2 + kh) * (kRows * 64)) + row;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q * kRows] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        if (kh == 0) p.exp_alpha[eb * kRows + row] = alpha;
+                        const bool any = __any_sync(0xffffffffu, j >= 1 && alpha != 1.f);
+                        if (lane == 0) p.exp_flag[eb * 8 + (warp - 2)] = any ? 1 : 0;
+                    }
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -780,6 +832,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
             ok = __all_sync(0xffffffffu, ok && mla_swap(&xa[quad], &xb[quad], x, my_red, peer_red, l, l_peer));
             if (!ok) break;
             l += l_peer;
+            if (xp && kh == 0) p.exp_l[((size_t)idx * 2 + rank) * kRows + row] = l;
             const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
             for (int c = 0; c < 128 / 32; ++c) {
@@ -815,6 +868,344 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     if (warp == 1) tmem_dealloc_pair(tmem, 512);
 }
 
+namespace mla {
+constexpr int kRStages = 12;              // replay ring: P chunks and V slots, 16 KB each
+constexpr int kRBars = 2 * kRStages + 10;
+constexpr int kRSmemBytes = 1024 + kRStages * kSlot + kRBars * 8 + 32;
+static_assert(kRSmemBytes <= 232448, "shared memory per CTA");
+}  // namespace mla
+
+// The second output half of every row tile with keys, from what the first
+// half's tasks exported (replay): per key block j, O += P(j).V(j) with the
+// exported bf16 P(j) as the shared-memory A operand (copied as exported:
+// K-major without swizzle, 8 keys of every row per 2 KB, so that the
+// exporting warps' stores are coalesced), and before a block for which the first half
+// rescaled its O, the same rescale of this O by the exported factors; at the
+// end O / l with the exported row sums.  The arithmetic is the first half
+// task's, so the result equals computing S again for this half.
+//
+// Same pairs as the prefill kernel: CTA r holds rows 128r .. 128r + 127 of
+// the tile, their 256 output columns O in TMEM, and loads its 128 rows of
+// each P chunk (keys 64c .. 64c + 63 of a block) and 128 of the 256 output
+// columns of V; CTA 0's one thread issues the MMAs (M = 256, N = 256).
+// Ring order per block: P chunk 0, V keys 0-63, P chunk 1, V keys 64-127.
+// A rescale is a hand-off: the MMA thread lets every MMA issued so far
+// complete (drain), asks the scale warps of both CTAs (resc_req), and waits
+// for all of them (resc_done) before the block's MMAs.  Each request is
+// answered before the next, and each task's O is read out (o_free) before
+// the next task's first MMA overwrites it, so every wait has one phase
+// outstanding.
+template <bool STRESS>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
+    mla_replay_kernel(const MlaParams p, const __grid_constant__ CUtensorMap tm_p,
+                      const __grid_constant__ CUtensorMap tm_v) {
+    using namespace mla;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sRing = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + kRStages * kSlot);
+    uint64_t* full = bars;                     // [kRStages] CTA 0: both CTAs' copies of a slot landed
+    uint64_t* empty = bars + kRStages;         // [kRStages] the MMAs read the slot (both CTAs)
+    uint64_t* resc_req = empty + kRStages;     // O may be rescaled (both CTAs)
+    uint64_t* resc_done = resc_req + 1;        // CTA 0: every scale warp of both CTAs rescaled
+    uint64_t* o_ready = resc_done + 1;         // the task's MMAs are done (both CTAs)
+    uint64_t* o_free = o_ready + 1;            // CTA 0: every warp of both CTAs read O out
+    uint64_t* drain = o_free + 1;              // CTA 0: the MMAs issued so far are done
+    uint64_t* mma_done = drain + 1;            // both CTAs: the last MMA is done
+    uint64_t* task_bar = mma_done + 1;         // [4] a task index handed out is in task_slot (both CTAs)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kRBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* task_slot = reinterpret_cast<int*>(tmem_slot + 2);   // [4]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();   // 0 issues the MMAs
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(resc_req, 1);
+        mbar_init(resc_done, 2 * kSoftmaxWarps);
+        mbar_init(o_ready, 1);
+        mbar_init(o_free, 2 * kSoftmaxWarps);
+        mbar_init(drain, 1);
+        mbar_init(mma_done, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&task_bar[i], 1);
+        fence_barrier_init();
+        *abort_flag = 0;
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, 256);
+        tmem_relinquish_pair();
+    }
+    // the lists and the export are written by the preceding grids
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int n_rep = p.task_count[4], L = p.task_count[5];
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // replay tasks handed out one at a time by CTA 0's producer (as in the prefill kernel)
+    auto hand_out = [&](int r) -> int {
+        int pos = atomicAdd(&p.task_count[3], 1);
+        if (pos >= n_rep) pos = -1;
+        task_slot[r & 3] = pos;
+        st_shared_cluster(mapa_shared(smem_u32(&task_slot[r & 3]), 1), pos);
+        mbar_arrive(&task_bar[r & 3]);
+        mbar_arrive_release_cluster(mapa_shared(smem_u32(&task_bar[r & 3]), 1));
+        return pos;
+    };
+    auto next_task = [&](int r) -> int {
+        if (!mbar_wait_acq_cluster(&task_bar[r & 3], (r >> 2) & 1)) return -2;
+        return *reinterpret_cast<volatile int*>(&task_slot[r & 3]);
+    };
+    // some row of the pair was rescaled before export block xb (16 flag bytes)
+    auto flags_of = [&](int xb) -> uint4 { return *reinterpret_cast<const uint4*>(p.exp_flag + (size_t)xb * 16); };
+    auto any_flag = [](uint4 f) { return (f.x | f.y | f.z | f.w) != 0u; };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tensormap(&tm_p);
+            prefetch_tensormap(&tm_v);
+            const bool lead = rank == 0;
+            bool ok = true;
+            int k = 0, stage = 0;   // ring slots, ring index
+            uint32_t phase = 0;
+            // P chunk c of export block xb (this CTA's 128 rows), or V keys
+            // row + 64c .. + 63 (this CTA's 128 of the second half's columns)
+            auto load = [&](int xb, int row, int c, bool is_p) -> bool {
+                if (k >= kRStages && !(mbar_wait(&empty[stage], phase ^ 1) && *abort_flag == 0)) return false;
+                uint8_t* dst = sRing + stage * kSlot;
+                const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+                if (lead) mbar_arrive_expect_tx(&full[stage], 2 * kSlot);
+                if (is_p) {
+                    tma_load_2d_pair(dst, &tm_p, bar, 0, ((xb * 2 + (int)rank) * 2 + c) * kRows);
+                } else {
+#pragma unroll
+                    for (int w = 0; w < 2; ++w)
+#pragma unroll
+                        for (int nn = 0; nn < 2; ++nn)
+                            tma_load_2d_pair(dst + w * kSub + nn * 4096, &tm_v, bar, 256 + (int)rank * 128 + nn * 64,
+                                             row + c * 64 + w * 32);
+                }
+                if (STRESS && p.stress_ns) __nanosleep(p.stress_ns);
+                ++k;
+                if (++stage == kRStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+                return true;
+            };
+            for (int r = 0; ok; ++r) {
+                const int pos = lead ? hand_out(r) : next_task(r);
+                if (pos < 0) {
+                    ok = pos == -1;
+                    break;
+                }
+                const int4 e = p.tasks[L + pos];
+                const int J = e.w & 0x3FFFFFFF, xb0 = p.exp_base[pos];
+                for (int j = 0; j < J && ok; ++j)
+                    for (int c = 0; c < 2 && ok; ++c) {
+                        ok = load(xb0 + j, 0, c, true);
+                        ok = ok && load(0, e.z + j * kKeys, c, false);
+                    }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(p.err, kErrTimeout);
+            }
+            // CTA 0: no copy into either CTA's shared memory still in flight
+            if (lead)
+                for (int kk = max(0, k - kRStages); kk < k; ++kk) mbar_wait(&full[kk % kRStages], (kk / kRStages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1 && rank == 1) {
+        if (lane == 0) mbar_wait(mma_done, 0);
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ CTA 0: the MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = umma_idesc_bf16_f32(2 * kRows, 256, true);
+            // P: K-major without swizzle, as exported: 8 keys (16 bytes) of 128 rows per 2 KB,
+            // 8-row core matrices 128 bytes apart
+            const uint64_t da = umma_desc_noswizzle(smem_u32(sRing), 2048, 128);
+            const uint64_t dv = umma_desc_sw128(smem_u32(sRing), 4096, 1024);   // V: MN-major, as in the prefill kernel
+            bool ok = true;
+            int stage = 0, n = 0, nreq = 0;   // ring index, tasks done, rescales (= drains) requested
+            uint32_t phase = 0;
+            auto next = [&]() {
+                if (++stage == kRStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            };
+            for (int r = 0; ok; ++r) {
+                const int pos = next_task(r);
+                if (pos < 0) {
+                    ok = pos == -1;
+                    break;
+                }
+                const int4 e = p.tasks[L + pos];
+                const int J = e.w & 0x3FFFFFFF, xb0 = p.exp_base[pos];
+                const bool fits = xb0 + J <= p.exp_cap;
+                // the previous task's O is read out before this task's first MMA overwrites it
+                if (n >= 1) {
+                    if (!(mbar_wait_acq_cluster(o_free, (n - 1) & 1) && *abort_flag == 0)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                uint4 fl = make_uint4(0u, 0u, 0u, 0u);   // flags of block j, loaded a block ahead
+                if (fits && J > 1) fl = flags_of(xb0 + 1);
+                for (int j = 0; j < J && ok; ++j) {
+                    uint4 f = make_uint4(0u, 0u, 0u, 0u);
+                    if (j >= 1) {
+                        f = fl;
+                        if (fits && j + 1 < J) fl = flags_of(xb0 + j + 1);
+                    }
+                    if (j >= 1 && any_flag(f)) {
+                        umma_commit_pair_mc(drain, 1);   // O += P(j - 1).V and all before it
+                        ok = mbar_wait(drain, nreq & 1);
+                        tc_fence_after();
+                        mbar_arrive(resc_req);
+                        mbar_arrive_release_cluster(mapa_shared(smem_u32(resc_req), 1));
+                        ok = ok && mbar_wait_acq_cluster(resc_done, nreq & 1) && *abort_flag == 0;
+                        ++nreq;
+                        tc_fence_after();
+                        if (!ok) break;
+                    }
+                    for (int c = 0; c < 2 && ok; ++c) {
+                        if (!mbar_wait(&full[stage], phase)) {
+                            ok = false;
+                            break;
+                        }
+                        const int sp = stage;
+                        const uint64_t a0 = da + (uint64_t)((stage * kSlot) >> 4);
+                        next();
+                        if (!mbar_wait(&full[stage], phase)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint64_t b0 = dv + (uint64_t)((stage * kSlot) >> 4);
+                        // keys 16i .. 16i + 15 of the chunk: A key groups 2i, 2i + 1 (4 KB per
+                        // 16 keys), B rows of V sub-chunk i / 2 (2 KB per 16 keys)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            umma_bf16_pair(tmem, a0 + (uint64_t)((i * 4096) >> 4),
+                                           b0 + (uint64_t)((((i >> 1) * kSub) + (i & 1) * 2048) >> 4), idesc,
+                                           (j | c | i) != 0);
+                        umma_commit_pair_mc(&empty[sp], kBothCtas);
+                        umma_commit_pair_mc(&empty[stage], kBothCtas);
+                        next();
+                        if (STRESS && p.stress_consumer_ns) __nanosleep(p.stress_consumer_ns);
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair_mc(o_ready, kBothCtas);
+                ++n;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(p.err, kErrTimeout);
+            }
+            umma_commit_pair_mc(mma_done, kBothCtas);
+            mbar_wait(mma_done, 0);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------- rescale and epilogue
+        // Warp (quad, kh) as in the prefill kernel: rows quad * 32 + lane, O
+        // columns 128 kh .. 128 kh + 127 of this half.
+        const int quad = warp & 3;
+        const int kh = (warp - 2) >> 2;
+        const int row = quad * 32 + lane;
+        const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16);
+        int n = 0, nreq = 0;
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+            int pos = 0;
+            if (lane == 0) pos = next_task(r);
+            pos = __shfl_sync(0xffffffffu, pos, 0);
+            if (pos < 0) {
+                ok = pos == -1;
+                break;
+            }
+            const MlaTask t = mla_task(p, L + pos, rank);
+            const int xb0 = p.exp_base[pos];
+            const bool fits = xb0 + t.J <= p.exp_cap;
+            const float l = fits ? p.exp_l[((size_t)pos * 2 + rank) * kRows + row] : 0.f;
+            for (int j = 1; j < t.J && fits; ++j) {
+                if (!any_flag(flags_of(xb0 + j))) continue;
+                const bool got = mbar_wait_acq_cluster(resc_req, nreq & 1);
+                ++nreq;
+                if (!__all_sync(0xffffffffu, got && *abort_flag == 0)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const size_t eb = (size_t)(xb0 + j) * 2 + rank;
+                if (p.exp_flag[eb * 8 + (warp - 2)]) {   // this warp's rows: as the first half did
+                    const float alpha = p.exp_alpha[eb * kRows + row];
+#pragma unroll 1
+                    for (int c = 0; c < 128 / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(t_row + kh * 128 + c * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(t_row + kh * 128 + c * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(resc_done), 0));
+            }
+            if (!ok) break;
+            ok = __all_sync(0xffffffffu, mbar_wait(o_ready, n & 1) && *abort_flag == 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int tok = t.tok0 + row / kHeads;
+            const bool live = row / kHeads < t.ntok;
+            const size_t tq = (size_t)(t.q0 + tok);
+            __nv_bfloat16* orow = p.out + (tq * kHeads + row % kHeads) * kDc + 256 + kh * 128;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < 128 / 32; ++c) {
+                float o[32];
+                tmem_ld32(t_row + kh * 128 + c * 32, o);
+                tmem_wait_ld();
+                if (live) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 v;
+                        v.x = Mma<__nv_bfloat16>::pack(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+                        v.y = Mma<__nv_bfloat16>::pack(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+                        v.z = Mma<__nv_bfloat16>::pack(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+                        v.w = Mma<__nv_bfloat16>::pack(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
+                        reinterpret_cast<uint4*>(orow + c * 32)[q4] = v;
+                    }
+                }
+            }
+            tc_fence_before();   // O read out before the next task's first MMA overwrites it
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(o_free), 0));
+            ++n;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0) atomicOr(p.err, kErrTimeout);
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, 256);
+}
+
 cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStream_t stream) {
     static std::atomic<bool> attr_set[kMaxDevices];
     static std::mutex attr_mu;
@@ -827,6 +1218,12 @@ cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStre
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(mla_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      mla::kSmemBytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(mla_replay_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     mla::kRSmemBytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(mla_replay_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     mla::kRSmemBytes);
         return r;
     });
     if (e != cudaSuccess) return e;
@@ -852,9 +1249,15 @@ cudaError_t launch_mla_prefill(const MlaParams& p, const MlaMaps& maps, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.stress_ns || p.stress_consumer_ns)
-        return cudaLaunchKernelEx(&cfg, mla_prefill_kernel<true>, p, maps.q_nope, maps.q_pe, maps.kv, maps.v);
-    return cudaLaunchKernelEx(&cfg, mla_prefill_kernel<false>, p, maps.q_nope, maps.q_pe, maps.kv, maps.v);
+    const bool stress = p.stress_ns || p.stress_consumer_ns;
+    e = stress ? cudaLaunchKernelEx(&cfg, mla_prefill_kernel<true>, p, maps.q_nope, maps.q_pe, maps.kv, maps.v)
+               : cudaLaunchKernelEx(&cfg, mla_prefill_kernel<false>, p, maps.q_nope, maps.q_pe, maps.kv, maps.v);
+    if (e != cudaSuccess || !p.replay) return e;
+    // the second output half from the export: the same persistent pairs, a
+    // programmatic dependent of the prefill grid (set-up overlaps its tail)
+    cfg.dynamicSmemBytes = mla::kRSmemBytes;
+    return stress ? cudaLaunchKernelEx(&cfg, mla_replay_kernel<true>, p, maps.p_exp, maps.v)
+                  : cudaLaunchKernelEx(&cfg, mla_replay_kernel<false>, p, maps.p_exp, maps.v);
 }
 
 }  // namespace pkv

@@ -104,9 +104,13 @@ def decode_partials(case: dict, dev: dict | None = None, opts=None, capacity: in
     return P2, ns2, m.double().cpu().numpy(), l.double().cpu().numpy(), acc.double().cpu().numpy()
 
 
-def mla_desc(case: dict) -> B.pkv_mla_desc:
-    return B.make_mla_desc(case["total_q"], case["batch"], case["num_pages"], int(case["kv_indptr"][-1]),
-                           case["H"], case["Dc"], case["Dr"])
+def mla_desc(case: dict, replay: bool = True) -> B.pkv_mla_desc:
+    """The call's description; replay=True passes the longest kv_len as max_kv_len (S once per
+    row tile, the second output half replayed from the first's softmax weights)."""
+    kv = np.asarray(case["kv_indptr"], dtype=np.int64)
+    max_kv = int(np.max(kv[1:] - kv[:-1], initial=0)) if replay else 0
+    return B.make_mla_desc(case["total_q"], case["batch"], case["num_pages"], int(kv[-1]),
+                           case["H"], case["Dc"], case["Dr"], max_kv_len=max_kv)
 
 
 def upload_mla_case(case: dict, device="cuda") -> dict:

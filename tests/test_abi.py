@@ -43,7 +43,7 @@ def test_library_exports_every_declared_function(B):
 
 
 def test_version_and_status_strings(B):
-    assert B.pkv_version() == 7
+    assert B.pkv_version() == 8
     assert B.status_string(0) == "ok"
     assert B.status_string(5) == "bad block table"
     assert B.status_string(99) == "unknown status"
@@ -253,7 +253,13 @@ def test_mla_workspace_size_and_argument_checks(B):
         tasks = 2 * ((2866 + 15) // 16 + batch)
         want = 256 + al(tasks * 16) + al((batch + 1) * 4) + al(batch * 4) + al(rows * 1152)
         assert B.pkv_mla_workspace_size(d) == want
-    for bad in (dict(nnz=-1), dict(total_q=-1), dict(num_pages=-3)):
+        # with a max_kv_len bound: per row tile an export base and 1 KB of row sums,
+        # per possible exported key block 64 KB of P, 1 KB of factors, 16 flag bytes
+        for max_kv in (1, 128, 129, 2124):
+            e = tasks // 2 * ((max_kv + 127) // 128)
+            want_r = want + al(tasks // 2 * 4) + al(e * 65536) + al(e * 1024) + al(e * 16) + al(tasks // 2 * 1024)
+            assert B.pkv_mla_workspace_size(B.make_mla_desc(2866, batch, 9000, nnz, max_kv_len=max_kv)) == want_r
+    for bad in (dict(nnz=-1), dict(total_q=-1), dict(num_pages=-3), dict(max_kv_len=-1)):
         kw = dict(total_q=100, batch=2, num_pages=50, nnz=40)
         kw.update(bad)
         with pytest.raises(B.PkvError) as e:

@@ -16,9 +16,11 @@ pytestmark = [pytest.mark.gpu,
 TOL_OUT, TOL_LSE = 1.6e-2, 1e-3
 
 
-def gpu_mla(case):
+def gpu_mla(case, replay=True):
+    """replay=True (the default of tensors.mla_desc) passes max_kv_len: S once per row tile,
+    the second output half computed from the first's exported softmax weights."""
     from paged_kv_gqa_table_gb300 import tensors
-    out, lse = tensors.mla_paged_prefill(case)
+    out, lse = tensors.mla_paged_prefill(case, desc=tensors.mla_desc(case, replay=replay))
     torch.cuda.synchronize()
     return out.double().cpu().numpy(), lse.double().cpu().numpy()
 
@@ -134,12 +136,14 @@ def test_mla_non_finite_rows_stay_in_their_sequence(seed):
     assert float(np.max(np.abs(lse[keep] - ref_lse[keep]))) <= TOL_LSE
 
 
-def _run_with(case, nnz=None, fill=None):
+def _run_with(case, nnz=None, fill=None, max_kv_len=None):
     from paged_kv_gqa_table_gb300 import binding as B
     from paged_kv_gqa_table_gb300 import tensors
     desc = tensors.mla_desc(case)
     if nnz is not None:
         desc.nnz = int(nnz)
+    if max_kv_len is not None:
+        desc.max_kv_len = int(max_kv_len)
     ws = tensors.mla_workspace_for(desc)
     if fill is not None:
         ws[256:].fill_(fill)           # leave the error header zeroed
@@ -185,3 +189,40 @@ def test_mla_random_case_matches_oracle(i):
     if case["total_q"] == 0:
         pytest.skip("no query token")
     check(case, *gpu_mla(case))
+
+
+REPLAY_CASES = SMALL + [dict(batch=3, q_len_range=(40, 200), prefix_range=(300, 1500), slack_pages=4)]
+
+
+@pytest.mark.parametrize("idx", range(len(REPLAY_CASES)))
+def test_mla_replay_is_bit_identical_to_computing_s_twice(idx):
+    """With max_kv_len, the second 256 output columns come from the first half's
+    exported softmax weights, rescale factors and row sums instead of a second
+    S = Q.K^T; the arithmetic is the one the second half's own task did, so the
+    outputs and LSEs equal those of the call without the bound bit for bit."""
+    case = synth.mla_case(seed=50 + idx, poison=True, **REPLAY_CASES[idx])
+    a = gpu_mla(case, replay=False)
+    b = gpu_mla(case, replay=True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    check(case, *b)
+
+
+def test_mla_replay_full_size_is_bit_identical():
+    case = synth.mla_case(seed=0, **synth.MLA_WORKLOADS["mla_prefill_h16"])
+    a = gpu_mla(case, replay=False)
+    b = gpu_mla(case, replay=True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_mla_export_overflow_is_reported():
+    """max_kv_len below the longest kv_len: the export does not fit the
+    workspace; error bit 2 is set, nothing outside the workspace is touched,
+    and the first 256 output columns and the LSEs still match the oracle."""
+    case = synth.mla_case(seed=23, batch=3, q_len_range=(30, 60), prefix_range=(400, 900))
+    out, lse, err = _run_with(case, max_kv_len=100, fill=0xFF)
+    assert err == 4
+    T = case["total_q"]
+    ref_out, ref_lse = np.full(out.shape, np.nan), np.full(lse.shape, np.nan)
+    oracle.mla(case, 0, T, out=ref_out, lse=ref_lse)
+    assert float(np.max(np.abs(out[:, :, :256] - ref_out[:, :, :256]))) <= TOL_OUT
+    assert float(np.max(np.abs(lse - ref_lse))) <= TOL_LSE
