@@ -793,28 +793,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                     ok = false;
                     break;
                 }
-                {
-                    uint32_t pk[32];
+                uint32_t pk[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) pk[i] = Mma<__nv_bfloat16>::pack(s[2 * i], s[2 * i + 1]);
-                    tmem_st32(t_s, pk);   // over this warp's own scores, already read
-                    if (xp) {   // P (keys 2i, 2i + 1 in word i), the factor O was rescaled by, the flag
-                        // P chunk-major: 16 bytes (8 keys) of each row, row after row, so that
-                        // each store of the warp writes 512 contiguous bytes
-                        const size_t eb = (size_t)(xb0 + j) * 2 + rank;
-                        uint4* dst = reinterpret_cast<uint4*>(p.exp_p + (eb * 2 + kh) * (kRows * 64)) + row;
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q * kRows] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                        if (kh == 0) p.exp_alpha[eb * kRows + row] = alpha;
-                        const bool any = __any_sync(0xffffffffu, j >= 1 && alpha != 1.f);
-                        if (lane == 0) p.exp_flag[eb * 8 + (warp - 2)] = any ? 1 : 0;
-                    }
-                }
+                for (int i = 0; i < 32; ++i) pk[i] = Mma<__nv_bfloat16>::pack(s[2 * i], s[2 * i + 1]);
+                tmem_st32(t_s, pk);   // over this warp's own scores, already read
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&p_full[g & 1]), 0));
+                if (xp) {
+                    // The export, after p_full so that O += P.V need not wait for it: P
+                    // (keys 2i, 2i + 1 in word i) chunk-major, 16 bytes (8 keys) of each
+                    // row, row after row, so that each store of the warp writes 512
+                    // contiguous bytes; the factor O was rescaled by; the flag.
+                    const size_t eb = (size_t)(xb0 + j) * 2 + rank;
+                    uint4* dst = reinterpret_cast<uint4*>(p.exp_p + (eb * 2 + kh) * (kRows * 64)) + row;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[q * kRows] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    if (kh == 0) p.exp_alpha[eb * kRows + row] = alpha;
+                    const bool any = __any_sync(0xffffffffu, j >= 1 && alpha != 1.f);
+                    if (lane == 0) p.exp_flag[eb * 8 + (warp - 2)] = any ? 1 : 0;
+                }
                 if (STRESS && p.stress_consumer_ns) __nanosleep(p.stress_consumer_ns);
             }
             if (!ok) break;
