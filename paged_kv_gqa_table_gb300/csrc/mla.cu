@@ -27,9 +27,17 @@
 // 128 output columns (its half of the N = 256 columns of O += P.V), 8 KB each,
 // two per 16 KB slot of a 5-slot ring, in the 128-byte-swizzled layout of the
 // UMMA descriptors.  A one-SM tile would read all of every chunk; the pair
-// halves the L2-to-SM bytes per MMA.  O in TMEM is why the two halves of the
-// output are separate pairs that each compute S (1.53x the algorithmic
-// tensor work).
+// halves the L2-to-SM bytes per MMA.  O in TMEM (256 of the 512 columns) is
+// why the two halves of the output are separate tasks.
+//
+// S once per tile (replay, when the caller bounds kv_len): only the first
+// half's tasks run here; each exports its key blocks' bf16 P (chunk-major,
+// 8 keys of all 128 rows per 2 KB, so that the softmax warps' stores are
+// coalesced), the factor O was rescaled by before each block, one flag per
+// softmax warp (did any row rescale) and the final row sums.
+// mla_replay_kernel, the next grid, computes the other half from them with
+// the same arithmetic, so S = Q.K^T runs once per tile; without the bound
+// each half computes S itself (1.53x the algorithmic tensor work).
 //
 // Page size 1 makes every key its own page.  Gathering 128-byte row pieces
 // per tile (up to ~100 tiles read each key) keeps too few bytes in flight
