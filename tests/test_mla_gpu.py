@@ -226,3 +226,23 @@ def test_mla_export_overflow_is_reported():
     oracle.mla(case, 0, T, out=ref_out, lse=ref_lse)
     assert float(np.max(np.abs(out[:, :, :256] - ref_out[:, :, :256]))) <= TOL_OUT
     assert float(np.max(np.abs(lse - ref_lse))) <= TOL_LSE
+
+
+@pytest.mark.parametrize("i", range(10))
+def test_mla_replay_random_cases_are_bit_identical(i):
+    """Seeded random batches (as test_mla_random_case_matches_oracle draws
+    them): the replayed second half equals the two-task result bit for bit,
+    and both match the oracle."""
+    import random
+    r = random.Random(7000 + i)
+    batch = r.randint(1, 5)
+    q_lens = [r.choice([0, 1, r.randint(1, 70), 8, 9, 16, 17]) for _ in range(batch)]
+    prefixes = [r.choice([0, r.randint(0, 600), 127, 128, 129, 255, 256]) for _ in range(batch)]
+    case = synth.mla_case(seed=100 + i, batch=batch, q_len_range=(1, 1), prefix_range=(0, 0), q_lens=q_lens,
+                          prefixes=prefixes, slack_pages=r.randint(0, 5), poison=True)
+    if case["total_q"] == 0:
+        pytest.skip("no query token")
+    a = gpu_mla(case, replay=False)
+    b = gpu_mla(case, replay=True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    check(case, *b)
