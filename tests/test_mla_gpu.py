@@ -246,3 +246,35 @@ def test_mla_replay_random_cases_are_bit_identical(i):
     b = gpu_mla(case, replay=True)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
     check(case, *b)
+
+
+def test_mla_long_sequence_shares_the_last_task_bin():
+    """A 300,000-key prefix: both of its row tiles hold 2,344 key blocks of 128,
+    above the 2,047 at which the task builder's block-count bins stop being
+    distinct, and its export spans 2,345 blocks per row tile.  The replayed
+    second half equals the two-task result bit for bit; every token of a short
+    sequence beside it, and sampled (token, head) pairs at the long sequence's
+    row-tile edges, match the oracle.  Heads are independent in the method, so
+    one head of a token is the oracle run on the query sliced to that head."""
+    case = synth.mla_case(seed=61, batch=2, q_len_range=(1, 1), prefix_range=(0, 0), q_lens=[24, 40],
+                          prefixes=[300_000, 1_000], slack_pages=5, poison=True)
+    a = gpu_mla(case, replay=False)
+    b = gpu_mla(case, replay=True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    got_out, got_lse = b
+    check(case, got_out, got_lse, tokens=list(range(24, 64)))
+    pairs = [(0, 0), (0, 11), (15, 4), (16, 15), (23, 7), (23, 8)]
+
+    def one(th):
+        t, h = th
+        sub = dict(case, H=1, q_nope=np.ascontiguousarray(case["q_nope"][:, h:h + 1]),
+                   q_pe=np.ascontiguousarray(case["q_pe"][:, h:h + 1]))
+        o, l = oracle.mla(sub, t, t + 1, out=np.full((case["total_q"], 1, 512), np.nan),
+                          lse=np.full((case["total_q"], 1), np.nan))
+        return o[t, 0], l[t, 0]
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(len(pairs)) as ex:
+        refs = list(ex.map(one, pairs))
+    for (t, h), (ro, rl) in zip(pairs, refs):
+        assert float(np.max(np.abs(got_out[t, h] - ro))) <= TOL_OUT, (t, h)
+        assert abs(float(got_lse[t, h]) - float(rl)) <= TOL_LSE, (t, h)
