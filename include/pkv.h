@@ -134,7 +134,7 @@ typedef struct {
 /* Text of a status code (static storage). */
 PKV_API const char* pkv_status_string(int status);
 
-/* ABI version of this header: 8 (7 had no pkv_mla_desc.max_kv_len; 6 no pkv_set_stress_delay; 5 no pkv_static_scratch_error and staged
+/* ABI version of this header: 9 (8 kept no split table for PKV_DECODE_PLAN_READY; 7 had no pkv_mla_desc.max_kv_len; 6 no pkv_set_stress_delay; 5 no pkv_static_scratch_error and staged
  * MLA keys unpadded; 4 no plan reuse; 3 no device plan; 2 no q_len; 1 no kv_dtype / k_scale / v_scale). */
 PKV_API int pkv_version(void);
 
@@ -162,10 +162,13 @@ PKV_API int pkv_plan_splits(const pkv_decode_desc* desc, const pkv_decode_opts* 
  * and these options (256-byte header, then fp32 split partials m, l
  * [B][q_len][Hq][NS] and acc [B][q_len][Hq][NS][D] when the plan has more
  * than one split; with PKV_DECODE_DEVICE_PLAN, NS is the split count of the
- * bounds).
+ * bounds and a split table of B * NS 16-byte entries follows; each of the
+ * four arrays starts on a 256-byte boundary).
  * num_sms as for pkv_plan_splits.  The workspace must be 256-byte aligned.
  * Word 0 of the header collects device-side error bits (bit 0: a pipeline
- * wait timed out); zero it once after allocating.
+ * wait timed out; bit 1: a call with PKV_DECODE_PLAN_READY found no valid
+ * plan of its problem in the workspace, and rows it could not place are
+ * unspecified); zero it once after allocating.
  */
 PKV_API int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_decode_opts* opts, int num_sms,
                               size_t* bytes);
@@ -207,11 +210,19 @@ PKV_API int pkv_decode_workspace_size(const pkv_decode_desc* desc, const pkv_dec
  * launches no CTA per empty split, and no planning kernel runs before it.
  * pkv_decode_partials does not take this flag.
  *
- * flags & PKV_DECODE_PLAN_READY (with PKV_DECODE_DEVICE_PLAN): states that an
- * earlier device-planned call with the same desc, partition options and
- * context_lens values ran on this workspace before this call (the layers of
- * one decode step).  Every device-planned call plans inside phase 1, so the
- * flag changes nothing in this version; it stays valid.
+ * A device-planned call also leaves its plan in the workspace: the partition,
+ * the split count and a table with the sequence, split and context length of
+ * every split of the plan.
+ *
+ * flags & PKV_DECODE_PLAN_READY (with PKV_DECODE_DEVICE_PLAN): states that the
+ * last device-planned call on this workspace had the same desc, partition
+ * options and context_lens values and completed without error bits (the
+ * layers of one decode step), and that no other call used the workspace
+ * since.  Phase 1 then takes its items from that plan instead of planning;
+ * the workspace keeps it for further such calls.  Every value read from the
+ * workspace is checked against the bounds first: if the statement is false,
+ * the result is unspecified and error bit 1 may be set, but no memory
+ * outside the arguments is accessed.
  */
 PKV_API int pkv_paged_decode_attention(const pkv_decode_desc* desc, const pkv_decode_opts* opts,
                                const void* q, const void* k_cache, const void* v_cache,

@@ -152,13 +152,17 @@ long long plan_items(const pkv_decode_desc* d, int ns) {
     return (long long)d->B * d->Hkv * column_tiles(d).rt * ns;
 }
 
-// Workspace: 256-byte header | split partials (more than one split).
+// The device plan's split table: a 16-byte entry per (sequence, split) of the bounds.
+size_t plan_table_bytes(const pkv_decode_desc* d, int ns) { return align256((size_t)d->B * ns * 16); }
+
+// Workspace: 256-byte header | split partials (more than one split) | the
+// device plan's split table (with PKV_DECODE_DEVICE_PLAN).
 size_t required_workspace(const pkv_decode_desc* d, const pkv_decode_opts* o, int ns) {
-    (void)o;
-    return kHeaderBytes + (ns > 1 ? partial_bytes(d, ns) : 0);
+    return kHeaderBytes + (ns > 1 ? partial_bytes(d, ns) : 0) + (device_plan(o) ? plan_table_bytes(d, ns) : 0);
 }
 
-// Header words of the device plan: {P, splits of the longest context}.
+// Header words of the device plan: {P, splits of the longest context, splits
+// of the plan (the table's entries)}.
 constexpr int kSchedHeaderWord = 4;
 // Phase-1 CTAs of the device plan: enough to fill the GPU many times over;
 // more items than this are taken in turns.
@@ -340,7 +344,7 @@ const char* pkv_status_string(int status) {
     }
 }
 
-int pkv_version(void) { return 8; }
+int pkv_version(void) { return 9; }
 
 int pkv_set_stress_delay(uint32_t producer_delay_ns, uint32_t consumer_delay_ns) {
     if (producer_delay_ns > 1000000u || consumer_delay_ns > 1000000u) return PKV_INVALID_ARG;
@@ -430,6 +434,8 @@ int pkv::paged_decode_impl(const pkv_decode_desc* desc, const pkv_decode_opts* o
         // The rule counts the description's KV heads, as the host planner does;
         // items are per grid KV head (a pair under head pairs).
         p.plan_hdr = reinterpret_cast<int*>(ws) + kSchedHeaderWord;
+        p.plan_tab = reinterpret_cast<int4*>(parts + (ns > 1 ? partial_bytes(desc, ns) : 0));
+        p.plan_ready = (opts->flags & PKV_DECODE_PLAN_READY) ? 1 : 0;
         const int hr_rule = desc->Hkv * ct.rt;
         p.rule = PlanRule{opts->partition_tokens > 0 ? P : 0, opts->partition_tokens > 0 ? 0 : opts->num_splits,
                           (int)base_partition(desc), (6 * sms + hr_rule - 1) / hr_rule, ns,

@@ -67,8 +67,12 @@ struct DecodeParams {
     int partials_only;       // 1: always write partials (+ sentinels), never out
     // Device plan (plan_hdr != nullptr): every CTA plans from ctx with `rule`
     // and takes the non-empty items blockIdx.x, blockIdx.x + gridDim.x, ...;
-    // CTA 0 writes {P, splits of the longest context} to plan_hdr for the combine.
+    // CTA 0 writes {P, splits of the longest context} to plan_hdr[0..1] for the
+    // combine, and the plan's splits go to plan_tab (plan_hdr[2] of them) for
+    // the calls that reuse it (plan_ready).
     int* plan_hdr;
+    int4* plan_tab;          // [B * rule.NS_cap] {sequence, split, clamped context, 0} in item order
+    int plan_ready;          // 1: take the items from plan_hdr / plan_tab instead of planning
     PlanRule rule;
     uint32_t stress_ns;      // producer pause after each page's copies (pkv_set_stress_delay), 0: none
     uint32_t stress_consumer_ns;   // consumer warp pause after each page, 0: none
@@ -108,15 +112,18 @@ struct DecodeTile {
 
 // GEN: the general kernel (several query tokens per sequence, ALiBi), compiled
 // separately so that the one-token kernel without bias keeps its registers.
-// SCHED (with GEN): the CTA takes the device plan's listed items in turn
-// instead of its one grid-order item; compiled separately too, the item loop
-// costs registers.
+// SCHED (with GEN): the CTA takes the device plan's items in turn instead of
+// its one grid-order item, planning them (kSchedPlan) or reading them from the
+// plan an earlier call left (kSchedReuse); each compiled separately, since the
+// item loops cost registers and the kernel with shared Q tiles is at its limit.
 // STRESS: compiled with the pauses of pkv_set_stress_delay (race testing); the
 // ordinary instantiations have none, so the test facility costs them nothing.
-template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED, bool STRESS>
+constexpr int kSchedGrid = 0, kSchedPlan = 1, kSchedReuse = 2;
+
+template <typename T, int LAYOUT, int D, int NT, bool GEN, int SCHED, bool STRESS>
 __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const CUtensorMap& tmk,
                                                    const CUtensorMap& tmv) {
-    static_assert(GEN || !SCHED, "the device plan runs the general kernel");
+    static_assert(GEN || SCHED == kSchedGrid, "the device plan runs the general kernel");
     using Tile = DecodeTile<D, LAYOUT>;
     constexpr bool KV8 = LAYOUT == kLayoutNHD8 || LAYOUT == kLayoutNHD8x2;
     constexpr int HEADS = Tile::HEADS;
@@ -427,7 +434,7 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
         }
     };   // run_item
 
-    if constexpr (!SCHED) {   // grid order: this CTA's one item
+    if constexpr (SCHED == kSchedGrid) {   // grid order: this CTA's one item
         int item = blockIdx.x;
         const int s = item % p.NS;
         item /= p.NS;
@@ -439,46 +446,93 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
         run_item(item / p.Hkv, item % p.Hkv, rt, s, p.P, -1);
         return;
     }
-    // Device plan (device_plan.cuh): every warp plans from the context lengths
-    // and finds this CTA's items one by one (the same in each warp, so no
-    // broadcast and no barrier precede the first item); CTA 0 publishes the
-    // partition for the combine kernel.
     const int HR = p.Hkv * p.RT;
-    PlanCursor cur{0, 0};
-    int P = 0, b = 0, j = 0, n = 0;
-    bool found = false, only = false;
-    {
-        PlanRegs pr;
-        int mx = 0;
-        long long sum = 0, total = -1;
-        warp_context_stats(p.ctx, p.B, p.n_cap, p.rule.sum32 != 0, lane, pr, &mx, &sum);
-        P = device_plan_partition_rule(p.rule, mx, sum);
-        if (blockIdx.x == 0 && threadIdx.x == 0) {
-            p.plan_hdr[0] = P;
-            p.plan_hdr[1] = mx > 0 ? (mx - 1) / P + 1 : 1;
+    if constexpr (SCHED == kSchedReuse) {
+        // The plan an earlier call of the same problem and context lengths
+        // left in the workspace: the partition and split count from the
+        // header, and item k's sequence, split and context from entry k / HR
+        // of the table (a split's HR items are consecutive).  The first entry
+        // is requested before the header arrives.  Every value is checked
+        // against the bounds before use, so a workspace without this
+        // problem's plan costs wrong rows and error bit 1, never an access
+        // outside the arguments.
+        const int tab_len = p.B * p.rule.NS_cap;
+        const int hsh = log2_if_pow2(HR);
+        const int g0 = hsh >= 0 ? (int)(blockIdx.x >> hsh) : (int)blockIdx.x / HR;
+        int4 e = g0 < tab_len ? __ldg(p.plan_tab + g0) : make_int4(-1, 0, 0, 0);
+        const int P = p.plan_hdr[0], G = p.plan_hdr[2];
+        if (P <= 0 || G < p.B || G > tab_len) {
+            if (blockIdx.x == 0 && threadIdx.x == 0 && p.err) atomicOr(p.err, kErrStalePlan);
+            return;
+        }
+        // Items: G * HR <= B * NS_cap * HR < 2^31 (the host bounds the plan's
+        // items), so k + gridDim.x stays below 2^32.
+        const unsigned total = (unsigned)G * (unsigned)HR;
+        if (threadIdx.x == 0) *abort_flag = 0;
+        for (unsigned k = blockIdx.x; k < total; k += gridDim.x) {
+            const int g = (int)(hsh >= 0 ? k >> hsh : k / (unsigned)HR);   // < G <= tab_len
+            if (k != blockIdx.x) e = __ldg(p.plan_tab + g);
+            const int b = e.x, sp = e.y, n = e.z;
+            if (b < 0 || b >= p.B || sp < 0 || sp >= p.rule.NS_cap || n < 0 || n > p.n_cap ||
+                (long long)sp * P >= (long long)max(n, 1)) {
+                if (threadIdx.x == 0 && p.err) atomicOr(p.err, kErrStalePlan);
+                continue;   // uniform in the CTA: every thread read the same entry
+            }
+            const int kr = (int)k - g * HR;
+            run_item(b, p.RT == 1 ? kr : kr / p.RT, p.RT == 1 ? 0 : kr % p.RT, sp, P, n);
+            if (k + gridDim.x >= total) return;   // no further item: free the SM's slot at once
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (*abort_flag) break;
+        }
+        return;
+    } else {
+        // Device plan (device_plan.cuh): every warp plans from the context lengths
+        // and finds this CTA's items one by one (the same in each warp, so no
+        // broadcast and no barrier precede the first item); CTA 0 publishes the
+        // partition for the combine kernel, and the first item of each split
+        // records the split in the table for the calls that reuse the plan.
+        PlanCursor cur{0, 0};
+        int P = 0, b = 0, j = 0, n = 0;
+        bool found = false, only = false;
+        {
+            PlanRegs pr;
+            int mx = 0;
+            long long sum = 0, total = -1;
+            warp_context_stats(p.ctx, p.B, p.n_cap, p.rule.sum32 != 0, lane, pr, &mx, &sum);
+            P = device_plan_partition_rule(p.rule, mx, sum);
+            if (blockIdx.x == 0 && threadIdx.x == 0) {
+                p.plan_hdr[0] = P;
+                p.plan_hdr[1] = mx > 0 ? (mx - 1) / P + 1 : 1;
+            }
+            const PlanDiv dv(P, HR);
+            found = warp_plan_first_item(pr, p.B, dv, blockIdx.x, cur, lane, &b, &j, &n, &total);
+            if (!found) found = warp_plan_item(p.ctx, p.B, p.n_cap, dv, blockIdx.x, cur, lane, &b, &j, &n);
+            only = total >= 0 && (long long)blockIdx.x + gridDim.x >= total;   // no second item
         }
         const PlanDiv dv(P, HR);
-        found = warp_plan_first_item(pr, p.B, dv, blockIdx.x, cur, lane, &b, &j, &n, &total);
-        if (!found) found = warp_plan_item(p.ctx, p.B, p.n_cap, dv, blockIdx.x, cur, lane, &b, &j, &n);
-        only = total >= 0 && (long long)blockIdx.x + gridDim.x >= total;   // no second item
-    }
-    const PlanDiv dv(P, HR);
-    // Read after each item's closing barrier; an empty item does not set it.
-    if (threadIdx.x == 0) *abort_flag = 0;
-    for (long long k = blockIdx.x;; k += gridDim.x) {
-        if (k != blockIdx.x) found = warp_plan_item(p.ctx, p.B, p.n_cap, dv, k, cur, lane, &b, &j, &n);
-        if (!found) break;
-        const int s = dv.split_of(j);   // item j of a sequence: split s, then (grid KV head, row tile) kr
-        const int kr = j - s * HR;
-        run_item(b, p.RT == 1 ? kr : kr / p.RT, p.RT == 1 ? 0 : kr % p.RT, s, P, n);
-        if (only) return;           // leave at once, freeing the SM's slot for the next CTA
-        fence_proxy_async_smem();   // this item's generic writes to the ring before the next item's copies
-        __syncthreads();            // every role is done with the ring, the barriers and the Q tile
-        if (*abort_flag) break;     // a wait timed out (already reported): take no further item
+        // Read after each item's closing barrier; an empty item does not set it.
+        if (threadIdx.x == 0) *abort_flag = 0;
+        for (long long k = blockIdx.x;; k += gridDim.x) {
+            if (k != blockIdx.x) found = warp_plan_item(p.ctx, p.B, p.n_cap, dv, k, cur, lane, &b, &j, &n);
+            if (!found) break;
+            const int s = dv.split_of(j);   // item j of a sequence: split s, then (grid KV head, row tile) kr
+            const int kr = j - s * HR;
+            if (kr == 0 && threadIdx.x == 0) {   // split k / HR of the plan (< B * NS_cap: P bounds the splits)
+                const int g = dv.split_of((int)k);
+                p.plan_tab[g] = make_int4(b, s, n, 0);
+                if (b == p.B - 1 && (long long)(s + 1) * P >= n) p.plan_hdr[2] = g + 1;   // the last split
+            }
+            run_item(b, p.RT == 1 ? kr : kr / p.RT, p.RT == 1 ? 0 : kr % p.RT, s, P, n);
+            if (only) return;           // leave at once, freeing the SM's slot for the next CTA
+            fence_proxy_async_smem();   // this item's generic writes to the ring before the next item's copies
+            __syncthreads();            // every role is done with the ring, the barriers and the Q tile
+            if (*abort_flag) break;     // a wait timed out (already reported): take no further item
+        }
     }
 }
 
-template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED, bool STRESS>
+template <typename T, int LAYOUT, int D, int NT, bool GEN, int SCHED, bool STRESS>
 __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
     decode_phase1_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv) {
@@ -486,7 +540,7 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32)
 }
 
 // The same for the shared-Q tiles, compiled for four CTAs per SM.
-template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED, bool STRESS>
+template <typename T, int LAYOUT, int D, int NT, bool GEN, int SCHED, bool STRESS>
 __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32, DecodeTile<D, LAYOUT>::QS_MIN_BLOCKS)
     decode_phase1_kernel_qs(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv) {
@@ -495,7 +549,7 @@ __global__ void __launch_bounds__((DecodeTile<D, LAYOUT>::NWC + 1) * 32, DecodeT
 
 // Host-side launcher for one instantiation (one-token without bias, general,
 // or general over the device plan's items; STRESS: with the race-testing pauses).
-template <typename T, int LAYOUT, int D, int NT, bool GEN, bool SCHED, bool STRESS>
+template <typename T, int LAYOUT, int D, int NT, bool GEN, int SCHED, bool STRESS>
 cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                          const CUtensorMap& tmv, cudaStream_t stream) {
     using Tile = DecodeTile<D, LAYOUT>;
@@ -522,11 +576,15 @@ cudaError_t launch_decode_phase1_variant(const DecodeParams& p, long long grid, 
 template <typename T, int LAYOUT, int D, int NT, bool STRESS>
 cudaError_t launch_decode_phase1_kind(const DecodeParams& p, long long grid, const CUtensorMap& tmk,
                                       const CUtensorMap& tmv, cudaStream_t stream) {
+    // A reused plan under the race-testing pauses is planned again: the same
+    // items, and no third stress instantiation.
+    if (p.plan_hdr && p.plan_ready && !STRESS)
+        return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, kSchedReuse, STRESS>(p, grid, tmk, tmv, stream);
     if (p.plan_hdr)
-        return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, true, STRESS>(p, grid, tmk, tmv, stream);
+        return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, kSchedPlan, STRESS>(p, grid, tmk, tmv, stream);
     if (p.alibi || p.q_len > 1)
-        return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, false, STRESS>(p, grid, tmk, tmv, stream);
-    return launch_decode_phase1_variant<T, LAYOUT, D, NT, false, false, STRESS>(p, grid, tmk, tmv, stream);
+        return launch_decode_phase1_variant<T, LAYOUT, D, NT, true, kSchedGrid, STRESS>(p, grid, tmk, tmv, stream);
+    return launch_decode_phase1_variant<T, LAYOUT, D, NT, false, kSchedGrid, STRESS>(p, grid, tmk, tmv, stream);
 }
 
 template <typename T, int LAYOUT, int D, int NT>

@@ -26,11 +26,24 @@
 // with one warp scan of the lanes' item counts and a search among one lane's
 // 8 sequences; sequences past the first 256, and a CTA's later items, are
 // walked 32 at a time from memory.
+//
+// The plan depends only on the context lengths and the problem, which the
+// layers of one decode step share.  So the planning call also records it for
+// them: the first item of each split writes {sequence, split, context} to
+// entry k / HR of a table in the workspace (item k; a split's HR items are
+// consecutive) and the one holding the last split writes the split count.  A
+// call flagged PKV_DECODE_PLAN_READY reads its items from there -- one load
+// of the header and of its first entry in flight together, in place of the
+// planning chain -- after checking every value against the bounds.
 #pragma once
 
 #include "decode_common.cuh"
 
 namespace pkv {
+
+// Error bit of a call that reuses a plan (PKV_DECODE_PLAN_READY) and finds
+// none of this problem in the workspace: the affected rows are unspecified.
+constexpr uint32_t kErrStalePlan = 2u;
 
 struct PlanRule {
     int P_fixed;     // > 0: this partition (caller option)

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_function(B):
 
 
 def test_version_and_status_strings(B):
-    assert B.pkv_version() == 8
+    assert B.pkv_version() == 9
     assert B.status_string(0) == "ok"
     assert B.status_string(5) == "bad block table"
     assert B.status_string(99) == "unknown status"
@@ -168,9 +168,11 @@ def test_device_plan_options(B):
     d = desc(B)
     ns, P = B.pkv_plan_splits(d, None, 152)
     plain = B.pkv_decode_workspace_size(d, None, 152)
-    # phase 1 plans on the device itself: the workspace is that of the bounds' host plan
+    # phase 1 plans on the device itself: the workspace is that of the bounds' host plan, plus the
+    # split table the plan is kept in for the calls that reuse it (16 bytes per sequence and split)
     dev = B.pkv_decode_workspace_size(d, B.make_opts(device_plan=True), 152)
-    assert dev == plain
+    assert dev == plain + al(d.B * ns * 16)
+    assert B.pkv_decode_workspace_size(d, B.make_opts(plan_ready=True), 152) == dev
     assert B.pkv_plan_splits(d, B.make_opts(device_plan=True), 152) == (ns, P)
     assert B.pkv_plan_splits(d, B.make_opts(plan_ready=True), 152) == (ns, P)   # flags 3
     assert B.make_opts(plan_ready=True).flags == B.PKV_DECODE_DEVICE_PLAN | B.PKV_DECODE_PLAN_READY

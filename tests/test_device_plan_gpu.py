@@ -209,3 +209,97 @@ def test_plan_made_once_reused_by_later_layers(q_len):
     assert int(ws[:4].view(torch.int32).item()) == 0
     for c, out in zip(layers, outs):
         check(c, out)
+
+
+def _call(case, desc, opts, dev, ws, out):
+    B = _binding()
+    B.pkv_paged_decode_attention(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
+                                 dev["context_lens"], case["scale"], out, ws, opts=opts)
+
+
+REUSE_CASES = CASES + [
+    # more sequences than the planner keeps in registers (its walk from memory writes the table)
+    dict(B=300, Hq=8, Hkv=2, D=64, dtype=synth.F16, layout=synth.NHD, ctx_range=(0, 400)),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(REUSE_CASES)))
+@pytest.mark.parametrize("bounds", ["exact", "capacity"])
+@pytest.mark.parametrize("opt", [dict(), dict(partition_tokens=32)])
+def test_reused_plan_is_bit_identical_to_planning(idx, bounds, opt):
+    # A call with PKV_DECODE_PLAN_READY takes its items from the split table the planning call
+    # left in the workspace: the same items, so the same bits; a second reuse finds the table
+    # unchanged.
+    B, T = _binding(), _tensors()
+    case = synth.decode_case(seed=670 + idx, block_size=16, max_blocks_per_seq=256, **REUSE_CASES[idx])
+    dev = T.upload_decode_case(case)
+    desc = T.decode_desc(case)
+    if bounds == "capacity":
+        desc = loose(case, desc)
+    plan, reuse = B.make_opts(device_plan=True, **opt), B.make_opts(plan_ready=True, **opt)
+    ws = T.workspace_for(desc, plan)
+    outs = []
+    for opts in (plan, reuse, reuse):
+        out = torch.full(case["q"].shape, float("nan"), dtype=T.TORCH_DTYPE[case["dtype"]], device="cuda")
+        _call(case, desc, opts, dev, ws, out)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    check(case, outs[1])
+
+
+def test_split_table_contents():
+    # Header word 6 holds the plan's split count; entry g of the table (after the partials) is
+    # {sequence, split, clamped context, 0} for the g-th split in (sequence, split) order.
+    B, T = _binding(), _tensors()
+    lens = [0, 1, 700, 1024, 1025, 300]
+    case = synth.decode_case(seed=641, B=6, Hq=8, Hkv=2, D=128, block_size=16, dtype=synth.BF16,
+                             layout=synth.NHD, context_lens=lens, max_blocks_per_seq=128)
+    desc = loose(case, T.decode_desc(case))          # bounds 2048: 4 splits of 512 per sequence
+    opts = B.make_opts(partition_tokens=512, device_plan=True)
+    ns, P = B.pkv_plan_splits(desc, opts)
+    dev = T.upload_decode_case(case)
+    out = torch.empty(case["q"].shape, dtype=torch.bfloat16, device="cuda")
+    ws = T.workspace_for(desc, opts)
+    _call(case, desc, opts, dev, ws, out)
+    torch.cuda.synchronize()
+    want = [(b, s, n) for b, n in enumerate(lens) for s in range(max(1, -(-n // 512)))]
+    assert ws[16:28].view(torch.int32).cpu().tolist() == [512, 3, len(want)]
+    tab_bytes = (6 * ns * 16 + 255) // 256 * 256
+    tab = ws[ws.numel() - tab_bytes:].view(torch.int32).view(-1, 4).cpu().numpy()
+    assert [tuple(int(v) for v in row[:3]) for row in tab[:len(want)]] == want
+    assert np.all(tab[:len(want), 3] == 0)
+
+
+def test_reuse_without_a_plan_is_reported():
+    # The flag states that the workspace holds this problem's plan.  A workspace that holds none
+    # (a header of all ones) sets error bit 1 and reads nothing else of it; a table whose entries
+    # are out of range (all ones after a real plan) sets it too and skips those items.  Either way
+    # no memory outside the arguments is touched, and the next planning call is correct.
+    B, T = _binding(), _tensors()
+    case = synth.decode_case(seed=642, B=16, Hq=32, Hkv=8, D=128, block_size=16, dtype=synth.BF16,
+                             layout=synth.NHD, ctx_range=(1, 3000), max_blocks_per_seq=256)
+    desc = T.decode_desc(case)
+    plan, reuse = B.make_opts(device_plan=True), B.make_opts(plan_ready=True)
+    ns, _ = B.pkv_plan_splits(desc, plan)
+    dev = T.upload_decode_case(case)
+    out = torch.zeros(case["q"].shape, dtype=torch.bfloat16, device="cuda")
+    ws = T.workspace_for(desc, plan)
+    ws.fill_(0xFF)
+    ws[:4].zero_()
+    _call(case, desc, reuse, dev, ws, out)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 2
+    tab_bytes = (case["B"] * ns * 16 + 255) // 256 * 256
+    ws[:4].zero_()
+    _call(case, desc, plan, dev, ws, out)
+    ws[ws.numel() - tab_bytes:].fill_(0xFF)
+    _call(case, desc, reuse, dev, ws, out)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 2
+    ws[:4].zero_()
+    _call(case, desc, plan, dev, ws, out)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    check(case, out)
