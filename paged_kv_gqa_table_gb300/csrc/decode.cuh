@@ -34,6 +34,7 @@
 //         for ldmatrix), V [D][BS] (two-way conflicts at most).
 #pragma once
 
+#include <climits>
 #include <type_traits>
 
 #include "decode_common.cuh"
@@ -453,15 +454,18 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
         // header, and item k's sequence, split and context from entry k / HR
         // of the table (a split's HR items are consecutive).  The first entry
         // is requested before the header arrives.  Every value is checked
-        // against the bounds before use, so a workspace without this
-        // problem's plan costs wrong rows and error bit 1, never an access
-        // outside the arguments.
+        // before use -- P a positive multiple of the page, as every plan's;
+        // an entry's sequence, split and context inside the bounds, its first
+        // key below its context, and (s + 1) P + n within int, so that no
+        // key or page index of run_item overflows -- so a workspace without
+        // this problem's plan costs wrong rows and error bit 1, never an
+        // access outside the arguments.
         const int tab_len = p.B * p.rule.NS_cap;
         const int hsh = log2_if_pow2(HR);
         const int g0 = hsh >= 0 ? (int)(blockIdx.x >> hsh) : (int)blockIdx.x / HR;
         int4 e = g0 < tab_len ? __ldg(p.plan_tab + g0) : make_int4(-1, 0, 0, 0);
         const int P = p.plan_hdr[0], G = p.plan_hdr[2];
-        if (P <= 0 || G < p.B || G > tab_len) {
+        if (P < kPageTokens || (P & (kPageTokens - 1)) != 0 || G < p.B || G > tab_len) {
             if (blockIdx.x == 0 && threadIdx.x == 0 && p.err) atomicOr(p.err, kErrStalePlan);
             return;
         }
@@ -474,7 +478,7 @@ __device__ __forceinline__ void decode_phase1_body(const DecodeParams& p, const 
             if (k != blockIdx.x) e = __ldg(p.plan_tab + g);
             const int b = e.x, sp = e.y, n = e.z;
             if (b < 0 || b >= p.B || sp < 0 || sp >= p.rule.NS_cap || n < 0 || n > p.n_cap ||
-                (long long)sp * P >= (long long)max(n, 1)) {
+                (long long)sp * P >= (long long)max(n, 1) || (long long)(sp + 1) * P + n > INT_MAX) {
                 if (threadIdx.x == 0 && p.err) atomicOr(p.err, kErrStalePlan);
                 continue;   // uniform in the CTA: every thread read the same entry
             }

@@ -279,7 +279,7 @@ def test_reuse_without_a_plan_is_reported():
     # no memory outside the arguments is touched, and the next planning call is correct.
     B, T = _binding(), _tensors()
     case = synth.decode_case(seed=642, B=16, Hq=32, Hkv=8, D=128, block_size=16, dtype=synth.BF16,
-                             layout=synth.NHD, ctx_range=(1, 3000), max_blocks_per_seq=256)
+                             layout=synth.NHD, ctx_range=(16, 3000), max_blocks_per_seq=256)
     desc = T.decode_desc(case)
     plan, reuse = B.make_opts(device_plan=True), B.make_opts(plan_ready=True)
     ns, _ = B.pkv_plan_splits(desc, plan)
@@ -298,6 +298,16 @@ def test_reuse_without_a_plan_is_reported():
     _call(case, desc, reuse, dev, ws, out)
     torch.cuda.synchronize()
     assert int(ws[:4].view(torch.int32).item()) == 2
+    # A partition that is not a page multiple is refused; one near 2^31 fails the entries whose
+    # last key or page index would overflow (every context here is longer than 15 tokens).
+    assert min(case["context_lens"]) > 15
+    for bad_p in (17, 0x7FFFFFF0):
+        ws[:4].zero_()
+        _call(case, desc, plan, dev, ws, out)
+        ws[16:20].view(torch.int32).fill_(bad_p)
+        _call(case, desc, reuse, dev, ws, out)
+        torch.cuda.synchronize()
+        assert int(ws[:4].view(torch.int32).item()) == 2, bad_p
     ws[:4].zero_()
     _call(case, desc, plan, dev, ws, out)
     torch.cuda.synchronize()
