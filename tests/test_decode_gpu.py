@@ -383,3 +383,23 @@ def test_decode_step_replays_in_a_cuda_graph(kv8):
         torch.cuda.synchronize()
         sub = dict(case, context_lens=lens)
         check_rows(sub, out.double().cpu().numpy(), list(range(12)))
+
+
+def test_million_token_context():
+    # One sequence of 1,000,003 tokens beside a short one: 1,954 splits of 512 tokens merged by the
+    # wide combine, a block-table row of 62,501 pages (a random permutation of the pool), and the
+    # unread tail slots poisoned.  Host plan and device plan (exact bounds: the same items, so the
+    # same bits) against the oracle on both rows.
+    B, T = _binding(), _tensors()
+    case = _case(31, B=2, Hq=8, Hkv=1, D=128, block_size=16, dtype=synth.BF16, layout=synth.NHD,
+                 context_lens=[1_000_003, 777], max_blocks_per_seq=62_501, slack_pages=3, poison=True)
+    desc = T.decode_desc(case)
+    assert B.pkv_plan_splits(desc) == (1954, 512)
+    dev = T.upload_decode_case(case)
+    outs = []
+    for opts in (None, B.make_opts(device_plan=True)):
+        out = T.paged_decode_attention(case, dev=dev, opts=opts)
+        torch.cuda.synchronize()
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
+    check_rows(case, outs[0].double().cpu().numpy(), [0, 1])
