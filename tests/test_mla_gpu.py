@@ -278,3 +278,24 @@ def test_mla_long_sequence_shares_the_last_task_bin():
     for (t, h), (ro, rl) in zip(pairs, refs):
         assert float(np.max(np.abs(got_out[t, h] - ro))) <= TOL_OUT, (t, h)
         assert abs(float(got_lse[t, h]) - float(rl)) <= TOL_LSE, (t, h)
+
+
+def test_mla_batch_of_600_sequences():
+    """600 sequences: the task builder's scans over the batch (256 sequences per pass, carried
+    across passes), its tile loops and its export-block scan all take several passes.  Query
+    lengths include 0 and the 16-token tile edges, prefixes 0 and the 128-key block edges.  The
+    replay equals the two-task result bit for bit; the first and last token of every sequence
+    match the oracle."""
+    import random
+    r = random.Random(8600)
+    batch = 600
+    q_lens = [r.choice([0, 1, 5, 16, 17, 40]) for _ in range(batch)]
+    prefixes = [r.choice([0, 1, 127, 128, 300]) for _ in range(batch)]
+    case = synth.mla_case(seed=86, batch=batch, q_len_range=(1, 1), prefix_range=(0, 0), q_lens=q_lens,
+                          prefixes=prefixes, slack_pages=9, poison=True)
+    a = gpu_mla(case, replay=False)
+    b = gpu_mla(case, replay=True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    qo = case["qo_indptr"]
+    tokens = sorted({int(t) for i in range(batch) if qo[i + 1] > qo[i] for t in (qo[i], qo[i + 1] - 1)})
+    check(case, *b, tokens=tokens)
