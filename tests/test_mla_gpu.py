@@ -299,3 +299,19 @@ def test_mla_batch_of_600_sequences():
     qo = case["qo_indptr"]
     tokens = sorted({int(t) for i in range(batch) if qo[i + 1] > qo[i] for t in (qo[i], qo[i + 1] - 1)})
     check(case, *b, tokens=tokens)
+
+
+def test_mla_one_long_query_sequence():
+    """One sequence of 4,096 query tokens over a 100-key prefix: 256 row tiles of one sequence
+    whose block counts run from 1 to 33, so the causal diagonal crosses every position inside a
+    key block.  The replay equals the two-task result bit for bit; tokens at row-tile edges and
+    at key-block edges match the oracle."""
+    case = synth.mla_case(seed=87, batch=1, q_len_range=(1, 1), prefix_range=(0, 0), q_lens=[4096],
+                          prefixes=[100], slack_pages=4, poison=True)
+    a = gpu_mla(case, replay=False)
+    b = gpu_mla(case, replay=True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # token t sees keys 0 .. 100 + t: edges of 16-token tiles and of 128-key blocks
+    tokens = sorted({0, 1, 15, 16, 27, 28, 155, 156, 2047, 2048, 4080, 4095} |
+                    {128 * k - 101 for k in range(1, 33)} | {128 * k - 100 for k in range(1, 33)})
+    check(case, *b, tokens=[t for t in tokens if 0 <= t < 4096])
