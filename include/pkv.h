@@ -355,14 +355,16 @@ PKV_API int pkv_mla_paged_prefill(const pkv_mla_desc* desc, const void* q_nope, 
  * that carves all device memory out of a fixed pool at start-up, or a
  * latency-critical loop where cudaMalloc could synchronise the device.
  *
- * The step's scratch (error word and split partials) lives in one
+ * The step's scratch (error word, split partials and, with the device plan,
+ * the plan's header words and split table) lives in one
  * file-scope device array of PKV_STATIC_SCRATCH_BYTES (32 MiB), which
  * every GPU that loads libpkv reserves until the process exits.  This call
  * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  * Once every argument has passed the regular entry point's checks, it clears
  * the array's 4-byte error word (word 0 of the header) with cudaMemsetAsync
  * on `stream` and runs the regular entry point on the array; the rest of the
- * header keeps the previous call's contents.  pkv_static_scratch_error reads the error word.
+ * array (a device plan's header words and split table included) keeps the
+ * previous call's contents.  pkv_static_scratch_error reads the error word.
  *  - A problem whose workspace (pkv_decode_workspace_size) exceeds the array
  *    is refused with PKV_WORKSPACE_TOO_SMALL before anything is launched.
  *  - PKV_DECODE_PLAN_READY is refused (PKV_INVALID_ARG) unless the previous

@@ -87,9 +87,10 @@ int pkv_paged_decode_attention_static(const pkv_decode_desc* desc, const pkv_dec
           d->last.partition_tokens == opts->partition_tokens && d->last.num_splits == opts->num_splits))
         return PKV_INVALID_ARG;
     // Every argument is checked before the array is touched; the error word is
-    // then cleared on the stream (the rest of the header may hold a device plan
-    // an earlier call made for reuse); the partials are fully written by phase
-    // 1 before phase 2 reads them, so they need no clearing.
+    // then cleared on the stream (the rest of the header and the split table
+    // may hold a device plan an earlier call made for reuse); the partials are
+    // fully written by phase 1 before phase 2 reads them, so they need no
+    // clearing.
     st = pkv::paged_decode_impl(desc, opts, q, k_cache, v_cache, block_table, context_lens, scale, out, d->addr,
                                 kStaticScratchBytes, stream, true);
     if (st == PKV_OK) {
