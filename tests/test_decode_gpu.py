@@ -156,7 +156,7 @@ def test_phase1_partials_match_oracle_split_mode(layout, dtype, D, G, P):
     assert np.all(m[sentinel] == -np.inf) and np.all(l[sentinel] == 0) and np.all(acc[sentinel] == 0)
     live = ~sentinel
     np.testing.assert_allclose(m[live] + np.log(l[live]), rm[live] + np.log(rl[live]), rtol=0, atol=1e-3)
-    np.testing.assert_allclose((acc / l[..., None])[live], (racc / rl[..., None])[live], rtol=0, atol=TOL[dtype])
+    np.testing.assert_allclose(acc[live] / l[live][..., None], racc[live] / rl[live][..., None], rtol=0, atol=TOL[dtype])
 
 
 @pytest.mark.parametrize("dtype,D,P", [(synth.BF16, 128, 64), (synth.F16, 64, 64), (synth.F16, 256, 64),

@@ -131,7 +131,7 @@ def test_multi_token_partials_match_oracle(P):
     live = ~sentinel
     assert np.all(np.isfinite(m[live])) and np.all(l[live] > 0)
     np.testing.assert_allclose(m[live] + np.log(l[live]), rm[live] + np.log(rl[live]), rtol=0, atol=1e-3)
-    np.testing.assert_allclose((acc / l[..., None])[live], (racc / rl[..., None])[live], rtol=0,
+    np.testing.assert_allclose(acc[live] / l[live][..., None], racc[live] / rl[live][..., None], rtol=0,
                                atol=TOL[synth.BF16])
 
 
