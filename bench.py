@@ -5,7 +5,9 @@
 The default workload is the largest single-GPU decode configuration
 (gqa6_d256_vllm_decode: 128 sequences, GQA-6, D = 256, vLLM layout); the same
 run measures the other configurations (Llama-3-8B-shaped, long-context, FP8,
-4-token and the MLA prefill) and reports them under "per_config".
+4-token and the MLA prefill) and reports them under "per_config", the
+Llama-3-8B-shaped one with what the device plan costs there ("device_plan":
+host plan, planning in phase 1, a reused plan at exact and capacity bounds).
 
 One step = one full decode step of the workload (phase 1 + cross-split
 combine) on synthetic inputs already resident in HBM.  Between timed steps a
@@ -454,9 +456,65 @@ def measure_decode(name, device, steps, warmup, world=1, rank=0, e2e_leg=True, c
     return fields, case
 
 
+DEVICE_PLAN_STEPS = 100
+
+
+def measure_device_plan(name, device, steps, warmup):
+    """What the device plan (PKV_DECODE_DEVICE_PLAN) costs on one decode workload: mean µs per
+    step, cold L2 before each, with the host plan, with phase 1 planning from the device's
+    context lengths, and with the plan an earlier call left in the workspace reused
+    (PKV_DECODE_PLAN_READY, as the later layers of one decode step do) -- at exact bounds and at
+    capacity bounds (every context may fill its block-table row, as in a captured graph)."""
+    import torch
+    from paged_kv_gqa_table_gb300 import binding as B
+    from paged_kv_gqa_table_gb300 import synth, tensors
+
+    case = synth.decode_case(seed=0, **synth.WORKLOADS[name])
+    dev = tensors.upload_decode_case(case, device)
+    out = torch.empty(case["q"].shape, dtype=tensors.TORCH_DTYPE[case["dtype"]], device=device)
+    flush = ColdL2(torch, device)
+    stream = torch.cuda.current_stream(device)
+    legs = (("host_plan", False, None), ("device_plan", False, B.make_opts(device_plan=True)),
+            ("plan_reused", False, B.make_opts(plan_ready=True)),
+            ("plan_reused_capacity_bounds", True, B.make_opts(plan_ready=True)))
+    res = {}
+    for label, capacity, opts in legs:
+        desc = tensors.decode_desc(case)
+        if capacity:
+            desc.max_context_len = desc.max_blocks_per_seq * desc.block_size
+            desc.sum_context_len = desc.B * desc.max_context_len
+        ws = tensors.workspace_for(desc, opts, device=device)
+
+        def call(o):
+            B.pkv_paged_decode_attention(desc, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
+                                         dev["context_lens"], case["scale"], out, ws, opts=o, stream=stream)
+        if opts is not None and opts.flags & B.PKV_DECODE_PLAN_READY:
+            call(B.make_opts(device_plan=True))   # the earlier layer, which plans
+        for _ in range(warmup):
+            flush()
+            call(opts)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            flush()
+            a.record(stream)
+            call(opts)
+            b.record(stream)
+        torch.cuda.synchronize(device)
+        err = int(ws[:4].view(torch.int32).item())
+        if err:
+            raise RuntimeError("device error word %d in the %s leg" % (err, label))
+        res[label + "_us"] = float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1e3
+    res["device_plan_overhead_us"] = res["device_plan_us"] - res["host_plan_us"]
+    res["plan_reused_overhead_us"] = res["plan_reused_us"] - res["host_plan_us"]
+    res["plan_reused_capacity_bounds_overhead_us"] = res["plan_reused_capacity_bounds_us"] - res["host_plan_us"]
+    res["steps_per_leg"] = steps
+    return res
+
+
 # The headline workload is the largest single-GPU configuration; the others are
 # measured in the same run and reported under "per_config".
 HEADLINE = "gqa6_d256_vllm_decode"
+DEVICE_PLAN_WORKLOAD = "llama3_8b_decode"
 PER_CONFIG = ["llama3_8b_decode", "long_context_decode", "llama3_8b_decode_fp8", "llama3_8b_spec_decode_q4",
               "mla_prefill_h16"]
 PER_CONFIG_STEPS = 300
@@ -490,6 +548,9 @@ def run_gpu(args):
                                                   "cpu_baseline", "gpu_launches", "config") if k in f}
             if "hbm_frac_of_measured_peak" in f:
                 per_config[name]["hbm_frac_of_measured_peak"] = f["hbm_frac_of_measured_peak"]
+            if name == DEVICE_PLAN_WORKLOAD:
+                per_config[name]["device_plan"] = measure_device_plan(name, device, min(steps, DEVICE_PLAN_STEPS),
+                                                                      args.warmup)
     if rank == 0:
         line = {"metric": METRIC, "n_gpus": world, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None,
