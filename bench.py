@@ -500,10 +500,10 @@ def measure_device_plan(name, device, steps, warmup):
             call(opts)
             b.record(stream)
         torch.cuda.synchronize(device)
-        err = int(ws[:4].view(torch.int32).item())
-        if err:
-            raise RuntimeError("device error word %d in the %s leg" % (err, label))
         res[label + "_us"] = float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1e3
+        err = int(ws[:4].view(torch.int32).item())
+        if err:   # reported, not raised: the rest of the line still prints
+            res[label + "_device_error_word"] = err
     res["device_plan_overhead_us"] = res["device_plan_us"] - res["host_plan_us"]
     res["plan_reused_overhead_us"] = res["plan_reused_us"] - res["host_plan_us"]
     res["plan_reused_capacity_bounds_overhead_us"] = res["plan_reused_capacity_bounds_us"] - res["host_plan_us"]
